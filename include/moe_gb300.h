@@ -1,0 +1,264 @@
+/*
+ * moe_gb300.h -- C ABI of the GB300 (sm_103a) routed-expert MoE layer with
+ * 2-bit / 3-bit block-quantised experts.
+ *
+ * The layer this library computes, per token x (bf16, hidden size H):
+ *   logits = W_router x + b                      (fp32, E experts)
+ *   ids, w = top-k of logits, ties to the lower id; w = the kept softmax
+ *            probabilities renormalised to sum to 1
+ *   out    = S(x) + sum_j w_j * FFN_{ids_j}(x)
+ *   FFN_e(x) = Wd_e (silu(Wg_e x) * (Wu_e x)),  silu(g) = g / (1 + e^-g)
+ *   S(x)   = the always-on shared expert, the same SwiGLU with bf16 weights.
+ * The routed experts are stored in 32-weight blocks along each row's input
+ * dimension with one fp16 scale s per block; a 2-bit code c stands for
+ * (c - 1.5) s and a 3-bit code for (c - 3.5) s.
+ *
+ * Where this comes from.  "How Strata runs a 125-billion-parameter model on
+ * a single 12 GB to 24 GB graphics card" (introduction and the Step 1
+ * byte-census table) and "Strata Open-Source Runtime: Running a 125B-Parameter
+ * Qwen3 Model on a 12GB GPU" (section "The Model Itself") describe a router
+ * that keeps 10 of 512 experts per layer for every token, an always-on shared
+ * expert, 48 layers, and 2-bit ("Q2_0") routed experts of which one token
+ * reads 0.66 GB of 34.0 GB; "Strata serves a 125B MoE at 94 tokens/s from a
+ * 12 GB card and 64 GB of RAM" (Table 1, "Where the weights live") repeats the
+ * census.  The first page, Step 2, sums the finished expert vectors on the
+ * GPU.  The pages give no bit layout, activation function, router
+ * normalisation or shared-expert precision; the statements above are the
+ * readings this library takes.
+ *
+ * Conventions for every call:
+ *  - Status.  Every call returns a moe_status.  Argument errors are found on
+ *    the host before anything is launched and leave all buffers untouched.
+ *    A non-OK return also sets a thread-local message, moe_last_error(),
+ *    that names the argument and, for sizes, the bytes or MiB involved.
+ *  - Device-detected errors (bad ids, NaN logits, codes that do not fit) are
+ *    written into a caller-provided int32 status word in device memory
+ *    (dev_status; the first error wins, 0 means OK; it may be NULL, in which
+ *    case such errors are not reported).  Read it with moe_check_status().
+ *    A kernel that detects such an error skips the offending element and
+ *    still writes every output it owns.
+ *  - Ownership.  The caller allocates every buffer and passes raw device
+ *    pointers (unless a parameter says "host").  The library never allocates
+ *    or frees memory and never synchronises a stream, except
+ *    moe_check_status(), which synchronises the stream it is given.  Scratch
+ *    memory comes from a caller-provided workspace whose size the matching
+ *    *_workspace_size() call returns; a smaller workspace returns
+ *    MOE_ERR_WORKSPACE with the bytes needed in the message.
+ *  - Asynchrony.  Work is enqueued on `stream` and returns at once.
+ *  - Shapes.  H and I are multiples of 32; 1 <= E <= 1024;
+ *    1 <= k <= min(E, 16); T >= 0 (T = 0 is a no-op that returns MOE_OK).
+ *  - Types.  bf16 and fp16 values are passed as uint16_t bit patterns.
+ *    Row-major everywhere.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same handle type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1, /* a bad pointer, shape, code or scale           */
+    MOE_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement */
+    MOE_ERR_WORKSPACE = 3,   /* workspace smaller than *_workspace_size()     */
+    MOE_ERR_CUDA = 4,        /* a CUDA runtime call failed                    */
+    MOE_ERR_TIMEOUT = 5,     /* a device-side wait ran out of its time limit  */
+    MOE_ERR_NONFINITE = 6,   /* a NaN router logit                            */
+    MOE_ERR_BOUNDS = 7       /* an expert id outside [0, E)                   */
+} moe_status;
+
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef enum moe_path {
+    MOE_PATH_AUTO = 0,    /* DECODE for T <= 8, PREFILL otherwise           */
+    MOE_PATH_DECODE = 1,  /* dequant-fused GEMVs on CUDA cores, fp32 maths  */
+    MOE_PATH_PREFILL = 2  /* grouped GEMM over the experts' token lists     */
+} moe_path;
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char *moe_last_error(void);
+
+/* Short name of a status code, e.g. "MOE_ERR_BOUNDS". */
+const char *moe_status_name(moe_status s);
+
+/*
+ * Synchronise `stream`, read the int32 device status word and return it as a
+ * moe_status (setting moe_last_error() when it is not MOE_OK).  If `reset` is
+ * non-zero the word is set back to 0 afterwards.
+ */
+moe_status moe_check_status(int32_t *dev_status, int reset, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Packed block format                                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Bytes of one packed [rows][cols] matrix.  cols is a multiple of 32.
+ *   code plane:  rows * row_bytes, row_bytes = cols/4 (2-bit) or 3*cols/8
+ *                (3-bit);
+ *   scale plane: rows * (cols/32) fp16 values = rows * cols/16 bytes.
+ * Layout of one packed row of codes:
+ *   bytes [0, cols/4):     weight i's two low code bits at bits
+ *                          2*(i%4) .. 2*(i%4)+1 of byte i/4;
+ *   bytes [cols/4, 3cols/8) (3-bit only): one little-endian 32-bit word per
+ *                          32-weight block b, at byte cols/4 + 4b, holding
+ *                          the high bit of weight 32b+i at bit
+ *                          (i&7) | ((i&8)<<1) | ((i&16)>>1).
+ * The scale plane is [rows][cols/32] fp16, block b of row r covering weights
+ * 32b .. 32b+31 of that row.  Sizes follow the byte census of the pages (a
+ * 2-bit expert with H=2048, I=768 is 1,474,560 bytes; see the Step 1 table of
+ * "How Strata runs a 125-billion-parameter model ...").
+ */
+moe_status moe_packed_size(int bits, int64_t rows, int64_t cols, size_t *code_bytes,
+                           size_t *scale_bytes);
+
+/*
+ * Pack n_mats matrices of [rows][cols] logical codes (one code per byte,
+ * device, 16-byte aligned) and their fp16 scales [rows][cols/32] (device) into
+ * the layout of moe_packed_size.  packed_scales may equal scales (in place:
+ * no copy).  A code >= 2^bits or a non-finite scale sets *dev_status to
+ * MOE_ERR_INVALID_ARG; that block is still written, with the codes' low bits
+ * and the scale as given.
+ */
+moe_status moe_pack_experts(int bits, int64_t n_mats, int64_t rows, int64_t cols,
+                            const uint8_t *codes, const uint16_t *scales, uint8_t *packed_codes,
+                            uint16_t *packed_scales, int32_t *dev_status, moe_stream_t stream);
+
+/* Inverse of moe_pack_experts for the code plane: packed -> one code per byte. */
+moe_status moe_unpack_experts(int bits, int64_t n_mats, int64_t rows, int64_t cols,
+                              const uint8_t *packed_codes, uint8_t *codes, moe_stream_t stream);
+
+/*
+ * The routed experts of one layer, resident in device memory (structure of
+ * arrays; expert e's data starts at e times the per-expert size):
+ *   gu_codes  [E][2I rows][row_bytes(H)]   rows 0..I-1 gate, I..2I-1 up
+ *   gu_scales [E][2I][H/32] fp16
+ *   d_codes   [E][H rows][row_bytes(I)]
+ *   d_scales  [E][H][I/32] fp16
+ * Every pointer must be 16-byte aligned.
+ */
+typedef struct moe_expert_arena {
+    int32_t bits; /* 2 or 3 */
+    int32_t H;
+    int32_t I;
+    int32_t E;
+    const uint8_t *gu_codes;
+    const uint16_t *gu_scales;
+    const uint8_t *d_codes;
+    const uint16_t *d_scales;
+} moe_expert_arena;
+
+/* ------------------------------------------------------------------------ */
+/* Router                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * logits[t][e] = bias[e] + sum_i W[e][i] * x[t][i] in fp32; then the top-k
+ * selection and weights of moe_topk_from_logits.
+ *   x_bf16      [T][H] bf16
+ *   w_router    [E][H] fp32 (16-byte aligned)
+ *   bias        [E] fp32, or NULL for none
+ *   logits_out  [T][E] fp32, or NULL (then the workspace holds them)
+ *   topk_ids    [T][k] int32,  topk_w [T][k] fp32
+ * Workspace: moe_router_workspace_size (0 bytes when logits_out is given).
+ * The pages: the router keeps 10 of 512 experts per token per layer
+ * ("Strata Open-Source Runtime ...", section "The Model Itself").
+ */
+moe_status moe_router_workspace_size(int T, int E, int logits_given, size_t *bytes);
+moe_status moe_router_topk(const uint16_t *x_bf16, int T, int H, const float *w_router,
+                           const float *bias, int E, int k, float *logits_out, int32_t *topk_ids,
+                           float *topk_w, void *ws, size_t ws_bytes, int32_t *dev_status,
+                           moe_stream_t stream);
+
+/*
+ * Top-k of fp32 logits [T][E]:
+ *   ids[t][j]: experts in the order (logit descending, id ascending), compared
+ *              as IEEE floats (-0 == +0, so the lower id wins);
+ *   w[t][j]  = softmax(logits[t])[ids[t][j]] / sum over the kept ones, which
+ *              equals the softmax of the k kept logits; when the largest logit
+ *              is infinite the weights are uniform over the kept experts that
+ *              hold it (the softmax's limit).
+ * A NaN logit sets *dev_status = MOE_ERR_NONFINITE; that token's ids are set
+ * to 0..k-1 and its weights to 1/k.
+ */
+moe_status moe_topk_from_logits(const float *logits, int T, int E, int k, int32_t *ids, float *w,
+                                int32_t *dev_status, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Token -> expert permutation                                              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Stable counting sort of the T*k (token, slot) pairs by expert id:
+ *   offsets [E+1]: offsets[e] = pairs with id < e, offsets[E] = T*k;
+ *   perm    [T*k]: perm[p] = t*k + j of the p-th pair in (expert, t*k+j) order;
+ *   inv_perm[T*k]: inv_perm[perm[p]] = p.
+ * Bit-exact and deterministic.  An id outside [0, E) sets *dev_status to
+ * MOE_ERR_BOUNDS; that pair is left out (offsets then count only valid
+ * pairs, its inv_perm entry is -1 and perm entries past offsets[E] are -1).
+ * The pages group the tokens of a verify window that share an expert
+ * ("Strata serves a 125B MoE ...", section "Six billion active parameters
+ * per token").
+ */
+moe_status moe_permute_workspace_size(int T, int k, int E, size_t *bytes);
+moe_status moe_permute(const int32_t *ids, int T, int k, int E, int32_t *offsets, int32_t *perm,
+                       int32_t *inv_perm, void *ws, size_t ws_bytes, int32_t *dev_status,
+                       moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Routed experts                                                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * out[t] = (accumulate ? out[t] : 0) + sum_{j<k} w[t][j] * FFN_{ids[t][j]}(x[t]),
+ * the slot sum taken in slot order.  ids/w/offsets/perm/inv_perm come from
+ * moe_router_topk (or the caller) and moe_permute.
+ *   out: [T][H], fp32 (MOE_F32) or bf16 (MOE_BF16, round-to-nearest-even of
+ *        the fp32 result).
+ * DECODE: fp32 dequantisation and accumulation; a token's result does not
+ *   depend on which other tokens share the call (bit-identical alone or in a
+ *   group).  PREFILL: grouped GEMM over the experts' token lists.
+ * Workspace: moe_expert_forward_workspace_size for the same arguments.
+ */
+moe_status moe_expert_forward_workspace_size(const moe_expert_arena *arena, int T, int k,
+                                             moe_path path, size_t *bytes);
+moe_status moe_expert_forward(const moe_expert_arena *arena, const uint16_t *x_bf16, int T,
+                              const int32_t *ids, const float *w, int k, const int32_t *offsets,
+                              const int32_t *perm, const int32_t *inv_perm, void *out,
+                              moe_dtype out_dtype, int accumulate, moe_path path, void *ws,
+                              size_t ws_bytes, int32_t *dev_status, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Shared expert                                                            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * out[t] = (accumulate ? out[t] : 0) + Wd (silu(Wg x[t]) * (Wu x[t])),
+ * bf16 weights wg [I][H], wu [I][H], wd [H][I] (I here is the shared
+ * expert's width), fp32 accumulation.  The pages: one always-on shared
+ * expert per layer ("Strata Open-Source Runtime ...", section "The Model
+ * Itself").  Workspace: moe_shared_expert_workspace_size.
+ */
+moe_status moe_shared_expert_workspace_size(int H, int I, int T, size_t *bytes);
+moe_status moe_shared_expert(const uint16_t *wg, const uint16_t *wu, const uint16_t *wd, int H,
+                             int I, const uint16_t *x_bf16, int T, void *out, moe_dtype out_dtype,
+                             int accumulate, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Residual stream helper                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* out_bf16[i] = round-to-nearest-even bf16 of in_f32[i], n elements. */
+moe_status moe_f32_to_bf16(const float *in_f32, uint16_t *out_bf16, int64_t n, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */
