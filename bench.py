@@ -1,0 +1,350 @@
+"""Benchmark: MoE-layer decode throughput on GB300.
+
+Workload (one step): one token through 48 stacked routed-expert layers with a
+residual stream, H=2048, 512 experts per layer, expert width I=768, top-10,
+2-bit block-quantised experts (36.2 GB resident), a bf16 shared expert
+(I=768) and an fp32 router biased for Zipf(1.1) expert popularity; seeded
+synthetic data.  Each step is one CUDA-graph replay of the library calls
+router_topk -> permute -> shared_expert -> expert_forward for all 48 layers.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  ``--impl reference`` times the oracle (plain scalar
+CPU code) on a bounded sample of the same workload instead.  Under torchrun
+every rank runs an independent replica (the layer does not shard across GPUs
+here); rank 0 prints the whole-job throughput.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+LAYERS, H, E, I, K_TOP, IS = 48, 2048, 512, 768, 10, 768
+EXPERT_BYTES = 1_474_560
+ROUTER_BYTES = E * H * 4
+SHARED_BYTES = 3 * H * IS * 2
+BYTES_PER_TOKEN = LAYERS * (K_TOP * EXPERT_BYTES + ROUTER_BYTES + SHARED_BYTES)  # 1,362,100,224
+KERNELS_PER_LAYER = 10  # f32_to_bf16, router gemv, topk, permute, shared (2 gemv + add), experts (2 gemv + combine)
+WORKLOAD = ("decode: 1 token x 48 layers, H=2048, E=512, I=768, top-10, 2-bit experts (32-weight blocks, fp16 "
+            "scales) + bf16 shared expert I=768, fp32 router with Zipf(1.1) bias, fp32 residual stream")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        sm = []
+        smax = 0.0
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[0]))
+                smax = max(smax, float(r[1]))
+                for n, v in zip(names, r[4:8]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if os.environ.get("BENCH_GLOO") is None else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- oracle leg
+
+def oracle_decode_sample(n_layers: int, seed: int = 0, step: int = 0):
+    """Time the oracle on one token through `n_layers` layers of the workload.
+
+    Returns (seconds of oracle compute, layers).  Weights of the experts the
+    token picks are regenerated on the host from the seeded generator; that
+    generation is not timed.
+    """
+    import oracle
+    from bit_expert_ffn_gb300 import synth
+
+    x = synth.activations(seed, 1, H, step=step)
+    xres = synth.bf16_bits_to_f32(x).astype(np.float64)
+    t_oracle = 0.0
+    for layer in range(n_layers):
+        xb = synth.f32_to_bf16_bits(xres.astype(np.float32))
+        wr = synth.router_weights(seed, layer, E, H)
+        b = synth.zipf_bias(seed, layer, E, 1.1)
+        shared = synth.shared_weights(seed, layer, H, IS)
+        t0 = time.perf_counter()
+        logits = oracle.router_logits(xb, wr, b).astype(np.float32)
+        ids, w = oracle.topk(logits, K_TOP)
+        t_oracle += time.perf_counter() - t0
+        parts = [[], [], [], [], [], []]
+        for e in ids[0]:
+            g, u, d = synth.expert_codes(seed, layer, int(e), 2, H, I)
+            gus, ds = synth.expert_scales(seed, layer, int(e), H, I)
+            for lst, a in zip(parts, (g, gus[0], u, gus[1], d, ds)):
+                lst.append(a)
+        arena = [np.stack(p) for p in parts]
+        t0 = time.perf_counter()
+        y = oracle.moe_layer(2, xb, np.arange(K_TOP, dtype=np.int32)[None, :], w, *arena, shared=shared)
+        t_oracle += time.perf_counter() - t0
+        xres = xres + y
+    return t_oracle, n_layers
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    t_total = 0.0
+    layers_total = 0
+    for s in range(args.warmup):
+        oracle_decode_sample(1, step=s)
+    for s in range(args.steps):
+        t, n = oracle_decode_sample(1, step=1000 + s)
+        t_total += t
+        layers_total += n
+    tok_s = layers_total / LAYERS / t_total
+    sample = f"{args.steps} steps, each one token through 1 of the 48 layers (oracle compute only), scaled by 1/48"
+    line = {"impl": "reference", "metric": "decode tokens/s (48-layer MoE stack, 1 token per step)", "value": tok_s,
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * t_total / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator)",
+            "config": {"workload": WORKLOAD, "tokens_per_step": 1, "layers": LAYERS},
+            "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our leg
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import bit_expert_ffn_gb300 as m
+    from bit_expert_ffn_gb300 import synth
+    from bit_expert_ffn_gb300.model import LayerShape, MoeLayer, StepBuffers, Workspace, residual_step
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    m.load()
+    shape = LayerShape(H=H, I=I, E=E, k=K_TOP, Is=IS, bits=2)
+    layers = []
+    for layer in range(LAYERS):
+        L = MoeLayer(shape, dev)
+        L.fill_device(seed=0, layer=layer, zipf_s=1.1)
+        layers.append(L)
+    torch.cuda.synchronize()
+    for L in layers:
+        assert m.moe_check_status(L.status) == 0, m.moe_last_error()
+
+    n_steps = args.warmup + args.steps
+    X = torch.from_numpy(synth.bf16_bits_to_f32(synth.activations(0, n_steps, H, step=rank)).reshape(n_steps, H)).to(dev)
+    x_res = torch.zeros(1, H, dtype=torch.float32, device=dev)
+    x_bf16 = torch.zeros(1, H, dtype=torch.int16, device=dev)
+    bufs = StepBuffers(1, E, K_TOP, dev)
+    ws = Workspace(dev)
+    ws.get(8 << 20)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        x_res.copy_(X[0:1])
+        residual_step(layers, x_res, x_bf16, 1, ws, bufs)  # eager warm-up (sizes the workspace)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            residual_step(layers, x_res, x_bf16, 1, ws, bufs)
+    torch.cuda.synchronize()
+
+    def step(i):
+        x_res.copy_(X[i:i + 1])
+        graph.replay()
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.warmup, n_steps):
+            step(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    ms = max_over_ranks(world, ms)
+    tok_s = world * args.steps / (ms / 1000.0)
+
+    # -- dominant call: the routed experts of one layer (decode), timed alone per layer
+    evs = []
+    with torch.cuda.stream(stream):
+        xb = torch.from_numpy(synth.activations(0, 1, H, step=10_000 + rank).view(np.int16)).to(dev)
+        for L in layers:
+            m.moe_router_topk(xb, 1, H, L.router_w, L.router_b, E, K_TOP, bufs.logits, bufs.ids, bufs.w,
+                              dev_status=L.status)
+            m.moe_permute(bufs.ids, 1, K_TOP, E, bufs.offsets, bufs.perm, bufs.inv)
+            nb = m.moe_expert_forward_workspace_size(L.arena, 1, K_TOP, m.MOE_PATH_DECODE)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            m.moe_expert_forward(L.arena, xb, 1, bufs.ids, bufs.w, K_TOP, bufs.offsets, bufs.perm, bufs.inv, x_res,
+                                 m.MOE_F32, True, m.MOE_PATH_DECODE, ws.get(nb), nb)
+            b.record(stream)
+            evs.append((a, b))
+    torch.cuda.synchronize()
+    call_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    peak, peak_kind = peaks()
+    achieved = K_TOP * EXPERT_BYTES / (call_ms / 1000.0) / 1e9
+
+    # -- end to end through host buffers: pinned x in, result out, every step
+    x_host = torch.empty(1, H, dtype=torch.float32, pin_memory=True)
+    y_host = torch.empty(1, H, dtype=torch.float32, pin_memory=True)
+    x_host.copy_(X[0:1].cpu())
+    n_e2e = min(args.steps, 50)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(n_e2e):
+            x_res.copy_(x_host, non_blocking=True)
+            graph.replay()
+            y_host.copy_(x_res, non_blocking=True)
+            stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_s = max_over_ranks(world, e2e_s)
+    e2e = {"value": world * n_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 4 * H,
+           "d2h_bytes_per_step": 4 * H}
+
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline:
+            t_or, n_l = oracle_decode_sample(2)
+            cpu = {"value": n_l / LAYERS / t_or, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                   "sample": "one token through 2 of the 48 layers, oracle compute only, scaled by 1/24 "
+                             "(fp64 scalar C, one host core)"}
+        line = {
+            "metric": "decode tokens/s (48-layer MoE stack, 1 token per step)",
+            "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (seeded generator, weights drawn on the GPU)",
+            "config": {"workload": WORKLOAD, "tokens_per_step": 1, "layers": LAYERS, "parallelism": "replicas",
+                       "l2": "no flush: each step reads 1.36 GB of weights, 10x the 129 MB L2"},
+            "hbm_roofline": {"bytes_per_token": BYTES_PER_TOKEN,
+                             "achieved_gbs": BYTES_PER_TOKEN * tok_s / world / 1e9,
+                             "frac_of_measured": BYTES_PER_TOKEN * tok_s / world / 1e9 / peak},
+            "roofline": {"kernel": "moe_expert_forward decode call (2 dequant GEMVs + combine), one layer",
+                         "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                         "bytes_per_launch": K_TOP * EXPERT_BYTES, "avg_call_ms": call_ms},
+            "clocks": clocks,
+            "e2e": e2e,
+            "gpu_launches": KERNELS_PER_LAYER * LAYERS * args.steps,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,184 @@
+"""Resident MoE layers on one GPU, driven through the C ABI.
+
+Weights are drawn with the seeded generator (host numpy for small shapes,
+the device generator of ``libmoe_synth.so`` for full-size arenas), packed by
+``moe_pack_experts`` and kept in HBM.  :meth:`MoeLayer.forward` runs one
+layer as the sequence of library calls
+
+    router_topk -> permute -> shared_expert -> expert_forward
+
+writing ``out = residual + S(x) + sum_j w_j FFN_j(x)`` in fp32.  Nothing here
+computes any part of the layer itself.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import (MOE_F32, MOE_PATH_AUTO, load, make_arena, moe_expert_forward, moe_expert_forward_workspace_size,
+               moe_f32_to_bf16, moe_pack_experts, moe_permute, moe_permute_workspace_size, moe_router_topk,
+               moe_shared_expert, moe_shared_expert_workspace_size, synth, synth_lib)
+
+
+def _u16(a: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+
+def device_codes(key: int, n: int, bits: int, out: torch.Tensor, start: int = 0):
+    r = synth_lib().moe_synth_codes(key, start, n, bits, out.data_ptr(),
+                                    ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    if r != 0:
+        raise RuntimeError(f"moe_synth_codes failed ({r})")
+
+
+def device_normal(key: int, n: int, sigma: float, kind: int, out: torch.Tensor, start: int = 0):
+    """kind 0: fp32 N(0, sigma); 1: bf16 N(0, sigma); 2: fp16 |N(0, sigma)|."""
+    r = synth_lib().moe_synth_normal(key, start, n, float(synth.IH_SCALE), float(np.float32(sigma)), kind,
+                                     out.data_ptr(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    if r != 0:
+        raise RuntimeError(f"moe_synth_normal failed ({r})")
+
+
+@dataclass
+class LayerShape:
+    H: int = 2048
+    I: int = 768
+    E: int = 512
+    k: int = 10
+    Is: int = 768
+    bits: int = 2
+
+
+class Workspace:
+    """One growing device byte buffer shared by the calls of a layer."""
+
+    def __init__(self, dev):
+        self.dev = dev
+        self.buf = torch.empty(0, dtype=torch.uint8, device=dev)
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf.numel() < nbytes:
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.dev)
+        return self.buf
+
+
+class MoeLayer:
+    """One routed-expert layer resident on the device."""
+
+    def __init__(self, shape: LayerShape, dev="cuda"):
+        load()
+        self.s = shape
+        self.dev = torch.device(dev)
+        H, I, E, bits = shape.H, shape.I, shape.E, shape.bits
+        cgu, sgu = _pk(bits, 2 * I, H)
+        cd, sd = _pk(bits, H, I)
+        self.gu_codes = torch.empty(E * cgu, dtype=torch.uint8, device=self.dev)
+        self.gu_scales = torch.empty(E * sgu // 2, dtype=torch.int16, device=self.dev)
+        self.d_codes = torch.empty(E * cd, dtype=torch.uint8, device=self.dev)
+        self.d_scales = torch.empty(E * sd // 2, dtype=torch.int16, device=self.dev)
+        self.router_w = torch.empty(E, H, dtype=torch.float32, device=self.dev)
+        self.router_b = torch.zeros(E, dtype=torch.float32, device=self.dev)
+        self.shared = None
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.dev)
+        self.arena = make_arena(bits, H, I, E, self.gu_codes, self.gu_scales, self.d_codes, self.d_scales)
+
+    # -- filling --------------------------------------------------------
+    def load_host(self, gate, gate_s, up, up_s, down, down_s, router_w, router_b=None, shared=None):
+        """Logical codes [E][I][H] / [E][H][I] and fp16-bit scales from the host; packed on the device."""
+        s = self.s
+        gu = np.concatenate([gate, up], axis=1)  # [E][2I][H]
+        gus = np.concatenate([gate_s, up_s], axis=1)
+        self._pack(gu, gus, self.gu_codes, self.gu_scales, 2 * s.I, s.H)
+        self._pack(down, down_s, self.d_codes, self.d_scales, s.H, s.I)
+        self.router_w.copy_(torch.from_numpy(np.ascontiguousarray(router_w, np.float32)))
+        if router_b is not None:
+            self.router_b.copy_(torch.from_numpy(np.ascontiguousarray(router_b, np.float32)))
+        if shared is not None:
+            self.shared = tuple(_u16(a, self.dev) for a in shared)
+
+    def _pack(self, codes, scales, pc, ps, rows, cols):
+        E = self.s.E
+        c = torch.from_numpy(np.ascontiguousarray(codes, np.uint8).reshape(-1)).to(self.dev)
+        sc = _u16(np.asarray(scales, np.uint16).reshape(-1), self.dev)
+        moe_pack_experts(self.s.bits, E, rows, cols, c, sc, pc, ps, self.status)
+
+    def fill_device(self, seed: int, layer: int, zipf_s: float = 0.0, chunk_experts: int = 64):
+        """Draw every tensor of the layer on the device with the seeded generator and pack it."""
+        s = self.s
+        H, I, E, bits = s.H, s.I, s.E, s.bits
+        for mat, (rows, cols, tag_c, tag_s, pc, ps) in enumerate((
+                (2 * I, H, synth.TAG_GU_CODES, synth.TAG_GU_SCALES, self.gu_codes, self.gu_scales),
+                (H, I, synth.TAG_D_CODES, synth.TAG_D_SCALES, self.d_codes, self.d_scales))):
+            cb, sb = _pk(bits, rows, cols)
+            per = rows * cols
+            nsc = rows * cols // 32
+            tmp_c = torch.empty(min(E, chunk_experts) * per, dtype=torch.uint8, device=self.dev)
+            tmp_s = torch.empty(min(E, chunk_experts) * nsc, dtype=torch.int16, device=self.dev)
+            for e0 in range(0, E, chunk_experts):
+                ne = min(chunk_experts, E - e0)
+                for j in range(ne):
+                    e = e0 + j
+                    device_codes(synth.stream_key(seed, tag_c, layer, e), per, bits, tmp_c[j * per:(j + 1) * per])
+                    device_normal(synth.stream_key(seed, tag_s, layer, e), nsc, 0.02, 2, tmp_s[j * nsc:(j + 1) * nsc])
+                moe_pack_experts(bits, ne, rows, cols, tmp_c, tmp_s, pc[e0 * cb:(e0 + ne) * cb],
+                                 ps[e0 * sb // 2:(e0 + ne) * sb // 2], self.status)
+            del tmp_c, tmp_s
+        device_normal(synth.stream_key(seed, synth.TAG_ROUTER, layer), E * H, 0.02, 0, self.router_w)
+        self.router_b.copy_(torch.from_numpy(synth.zipf_bias(seed, layer, E, zipf_s)))
+        sh = []
+        for tag, n in ((synth.TAG_SHARED_G, s.Is * H), (synth.TAG_SHARED_U, s.Is * H), (synth.TAG_SHARED_D, H * s.Is)):
+            t = torch.empty(n, dtype=torch.int16, device=self.dev)
+            device_normal(synth.stream_key(seed, tag, layer), n, 0.02, 1, t)
+            sh.append(t)
+        self.shared = tuple(sh)
+
+    # -- running --------------------------------------------------------
+    def forward(self, x_bf16, T, out_f32, ws: Workspace, bufs: "StepBuffers", accumulate=True, path=MOE_PATH_AUTO,
+                with_shared=True):
+        """out_f32 (+)= S(x) + routed(x), through the library calls only."""
+        s = self.s
+        moe_router_topk(x_bf16, T, s.H, self.router_w, self.router_b, s.E, s.k, bufs.logits, bufs.ids, bufs.w,
+                        dev_status=self.status)
+        pws = moe_permute_workspace_size(T, s.k, s.E)
+        ews = moe_expert_forward_workspace_size(self.arena, T, s.k, path)
+        sws = moe_shared_expert_workspace_size(s.H, s.Is, T) if with_shared and self.shared is not None else 0
+        need = max(pws, ews, sws)
+        buf = ws.get(need)
+        moe_permute(bufs.ids, T, s.k, s.E, bufs.offsets, bufs.perm, bufs.inv, buf if pws else None, pws,
+                    dev_status=self.status)
+        acc = accumulate
+        if with_shared and self.shared is not None:
+            moe_shared_expert(*self.shared, s.H, s.Is, x_bf16, T, out_f32, MOE_F32, acc, buf, sws)
+            acc = True
+        moe_expert_forward(self.arena, x_bf16, T, bufs.ids, bufs.w, s.k, bufs.offsets, bufs.perm, bufs.inv, out_f32,
+                           MOE_F32, acc, path, buf, ews, dev_status=self.status)
+
+
+class StepBuffers:
+    """Routing buffers for up to T tokens."""
+
+    def __init__(self, T, E, k, dev="cuda"):
+        d = torch.device(dev)
+        self.logits = torch.empty(max(T, 1), E, dtype=torch.float32, device=d)
+        self.ids = torch.empty(max(T, 1), k, dtype=torch.int32, device=d)
+        self.w = torch.empty(max(T, 1), k, dtype=torch.float32, device=d)
+        self.offsets = torch.empty(E + 1, dtype=torch.int32, device=d)
+        self.perm = torch.empty(max(T * k, 1), dtype=torch.int32, device=d)
+        self.inv = torch.empty(max(T * k, 1), dtype=torch.int32, device=d)
+
+
+def residual_step(layers, x_res, x_bf16, T, ws, bufs, path=MOE_PATH_AUTO):
+    """x_res <- x_res + MoE_l(bf16(x_res)) for every layer, in place (fp32 residual stream)."""
+    n = x_res.numel()
+    for L in layers:
+        moe_f32_to_bf16(x_res, x_bf16, n)
+        L.forward(x_bf16, T, x_res, ws, bufs, accumulate=True, path=path)
+
+
+def _pk(bits, rows, cols):
+    from . import moe_packed_size
+
+    return moe_packed_size(bits, rows, cols)

@@ -1,0 +1,323 @@
+"""GPU parity: every C ABI call against the oracle on the same seeded inputs.
+
+Bars: integer outputs (packed bytes, ids, permutation) bit-exact; routing
+weights within 1e-6 relative; layer outputs within relative L2 1e-3 (the
+stated bar) and, for the fp32 paths, within 2e-5 (what exact dequantisation
+with fp32 accumulation gives, so that a small systematic slip still shows).
+Sizes span several tiles and ragged tails; full-size shapes are checked on
+sampled tokens and experts.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bit_expert_ffn_gb300 as m
+import oracle
+from bit_expert_ffn_gb300 import synth
+from bit_expert_ffn_gb300.model import LayerShape, MoeLayer, StepBuffers, Workspace, device_codes, device_normal
+from helpers import bf16_rne, host_layer, rel_l2, u16
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL = 1e-3
+TIGHT = 2e-5
+
+
+def dev_u16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.uint16).view(np.int16)).to(DEV)
+
+
+def status():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+# ---------------------------------------------------------------- packing
+
+@pytest.mark.parametrize("bits,rows,cols", [(2, 7, 2048), (2, 33, 96), (3, 5, 768), (3, 3, 32)])
+def test_pack_bytes_equal_oracle(moe, bits, rows, cols):
+    codes = synth.codes(synth.stream_key(11, 1), 2 * rows * cols, bits).reshape(2, rows, cols)
+    scales = synth.f32_to_fp16_bits(np.abs(synth.normal_sigma(synth.stream_key(11, 2), 2 * rows * cols // 32, 0.02)))
+    cb, sb = m.moe_packed_size(bits, rows, cols)
+    pc = torch.zeros(2 * cb, dtype=torch.uint8, device=DEV)
+    ps = torch.zeros(2 * sb // 2, dtype=torch.int16, device=DEV)
+    st = status()
+    m.moe_pack_experts(bits, 2, rows, cols, torch.from_numpy(codes.reshape(-1)).to(DEV), dev_u16(scales), pc, ps, st)
+    assert m.moe_check_status(st) == 0
+    want = oracle.pack(bits, codes.reshape(2 * rows, cols)).reshape(-1)
+    assert np.array_equal(pc.cpu().numpy(), want)
+    assert np.array_equal(u16(ps), scales)
+    back = torch.zeros(2 * rows * cols, dtype=torch.uint8, device=DEV)
+    m.moe_unpack_experts(bits, 2, rows, cols, pc, back)
+    assert np.array_equal(back.cpu().numpy(), codes.reshape(-1))
+
+
+def test_pack_flags_bad_codes_and_scales(moe):
+    codes = np.zeros((1, 32), np.uint8)
+    codes[0, 5] = 4
+    cb, sb = m.moe_packed_size(2, 1, 32)
+    pc = torch.zeros(cb, dtype=torch.uint8, device=DEV)
+    ps = torch.zeros(1, dtype=torch.int16, device=DEV)
+    st = status()
+    m.moe_pack_experts(2, 1, 1, 32, torch.from_numpy(codes.reshape(-1)).to(DEV), dev_u16(np.array([0x3C00])), pc, ps, st)
+    assert m.moe_check_status(st) == m.MOE_ERR_INVALID_ARG
+    codes[0, 5] = 3
+    m.moe_pack_experts(2, 1, 1, 32, torch.from_numpy(codes.reshape(-1)).to(DEV), dev_u16(np.array([0x7C00])), pc, ps, st)
+    assert m.moe_check_status(st) == m.MOE_ERR_INVALID_ARG
+    m.moe_pack_experts(2, 1, 1, 32, torch.from_numpy(codes.reshape(-1)).to(DEV), dev_u16(np.array([0x3C00])), pc, ps, st)
+    assert m.moe_check_status(st) == 0
+
+
+def test_device_generator_matches_host(moe):
+    key = synth.stream_key(5, synth.TAG_GU_CODES, 3, 17)
+    for bits in (2, 3):
+        out = torch.empty(100_003, dtype=torch.uint8, device=DEV)
+        device_codes(key, out.numel(), bits, out, start=12345)
+        assert np.array_equal(out.cpu().numpy(), synth.codes(key, out.numel(), bits, start=12345))
+    f = torch.empty(50_001, dtype=torch.float32, device=DEV)
+    device_normal(key, f.numel(), 0.02, 0, f, start=7)
+    assert np.array_equal(f.cpu().numpy(), synth.normal_sigma(key, f.numel(), 0.02, start=7))
+    b = torch.empty(50_001, dtype=torch.int16, device=DEV)
+    device_normal(key, b.numel(), 0.02, 1, b)
+    assert np.array_equal(u16(b), synth.f32_to_bf16_bits(synth.normal_sigma(key, b.numel(), 0.02)))
+    device_normal(key, b.numel(), 0.02, 2, b)
+    assert np.array_equal(u16(b), synth.f32_to_fp16_bits(np.abs(synth.normal_sigma(key, b.numel(), 0.02))))
+
+
+# ---------------------------------------------------------------- router
+
+@pytest.mark.parametrize("T,H,E,k,zipf", [(8, 256, 16, 2, 0.0), (1, 2048, 512, 10, 1.1), (4, 2048, 512, 10, 1.1),
+                                          (3, 2048, 512, 10, 0.0), (77, 2048, 512, 10, 1.1), (130, 256, 1024, 16, 0.0)])
+def test_router_topk(moe, T, H, E, k, zipf):
+    x = synth.activations(21, T, H)
+    wr = synth.router_weights(21, 0, E, H)
+    b = synth.zipf_bias(21, 0, E, zipf)
+    logits = torch.empty(T, E, dtype=torch.float32, device=DEV)
+    ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, dtype=torch.float32, device=DEV)
+    st = status()
+    m.moe_router_topk(dev_u16(x), T, H, torch.from_numpy(wr).to(DEV), torch.from_numpy(b).to(DEV), E, k, logits, ids,
+                      w, dev_status=st)
+    assert m.moe_check_status(st) == 0
+    gl = logits.cpu().numpy()
+    ol = oracle.router_logits(x, wr, b)
+    scale = np.abs(ol).max()
+    assert np.abs(gl - ol).max() <= 1e-5 * scale
+    # (i) ids bit-exact against the oracle's selection on the GPU's own logits
+    oids, ow = oracle.topk(gl, k)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=1e-6, atol=1e-7)
+    # (iii) ids from the oracle's own logits agree except at near-ties
+    oids2, _ = oracle.topk(ol.astype(np.float32), k)
+    srt = -np.sort(-ol, axis=1)
+    margin = srt[:, k - 1] - (srt[:, k] if k < E else -np.inf)
+    near = margin < 1e-5 * scale
+    assert np.array_equal(oids2[~near], oids[~near])
+
+
+@pytest.mark.parametrize("E,k", [(4, 2), (16, 5), (512, 10), (1024, 16), (1, 1), (33, 33 // 3)])
+def test_topk_ties_and_specials(moe, E, k):
+    rng = np.random.default_rng(E * 100 + k)
+    T = 64
+    l = rng.integers(-3, 4, (T, E)).astype(np.float32)  # many exact ties
+    l[0, :] = 0.0
+    l[1, ::2] = -0.0
+    if E > 2:
+        l[2, 1] = np.inf
+        l[3, :] = -np.inf
+        l[4, 0] = np.inf
+        l[4, E - 1] = np.inf
+    gl = torch.from_numpy(l).to(DEV)
+    ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, dtype=torch.float32, device=DEV)
+    st = status()
+    m.moe_topk_from_logits(gl, T, E, k, ids, w, st)
+    assert m.moe_check_status(st) == 0
+    oids, ow = oracle.topk(l, k)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=1e-6, atol=1e-7)
+
+
+def test_topk_nan_reports_status(moe):
+    l = np.zeros((3, 16), np.float32)
+    l[1, 7] = np.nan
+    ids = torch.empty(3, 4, dtype=torch.int32, device=DEV)
+    w = torch.empty(3, 4, dtype=torch.float32, device=DEV)
+    st = status()
+    m.moe_topk_from_logits(torch.from_numpy(l).to(DEV), 3, 16, 4, ids, w, st)
+    assert m.moe_check_status(st) == m.MOE_ERR_NONFINITE
+    assert list(ids.cpu().numpy()[1]) == [0, 1, 2, 3]
+
+
+# ---------------------------------------------------------------- permute
+
+@pytest.mark.parametrize("T,k,E", [(1, 10, 512), (4, 10, 512), (8, 2, 16), (409, 10, 512), (410, 10, 512),
+                                   (32768, 10, 512), (5000, 16, 1024), (3, 1, 1)])
+def test_permute_equals_oracle(moe, T, k, E):
+    rng = np.random.default_rng(T + 7 * k)
+    if E >= k:
+        ids = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    else:
+        ids = rng.integers(0, E, (T, k)).astype(np.int32)
+    ws_b = m.moe_permute_workspace_size(T, k, E)
+    ws = torch.empty(max(ws_b, 1), dtype=torch.uint8, device=DEV)
+    off = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    inv = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    st = status()
+    m.moe_permute(torch.from_numpy(ids).to(DEV), T, k, E, off, perm, inv, ws, ws_b, st)
+    assert m.moe_check_status(st) == 0
+    oo, op, oi = oracle.permute(ids, E)
+    assert np.array_equal(off.cpu().numpy(), oo)
+    assert np.array_equal(perm.cpu().numpy(), op)
+    assert np.array_equal(inv.cpu().numpy(), oi)
+
+
+def test_permute_bad_id_reports_bounds(moe):
+    ids = np.array([[0, 3], [9, 1], [2, -1]], np.int32)
+    off = torch.empty(6, dtype=torch.int32, device=DEV)
+    perm = torch.empty(6, dtype=torch.int32, device=DEV)
+    inv = torch.empty(6, dtype=torch.int32, device=DEV)
+    st = status()
+    m.moe_permute(torch.from_numpy(ids).to(DEV), 3, 2, 5, off, perm, inv, None, 0, st)
+    assert m.moe_check_status(st) == m.MOE_ERR_BOUNDS
+    good = ids.reshape(-1)
+    valid = (good >= 0) & (good < 5)
+    assert off.cpu().numpy()[-1] == valid.sum()
+    invh = inv.cpu().numpy()
+    assert np.all(invh[~valid] == -1)
+    ph = perm.cpu().numpy()
+    assert np.all(ph[valid.sum():] == -1)
+    assert sorted(ph[:valid.sum()]) == sorted(np.nonzero(valid)[0])
+
+
+# ---------------------------------------------------------------- layer
+
+def run_layer(L, x, T, path, with_shared=True, out_dtype=m.MOE_F32):
+    bufs = StepBuffers(T, L.s.E, L.s.k)
+    ws = Workspace(DEV)
+    out = torch.zeros(T, L.s.H, dtype=torch.float32, device=DEV)
+    L.forward(dev_u16(x), T, out, ws, bufs, accumulate=False, path=path, with_shared=with_shared)
+    assert m.moe_check_status(L.status) == 0
+    return out.cpu().numpy(), bufs
+
+
+def make_layer(bits=2, H=256, I=128, E=16, k=2, Is=128, zipf=0.0, seed=0):
+    arena, wr, b, shared = host_layer(seed=seed, bits=bits, H=H, I=I, E=E, Is=Is, zipf=zipf)
+    L = MoeLayer(LayerShape(H=H, I=I, E=E, k=k, Is=Is, bits=bits), DEV)
+    L.load_host(arena[0], arena[1], arena[2], arena[3], arena[4], arena[5], wr, b, shared)
+    return L, arena, shared
+
+
+@pytest.mark.parametrize("path", [m.MOE_PATH_DECODE, m.MOE_PATH_PREFILL])
+@pytest.mark.parametrize("bits", [2, 3])
+def test_tiny_layer_matches_oracle(moe, path, bits):
+    """H=256, E=16, I=128, top-2, T=8, bf16 shared expert I=128: the tiny configuration."""
+    L, arena, shared = make_layer(bits=bits)
+    x = synth.activations(0, 8, 256)
+    got, bufs = run_layer(L, x, 8, path)
+    ids = bufs.ids.cpu().numpy()
+    w = bufs.w.cpu().numpy().astype(np.float64)
+    want = oracle.moe_layer(bits, x, ids, w, *arena, shared=shared)
+    err = rel_l2(got, want)
+    assert err <= TOL
+    assert err <= TIGHT, err
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 5, 8])
+def test_decode_token_counts(moe, T):
+    L, arena, shared = make_layer(k=4, E=16, zipf=1.1)
+    x = synth.verify_window(3, T, 256)
+    got, bufs = run_layer(L, x, T, m.MOE_PATH_DECODE)
+    want = oracle.moe_layer(2, x, bufs.ids.cpu().numpy(), bufs.w.cpu().numpy().astype(np.float64), *arena,
+                            shared=shared)
+    assert rel_l2(got, want) <= TIGHT
+
+
+@pytest.mark.parametrize("T,E,k", [(100, 16, 2), (257, 32, 4), (1000, 64, 8)])
+def test_prefill_ragged(moe, T, E, k):
+    L, arena, shared = make_layer(E=E, k=k, zipf=1.4, seed=T)
+    x = synth.activations(T, T, 256)
+    got, bufs = run_layer(L, x, T, m.MOE_PATH_PREFILL)
+    counts = np.diff(bufs.offsets.cpu().numpy())
+    assert counts.max() > 64 and (counts % 64 != 0).any()  # several tiles and ragged tails
+    want = oracle.moe_layer(2, x, bufs.ids.cpu().numpy(), bufs.w.cpu().numpy().astype(np.float64), *arena,
+                            shared=shared)
+    assert rel_l2(got, want) <= TIGHT
+
+
+def test_decode_batch_invariance(moe):
+    """A token's decode output is bit-identical alone and inside a 4-token window."""
+    L, arena, shared = make_layer(k=4, E=16)
+    x = synth.verify_window(9, 4, 256)
+    group, _ = run_layer(L, x, 4, m.MOE_PATH_DECODE)
+    for t in range(4):
+        alone, _ = run_layer(L, x[t:t + 1], 1, m.MOE_PATH_DECODE)
+        assert np.array_equal(alone[0], group[t])
+
+
+def test_bf16_output_is_rne_of_f32(moe):
+    L, arena, shared = make_layer()
+    x = synth.activations(4, 8, 256)
+    f32, bufs = run_layer(L, x, 8, m.MOE_PATH_DECODE, with_shared=False)
+    out = torch.zeros(8, 256, dtype=torch.int16, device=DEV)
+    ws = Workspace(DEV)
+    nb = m.moe_expert_forward_workspace_size(L.arena, 8, 2, m.MOE_PATH_DECODE)
+    m.moe_expert_forward(L.arena, dev_u16(x), 8, bufs.ids, bufs.w, 2, bufs.offsets, bufs.perm, bufs.inv, out,
+                         m.MOE_BF16, False, m.MOE_PATH_DECODE, ws.get(nb), nb)
+    assert np.array_equal(u16(out), bf16_rne(f32))
+
+
+def test_zero_tokens_is_a_noop(moe):
+    L, arena, shared = make_layer()
+    out = torch.full((1, 256), 7.0, device=DEV)
+    m.moe_expert_forward(L.arena, dev_u16(np.zeros((1, 256), np.uint16)), 0, 16, 16, 2, 16, 16, 16, out)
+    m.moe_shared_expert(*L.shared, 256, 128, dev_u16(np.zeros((1, 256), np.uint16)), 0, out)
+    assert torch.all(out == 7.0)
+
+
+@pytest.mark.parametrize("T", [1, 4, 8, 9, 100])
+def test_shared_expert(moe, T):
+    H, Is = 512, 256
+    wg, wu, wd = synth.shared_weights(8, 0, H, Is)
+    x = synth.activations(8, T, H)
+    out = torch.zeros(T, H, dtype=torch.float32, device=DEV)
+    nb = m.moe_shared_expert_workspace_size(H, Is, T)
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    m.moe_shared_expert(dev_u16(wg), dev_u16(wu), dev_u16(wd), H, Is, dev_u16(x), T, out, m.MOE_F32, False, ws, nb)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    want = np.stack([oracle.shared_expert(wg, wu, wd, xf[t]) for t in range(T)])
+    assert rel_l2(out.cpu().numpy(), want) <= TIGHT
+
+
+# ---------------------------------------------------------------- full size, sampled
+
+def sampled_reference(seed, layer, bits, H, I, x, ids, w, shared, tokens):
+    """Oracle layer for the given tokens, regenerating only the experts they picked."""
+    used = sorted(set(int(e) for t in tokens for e in ids[t]))
+    remap = {e: i for i, e in enumerate(used)}
+    parts = [[], [], [], [], [], []]
+    for e in used:
+        g, u, d = synth.expert_codes(seed, layer, e, bits, H, I)
+        gus, ds = synth.expert_scales(seed, layer, e, H, I)
+        for lst, a in zip(parts, (g, gus[0], u, gus[1], d, ds)):
+            lst.append(a)
+    arena = [np.stack(p) for p in parts]
+    cids = np.array([[remap[int(e)] for e in ids[t]] for t in tokens], np.int32)
+    return oracle.moe_layer(bits, x[tokens], cids, w[tokens].astype(np.float64), *arena, shared=shared)
+
+
+@pytest.mark.parametrize("T,path", [(1, m.MOE_PATH_DECODE), (4, m.MOE_PATH_DECODE), (2048, m.MOE_PATH_PREFILL)])
+def test_full_size_layer_sampled(moe, T, path):
+    """H=2048, E=512, I=768, top-10, 2-bit, Zipf(1.1) routing, bf16 shared expert, weights drawn on the GPU."""
+    seed, layer = 1, 2
+    s = LayerShape()
+    L = MoeLayer(s, DEV)
+    L.fill_device(seed, layer, zipf_s=1.1)
+    x = synth.verify_window(seed, T, s.H) if T <= 4 else synth.activations(seed, T, s.H)
+    got, bufs = run_layer(L, x, T, path)
+    ids = bufs.ids.cpu().numpy()
+    w = bufs.w.cpu().numpy()
+    shared = synth.shared_weights(seed, layer, s.H, s.Is)
+    tokens = list(range(T)) if T <= 4 else sorted(np.random.default_rng(0).choice(T, 6, replace=False))
+    want = sampled_reference(seed, layer, 2, s.H, s.I, x, ids, w, shared, tokens)
+    assert rel_l2(got[tokens], want) <= TIGHT
