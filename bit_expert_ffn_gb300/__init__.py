@@ -65,6 +65,7 @@ _SIGS = {
     "moe_topk_from_logits": [_P, _I32, _I32, _I32, _P, _P, _P, _P],
     "moe_permute_workspace_size": [_I32, _I32, _I32, _PSZ],
     "moe_permute": [_P, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P, _P],
+    "moe_permute_noalloc": [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P],
     "moe_expert_forward_workspace_size": [ctypes.POINTER(moe_expert_arena), _I32, _I32, _I32, _PSZ],
     "moe_expert_forward": [ctypes.POINTER(moe_expert_arena), _P, _I32, _P, _P, _I32, _P, _P, _P, _P, _I32, _I32,
                            _I32, _P, _SZ, _P, _P],
@@ -206,6 +207,12 @@ def moe_permute_workspace_size(T, k, E):
 def moe_permute(ids, T, k, E, offsets, perm, inv_perm, ws=None, ws_bytes=0, dev_status=None, stream=None):
     _check(lib().moe_permute(_ptr(ids), T, k, E, _ptr(offsets), _ptr(perm), _ptr(inv_perm), _ptr(ws), ws_bytes,
                              _ptr(dev_status), _stream(stream)), "moe_permute")
+
+
+def moe_permute_noalloc(ids, T, k, E, offsets, perm, inv_perm, dev_status=None, stream=None):
+    """moe_permute without a workspace, for callers that cannot allocate (see the header)."""
+    _check(lib().moe_permute_noalloc(_ptr(ids), T, k, E, _ptr(offsets), _ptr(perm), _ptr(inv_perm), _ptr(dev_status),
+                                     _stream(stream)), "moe_permute_noalloc")
 
 
 # ----------------------------------------------------------------- experts

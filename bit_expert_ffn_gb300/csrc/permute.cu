@@ -209,3 +209,73 @@ extern "C" moe_status moe_permute(const int32_t *ids, int T, int k, int E, int32
     permute_place_kernel<<<(unsigned)c, 32, 0, s>>>(ids, n, E, base, perm, inv_perm);
     return check_launch("permute_place");
 }
+
+// --------------------------------------------------------------------------
+// moe_permute_noalloc: the three-pass sort above with its scratch in a fixed
+// device array of this library instead of a caller workspace.
+// --------------------------------------------------------------------------
+#include <mutex>
+
+namespace moe {
+
+// Per-chunk counts and per-chunk bases, kNoAllocScratchInts int32 each.
+constexpr int64_t kNoAllocScratchInts = 32768;  // chunks * E <= 32768 -> 2 x 128 KiB
+static __device__ __align__(256) int32_t g_permute_scratch[2 * kNoAllocScratchInts];
+
+// Device address of g_permute_scratch on the current device, looked up once
+// per device (with that device current) and cached.
+static moe_status permute_scratch_address(int32_t **out)
+{
+    static std::mutex mu;
+    static int32_t *addr[64] = {nullptr};
+    int dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return fail(MOE_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);
+        if (e != cudaSuccess)
+            return fail(MOE_ERR_CUDA, "cudaGetSymbolAddress(g_permute_scratch) on device %d: %s", dev,
+                        cudaGetErrorString(e));
+        addr[dev] = static_cast<int32_t *>(p);
+    }
+    *out = addr[dev];
+    return MOE_OK;
+}
+
+}  // namespace moe
+
+extern "C" moe_status moe_permute_noalloc(const int32_t *ids, int T, int k, int E, int32_t *offsets, int32_t *perm,
+                                          int32_t *inv_perm, int32_t *dev_status, moe_stream_t stream)
+{
+    MOE_REQUIRE(T >= 0 && k >= 1 && k <= 16, "T >= 0 and 1 <= k <= 16 (got T=%d k=%d)", T, k);
+    MOE_REQUIRE(E >= 1 && E <= 1024, "E must be in [1, 1024] (got %d)", E);
+    MOE_REQUIRE(offsets, "offsets is NULL");
+    int64_t n = (int64_t)T * k;
+    int64_t c = n_chunks_for(n);
+    if (c * E > kNoAllocScratchInts)
+        return fail(MOE_ERR_INVALID_ARG,
+                    "moe_permute_noalloc holds at most %lld (chunks x experts) counters in its fixed scratch: "
+                    "T*k=%lld pairs form %lld chunks of %d, times E=%d is %lld; use moe_permute with a workspace",
+                    (long long)kNoAllocScratchInts, (long long)n, (long long)c, kPermChunk, E, (long long)(c * E));
+    cudaStream_t s = to_cuda(stream);
+    if (n == 0) {
+        MOE_CUDA_TRY(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s));
+        return MOE_OK;
+    }
+    MOE_REQUIRE(ids && perm && inv_perm, "NULL pointer");
+    int32_t *scratch = nullptr;
+    moe_status st = permute_scratch_address(&scratch);
+    if (st != MOE_OK) return st;
+    int32_t *counts = scratch;                      // every cell read below is written
+    int32_t *base = scratch + kNoAllocScratchInts;  // earlier in the same call
+    permute_count_kernel<<<(unsigned)c, 256, 0, s>>>(ids, n, E, counts, dev_status);
+    st = check_launch("permute_count (no-alloc)");
+    if (st != MOE_OK) return st;
+    permute_scan_kernel<<<1, 1024, 0, s>>>(counts, (int)c, E, n, base, offsets, perm);
+    st = check_launch("permute_scan (no-alloc)");
+    if (st != MOE_OK) return st;
+    permute_place_kernel<<<(unsigned)c, 32, 0, s>>>(ids, n, E, base, perm, inv_perm);
+    return check_launch("permute_place (no-alloc)");
+}

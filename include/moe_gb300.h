@@ -212,6 +212,33 @@ moe_status moe_permute(const int32_t *ids, int T, int k, int E, int32_t *offsets
                        int32_t *inv_perm, void *ws, size_t ws_bytes, int32_t *dev_status,
                        moe_stream_t stream);
 
+/*
+ * moe_permute_noalloc -- the same stable counting sort as moe_permute, for
+ * callers that cannot allocate device memory.  (This entry point has no
+ * counterpart in the pages: it is a convenience of this library.)  Some
+ * callers cannot call cudaMalloc or hand the library a workspace: a plugin
+ * whose host framework owns every device allocation and offers no scratch
+ * buffer, or a serving loop that must not allocate after start-up because an
+ * allocation may synchronise the device or fail under memory pressure.  This
+ * call allocates nothing and takes no workspace: its scratch is a fixed array
+ * of 2 x 32,768 int32 (256 KiB) inside the library, which every GPU that
+ * loads the library holds until the process exits.
+ *   - Limit: ceil(T*k / 2048) * E <= 32,768 (e.g. T*k <= 65,536 pairs for
+ *     E = 1024, <= 131,072 for E = 512); larger requests return
+ *     MOE_ERR_INVALID_ARG with the sizes in the message.
+ *   - Outputs, errors and ordering are those of moe_permute.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array, and each call overwrites
+ *     the cells it reads (nothing needs clearing between calls); calls whose
+ *     kernels overlap on the GPU (other streams, other host threads) race on
+ *     it, so serialise them.
+ */
+moe_status moe_permute_noalloc(const int32_t *ids, int T, int k, int E, int32_t *offsets,
+                               int32_t *perm, int32_t *inv_perm, int32_t *dev_status,
+                               moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Routed experts                                                           */
 /* ------------------------------------------------------------------------ */
