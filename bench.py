@@ -4,8 +4,10 @@ Workload (one step): one token through 48 stacked routed-expert layers with a
 residual stream, H=2048, 512 experts per layer, expert width I=768, top-10,
 2-bit block-quantised experts (36.2 GB resident), a bf16 shared expert
 (I=768) and an fp32 router biased for Zipf(1.1) expert popularity; seeded
-synthetic data.  Each step is one CUDA-graph replay of the library calls
-router_topk -> permute -> shared_expert -> expert_forward for all 48 layers.
+synthetic data.  Each step is one launch of moe_decode_forward (all 48
+layers in one persistent kernel); ``--path modular`` times instead a CUDA
+graph of the per-layer calls router_topk -> permute -> shared_expert ->
+expert_forward.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -194,6 +196,8 @@ def run_reference(args, world, rank):
 # ---------------------------------------------------------------- our leg
 
 def run_ours(args, world, rank, local):
+    import ctypes
+
     import torch
 
     import bit_expert_ffn_gb300 as m
@@ -202,7 +206,7 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    m.load()
+    lib = m.load()
     shape = LayerShape(H=H, I=I, E=E, k=K_TOP, Is=IS, bits=2)
     layers = []
     for layer in range(LAYERS):
@@ -216,29 +220,47 @@ def run_ours(args, world, rank, local):
     n_steps = args.warmup + args.steps
     X = torch.from_numpy(synth.bf16_bits_to_f32(synth.activations(0, n_steps, H, step=rank)).reshape(n_steps, H)).to(dev)
     x_res = torch.zeros(1, H, dtype=torch.float32, device=dev)
-    x_bf16 = torch.zeros(1, H, dtype=torch.int16, device=dev)
-    bufs = StepBuffers(1, E, K_TOP, dev)
-    ws = Workspace(dev)
-    ws.get(8 << 20)
-
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    with torch.cuda.stream(stream):
-        x_res.copy_(X[0:1])
-        residual_step(layers, x_res, x_bf16, 1, ws, bufs)  # eager warm-up (sizes the workspace)
-        stream.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            residual_step(layers, x_res, x_bf16, 1, ws, bufs)
-    torch.cuda.synchronize()
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+
+    if args.path == "fused":
+        descs = (m.moe_layer_weights * LAYERS)(*[L.weights() for L in layers])
+        nb = m.moe_decode_workspace_size(1, H, I, E, K_TOP, IS)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        kernels_per_step = 1
+
+        def call():
+            st = lib.moe_decode_forward(descs, LAYERS, x_res.data_ptr(), 1, K_TOP, None, None, ws.data_ptr(), nb,
+                                        status.data_ptr(), sptr)
+            if st:
+                raise m.MoeError(st, m.moe_last_error())
+    else:
+        x_bf16 = torch.zeros(1, H, dtype=torch.int16, device=dev)
+        bufs = StepBuffers(1, E, K_TOP, dev)
+        wsp = Workspace(dev)
+        wsp.get(8 << 20)
+        kernels_per_step = KERNELS_PER_LAYER * LAYERS
+        with torch.cuda.stream(stream):
+            residual_step(layers, x_res, x_bf16, 1, wsp, bufs)  # eager warm-up (sizes the workspace)
+            stream.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                residual_step(layers, x_res, x_bf16, 1, wsp, bufs)
+        torch.cuda.synchronize()
+
+        def call():
+            graph.replay()
 
     def step(i):
         x_res.copy_(X[i:i + 1])
-        graph.replay()
+        call()
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             step(i)
     torch.cuda.synchronize()
+    assert m.moe_check_status(status) == 0, m.moe_last_error()
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -254,29 +276,25 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
+    assert m.moe_check_status(status) == 0, m.moe_last_error()
     ms = e0.elapsed_time(e1)
     ms = max_over_ranks(world, ms)
     tok_s = world * args.steps / (ms / 1000.0)
 
-    # -- dominant call: the routed experts of one layer (decode), timed alone per layer
+    # -- the dominant kernel, timed per launch with events on its own stream
     evs = []
     with torch.cuda.stream(stream):
-        xb = torch.from_numpy(synth.activations(0, 1, H, step=10_000 + rank).view(np.int16)).to(dev)
-        for L in layers:
-            m.moe_router_topk(xb, 1, H, L.router_w, L.router_b, E, K_TOP, bufs.logits, bufs.ids, bufs.w,
-                              dev_status=L.status)
-            m.moe_permute(bufs.ids, 1, K_TOP, E, bufs.offsets, bufs.perm, bufs.inv)
-            nb = m.moe_expert_forward_workspace_size(L.arena, 1, K_TOP, m.MOE_PATH_DECODE)
+        for i in range(min(args.steps, 20)):
+            x_res.copy_(X[i:i + 1])
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            m.moe_expert_forward(L.arena, xb, 1, bufs.ids, bufs.w, K_TOP, bufs.offsets, bufs.perm, bufs.inv, x_res,
-                                 m.MOE_F32, True, m.MOE_PATH_DECODE, ws.get(nb), nb)
+            call()
             b.record(stream)
             evs.append((a, b))
     torch.cuda.synchronize()
     call_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
     peak, peak_kind = peaks()
-    achieved = K_TOP * EXPERT_BYTES / (call_ms / 1000.0) / 1e9
+    achieved = BYTES_PER_TOKEN / (call_ms / 1000.0) / 1e9
 
     # -- end to end through host buffers: pinned x in, result out, every step
     x_host = torch.empty(1, H, dtype=torch.float32, pin_memory=True)
@@ -288,7 +306,7 @@ def run_ours(args, world, rank, local):
     with torch.cuda.stream(stream):
         for _ in range(n_e2e):
             x_res.copy_(x_host, non_blocking=True)
-            graph.replay()
+            call()
             y_host.copy_(x_res, non_blocking=True)
             stream.synchronize()
     e2e_s = time.perf_counter() - t0
@@ -303,23 +321,25 @@ def run_ours(args, world, rank, local):
             cpu = {"value": n_l / LAYERS / t_or, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                    "sample": "one token through 2 of the 48 layers, oracle compute only, scaled by 1/24 "
                              "(fp64 scalar C, one host core)"}
+        kernel = ("decode_kernel (moe_decode_forward: 48 layers, one cooperative launch)" if args.path == "fused"
+                  else "whole modular step (CUDA graph of 480 launches)")
         line = {
             "metric": "decode tokens/s (48-layer MoE stack, 1 token per step)",
             "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic (seeded generator, weights drawn on the GPU)",
             "config": {"workload": WORKLOAD, "tokens_per_step": 1, "layers": LAYERS, "parallelism": "replicas",
+                       "path": args.path,
                        "l2": "no flush: each step reads 1.36 GB of weights, 10x the 129 MB L2"},
             "hbm_roofline": {"bytes_per_token": BYTES_PER_TOKEN,
                              "achieved_gbs": BYTES_PER_TOKEN * tok_s / world / 1e9,
                              "frac_of_measured": BYTES_PER_TOKEN * tok_s / world / 1e9 / peak},
-            "roofline": {"kernel": "moe_expert_forward decode call (2 dequant GEMVs + combine), one layer",
-                         "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "roofline": {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
-                         "bytes_per_launch": K_TOP * EXPERT_BYTES, "avg_call_ms": call_ms},
+                         "bytes_per_launch": BYTES_PER_TOKEN, "avg_launch_ms": call_ms},
             "clocks": clocks,
             "e2e": e2e,
-            "gpu_launches": KERNELS_PER_LAYER * LAYERS * args.steps,
+            "gpu_launches": kernels_per_step * args.steps,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -332,6 +352,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="fused", choices=["fused", "modular"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -48,6 +48,18 @@ class moe_expert_arena(ctypes.Structure):
     ]
 
 
+class moe_layer_weights(ctypes.Structure):
+    _fields_ = [
+        ("experts", moe_expert_arena),
+        ("w_router", ctypes.c_void_p),
+        ("bias", ctypes.c_void_p),
+        ("shared_wg", ctypes.c_void_p),
+        ("shared_wu", ctypes.c_void_p),
+        ("shared_wd", ctypes.c_void_p),
+        ("shared_I", ctypes.c_int32),
+    ]
+
+
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int
 _I64 = ctypes.c_int64
@@ -72,6 +84,9 @@ _SIGS = {
     "moe_shared_expert_workspace_size": [_I32, _I32, _I32, _PSZ],
     "moe_shared_expert": [_P, _P, _P, _I32, _I32, _P, _I32, _P, _I32, _I32, _P, _SZ, _P],
     "moe_f32_to_bf16": [_P, _P, _I64, _P],
+    "moe_decode_workspace_size": [_I32, _I32, _I32, _I32, _I32, _I32, _PSZ],
+    "moe_decode_forward": [ctypes.POINTER(moe_layer_weights), _I32, _P, _I32, _I32, _P, _P, _P, _SZ, _P, _P],
+    "moe_selftest_barrier": [ctypes.c_uint, _I32, _P, _SZ, _P, _P],
 }
 
 
@@ -244,6 +259,22 @@ def moe_shared_expert(wg, wu, wd, H, I, x_bf16, T, out, out_dtype=MOE_F32, accum
 
 def moe_f32_to_bf16(in_f32, out_bf16, n, stream=None):
     _check(lib().moe_f32_to_bf16(_ptr(in_f32), _ptr(out_bf16), n, _stream(stream)), "moe_f32_to_bf16")
+
+
+def moe_decode_workspace_size(T, H, I, E, k, shared_I):
+    return _size(lib().moe_decode_workspace_size, T, H, I, E, k, shared_I)
+
+
+def moe_decode_forward(layers, x, T, k, ids_out=None, w_out=None, ws=None, ws_bytes=0, dev_status=None, stream=None):
+    """layers: a sequence of moe_layer_weights (host); x: [T][H] fp32 device tensor, updated in place."""
+    arr = (moe_layer_weights * len(layers))(*layers)
+    _check(lib().moe_decode_forward(arr, len(layers), _ptr(x), T, k, _ptr(ids_out), _ptr(w_out), _ptr(ws), ws_bytes,
+                                    _ptr(dev_status), _stream(stream)), "moe_decode_forward")
+
+
+def moe_selftest_barrier(extra_arrivals, timeout_ms, ws, ws_bytes, dev_status=None, stream=None):
+    _check(lib().moe_selftest_barrier(extra_arrivals, timeout_ms, _ptr(ws), ws_bytes, _ptr(dev_status),
+                                      _stream(stream)), "moe_selftest_barrier")
 
 
 def header_functions():

@@ -135,6 +135,15 @@ class MoeLayer:
             sh.append(t)
         self.shared = tuple(sh)
 
+    def weights(self):
+        """This layer as a moe_layer_weights descriptor for moe_decode_forward."""
+        from . import moe_layer_weights
+
+        sh = self.shared
+        return moe_layer_weights(self.arena, self.router_w.data_ptr(), self.router_b.data_ptr(),
+                                 sh[0].data_ptr() if sh else None, sh[1].data_ptr() if sh else None,
+                                 sh[2].data_ptr() if sh else None, self.s.Is if sh else 0)
+
     # -- running --------------------------------------------------------
     def forward(self, x_bf16, T, out_f32, ws: Workspace, bufs: "StepBuffers", accumulate=True, path=MOE_PATH_AUTO,
                 with_shared=True):

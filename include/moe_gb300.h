@@ -279,6 +279,54 @@ moe_status moe_shared_expert(const uint16_t *wg, const uint16_t *wu, const uint1
                              int accumulate, void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Fused decode over a stack of layers                                      */
+/* ------------------------------------------------------------------------ */
+
+/* The weights of one layer for moe_decode_forward (device pointers). */
+typedef struct moe_layer_weights {
+    moe_expert_arena experts;      /* routed experts (same shape in every layer) */
+    const float *w_router;         /* [E][H] fp32 */
+    const float *bias;             /* [E] fp32, or NULL */
+    const uint16_t *shared_wg;     /* [shared_I][H] bf16 (ignored if shared_I == 0) */
+    const uint16_t *shared_wu;     /* [shared_I][H] bf16 */
+    const uint16_t *shared_wd;     /* [H][shared_I] bf16 */
+    int32_t shared_I;              /* shared expert width, 0 for none */
+} moe_layer_weights;
+
+/*
+ * Decode up to 4 tokens through n_layers (<= 64) MoE layers in one
+ * persistent cooperative kernel, updating the fp32 residual stream in place:
+ *   for each layer l:  x[t] += S_l(bf16(x[t])) + sum_j w_tj FFN_{l,ids_tj}(bf16(x[t]))
+ * with the routing of moe_router_topk (fp32 logits, ties to the lower id,
+ * renormalised softmax weights) and fp32 dequantisation and accumulation.
+ *   layers   host array of n_layers descriptors (copied into the launch)
+ *   x        [T][H] fp32, device, 16-byte aligned, in/out
+ *   ids_out, w_out  [n_layers][T][k] device outputs of the routing, or both NULL
+ * A token's result does not depend on the other tokens of the call.  Shapes:
+ * H a multiple of 32 up to 1024, or 2048 or 4096; I and shared_I multiples
+ * of 32 up to 1024.  The kernel's grid barriers give up after about 2 s and
+ * report MOE_ERR_TIMEOUT through dev_status.  The pages: 48 layers of a
+ * router, ten of 512 experts and a shared expert, verify windows of up to
+ * four tokens ("Strata serves a 125B MoE ...", section "Six billion active
+ * parameters per token").
+ */
+moe_status moe_decode_workspace_size(int T, int H, int I, int E, int k, int shared_I, size_t *bytes);
+moe_status moe_decode_forward(const moe_layer_weights *layers, int n_layers, float *x, int T, int k,
+                              int32_t *ids_out, float *w_out, void *ws, size_t ws_bytes,
+                              int32_t *dev_status, moe_stream_t stream);
+
+/*
+ * Self-test of the grid barrier's time limit used by moe_decode_forward: one
+ * cooperative launch (one CTA per SM) runs a single barrier whose target is
+ * `extra_arrivals` above the number of CTAs.  With extra_arrivals = 0 it
+ * completes; otherwise every CTA gives up after timeout_ms, writes
+ * MOE_ERR_TIMEOUT to *dev_status and returns, leaving the context usable.
+ * ws: 8 bytes (int at ws+4 counts the CTAs that passed the barrier).
+ */
+moe_status moe_selftest_barrier(unsigned extra_arrivals, int timeout_ms, void *ws, size_t ws_bytes,
+                                int32_t *dev_status, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Residual stream helper                                                   */
 /* ------------------------------------------------------------------------ */
 

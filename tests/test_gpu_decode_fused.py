@@ -1,0 +1,140 @@
+"""GPU parity of moe_decode_forward (the fused multi-layer decode) against the
+oracle, teacher-forced layer by layer with the routing the kernel reports,
+plus its batch invariance and the grid barrier's time limit."""
+import numpy as np
+import pytest
+import torch
+
+import bit_expert_ffn_gb300 as m
+import oracle
+from bit_expert_ffn_gb300 import synth
+from bit_expert_ffn_gb300.model import LayerShape, MoeLayer, StepBuffers, Workspace, residual_step
+from helpers import host_layer, rel_l2
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def tiny_stack(n_layers, bits=2, H=256, I=128, E=16, k=2, Is=128, zipf=1.1):
+    layers, hosts = [], []
+    for l in range(n_layers):
+        arena, wr, b, shared = host_layer(seed=40 + l, layer=l, bits=bits, H=H, I=I, E=E, Is=Is, zipf=zipf)
+        L = MoeLayer(LayerShape(H=H, I=I, E=E, k=k, Is=Is, bits=bits), DEV)
+        L.load_host(arena[0], arena[1], arena[2], arena[3], arena[4], arena[5], wr, b, shared)
+        layers.append(L)
+        hosts.append((arena, wr, b, shared))
+    return layers, hosts
+
+
+def run_fused(layers, x0, k):
+    T, H = x0.shape
+    s = layers[0].s
+    x = torch.from_numpy(x0.copy()).to(DEV)
+    n = len(layers)
+    ids = torch.empty(n, T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(n, T, k, dtype=torch.float32, device=DEV)
+    nb = m.moe_decode_workspace_size(T, s.H, s.I, s.E, k, s.Is)
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.moe_decode_forward([L.weights() for L in layers], x, T, k, ids, w, ws, nb, st)
+    assert m.moe_check_status(st) == 0, m.moe_last_error()
+    return x.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
+
+
+def oracle_stack(bits, x0, ids, w, host_arenas):
+    """Residual stack in fp64, routing taken from the kernel, bf16 inputs per layer."""
+    xr = x0.astype(np.float64)
+    for l, (arena, wr, b, shared) in enumerate(host_arenas):
+        xb = synth.f32_to_bf16_bits(xr.astype(np.float32))
+        xr = xr + oracle.moe_layer(bits, xb, ids[l], w[l].astype(np.float64), *arena, shared=shared)
+    return xr
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+@pytest.mark.parametrize("bits", [2, 3])
+def test_one_layer_matches_oracle(moe, T, bits):
+    layers, hosts = tiny_stack(1, bits=bits)
+    x0 = synth.bf16_bits_to_f32(synth.verify_window(5, T, 256))
+    x1, ids, w = run_fused(layers, x0, 2)
+    want = oracle_stack(bits, x0, ids, w, hosts)
+    assert rel_l2(x1 - x0, want - x0) <= 2e-5
+    # routing: the oracle's own selection on its own logits agrees (no near-ties at this size)
+    wr, b = hosts[0][1], hosts[0][2]
+    lg = oracle.router_logits(synth.f32_to_bf16_bits(x0), wr, b)
+    oids, ow = oracle.topk(lg.astype(np.float32), 2)
+    assert np.array_equal(oids, ids[0])
+    np.testing.assert_allclose(w[0], ow, rtol=2e-6, atol=1e-7)
+
+
+def test_three_layers_teacher_forced(moe):
+    layers, hosts = tiny_stack(3, k=4)
+    x0 = synth.bf16_bits_to_f32(synth.verify_window(6, 4, 256))
+    x3, ids, w = run_fused(layers, x0, 4)
+    want = oracle_stack(2, x0, ids, w, hosts)
+    assert rel_l2(x3 - x0, want - x0) <= 1e-4
+
+
+def test_batch_invariance(moe):
+    """Each token's result is bit-identical alone and inside a 4-token window."""
+    layers, _ = tiny_stack(2, k=4)
+    x0 = synth.bf16_bits_to_f32(synth.verify_window(7, 4, 256))
+    group, gids, _ = run_fused(layers, x0, 4)
+    for t in range(4):
+        alone, aids, _ = run_fused(layers, x0[t:t + 1], 4)
+        assert np.array_equal(aids[:, 0], gids[:, t])
+        assert np.array_equal(alone[0], group[t])
+
+
+def test_agrees_with_modular_path(moe):
+    layers, _ = tiny_stack(2, k=2)
+    x0 = synth.bf16_bits_to_f32(synth.verify_window(8, 3, 256))
+    fused, ids, _ = run_fused(layers, x0, 2)
+    x = torch.from_numpy(x0.copy()).to(DEV)
+    xb = torch.empty(3, 256, dtype=torch.int16, device=DEV)
+    residual_step(layers, x, xb, 3, Workspace(DEV), StepBuffers(3, 16, 2, DEV), path=m.MOE_PATH_DECODE)
+    assert rel_l2(fused - x0, x.cpu().numpy() - x0) <= 2e-5
+
+
+def test_full_size_two_layers_sampled(moe):
+    """H=2048, E=512, I=768, top-10, 2-bit, Zipf(1.1), bf16 shared I=768, T=4 verify window."""
+    seed = 3
+    s = LayerShape()
+    layers = []
+    for l in range(2):
+        L = MoeLayer(s, DEV)
+        L.fill_device(seed, l, zipf_s=1.1)
+        layers.append(L)
+    x0 = synth.bf16_bits_to_f32(synth.verify_window(seed, 4, s.H))
+    x2, ids, w = run_fused(layers, x0, 10)
+    xr = x0.astype(np.float64)
+    for l in range(2):
+        used = sorted(set(int(e) for e in ids[l].ravel()))
+        remap = {e: i for i, e in enumerate(used)}
+        parts = [[], [], [], [], [], []]
+        for e in used:
+            g, u, d = synth.expert_codes(seed, l, e, 2, s.H, s.I)
+            gus, ds = synth.expert_scales(seed, l, e, s.H, s.I)
+            for lst, a in zip(parts, (g, gus[0], u, gus[1], d, ds)):
+                lst.append(a)
+        arena = [np.stack(p) for p in parts]
+        cids = np.vectorize(remap.get)(ids[l]).astype(np.int32)
+        shared = synth.shared_weights(seed, l, s.H, s.Is)
+        xb = synth.f32_to_bf16_bits(xr.astype(np.float32))
+        xr = xr + oracle.moe_layer(2, xb, cids, w[l].astype(np.float64), *arena, shared=shared)
+    assert rel_l2(x2 - x0, xr - x0) <= 1e-4
+
+
+def test_barrier_completes_and_times_out(moe):
+    ws = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.moe_selftest_barrier(0, 1000, ws, 16, st)
+    assert m.moe_check_status(st) == 0
+    passed = ws.view(torch.int32)[1].item()
+    assert passed == torch.cuda.get_device_properties(0).multi_processor_count
+    # an unreachable target: every CTA gives up after 200 ms and reports the timeout
+    m.moe_selftest_barrier(1, 200, ws, 16, st)
+    assert m.moe_check_status(st, reset=True) == m.MOE_ERR_TIMEOUT
+    assert ws.view(torch.int32)[1].item() == 0
+    # the context is still usable
+    m.moe_selftest_barrier(0, 1000, ws, 16, st)
+    assert m.moe_check_status(st) == 0
