@@ -36,9 +36,10 @@ EXPERT_BYTES = 1_474_560
 ROUTER_BYTES = E * H * 4
 SHARED_BYTES = 3 * H * IS * 2
 BYTES_PER_TOKEN = LAYERS * (K_TOP * EXPERT_BYTES + ROUTER_BYTES + SHARED_BYTES)  # 1,362,100,224
-KERNELS_PER_LAYER = 10  # f32_to_bf16, router gemv, topk, permute, shared (2 gemv + add), experts (2 gemv + combine)
+KERNELS_PER_LAYER = 10  # rms_norm_bf16, router gemv, topk, permute, shared (2 gemv + add), experts (2 gemv + combine)
 WORKLOAD = ("decode: 1 token x 48 layers, H=2048, E=512, I=768, top-10, 2-bit experts (32-weight blocks, fp16 "
-            "scales) + bf16 shared expert I=768, fp32 router with Zipf(1.1) bias, fp32 residual stream")
+            "scales) + bf16 shared expert I=768, fp32 router with Zipf(1.1) bias, fp32 residual stream "
+            "normalised (RMS) in front of each layer")
 
 
 def peaks():
@@ -148,7 +149,10 @@ def oracle_decode_sample(n_layers: int, seed: int = 0, step: int = 0):
     xres = synth.bf16_bits_to_f32(x).astype(np.float64)
     t_oracle = 0.0
     for layer in range(n_layers):
-        xb = synth.f32_to_bf16_bits(xres.astype(np.float32))
+        t0 = time.perf_counter()
+        xn = oracle.rms_norm(xres.astype(np.float32), 1e-6)
+        t_oracle += time.perf_counter() - t0
+        xb = synth.f32_to_bf16_bits(xn.astype(np.float32))
         wr = synth.router_weights(seed, layer, E, H)
         b = synth.zipf_bias(seed, layer, E, 1.1)
         shared = synth.shared_weights(seed, layer, H, IS)
@@ -208,8 +212,10 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     lib = m.load()
     shape = LayerShape(H=H, I=I, E=E, k=K_TOP, Is=IS, bits=2)
+    NL = args.layers
+    bytes_per_token = NL * (K_TOP * EXPERT_BYTES + ROUTER_BYTES + SHARED_BYTES)
     layers = []
-    for layer in range(LAYERS):
+    for layer in range(NL):
         L = MoeLayer(shape, dev)
         L.fill_device(seed=0, layer=layer, zipf_s=1.1)
         layers.append(L)
@@ -225,14 +231,14 @@ def run_ours(args, world, rank, local):
     sptr = ctypes.c_void_p(stream.cuda_stream)
 
     if args.path == "fused":
-        descs = (m.moe_layer_weights * LAYERS)(*[L.weights() for L in layers])
+        descs = (m.moe_layer_weights * NL)(*[L.weights() for L in layers])
         nb = m.moe_decode_workspace_size(1, H, I, E, K_TOP, IS)
         ws = torch.empty(nb, dtype=torch.uint8, device=dev)
         kernels_per_step = 1
 
         def call():
-            st = lib.moe_decode_forward(descs, LAYERS, x_res.data_ptr(), 1, K_TOP, None, None, ws.data_ptr(), nb,
-                                        status.data_ptr(), sptr)
+            st = lib.moe_decode_forward(descs, NL, x_res.data_ptr(), 1, K_TOP, m.RMS_EPS, None, None,
+                                        ws.data_ptr(), nb, status.data_ptr(), sptr)
             if st:
                 raise m.MoeError(st, m.moe_last_error())
     else:
@@ -240,7 +246,7 @@ def run_ours(args, world, rank, local):
         bufs = StepBuffers(1, E, K_TOP, dev)
         wsp = Workspace(dev)
         wsp.get(8 << 20)
-        kernels_per_step = KERNELS_PER_LAYER * LAYERS
+        kernels_per_step = KERNELS_PER_LAYER * NL
         with torch.cuda.stream(stream):
             residual_step(layers, x_res, x_bf16, 1, wsp, bufs)  # eager warm-up (sizes the workspace)
             stream.synchronize()
@@ -261,6 +267,9 @@ def run_ours(args, world, rank, local):
             step(i)
     torch.cuda.synchronize()
     assert m.moe_check_status(status) == 0, m.moe_last_error()
+    for L in layers:
+        assert m.moe_check_status(L.status) == 0, m.moe_last_error()
+    assert bool(torch.isfinite(x_res).all()), "residual stream is not finite"
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -294,7 +303,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     call_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
     peak, peak_kind = peaks()
-    achieved = BYTES_PER_TOKEN / (call_ms / 1000.0) / 1e9
+    achieved = bytes_per_token / (call_ms / 1000.0) / 1e9
 
     # -- end to end through host buffers: pinned x in, result out, every step
     x_host = torch.empty(1, H, dtype=torch.float32, pin_memory=True)
@@ -321,22 +330,23 @@ def run_ours(args, world, rank, local):
             cpu = {"value": n_l / LAYERS / t_or, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                    "sample": "one token through 2 of the 48 layers, oracle compute only, scaled by 1/24 "
                              "(fp64 scalar C, one host core)"}
-        kernel = ("decode_kernel (moe_decode_forward: 48 layers, one cooperative launch)" if args.path == "fused"
-                  else "whole modular step (CUDA graph of 480 launches)")
+        kernel = (f"decode_kernel (moe_decode_forward: {NL} layers, one cooperative launch)" if args.path == "fused"
+                  else f"whole modular step (CUDA graph of {kernels_per_step} launches)")
         line = {
             "metric": "decode tokens/s (48-layer MoE stack, 1 token per step)",
             "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic (seeded generator, weights drawn on the GPU)",
-            "config": {"workload": WORKLOAD, "tokens_per_step": 1, "layers": LAYERS, "parallelism": "replicas",
+            "config": {"workload": WORKLOAD if NL == LAYERS else WORKLOAD.replace("48 layers", f"{NL} layers"),
+                       "tokens_per_step": 1, "layers": NL, "parallelism": "replicas",
                        "path": args.path,
                        "l2": "no flush: each step reads 1.36 GB of weights, 10x the 129 MB L2"},
-            "hbm_roofline": {"bytes_per_token": BYTES_PER_TOKEN,
-                             "achieved_gbs": BYTES_PER_TOKEN * tok_s / world / 1e9,
-                             "frac_of_measured": BYTES_PER_TOKEN * tok_s / world / 1e9 / peak},
+            "hbm_roofline": {"bytes_per_token": bytes_per_token,
+                             "achieved_gbs": bytes_per_token * tok_s / world / 1e9,
+                             "frac_of_measured": bytes_per_token * tok_s / world / 1e9 / peak},
             "roofline": {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
-                         "bytes_per_launch": BYTES_PER_TOKEN, "avg_launch_ms": call_ms},
+                         "bytes_per_launch": bytes_per_token, "avg_launch_ms": call_ms},
             "clocks": clocks,
             "e2e": e2e,
             "gpu_launches": kernels_per_step * args.steps,
@@ -353,6 +363,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="fused", choices=["fused", "modular"])
+    ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (48 is the workload; fewer only "
+                    "for profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -23,6 +23,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_NONFINITE, MOE_ERR_BOUNDS = 4, 5, 6, 7
 MOE_F32, MOE_BF16 = 0, 1
 MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL = 0, 1, 2
+RMS_EPS = 1e-6  # normalisation in front of each stacked layer
 
 _lock = threading.Lock()
 _lib = None
@@ -85,7 +86,9 @@ _SIGS = {
     "moe_shared_expert": [_P, _P, _P, _I32, _I32, _P, _I32, _P, _I32, _I32, _P, _SZ, _P],
     "moe_f32_to_bf16": [_P, _P, _I64, _P],
     "moe_decode_workspace_size": [_I32, _I32, _I32, _I32, _I32, _I32, _PSZ],
-    "moe_decode_forward": [ctypes.POINTER(moe_layer_weights), _I32, _P, _I32, _I32, _P, _P, _P, _SZ, _P, _P],
+    "moe_decode_forward": [ctypes.POINTER(moe_layer_weights), _I32, _P, _I32, _I32, ctypes.c_float, _P, _P, _P, _SZ,
+                           _P, _P],
+    "moe_rms_norm_bf16": [_P, _P, _I32, _I32, ctypes.c_float, _P],
     "moe_selftest_barrier": [ctypes.c_uint, _I32, _P, _SZ, _P, _P],
 }
 
@@ -265,11 +268,17 @@ def moe_decode_workspace_size(T, H, I, E, k, shared_I):
     return _size(lib().moe_decode_workspace_size, T, H, I, E, k, shared_I)
 
 
-def moe_decode_forward(layers, x, T, k, ids_out=None, w_out=None, ws=None, ws_bytes=0, dev_status=None, stream=None):
+def moe_decode_forward(layers, x, T, k, rms_eps=RMS_EPS, ids_out=None, w_out=None, ws=None, ws_bytes=0,
+                       dev_status=None, stream=None):
     """layers: a sequence of moe_layer_weights (host); x: [T][H] fp32 device tensor, updated in place."""
     arr = (moe_layer_weights * len(layers))(*layers)
-    _check(lib().moe_decode_forward(arr, len(layers), _ptr(x), T, k, _ptr(ids_out), _ptr(w_out), _ptr(ws), ws_bytes,
-                                    _ptr(dev_status), _stream(stream)), "moe_decode_forward")
+    _check(lib().moe_decode_forward(arr, len(layers), _ptr(x), T, k, rms_eps, _ptr(ids_out), _ptr(w_out), _ptr(ws),
+                                    ws_bytes, _ptr(dev_status), _stream(stream)), "moe_decode_forward")
+
+
+def moe_rms_norm_bf16(x, out, T, H, eps=None, stream=None):
+    _check(lib().moe_rms_norm_bf16(_ptr(x), _ptr(out), T, H, RMS_EPS if eps is None else eps, _stream(stream)),
+           "moe_rms_norm_bf16")
 
 
 def moe_selftest_barrier(extra_arrivals, timeout_ms, ws, ws_bytes, dev_status=None, stream=None):

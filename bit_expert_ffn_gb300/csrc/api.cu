@@ -47,6 +47,25 @@ __global__ void f32_to_bf16_kernel(const float *__restrict__ in, uint16_t *__res
     for (; i < n; i += stride) out[i] = f32_to_bf16(in[i]);
 }
 
+// One CTA per token: x / sqrt(mean(x^2) + eps) rounded to bf16.  The sum of
+// squares is taken in a fixed order (per-thread strided sums, a warp tree,
+// then the warps in order), the same order the fused decode kernel uses.
+__global__ void rms_norm_bf16_kernel(const float *__restrict__ x, uint16_t *__restrict__ out, int H, float eps)
+{
+    __shared__ float wsum[32];
+    const float *xr = x + (int64_t)blockIdx.x * H;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane_id() == 0) wsum[warp_id()] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); w++) tot += wsum[w];
+    float inv = 1.0f / sqrtf(tot / (float)H + eps);
+    for (int i = threadIdx.x; i < H; i += blockDim.x) out[(int64_t)blockIdx.x * H + i] = f32_to_bf16(xr[i] * inv);
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -107,6 +126,16 @@ moe_status moe_f32_to_bf16(const float *in_f32, uint16_t *out_bf16, int64_t n, m
     if (blocks > cap) blocks = cap;
     f32_to_bf16_kernel<<<(unsigned)blocks, 256, 0, to_cuda(stream)>>>(in_f32, out_bf16, n);
     return check_launch("f32_to_bf16");
+}
+
+moe_status moe_rms_norm_bf16(const float *x, uint16_t *out, int T, int H, float eps, moe_stream_t stream)
+{
+    MOE_REQUIRE(T >= 0 && H > 0, "T >= 0 and H > 0 (got T=%d H=%d)", T, H);
+    MOE_REQUIRE(eps >= 0.f, "eps must be >= 0");
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(x && out, "NULL pointer");
+    rms_norm_bf16_kernel<<<T, 256, 0, to_cuda(stream)>>>(x, out, H, eps);
+    return check_launch("rms_norm_bf16");
 }
 
 }  // extern "C"

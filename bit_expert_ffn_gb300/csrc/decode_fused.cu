@@ -54,6 +54,7 @@ struct Args {
     Layer L[kMaxLayers];
     int n_layers, T, H, I, E, k, Is, bits;
     int rows_per_cta;
+    float rms_eps;     // < 0: no normalisation in front of each layer
     float *x;          // [T][H] residual stream, in/out
     float *logits;     // [T][E]
     float *h;          // [T*k][I] routed h in sorted pair order
@@ -76,6 +77,8 @@ struct Routing {
     float sel_v[kMaxT][kMaxK];
     int sel_i[kMaxT][kMaxK];
     float team[kWarps][kRB][2][kMaxT];  // phase-B partials of each warp
+    float wsum[kMaxT][kWarps];
+    float inv_rms[kMaxT];
     int abort;
 };
 
@@ -659,9 +662,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     unsigned nbar = 0;
     for (int l = 0; l < a.n_layers; l++) {
         const Layer &L = a.L[l];
-        // x -> bf16 -> fp32 copy in shared memory
+        // layer input: bf16(x / rms(x)) (or bf16(x)), as fp32 in shared memory.
+        // Per-token sum of squares in a fixed order: strided per thread, a warp
+        // tree, then the warps in order (independent of the other tokens).
+        if (a.rms_eps >= 0.f) {
+            for (int t = 0; t < T; t++) {
+                float ss = 0.f;
+                for (int i = threadIdx.x; i < a.H; i += kThreads) {
+                    float v = __ldcg(a.x + (int64_t)t * a.H + i);
+                    ss = fmaf(v, v, ss);
+                }
+                ss = warp_sum(ss);
+                if (lane_id() == 0) R.wsum[t][warp_id()] = ss;
+            }
+            __syncthreads();
+            if (threadIdx.x < T) {
+                float tot = 0.f;
+                for (int w = 0; w < kWarps; w++) tot += R.wsum[threadIdx.x][w];
+                R.inv_rms[threadIdx.x] = 1.0f / sqrtf(tot / (float)a.H + a.rms_eps);
+            }
+            __syncthreads();
+        } else if (threadIdx.x < T) {
+            R.inv_rms[threadIdx.x] = 1.0f;
+        }
+        __syncthreads();
         for (int i = threadIdx.x; i < T * a.H; i += kThreads) {
-            float v = bf16_round(__ldcg(a.x + i));
+            float v = bf16_round(__ldcg(a.x + i) * R.inv_rms[i / a.H]);
             int t = i / a.H, r = i - t * a.H;
             xs[i] = v;
             xsw[t * a.H + (r & 31) * C + (r >> 5)] = v;
@@ -751,7 +777,7 @@ extern "C" moe_status moe_decode_workspace_size(int T, int H, int I, int E, int 
 }
 
 extern "C" moe_status moe_decode_forward(const moe_layer_weights *layers, int n_layers, float *x, int T, int k,
-                                         int32_t *ids_out, float *w_out, void *ws, size_t ws_bytes,
+                                         float rms_eps, int32_t *ids_out, float *w_out, void *ws, size_t ws_bytes,
                                          int32_t *dev_status, moe_stream_t stream)
 {
     using namespace fused;
@@ -801,6 +827,7 @@ extern "C" moe_status moe_decode_forward(const moe_layer_weights *layers, int n_
     a.Is = Is;
     a.bits = bits;
     a.x = x;
+    a.rms_eps = rms_eps;
     a.logits = reinterpret_cast<float *>(wb + lay.logits);
     a.h = reinterpret_cast<float *>(wb + lay.h);
     a.hs = reinterpret_cast<float *>(wb + lay.hs);

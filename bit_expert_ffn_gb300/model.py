@@ -18,7 +18,7 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from . import (MOE_F32, MOE_PATH_AUTO, load, make_arena, moe_expert_forward, moe_expert_forward_workspace_size,
+from . import (MOE_F32, MOE_PATH_AUTO, RMS_EPS, load, moe_rms_norm_bf16, make_arena, moe_expert_forward, moe_expert_forward_workspace_size,
                moe_f32_to_bf16, moe_pack_experts, moe_permute, moe_permute_workspace_size, moe_router_topk,
                moe_shared_expert, moe_shared_expert_workspace_size, synth, synth_lib)
 
@@ -179,11 +179,13 @@ class StepBuffers:
         self.inv = torch.empty(max(T * k, 1), dtype=torch.int32, device=d)
 
 
-def residual_step(layers, x_res, x_bf16, T, ws, bufs, path=MOE_PATH_AUTO):
-    """x_res <- x_res + MoE_l(bf16(x_res)) for every layer, in place (fp32 residual stream)."""
-    n = x_res.numel()
+def residual_step(layers, x_res, x_bf16, T, ws, bufs, path=MOE_PATH_AUTO, rms_eps=RMS_EPS):
+    """x_res <- x_res + MoE_l(bf16(x_res / rms(x_res))) for every layer, in place (fp32 residual stream)."""
     for L in layers:
-        moe_f32_to_bf16(x_res, x_bf16, n)
+        if rms_eps is None:
+            moe_f32_to_bf16(x_res, x_bf16, x_res.numel())
+        else:
+            moe_rms_norm_bf16(x_res, x_bf16, T, L.s.H, rms_eps)
         L.forward(x_bf16, T, x_res, ws, bufs, accumulate=True, path=path)
 
 

@@ -296,7 +296,9 @@ typedef struct moe_layer_weights {
 /*
  * Decode up to 4 tokens through n_layers (<= 64) MoE layers in one
  * persistent cooperative kernel, updating the fp32 residual stream in place:
- *   for each layer l:  x[t] += S_l(bf16(x[t])) + sum_j w_tj FFN_{l,ids_tj}(bf16(x[t]))
+ *   for each layer l:  u = bf16(x[t] / sqrt(mean(x[t]^2) + rms_eps))
+ *                      x[t] += S_l(u) + sum_j w_tj FFN_{l,ids_tj}(u)
+ * (rms_eps < 0: u = bf16(x[t]), no normalisation; see moe_rms_norm_bf16)
  * with the routing of moe_router_topk (fp32 logits, ties to the lower id,
  * renormalised softmax weights) and fp32 dequantisation and accumulation.
  *   layers   host array of n_layers descriptors (copied into the launch)
@@ -312,7 +314,7 @@ typedef struct moe_layer_weights {
  */
 moe_status moe_decode_workspace_size(int T, int H, int I, int E, int k, int shared_I, size_t *bytes);
 moe_status moe_decode_forward(const moe_layer_weights *layers, int n_layers, float *x, int T, int k,
-                              int32_t *ids_out, float *w_out, void *ws, size_t ws_bytes,
+                              float rms_eps, int32_t *ids_out, float *w_out, void *ws, size_t ws_bytes,
                               int32_t *dev_status, moe_stream_t stream);
 
 /*
@@ -332,6 +334,15 @@ moe_status moe_selftest_barrier(unsigned extra_arrivals, int timeout_ms, void *w
 
 /* out_bf16[i] = round-to-nearest-even bf16 of in_f32[i], n elements. */
 moe_status moe_f32_to_bf16(const float *in_f32, uint16_t *out_bf16, int64_t n, moe_stream_t stream);
+
+/*
+ * The input of a stacked layer: out[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps))
+ * for x [T][H] fp32 (a root-mean-square normalisation without a gain).  The
+ * pages' layers read a residual stream; a stack of synthetic layers without
+ * this normalisation diverges, so the stacked workloads normalise in front
+ * of every layer.
+ */
+moe_status moe_rms_norm_bf16(const float *x, uint16_t *out, int T, int H, float eps, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -75,6 +75,8 @@ def _bind(path):
     L.oracle_moe_layer.argtypes = [i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P,
                                    i32, P, P, P, P]
     L.oracle_moe_layer.restype = i32
+    L.oracle_rms_norm.argtypes = [i32, i32, P, dbl, P]
+    L.oracle_rms_norm.restype = None
     return L
 
 
@@ -232,3 +234,12 @@ def moe_layer(bits, x_bf16, ids, w, gate_codes, gate_scales, up_codes, up_scales
     if st != OK:
         raise OracleError(st, "moe_layer")
     return out
+
+
+def rms_norm(x_f32: np.ndarray, eps: float) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) per row, fp64 result."""
+    x = _c(x_f32, np.float32)
+    T, H = x.shape
+    y = np.zeros((T, H), np.float64)
+    lib().oracle_rms_norm(T, H, _p(x), float(eps), _p(y))
+    return y

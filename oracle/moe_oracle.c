@@ -379,3 +379,26 @@ int oracle_moe_layer(int bits, int T, int H, int I, int E, int k, const uint16_t
     free(y);
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Residual stream                                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The input of each stacked layer: x / sqrt(mean(x^2) + eps) per token (a
+ * root-mean-square normalisation without a learned gain), in double.
+ *   x [T][H] fp32 residual stream;  y [T][H] double.
+ * The pages' model feeds every MoE layer from a residual stream ("How Strata
+ * runs a 125-billion-parameter model ...", Step 1 table: gated-residual
+ * hyper-connections); the normalisation in front of the layer is the reading
+ * taken for a stack of synthetic layers, whose plain residual sum diverges.
+ */
+void oracle_rms_norm(int T, int H, const float *x, double eps, double *y)
+{
+    for (int t = 0; t < T; t++) {
+        double ss = 0.0;
+        for (int i = 0; i < H; i++) ss += (double)x[(int64_t)t * H + i] * (double)x[(int64_t)t * H + i];
+        double r = sqrt(ss / (double)H + eps);
+        for (int i = 0; i < H; i++) y[(int64_t)t * H + i] = (double)x[(int64_t)t * H + i] / r;
+    }
+}

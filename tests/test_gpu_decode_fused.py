@@ -36,17 +36,21 @@ def run_fused(layers, x0, k):
     nb = m.moe_decode_workspace_size(T, s.H, s.I, s.E, k, s.Is)
     ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    m.moe_decode_forward([L.weights() for L in layers], x, T, k, ids, w, ws, nb, st)
+    m.moe_decode_forward([L.weights() for L in layers], x, T, k, m.RMS_EPS, ids, w, ws, nb, st)
     assert m.moe_check_status(st) == 0, m.moe_last_error()
     return x.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
 
 
+def layer_input(xr):
+    """bf16 of the normalised residual stream, as the stacked layers take it."""
+    return synth.f32_to_bf16_bits(oracle.rms_norm(xr.astype(np.float32), m.RMS_EPS).astype(np.float32))
+
+
 def oracle_stack(bits, x0, ids, w, host_arenas):
-    """Residual stack in fp64, routing taken from the kernel, bf16 inputs per layer."""
+    """Residual stack in fp64, routing taken from the kernel, normalised bf16 inputs per layer."""
     xr = x0.astype(np.float64)
     for l, (arena, wr, b, shared) in enumerate(host_arenas):
-        xb = synth.f32_to_bf16_bits(xr.astype(np.float32))
-        xr = xr + oracle.moe_layer(bits, xb, ids[l], w[l].astype(np.float64), *arena, shared=shared)
+        xr = xr + oracle.moe_layer(bits, layer_input(xr), ids[l], w[l].astype(np.float64), *arena, shared=shared)
     return xr
 
 
@@ -60,7 +64,7 @@ def test_one_layer_matches_oracle(moe, T, bits):
     assert rel_l2(x1 - x0, want - x0) <= 2e-5
     # routing: the oracle's own selection on its own logits agrees (no near-ties at this size)
     wr, b = hosts[0][1], hosts[0][2]
-    lg = oracle.router_logits(synth.f32_to_bf16_bits(x0), wr, b)
+    lg = oracle.router_logits(layer_input(x0), wr, b)
     oids, ow = oracle.topk(lg.astype(np.float32), 2)
     assert np.array_equal(oids, ids[0])
     np.testing.assert_allclose(w[0], ow, rtol=2e-6, atol=1e-7)
@@ -119,8 +123,7 @@ def test_full_size_two_layers_sampled(moe):
         arena = [np.stack(p) for p in parts]
         cids = np.vectorize(remap.get)(ids[l]).astype(np.int32)
         shared = synth.shared_weights(seed, l, s.H, s.Is)
-        xb = synth.f32_to_bf16_bits(xr.astype(np.float32))
-        xr = xr + oracle.moe_layer(2, xb, cids, w[l].astype(np.float64), *arena, shared=shared)
+        xr = xr + oracle.moe_layer(2, layer_input(xr), cids, w[l].astype(np.float64), *arena, shared=shared)
     assert rel_l2(x2 - x0, xr - x0) <= 1e-4
 
 
@@ -138,3 +141,23 @@ def test_barrier_completes_and_times_out(moe):
     # the context is still usable
     m.moe_selftest_barrier(0, 1000, ws, 16, st)
     assert m.moe_check_status(st) == 0
+
+
+def test_rms_norm_bf16_matches_oracle(moe):
+    rng = np.random.default_rng(11)
+    x = (rng.normal(0, 3, (5, 2048)) * rng.uniform(0.1, 50, (5, 1))).astype(np.float32)
+    out = torch.empty(5, 2048, dtype=torch.int16, device=DEV)
+    m.moe_rms_norm_bf16(torch.from_numpy(x).to(DEV), out, 5, 2048)
+    got = synth.bf16_bits_to_f32(out.cpu().numpy().view(np.uint16)).astype(np.float64)
+    want = oracle.rms_norm(x, m.RMS_EPS)
+    assert np.all(np.abs(got - want) <= np.abs(want) * 2.0 ** -8 + 1e-30)  # within one bf16 rounding
+    exact = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(want.astype(np.float32)))
+    assert np.mean(got == exact) > 0.999
+
+
+def test_long_stack_stays_finite(moe):
+    """Twenty normalised layers keep the residual stream finite (the plain residual sum would not)."""
+    layers, _ = tiny_stack(20, k=2)
+    x0 = synth.bf16_bits_to_f32(synth.activations(12, 2, 256))
+    x, ids, w = run_fused(layers, x0, 2)
+    assert np.all(np.isfinite(x))

@@ -40,6 +40,8 @@ MUTANTS = [
     ("permutation unstable", "int32_t pos = fill[ids[f]]++;", "int32_t pos = offsets[ids[f] + 1] - 1 - (fill[ids[f]]++ - offsets[ids[f]]);"),
     ("offsets shifted", "for (int64_t f = 0; f < n; f++) offsets[ids[f] + 1]++;", "for (int64_t f = 0; f < n; f++) offsets[ids[f]]++;"),
     ("bf16 read as the low half", "uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
+    ("rms norm without the mean", "double r = sqrt(ss / (double)H + eps);", "double r = sqrt(ss + eps);"),
+    ("rms norm eps outside the root", "double r = sqrt(ss / (double)H + eps);", "double r = sqrt(ss / (double)H) + eps;"),
 ]
 
 PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]

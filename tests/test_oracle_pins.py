@@ -413,3 +413,30 @@ def test_layer_3bit_vs_dense_numpy():
         ref = sum(w[t, j] * numpy_ffn(3, gate[e], gsc[e], up[e], usc[e], down[e], dsc[e], xf[t])
                   for j, e in enumerate(ids[t]))
         assert np.linalg.norm(out[t] - ref) <= 1e-12 * np.linalg.norm(ref)
+
+
+# ---------------------------------------------------------------------------
+# residual-stream normalisation in front of each stacked layer
+# ---------------------------------------------------------------------------
+
+def test_rms_norm_closed_forms():
+    H = 64
+    c = np.full((1, H), 3.0, np.float32)
+    np.testing.assert_allclose(oracle.rms_norm(c, 0.0), 1.0, rtol=1e-15)
+    # eps enters under the root: mean(x^2) = 9, so each entry is 3 / sqrt(9 + eps)
+    np.testing.assert_allclose(oracle.rms_norm(c, 7.0), 3.0 / 4.0, rtol=1e-15)
+    x = np.zeros((1, H), np.float32)
+    x[0, 5] = -2.0  # mean(x^2) = 4/H
+    y = oracle.rms_norm(x, 0.0)
+    np.testing.assert_allclose(y[0, 5], -2.0 / np.sqrt(4.0 / H), rtol=1e-15)
+    assert np.count_nonzero(y) == 1
+
+
+def test_rms_norm_properties():
+    rng = np.random.default_rng(3)
+    x = rng.normal(0, 5, (4, 2048)).astype(np.float32)
+    y = oracle.rms_norm(x, 0.0)
+    np.testing.assert_allclose((y ** 2).mean(axis=1), 1.0, rtol=1e-12)  # unit mean square
+    np.testing.assert_allclose(oracle.rms_norm(x * np.float32(8.0), 0.0), y, rtol=1e-12)  # scale invariant
+    ref = x.astype(np.float64) / np.sqrt((x.astype(np.float64) ** 2).mean(axis=1, keepdims=True) + 1e-6)
+    np.testing.assert_allclose(oracle.rms_norm(x, 1e-6), ref, rtol=1e-13)
