@@ -35,8 +35,8 @@ constexpr int kMaxT = 4;
 constexpr int kMaxK = 16;
 constexpr int kMaxPairs = kMaxT * kMaxK;
 constexpr int kMaxCand = 512;  // k lanes x 32 values per lane at most
-constexpr int kRB = 4;         // units per phase-B batch
-constexpr int kRowBlock = 8;   // rows per phase-C item
+constexpr int kRB = 4;         // units per phase-B batch (team partial sums)
+constexpr int kMaxChunks = 128;  // phase-B / phase-C chunk list entries per CTA
 constexpr unsigned long long kBarrierTimeoutNs = 2000000000ull;
 constexpr unsigned kAbort = 0x80000000u;
 
@@ -79,6 +79,8 @@ struct Routing {
     float team[kWarps][kRB][2][kMaxT];  // phase-B partials of each warp
     float wsum[kMaxT][kWarps];
     float inv_rms[kMaxT];
+    int b_g[kMaxChunks], b_r[kMaxChunks], b_n[kMaxChunks], nb;  // phase-B chunks: group, first row, rows
+    int c_g[kMaxChunks], c_n[kMaxChunks], nc;                   // phase-C chunks: first group, groups
     int abort;
 };
 
@@ -152,37 +154,100 @@ __device__ __forceinline__ bool before(float av, int ai, float bv, int bi)
     return av > bv || (av == bv && ai < bi);
 }
 
-// Top-k of one token's logits by one warp.  The k-th best of the 32 lane
-// maxima bounds the k-th best overall, so only values ranking at or before
-// it are candidates; candidates are ranked exactly among themselves.
-__device__ void topk_warp(const float *__restrict__ l, int E, int k, Routing &R, int t, int32_t *status)
+// ------------------------------------------------------------ async copies
+// Every thread copies its share of a contiguous range in 16-byte pieces
+// (cp.async, L2-only); a commit group then covers one logical transfer.
+__device__ __forceinline__ void cp16(void *dst, const void *src)
+{
+    uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp8(void *dst, const void *src)
+{
+    uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp4(void *dst, const void *src)
+{
+    uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
+}
+
+// Pieces of 16, 8 or 4 bytes, the largest that the addresses and length allow
+// (the host only admits shapes whose rows are multiples of 4 bytes).
+__device__ __forceinline__ void copy_range(void *dst, const void *src, uint32_t bytes)
+{
+    char *d = static_cast<char *>(dst);
+    const char *s = static_cast<const char *>(src);
+    uint32_t al = (uint32_t)(reinterpret_cast<uintptr_t>(d) | reinterpret_cast<uintptr_t>(s) | bytes);
+    if ((al & 15u) == 0) {
+        for (uint32_t off = threadIdx.x * 16u; off < bytes; off += kThreads * 16u) cp16(d + off, s + off);
+    } else if ((al & 7u) == 0) {
+        for (uint32_t off = threadIdx.x * 8u; off < bytes; off += kThreads * 8u) cp8(d + off, s + off);
+    } else {
+        for (uint32_t off = threadIdx.x * 4u; off < bytes; off += kThreads * 4u) cp4(d + off, s + off);
+    }
+}
+
+__device__ __forceinline__ void commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until commit group number `gi` (0-based, in commit order) has landed,
+// given that `ncommit` groups have been committed.  Waiting for more groups
+// than needed is always safe, so larger distances are clamped.
+__device__ __forceinline__ void wait_group_index(int gi, int ncommit)
+{
+    int n = ncommit - 1 - gi;
+    if (n <= 0) asm volatile("cp.async.wait_group 0;" ::: "memory");
+    else if (n == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else if (n == 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+    else if (n == 3) asm volatile("cp.async.wait_group 3;" ::: "memory");
+    else if (n == 4) asm volatile("cp.async.wait_group 4;" ::: "memory");
+    else if (n == 5) asm volatile("cp.async.wait_group 5;" ::: "memory");
+    else if (n == 6) asm volatile("cp.async.wait_group 6;" ::: "memory");
+    else asm volatile("cp.async.wait_group 7;" ::: "memory");
+}
+
+__device__ __forceinline__ void wait_all_copies() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// ------------------------------------------------------------ routing
+
+// Top-k of one token's logits by one warp.  Every logit is loaded once into
+// registers.  The k-th best of the 32 lane maxima bounds the k-th best
+// overall, so only values at or before it are candidates, and candidates are
+// ranked exactly among themselves.  Returns true for a NaN logit.
+__device__ bool topk_warp(const float *__restrict__ l, int E, int k, Routing &R, int t)
 {
     int lane = lane_id();
-    int nq = (E + 31) >> 5;
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 32; q++) {
+        int e = lane + 32 * q;
+        v[q] = (e < E) ? __ldcg(l + e) : 0.f;
+    }
     float mv = 0.f;
     int mi = INT32_MAX;
     bool nan = false;
-    for (int q = 0; q < nq; q++) {
+#pragma unroll
+    for (int q = 0; q < 32; q++) {
         int e = lane + 32 * q;
         if (e < E) {
-            float v = __ldcg(l + e);
-            nan |= isnan(v);
-            if (mi == INT32_MAX || before(v, e, mv, mi)) {
-                mv = v;
+            nan |= isnan(v[q]);
+            if (mi == INT32_MAX || before(v[q], e, mv, mi)) {
+                mv = v[q];
                 mi = e;
             }
         }
     }
     if (__any_sync(0xffffffffu, nan)) {
-        if (lane == 0) set_status(status, MOE_ERR_NONFINITE);
         if (lane < k) {
             R.sel_i[t][lane] = lane;
             R.sel_v[t][lane] = 0.f;
         }
         __syncwarp();
-        return;
+        return true;
     }
-    // rank of this lane's maximum among the lane maxima
     int rank = 0;
     for (int s = 0; s < 32; s++) {
         float ov = __shfl_sync(0xffffffffu, mv, s);
@@ -190,23 +255,18 @@ __device__ void topk_warp(const float *__restrict__ l, int E, int k, Routing &R,
         if (oi != INT32_MAX && mi != INT32_MAX && before(ov, oi, mv, mi)) rank++;
     }
     unsigned who = __ballot_sync(0xffffffffu, mi != INT32_MAX && rank == k - 1);
-    int src = __ffs(who) - 1;  // min(E, 32) >= k valid lane maxima, so exactly one lane has rank k-1
+    int src = __ffs(who) - 1;  // min(E, 32) >= k valid lane maxima: exactly one has rank k-1
     float tv = __shfl_sync(0xffffffffu, mv, src);
     int ti = __shfl_sync(0xffffffffu, mi, src);
-    // candidates: values at or before the threshold (tv, ti)
     int base = 0;
-    for (int q = 0; q < nq; q++) {
+#pragma unroll
+    for (int q = 0; q < 32; q++) {
         int e = lane + 32 * q;
-        bool c = false;
-        float v = 0.f;
-        if (e < E) {
-            v = __ldcg(l + e);
-            c = before(v, e, tv, ti) || (v == tv && e == ti);
-        }
+        bool c = e < E && (before(v[q], e, tv, ti) || (v[q] == tv && e == ti));
         unsigned m = __ballot_sync(0xffffffffu, c);
         if (c) {
             int pos = base + __popc(m & ((1u << lane) - 1u));
-            R.cand_v[t][pos] = v;
+            R.cand_v[t][pos] = v[q];
             R.cand_i[t][pos] = e;
         }
         base += __popc(m);
@@ -214,16 +274,17 @@ __device__ void topk_warp(const float *__restrict__ l, int E, int k, Routing &R,
     __syncwarp();
     int C = base;
     for (int c = lane; c < C; c += 32) {
-        float v = R.cand_v[t][c];
-        int e = R.cand_i[t][c];
+        float cv = R.cand_v[t][c];
+        int ce = R.cand_i[t][c];
         int r = 0;
-        for (int d = 0; d < C; d++) r += before(R.cand_v[t][d], R.cand_i[t][d], v, e) ? 1 : 0;
+        for (int d = 0; d < C; d++) r += before(R.cand_v[t][d], R.cand_i[t][d], cv, ce) ? 1 : 0;
         if (r < k) {
-            R.sel_v[t][r] = v;
-            R.sel_i[t][r] = e;
+            R.sel_v[t][r] = cv;
+            R.sel_i[t][r] = ce;
         }
     }
     __syncwarp();
+    return false;
 }
 
 // Renormalised softmax of the k kept logits of token t (lane j = slot j).
@@ -285,8 +346,8 @@ __device__ void build_groups(Routing &R, int n)
 }
 
 // ------------------------------------------------------------ chunk dots
-// (exact dequantisation through fp16x2 words with exponent of 1.0; see the
-// block-sum identity in gemv.cuh: sum (c - mid) v = 2^B sum (1 + c/2^B) v - (2^B + mid) sum v)
+// (exact dequantisation through fp16x2 words with exponent of 1.0, then the
+// block-sum identity sum (c - mid) v = 2^B sum (1 + c/2^B) v - (2^B + mid) sum v)
 
 __device__ __forceinline__ float2 h2f(uint32_t b)
 {
@@ -327,22 +388,23 @@ struct QChunk {
     uint16_t s;
 };
 
+// One 32-weight chunk of a packed row that sits in shared memory.
 template <int BITS>
-__device__ __forceinline__ QChunk qload(const uint8_t *rowc, const uint16_t *rows, int cols, int chunk)
+__device__ __forceinline__ QChunk qload_s(const uint8_t *rowc, const uint16_t *rows, int cols, int chunk)
 {
     QChunk c;
     if (BITS == 2) {
-        uint2 lo = __ldg(reinterpret_cast<const uint2 *>(rowc + 8 * chunk));
+        uint2 lo = *reinterpret_cast<const uint2 *>(rowc + 8 * chunk);
         c.lo0 = lo.x;
         c.lo1 = lo.y;
         c.hi = 0;
     } else {
         const uint32_t *lo = reinterpret_cast<const uint32_t *>(rowc + 8 * chunk);
-        c.lo0 = __ldg(lo);
-        c.lo1 = __ldg(lo + 1);
-        c.hi = __ldg(reinterpret_cast<const uint32_t *>(rowc + (cols / 4) + 4 * chunk));
+        c.lo0 = lo[0];
+        c.lo1 = lo[1];
+        c.hi = *reinterpret_cast<const uint32_t *>(rowc + (cols / 4) + 4 * chunk);
     }
-    c.s = __ldg(rows + chunk);
+    c.s = rows[chunk];
     return c;
 }
 
@@ -370,24 +432,71 @@ __device__ __forceinline__ float warp_sum(float v)
 
 __device__ __forceinline__ float bf16_round(float f) { return bf16_to_f32(f32_to_bf16(f)); }
 
-// ------------------------------------------------------------ phase A
-template <int T>
-__device__ void phase_a(const Args &a, const Layer &L, const float *xs)
+// ------------------------------------------------------------ per-CTA plan
+// Shapes and shared-memory layout, computed on the host and passed in Args.
+struct Plan {
+    int rb_gu, sb_gu, rb_d, sb_d;  // bytes per row: codes / scales of gate||up and down
+    int C;                         // chunks of 32 along H
+    int xsw_stride;                // C + 1 (padding keeps the interleaved copy conflict-free)
+    int uB;                        // bytes of one phase-B unit (gate+up row codes and scales)
+    int chB;                       // phase-B units per ring buffer
+    int gC;                        // bytes of one group's phase-C rows
+    int chC;                       // groups per phase-C ring buffer
+    int sC;                        // bytes of the shared expert's phase-C rows
+    int off_xsw, off_part, off_xown, off_ab, off_c;  // byte offsets in dynamic shared memory
+    int regAB, regC;
+};
+
+// Balanced contiguous split of n items over the grid.
+__device__ __forceinline__ void split_range(int n, int c, int G, int &lo, int &hi)
 {
-    int lane = lane_id();
-    int gw = blockIdx.x * kWarps + warp_id(), nw = gridDim.x * kWarps;
+    lo = (int)((int64_t)n * c / G);
+    hi = (int)((int64_t)n * (c + 1) / G);
+}
+
+// Phase A units: router rows [0, E) then shared gate/up row pairs [E, E+Is).
+__device__ void issue_a(const Args &a, const Plan &P, const Layer &L, char *ab)
+{
+    int lo, hi;
+    split_range(a.E + (L.swg ? a.Is : 0), blockIdx.x, gridDim.x, lo, hi);
+    int r0 = min(lo, a.E), r1 = min(hi, a.E);
+    uint32_t rbytes = (uint32_t)(r1 - r0) * a.H * 4u;
+    if (r1 > r0) copy_range(ab, L.w_router + (int64_t)r0 * a.H, rbytes);
+    int q0 = max(lo, a.E) - a.E, q1 = max(hi, a.E) - a.E;
+    if (q1 > q0) {
+        uint32_t qb = (uint32_t)(q1 - q0) * a.H * 2u;
+        copy_range(ab + rbytes, L.swg + (int64_t)q0 * a.H, qb);
+        copy_range(ab + rbytes + qb, L.swu + (int64_t)q0 * a.H, qb);
+    }
+    commit();
+}
+
+// Phase C shared-expert rows [o0, o0+nrows) of Wd_s.
+__device__ void issue_cs(const Args &a, const Plan &P, const Layer &L, char *cregion, int o0, int nrows)
+{
+    if (L.swg && nrows > 0) copy_range(cregion, L.swd + (int64_t)o0 * a.Is, (uint32_t)nrows * a.Is * 2u);
+    commit();
+}
+
+template <int T>
+__device__ void phase_a(const Args &a, const Plan &P, const Layer &L, const float *xs, const char *ab)
+{
+    int lane = lane_id(), warp = warp_id();
+    int lo, hi;
+    split_range(a.E + (L.swg ? a.Is : 0), blockIdx.x, gridDim.x, lo, hi);
     int H = a.H;
-    int units = a.E + (L.swg ? a.Is : 0);
-    for (int u = gw; u < units; u += nw) {
+    int r1 = min(hi, a.E), r0 = min(lo, a.E);
+    const char *qbase = ab + (size_t)(r1 - r0) * H * 4;
+    int nq = max(hi, a.E) - max(lo, a.E);
+    for (int u = lo + warp; u < hi; u += kWarps) {
         if (u < a.E) {
-            const float4 *wr = reinterpret_cast<const float4 *>(L.w_router + (int64_t)u * H);
+            const float4 *wr = reinterpret_cast<const float4 *>(ab + (size_t)(u - r0) * H * 4);
             float acc[T];
 #pragma unroll
             for (int t = 0; t < T; t++) acc[t] = 0.f;
-            int n4 = H >> 2;
-#pragma unroll 8
-            for (int c = lane; c < n4; c += 32) {
-                float4 w = __ldg(wr + c);
+#pragma unroll 4
+            for (int c = lane; c < (H >> 2); c += 32) {
+                float4 w = wr[c];
 #pragma unroll
                 for (int t = 0; t < T; t++) {
                     float4 xv = *reinterpret_cast<const float4 *>(xs + t * H + 4 * c);
@@ -404,16 +513,16 @@ __device__ void phase_a(const Args &a, const Layer &L, const float *xs)
                 if (lane == 0) a.logits[t * a.E + u] = s + b;
             }
         } else {
+            int q = u - max(lo, a.E);
             int r = u - a.E;
-            const uint4 *wg = reinterpret_cast<const uint4 *>(L.swg + (int64_t)r * H);
-            const uint4 *wu = reinterpret_cast<const uint4 *>(L.swu + (int64_t)r * H);
+            const uint4 *wg = reinterpret_cast<const uint4 *>(qbase + (size_t)q * H * 2);
+            const uint4 *wu = reinterpret_cast<const uint4 *>(qbase + (size_t)(nq + q) * H * 2);
             float g[T], uu[T];
 #pragma unroll
             for (int t = 0; t < T; t++) g[t] = uu[t] = 0.f;
-            int n8 = H >> 3;
-#pragma unroll 4
-            for (int c = lane; c < n8; c += 32) {
-                uint4 qg = __ldg(wg + c), qu = __ldg(wu + c);
+#pragma unroll 2
+            for (int c = lane; c < (H >> 3); c += 32) {
+                uint4 qg = wg[c], qu = wu[c];
                 uint32_t G[4] = {qg.x, qg.y, qg.z, qg.w}, U[4] = {qu.x, qu.y, qu.z, qu.w};
 #pragma unroll
                 for (int t = 0; t < T; t++) {
@@ -438,271 +547,322 @@ __device__ void phase_a(const Args &a, const Layer &L, const float *xs)
     }
 }
 
-// ------------------------------------------------------------ phase B
-// Routed gate/up.  A team of `team` warps shares each row (team = ceil(H/1024)
-// so that one 32-weight chunk per lane covers the row); units (group, row r)
-// are handed out in contiguous ranges per team, in batches of one group.
+// Phase-B chunk list: the CTA's range of (group, row) units cut at group
+// boundaries and at chB units.
+__device__ void plan_b(const Args &a, const Plan &P, Routing &R)
+{
+    if (threadIdx.x != 0) return;
+    int lo, hi;
+    split_range(R.ngroups * a.I, blockIdx.x, gridDim.x, lo, hi);
+    int n = 0;
+    for (int u = lo; u < hi && n < kMaxChunks;) {
+        int g = u / a.I, r = u % a.I;
+        int nr = min(P.chB, min(hi - u, a.I - r));
+        R.b_g[n] = g;
+        R.b_r[n] = r;
+        R.b_n[n] = nr;
+        n++;
+        u += nr;
+    }
+    R.nb = n;
+    int covered = n ? (R.b_g[n - 1] * a.I + R.b_r[n - 1] + R.b_n[n - 1]) : lo;
+    int nc = 0, gdone = 0;
+    for (int g = 0; g < R.ngroups && nc < kMaxChunks; g += P.chC) {
+        R.c_g[nc] = g;
+        R.c_n[nc] = min(P.chC, R.ngroups - g);
+        gdone = g + R.c_n[nc];
+        nc++;
+    }
+    R.nc = nc;
+    if (covered < hi || gdone < R.ngroups) set_status(a.status, MOE_ERR_UNSUPPORTED);  // never drop work silently
+}
+
+template <int BITS>
+__device__ void issue_b(const Args &a, const Plan &P, const Layer &L, const Routing &R, int i, char *ab)
+{
+    char *buf = ab + (size_t)(i & 1) * (P.regAB / 2);
+    int e = R.g_e[R.b_g[i]], r = R.b_r[i], nr = R.b_n[i];
+    const uint8_t *codes = L.gu_codes + (int64_t)e * 2 * a.I * P.rb_gu;
+    const char *scales = reinterpret_cast<const char *>(L.gu_scales) + (int64_t)e * 2 * a.I * P.sb_gu;
+    uint32_t cb = (uint32_t)nr * P.rb_gu, sb = (uint32_t)nr * P.sb_gu;
+    copy_range(buf, codes + (int64_t)r * P.rb_gu, cb);
+    copy_range(buf + cb, codes + (int64_t)(a.I + r) * P.rb_gu, cb);
+    copy_range(buf + 2 * cb, scales + (int64_t)r * P.sb_gu, sb);
+    copy_range(buf + 2 * cb + sb, scales + (int64_t)(a.I + r) * P.sb_gu, sb);
+    commit();
+}
+
+template <int BITS>
+__device__ void issue_cr(const Args &a, const Plan &P, const Layer &L, const Routing &R, int j, char *cregion,
+                         int o0, int nrows)
+{
+    char *buf = cregion + P.sC + (size_t)(j & 1) * P.chC * P.gC;
+    if (nrows > 0) {
+        for (int q = 0; q < R.c_n[j]; q++) {
+            int e = R.g_e[R.c_g[j] + q];
+            const uint8_t *codes = L.d_codes + (int64_t)e * a.H * P.rb_d + (int64_t)o0 * P.rb_d;
+            const char *scales = reinterpret_cast<const char *>(L.d_scales) + (int64_t)e * a.H * P.sb_d + (int64_t)o0 * P.sb_d;
+            char *d = buf + (size_t)q * P.gC;
+            copy_range(d, codes, (uint32_t)nrows * P.rb_d);
+            copy_range(d + (size_t)nrows * P.rb_d, scales, (uint32_t)nrows * P.sb_d);
+        }
+    }
+    commit();
+}
+
+// Phase B on one chunk in shared memory: rows r..r+nr of group g, gate and up.
+// A team of `team` warps shares each row (one 32-weight chunk per lane).
 template <int T, int BITS>
-__device__ void phase_b(const Args &a, const Layer &L, const float *xsw, Routing &R)
+__device__ void phase_b_chunk(const Args &a, const Plan &P, const float *xsw, Routing &R, int i, const char *ab,
+                              float (&v)[T][32], float (&X)[T], int &cur_g)
 {
     int lane = lane_id(), warp = warp_id();
-    int H = a.H, I = a.I;
-    int C = H / 32;
-    int team = (C + 31) / 32;
-    int kw = warp % team;
-    int teams_per_cta = kWarps / team;
-    int tid_team = warp / team;
-    int gteam = blockIdx.x * teams_per_cta + tid_team, nteams = gridDim.x * teams_per_cta;
+    int team = (P.C + 31) / 32;
+    int kw = warp % team, tid_team = warp / team, nteams = kWarps / team;
     int chunk = kw * 32 + lane;
-    bool active = chunk < C;
-    int64_t rb = BITS == 2 ? H / 4 : H / 4 + H / 8;
-    int64_t expert_codes = 2LL * I * rb, expert_scales = 2LL * I * (H / 32);
-    int total = R.ngroups * I;
-    int per = (total + nteams - 1) / nteams;
-    int u0 = gteam * per, u1 = min(total, u0 + per);
+    bool active = chunk < P.C;
+    const char *buf = ab + (size_t)(i & 1) * (P.regAB / 2);
+    int g = R.b_g[i], r0 = R.b_r[i], nr = R.b_n[i];
+    int n = R.g_n[g], p0 = R.g_p0[g];
+    if (g != cur_g) {
+        cur_g = g;
+#pragma unroll
+        for (int t = 0; t < T; t++) {
+            X[t] = 0.f;
+            int tok = t < n ? R.perm[p0 + t] / a.k : 0;
+            const float *xb = xsw + tok * 32 * P.xsw_stride + chunk;
+#pragma unroll
+            for (int q = 0; q < 32; q++) v[t][q] = (active && t < n) ? xb[q * P.xsw_stride] : 0.f;
+#pragma unroll
+            for (int q = 0; q < 32; q++) X[t] += v[t][q];
+        }
+    }
+    const uint8_t *gc = reinterpret_cast<const uint8_t *>(buf);
+    const uint8_t *uc = gc + (size_t)nr * P.rb_gu;
+    const uint16_t *gs = reinterpret_cast<const uint16_t *>(uc + (size_t)nr * P.rb_gu);
+    const uint16_t *us = gs + (size_t)nr * (P.sb_gu / 2);
     int bar_id = 1 + tid_team;
-    int cur_g = -1;
-    float v[T][32];
-    float X[T];
-    for (int u = u0; u < u1;) {
-        int g = u / I;
-        int r0 = u % I;
-        int nb = min(kRB, min(u1 - u, I - r0));  // stay inside one group
-        int n = R.g_n[g], p0 = R.g_p0[g], e = R.g_e[g];
-        if (g != cur_g) {
-            cur_g = g;
+    for (int u0 = tid_team * kRB; u0 < nr; u0 += nteams * kRB) {
+        int nbt = min(kRB, nr - u0);
+#pragma unroll
+        for (int b = 0; b < kRB; b++) {
+            if (b >= nbt) break;
+            int row = u0 + b;
+            float pg[T], pu[T];
+#pragma unroll
+            for (int t = 0; t < T; t++) pg[t] = pu[t] = 0.f;
+            if (active) {
+                QChunk cg = qload_s<BITS>(gc + (size_t)row * P.rb_gu, gs + (size_t)row * (P.sb_gu / 2), a.H, chunk);
+                QChunk cu = qload_s<BITS>(uc + (size_t)row * P.rb_gu, us + (size_t)row * (P.sb_gu / 2), a.H, chunk);
+                qdot<T, BITS>(cg, v, X, pg);
+                qdot<T, BITS>(cu, v, X, pu);
+            }
 #pragma unroll
             for (int t = 0; t < T; t++) {
-                X[t] = 0.f;
-                int tok = t < n ? R.perm[p0 + t] / a.k : 0;
-#pragma unroll
-                for (int i = 0; i < 32; i++) v[t][i] = (active && t < n) ? xsw[tok * H + i * C + chunk] : 0.f;
-#pragma unroll
-                for (int i = 0; i < 32; i++) X[t] += v[t][i];
-            }
-        }
-        const uint8_t *codes = L.gu_codes + (int64_t)e * expert_codes;
-        const uint16_t *scales = L.gu_scales + (int64_t)e * expert_scales;
-        QChunk c[kRB][2];
-#pragma unroll
-        for (int b = 0; b < kRB; b++) {
-            if (b < nb && active) {
-                int r = r0 + b;
-                c[b][0] = qload<BITS>(codes + (int64_t)r * rb, scales + (int64_t)r * (H / 32), H, chunk);
-                c[b][1] = qload<BITS>(codes + (int64_t)(I + r) * rb, scales + (int64_t)(I + r) * (H / 32), H, chunk);
-            }
-        }
-#pragma unroll
-        for (int b = 0; b < kRB; b++) {
-            if (b >= nb) break;
-#pragma unroll
-            for (int m = 0; m < 2; m++) {
-                float p[T];
-#pragma unroll
-                for (int t = 0; t < T; t++) p[t] = 0.f;
-                if (active) qdot<T, BITS>(c[b][m], v, X, p);
-#pragma unroll
-                for (int t = 0; t < T; t++) {
-                    float s = warp_sum(p[t]);
-                    if (lane == 0) R.team[warp][b][m][t] = s;
+                float sg = warp_sum(pg[t]), su = warp_sum(pu[t]);
+                if (lane == 0) {
+                    R.team[warp][b][0][t] = sg;
+                    R.team[warp][b][1][t] = su;
                 }
             }
         }
         if (team > 1) asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(team * 32) : "memory");
         else __syncwarp();
-        if (kw == 0 && lane < nb * T) {
+        if (kw == 0 && lane < nbt * T) {
             int b = lane / T, t = lane % T;
             if (t < n) {
-                float gs = 0.f, us = 0.f;
+                float sg = 0.f, su = 0.f;
                 for (int q = 0; q < team; q++) {
-                    gs += R.team[warp + q][b][0][t];
-                    us += R.team[warp + q][b][1][t];
+                    sg += R.team[warp + q][b][0][t];
+                    su += R.team[warp + q][b][1][t];
                 }
-                a.h[(int64_t)(p0 + t) * I + r0 + b] = silu(gs) * us;
+                a.h[(int64_t)(p0 + t) * a.I + r0 + u0 + b] = silu(sg) * su;
             }
         }
         if (team > 1) asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(team * 32) : "memory");
         else __syncwarp();
-        u += nb;
     }
 }
 
-// ------------------------------------------------------------ phase C
-// Down projections for this CTA's output rows.  Items are (unit, block of
-// kRowBlock rows); unit g < ngroups is a routed group (its pairs' h in
-// registers), unit ngroups is the shared expert (all tokens' h_s).
+// Phase C for one chunk of routed groups (weights in shared memory): each
+// warp takes whole groups, keeps their h in registers and runs all rows.
 template <int T, int BITS>
-__device__ void phase_c(const Args &a, const Layer &L, Routing &R, float *part, int o0, int nrows)
+__device__ void phase_c_chunk(const Args &a, const Plan &P, Routing &R, int j, const char *cregion, float *part,
+                              int nrows)
 {
     int lane = lane_id(), warp = warp_id();
-    int H = a.H, I = a.I;
-    int np = a.T * a.k;
-    int pstride = np + a.T;
-    int units = R.ngroups + (L.swg ? 1 : 0);
-    int nblk = (nrows + kRowBlock - 1) / kRowBlock;
-    int64_t rb = BITS == 2 ? I / 4 : I / 4 + I / 8;
-    int64_t expert_codes = (int64_t)H * rb, expert_scales = (int64_t)H * (I / 32);
-    for (int it = warp; it < units * nblk; it += kWarps) {
-        int unit = it / nblk, blk = it % nblk;
-        int rr0 = blk * kRowBlock, rr1 = min(nrows, rr0 + kRowBlock);
+    int np = a.T * a.k, pstride = np + a.T;
+    const char *buf = cregion + P.sC + (size_t)(j & 1) * P.chC * P.gC;
+    bool active = lane < a.I / 32;
+    for (int q = warp; q < R.c_n[j]; q += kWarps) {
+        int g = R.c_g[j] + q;
+        int n = R.g_n[g], p0 = R.g_p0[g];
         float v[T][32];
         float X[T];
-        if (unit < R.ngroups) {
-            int n = R.g_n[unit], p0 = R.g_p0[unit], e = R.g_e[unit];
-            bool active = lane < I / 32;
+#pragma unroll
+        for (int t = 0; t < T; t++) {
+            X[t] = 0.f;
+            if (active && t < n) {
+                const float4 *hp = reinterpret_cast<const float4 *>(a.h + (int64_t)(p0 + t) * a.I + 32 * lane);
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    float4 f = __ldcg(hp + i);
+                    v[t][4 * i] = f.x; v[t][4 * i + 1] = f.y; v[t][4 * i + 2] = f.z; v[t][4 * i + 3] = f.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; i++) v[t][i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; i++) X[t] += v[t][i];
+        }
+        const uint8_t *codes = reinterpret_cast<const uint8_t *>(buf + (size_t)q * P.gC);
+        const uint16_t *scales = reinterpret_cast<const uint16_t *>(codes + (size_t)nrows * P.rb_d);
+        for (int rr = 0; rr < nrows; rr++) {
+            float p[T];
+#pragma unroll
+            for (int t = 0; t < T; t++) p[t] = 0.f;
+            if (active) {
+                QChunk c = qload_s<BITS>(codes + (size_t)rr * P.rb_d, scales + (size_t)rr * (P.sb_d / 2), a.I, lane);
+                qdot<T, BITS>(c, v, X, p);
+            }
 #pragma unroll
             for (int t = 0; t < T; t++) {
-                X[t] = 0.f;
-                if (active && t < n) {
-                    const float4 *hp = reinterpret_cast<const float4 *>(a.h + (int64_t)(p0 + t) * I + 32 * lane);
-#pragma unroll
-                    for (int q = 0; q < 8; q++) {
-                        float4 f = __ldcg(hp + q);
-                        v[t][4 * q] = f.x; v[t][4 * q + 1] = f.y; v[t][4 * q + 2] = f.z; v[t][4 * q + 3] = f.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; i++) v[t][i] = 0.f;
-                }
-#pragma unroll
-                for (int i = 0; i < 32; i++) X[t] += v[t][i];
-            }
-            const uint8_t *codes = L.d_codes + (int64_t)e * expert_codes;
-            const uint16_t *scales = L.d_scales + (int64_t)e * expert_scales;
-            QChunk c[kRowBlock];
-#pragma unroll
-            for (int b = 0; b < kRowBlock; b++)
-                if (rr0 + b < rr1 && active) {
-                    int o = o0 + rr0 + b;
-                    c[b] = qload<BITS>(codes + (int64_t)o * rb, scales + (int64_t)o * (I / 32), I, lane);
-                }
-#pragma unroll
-            for (int b = 0; b < kRowBlock; b++) {
-                if (rr0 + b >= rr1) break;
-                float p[T];
-#pragma unroll
-                for (int t = 0; t < T; t++) p[t] = 0.f;
-                if (active) qdot<T, BITS>(c[b], v, X, p);
-#pragma unroll
-                for (int t = 0; t < T; t++) {
-                    float s = warp_sum(p[t]);
-                    if (lane == 0 && t < n) part[(rr0 + b) * pstride + p0 + t] = s;
-                }
-            }
-        } else {
-            int Is = a.Is;
-            bool active = lane < Is / 32;
-#pragma unroll
-            for (int t = 0; t < T; t++) {
-                if (active) {
-                    const float4 *hp = reinterpret_cast<const float4 *>(a.hs + (int64_t)t * Is + 32 * lane);
-#pragma unroll
-                    for (int q = 0; q < 8; q++) {
-                        float4 f = __ldcg(hp + q);
-                        v[t][4 * q] = f.x; v[t][4 * q + 1] = f.y; v[t][4 * q + 2] = f.z; v[t][4 * q + 3] = f.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; i++) v[t][i] = 0.f;
-                }
-            }
-            for (int b0 = rr0; b0 < rr1; b0 += 2) {
-                uint4 q[2][4];
-#pragma unroll
-                for (int b = 0; b < 2; b++)
-                    if (b0 + b < rr1 && active) {
-                        const uint4 *wp = reinterpret_cast<const uint4 *>(L.swd + (int64_t)(o0 + b0 + b) * Is + 32 * lane);
-#pragma unroll
-                        for (int j = 0; j < 4; j++) q[b][j] = __ldg(wp + j);
-                    }
-#pragma unroll
-                for (int b = 0; b < 2; b++) {
-                    if (b0 + b >= rr1) break;
-                    float p[T];
-#pragma unroll
-                    for (int t = 0; t < T; t++) p[t] = 0.f;
-                    if (active) {
-#pragma unroll
-                        for (int j = 0; j < 4; j++) {
-                            uint32_t w4[4] = {q[b][j].x, q[b][j].y, q[b][j].z, q[b][j].w};
-#pragma unroll
-                            for (int i = 0; i < 4; i++) {
-                                float lo = __uint_as_float(w4[i] << 16), hi = __uint_as_float(w4[i] & 0xffff0000u);
-#pragma unroll
-                                for (int t = 0; t < T; t++) {
-                                    p[t] = fmaf(lo, v[t][8 * j + 2 * i], p[t]);
-                                    p[t] = fmaf(hi, v[t][8 * j + 2 * i + 1], p[t]);
-                                }
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int t = 0; t < T; t++) {
-                        float s = warp_sum(p[t]);
-                        if (lane == 0) part[(b0 + b) * pstride + np + t] = s;
-                    }
-                }
+                float s = warp_sum(p[t]);
+                if (lane == 0 && t < n) part[rr * pstride + p0 + t] = s;
             }
         }
     }
 }
 
-template <int T, int BITS>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ Args a)
+// Phase C for the shared expert: rows of Wd_s in shared memory, h_s from L2.
+template <int T>
+__device__ void phase_c_shared(const Args &a, const Plan &P, const char *cregion, float *part, int nrows)
 {
-    extern __shared__ __align__(16) float dyn[];
+    int lane = lane_id(), warp = warp_id();
+    int np = a.T * a.k, pstride = np + a.T;
+    int Is = a.Is;
+    bool active = lane < Is / 32;
+    float v[T][32];
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        if (active) {
+            const float4 *hp = reinterpret_cast<const float4 *>(a.hs + (int64_t)t * Is + 32 * lane);
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                float4 f = __ldcg(hp + i);
+                v[t][4 * i] = f.x; v[t][4 * i + 1] = f.y; v[t][4 * i + 2] = f.z; v[t][4 * i + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; i++) v[t][i] = 0.f;
+        }
+    }
+    for (int rr = warp; rr < nrows; rr += kWarps) {
+        float p[T];
+#pragma unroll
+        for (int t = 0; t < T; t++) p[t] = 0.f;
+        if (active) {
+            const uint4 *wp = reinterpret_cast<const uint4 *>(cregion + (size_t)rr * Is * 2) + 4 * lane;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                uint4 q = wp[j];
+                uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    float lo = __uint_as_float(w4[i] << 16), hi = __uint_as_float(w4[i] & 0xffff0000u);
+#pragma unroll
+                    for (int t = 0; t < T; t++) {
+                        p[t] = fmaf(lo, v[t][8 * j + 2 * i], p[t]);
+                        p[t] = fmaf(hi, v[t][8 * j + 2 * i + 1], p[t]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < T; t++) {
+            float s = warp_sum(p[t]);
+            if (lane == 0) part[rr * pstride + np + t] = s;
+        }
+    }
+}
+
+template <int T, int BITS>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ Args a, const __grid_constant__ Plan P)
+{
+    extern __shared__ __align__(128) char dyn[];
     __shared__ Routing R;
-    float *xs = dyn;                    // [T][H] bf16(x) as fp32
-    float *xsw = dyn + T * a.H;         // [T][32][H/32]: the same, chunk-interleaved for phase B
-    float *part = dyn + 2 * T * a.H;    // [rows_per_cta][T*k + T]
-    int C = a.H / 32;
+    float *xs = reinterpret_cast<float *>(dyn);                 // [T][H] layer input as fp32
+    float *xsw = reinterpret_cast<float *>(dyn + P.off_xsw);    // [T][32][C+1] the same, chunk-interleaved
+    float *part = reinterpret_cast<float *>(dyn + P.off_part);  // [rows][T*k + T]
+    float *xown = reinterpret_cast<float *>(dyn + P.off_xown);  // [T][rows] this CTA's rows of x
+    char *ab = dyn + P.off_ab;                                  // phase A data / phase B ring
+    char *cregion = dyn + P.off_c;                              // phase C shared rows + ring
     int o0 = blockIdx.x * a.rows_per_cta;
     int nrows = max(0, min(a.H, o0 + a.rows_per_cta) - o0);
-    int np = T * a.k;
+    int np = T * a.k, pstride = np + T;
+    int H = a.H;
     unsigned nbar = 0;
+    int ncommit = 0;
+    for (int i = threadIdx.x; i < T * nrows; i += kThreads) {
+        int t = i / nrows, rr = i % nrows;
+        xown[t * nrows + rr] = __ldcg(a.x + (int64_t)t * H + o0 + rr);
+    }
+    issue_a(a, P, a.L[0], ab);
+    int gi_a = ncommit++;
+    issue_cs(a, P, a.L[0], cregion, o0, nrows);
+    int gi_cs = ncommit++;
     for (int l = 0; l < a.n_layers; l++) {
         const Layer &L = a.L[l];
-        // layer input: bf16(x / rms(x)) (or bf16(x)), as fp32 in shared memory.
-        // Per-token sum of squares in a fixed order: strided per thread, a warp
-        // tree, then the warps in order (independent of the other tokens).
-        if (a.rms_eps >= 0.f) {
-            for (int t = 0; t < T; t++) {
-                float ss = 0.f;
-                for (int i = threadIdx.x; i < a.H; i += kThreads) {
-                    float v = __ldcg(a.x + (int64_t)t * a.H + i);
-                    ss = fmaf(v, v, ss);
-                }
-                ss = warp_sum(ss);
-                if (lane_id() == 0) R.wsum[t][warp_id()] = ss;
+        // -- layer input: bf16(x / rms(x)) per token; sums of squares in a fixed order
+        for (int t = 0; t < T; t++) {
+            float ss = 0.f;
+            const float4 *xp = reinterpret_cast<const float4 *>(a.x + (int64_t)t * H);
+            for (int i = threadIdx.x; i < (H >> 2); i += kThreads) {
+                float4 v = __ldcg(xp + i);
+                ss = fmaf(v.x, v.x, ss);
+                ss = fmaf(v.y, v.y, ss);
+                ss = fmaf(v.z, v.z, ss);
+                ss = fmaf(v.w, v.w, ss);
             }
-            __syncthreads();
-            if (threadIdx.x < T) {
+            ss = warp_sum(ss);
+            if (lane_id() == 0) R.wsum[t][warp_id()] = ss;
+        }
+        __syncthreads();
+        if (threadIdx.x < T) {
+            float inv = 1.0f;
+            if (a.rms_eps >= 0.f) {
                 float tot = 0.f;
                 for (int w = 0; w < kWarps; w++) tot += R.wsum[threadIdx.x][w];
-                R.inv_rms[threadIdx.x] = 1.0f / sqrtf(tot / (float)a.H + a.rms_eps);
+                inv = 1.0f / sqrtf(tot / (float)H + a.rms_eps);
             }
-            __syncthreads();
-        } else if (threadIdx.x < T) {
-            R.inv_rms[threadIdx.x] = 1.0f;
+            R.inv_rms[threadIdx.x] = inv;
         }
         __syncthreads();
-        for (int i = threadIdx.x; i < T * a.H; i += kThreads) {
-            float v = bf16_round(__ldcg(a.x + i) * R.inv_rms[i / a.H]);
-            int t = i / a.H, r = i - t * a.H;
-            xs[i] = v;
-            xsw[t * a.H + (r & 31) * C + (r >> 5)] = v;
+        for (int i = threadIdx.x; i < T * (H >> 2); i += kThreads) {
+            int t = i / (H >> 2), c4 = i % (H >> 2);
+            float4 v = __ldcg(reinterpret_cast<const float4 *>(a.x + (int64_t)t * H) + c4);
+            float inv = R.inv_rms[t];
+            float4 o = make_float4(bf16_round(v.x * inv), bf16_round(v.y * inv), bf16_round(v.z * inv),
+                                   bf16_round(v.w * inv));
+            reinterpret_cast<float4 *>(xs + t * H)[c4] = o;
+            int r = 4 * c4;
+            float *dst = xsw + t * 32 * P.xsw_stride;
+            dst[((r + 0) & 31) * P.xsw_stride + ((r + 0) >> 5)] = o.x;
+            dst[((r + 1) & 31) * P.xsw_stride + ((r + 1) >> 5)] = o.y;
+            dst[((r + 2) & 31) * P.xsw_stride + ((r + 2) >> 5)] = o.z;
+            dst[((r + 3) & 31) * P.xsw_stride + ((r + 3) >> 5)] = o.w;
         }
+        // -- phase A from the prefetched rows
+        wait_group_index(gi_a, ncommit);
         __syncthreads();
-        phase_a<T>(a, L, xs);
-        if (!grid_barrier(a, R, ++nbar)) return;
-        // routing, redundantly in every CTA
+        phase_a<T>(a, P, L, xs, ab);
+        if (!grid_barrier(a, R, ++nbar)) { wait_all_copies(); return; }
+        // -- routing, redundantly in every CTA
         int w = warp_id();
-        bool nan_token = false;
         if (w < T) {
-            topk_warp(a.logits + w * a.E, a.E, a.k, R, w, a.status);
-            nan_token = false;
-            for (int e = lane_id(); e < a.E; e += 32) nan_token |= isnan(__ldcg(a.logits + w * a.E + e));
-            nan_token = __any_sync(0xffffffffu, nan_token);
+            bool nan_token = topk_warp(a.logits + w * a.E, a.E, a.k, R, w);
+            if (nan_token && lane_id() == 0) set_status(a.status, MOE_ERR_NONFINITE);
             topk_weights(R, w, a.k, nan_token);
         }
         __syncthreads();
@@ -712,37 +872,92 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             a.ids_out[(int64_t)l * np + threadIdx.x] = R.ids[threadIdx.x];
             a.w_out[(int64_t)l * np + threadIdx.x] = R.w[threadIdx.x];
         }
-        phase_b<T, BITS>(a, L, xsw, R);
-        if (!grid_barrier(a, R, ++nbar)) return;
-        phase_c<T, BITS>(a, L, R, part, o0, nrows);
+        plan_b(a, P, R);
         __syncthreads();
-        int pstride = np + T;
+        // -- prefetch phase B chunks 0,1 and phase C routed chunks 0,1
+        int gi_b[2] = {-1, -1}, gi_c[2] = {-1, -1};
+        for (int i = 0; i < 2 && i < R.nb; i++) {
+            issue_b<BITS>(a, P, L, R, i, ab);
+            gi_b[i] = ncommit++;
+        }
+        for (int j = 0; j < 2 && j < R.nc; j++) {
+            issue_cr<BITS>(a, P, L, R, j, cregion, o0, nrows);
+            gi_c[j] = ncommit++;
+        }
+        // -- phase B
+        {
+            float v[T][32];
+            float X[T];
+            int cur_g = -1;
+            for (int i = 0; i < R.nb; i++) {
+                wait_group_index(gi_b[i & 1], ncommit);
+                __syncthreads();
+                phase_b_chunk<T, BITS>(a, P, xsw, R, i, ab, v, X, cur_g);
+                __syncthreads();
+                if (i + 2 < R.nb) {
+                    issue_b<BITS>(a, P, L, R, i + 2, ab);
+                    gi_b[i & 1] = ncommit++;
+                }
+            }
+        }
+        // -- prefetch the next layer's phase A rows (the ring is free now)
+        if (l + 1 < a.n_layers) {
+            issue_a(a, P, a.L[l + 1], ab);
+            gi_a = ncommit++;
+        }
+        if (!grid_barrier(a, R, ++nbar)) { wait_all_copies(); return; }
+        // -- phase C
+        wait_group_index(gi_cs, ncommit);
+        __syncthreads();
+        if (L.swg) phase_c_shared<T>(a, P, cregion, part, nrows);
+        for (int j = 0; j < R.nc; j++) {
+            wait_group_index(gi_c[j & 1], ncommit);
+            __syncthreads();
+            phase_c_chunk<T, BITS>(a, P, R, j, cregion, part, nrows);
+            __syncthreads();
+            if (j + 2 < R.nc) {
+                issue_cr<BITS>(a, P, L, R, j + 2, cregion, o0, nrows);
+                gi_c[j & 1] = ncommit++;
+            }
+        }
+        __syncthreads();
         for (int i = threadIdx.x; i < nrows * T; i += kThreads) {
             int rr = i / T, t = i % T;
             float s = 0.f;
             for (int j = 0; j < a.k; j++) s = fmaf(R.w[t * a.k + j], part[rr * pstride + R.inv[t * a.k + j]], s);
             if (L.swg) s += part[rr * pstride + np + t];
-            float *xp = a.x + (int64_t)t * a.H + o0 + rr;
-            *xp = __ldcg(xp) + s;
+            float nx = xown[t * nrows + rr] + s;
+            xown[t * nrows + rr] = nx;
+            a.x[(int64_t)t * H + o0 + rr] = nx;
         }
-        if (!grid_barrier(a, R, ++nbar)) return;
+        __syncthreads();
+        if (l + 1 < a.n_layers) {
+            issue_cs(a, P, a.L[l + 1], cregion, o0, nrows);
+            gi_cs = ncommit++;
+        }
+        if (!grid_barrier(a, R, ++nbar)) { wait_all_copies(); return; }
     }
+    wait_all_copies();
 }
 
 template <int T, int BITS>
-static cudaError_t launch(const Args &a, int grid, size_t smem, cudaStream_t s)
+static cudaError_t launch(const Args &a, const Plan &P, int grid, size_t smem, cudaStream_t s)
 {
     auto fn = decode_kernel<T, BITS>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    void *args[] = {const_cast<Args *>(&a)};
+    void *args[] = {const_cast<Args *>(&a), const_cast<Plan *>(&P)};
     return cudaLaunchCooperativeKernel((const void *)fn, dim3(grid), dim3(kThreads), args, smem, s);
 }
 
 template <int T, int BITS>
-static cudaError_t occupancy(int *blocks, size_t smem)
+static cudaError_t occupancy(int *blocks, size_t smem, size_t *static_smem)
 {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, decode_kernel<T, BITS>);
+    if (e != cudaSuccess) return e;
+    *static_smem = fa.sharedSizeBytes;
+    e = cudaFuncSetAttribute(decode_kernel<T, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, decode_kernel<T, BITS>, kThreads, smem);
 }
@@ -760,6 +975,48 @@ static Ws ws_layout(int T, int H, int I, int E, int k, int Is)
     w.hs = w.h + align256((size_t)T * k * I * 4);
     w.total = w.hs + align256((size_t)T * std::max(Is, 1) * 4);
     return w;
+}
+
+static size_t al128(size_t n) { return (n + 127) & ~size_t(127); }
+
+// Shared-memory plan; returns false if the shapes do not fit.
+static bool make_plan(Plan &P, int T, int H, int I, int E, int k, int Is, int bits, int grid, int rows_per_cta,
+                      size_t budget)
+{
+    P.rb_gu = bits == 2 ? H / 4 : H / 4 + H / 8;
+    P.sb_gu = H / 16;
+    P.rb_d = bits == 2 ? I / 4 : I / 4 + I / 8;
+    P.sb_d = I / 16;
+    P.C = H / 32;
+    P.xsw_stride = P.C + 1;
+    P.uB = 2 * (P.rb_gu + P.sb_gu);
+    P.gC = (rows_per_cta * (P.rb_d + P.sb_d) + 15) & ~15;  // ring slots stay 16-byte aligned
+    P.sC = (int)al128((size_t)rows_per_cta * Is * 2);
+    int unitsA = (E + Is + grid - 1) / grid;
+    size_t regA = al128((size_t)unitsA * H * 4);
+    size_t fixed = al128((size_t)T * H * 4) + al128((size_t)T * 32 * P.xsw_stride * 4) +
+                   al128((size_t)rows_per_cta * (T * k + T) * 4) + al128((size_t)T * rows_per_cta * 4);
+    if (fixed + regA >= budget) return false;
+    size_t left = budget - fixed;
+    // phase C: shared rows + two ring buffers of up to 8 groups; phase A/B: the rest
+    int chC = 8;
+    while (chC > 1 && (size_t)P.sC + 2 * (size_t)chC * P.gC > left / 3) chC--;
+    size_t regC = al128((size_t)P.sC + 2 * (size_t)chC * P.gC);
+    if (regC + regA > left) return false;
+    size_t regAB = std::max(regA, (size_t)2 * P.uB);
+    regAB = std::min(left - regC, std::max(regAB, (size_t)2 * 32 * P.uB));  // room for 32 units per ring half
+    regAB &= ~size_t(255);
+    if (regAB < regA || regAB < (size_t)2 * P.uB) return false;
+    P.chB = (int)std::min<size_t>((regAB / 2) / P.uB, (size_t)1 << 20);
+    P.chC = chC;
+    P.regAB = (int)regAB;
+    P.regC = (int)regC;
+    P.off_xsw = (int)al128((size_t)T * H * 4);
+    P.off_part = P.off_xsw + (int)al128((size_t)T * 32 * P.xsw_stride * 4);
+    P.off_xown = P.off_part + (int)al128((size_t)rows_per_cta * (T * k + T) * 4);
+    P.off_ab = P.off_xown + (int)al128((size_t)T * rows_per_cta * 4);
+    P.off_c = P.off_ab + P.regAB;
+    return true;
 }
 
 }  // namespace fused
@@ -788,11 +1045,11 @@ extern "C" moe_status moe_decode_forward(const moe_layer_weights *layers, int n_
     const moe_expert_arena &A0 = layers[0].experts;
     int H = A0.H, I = A0.I, E = A0.E, bits = A0.bits, Is = layers[0].shared_I;
     MOE_REQUIRE(bits == 2 || bits == 3, "bits must be 2 or 3 (got %d)", bits);
-    MOE_REQUIRE(H % 32 == 0 && H >= 32 && (H <= 1024 || H == 2048 || H == 4096),
-                "the fused decode takes H a multiple of 32 up to 1024, or 2048 or 4096 (got %d)", H);
-    MOE_REQUIRE(I % 32 == 0 && I >= 32 && I <= 1024, "the fused decode takes I a multiple of 32 up to 1024 (got %d)", I);
+    MOE_REQUIRE(H % 64 == 0 && H >= 64 && (H <= 1024 || H == 2048 || H == 4096),
+                "the fused decode takes H a multiple of 64 up to 1024, or 2048 or 4096 (got %d)", H);
+    MOE_REQUIRE(I % 64 == 0 && I >= 64 && I <= 1024, "the fused decode takes I a multiple of 64 up to 1024 (got %d)", I);
     MOE_REQUIRE(E >= 1 && E <= 1024 && k >= 1 && k <= kMaxK && k <= E, "1 <= k <= min(E, 16), E <= 1024");
-    MOE_REQUIRE(Is >= 0 && Is % 32 == 0 && Is <= 1024, "shared_I must be a multiple of 32 up to 1024 (got %d)", Is);
+    MOE_REQUIRE(Is >= 0 && Is % 64 == 0 && Is <= 1024, "shared_I must be a multiple of 64 up to 1024 (got %d)", Is);
     MOE_REQUIRE(x && aligned16(x), "x must be a 16-byte aligned device pointer");
     MOE_REQUIRE(!ids_out == !w_out, "ids_out and w_out must both be given or both be NULL");
     Args a;
@@ -837,8 +1094,8 @@ extern "C" moe_status moe_decode_forward(const moe_layer_weights *layers, int n_
     a.status = dev_status;
     int grid = sm_count();
     a.rows_per_cta = (H + grid - 1) / grid;
-    size_t smem = (2 * (size_t)T * H + (size_t)a.rows_per_cta * (T * k + T)) * sizeof(float);
     int per_sm = 0;
+    size_t static_smem = 0;
     cudaError_t e = cudaSuccess;
 #define MOE_F_DISPATCH(FN, ...)                                           \
     switch (T * 10 + bits) {                                              \
@@ -851,14 +1108,25 @@ extern "C" moe_status moe_decode_forward(const moe_layer_weights *layers, int n_
     case 42: e = FN<4, 2>(__VA_ARGS__); break;                            \
     default: e = FN<4, 3>(__VA_ARGS__); break;                            \
     }
-    MOE_F_DISPATCH(occupancy, &per_sm, smem)
+    MOE_F_DISPATCH(occupancy, &per_sm, 0, &static_smem)
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "decode kernel attributes: %s", cudaGetErrorString(e));
+    int dev = 0, optin = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    MOE_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+    size_t budget = (size_t)optin > static_smem + 1024 ? (size_t)optin - static_smem - 1024 : 0;
+    Plan P;
+    if (!make_plan(P, T, H, I, E, k, Is, bits, grid, a.rows_per_cta, budget))
+        return fail(MOE_ERR_UNSUPPORTED, "the fused decode's buffers do not fit in %zu bytes of shared memory "
+                    "(T=%d H=%d I=%d E=%d k=%d shared_I=%d)", budget, T, H, I, E, k, Is);
+    size_t smem = (size_t)P.off_c + P.regC;
+    MOE_F_DISPATCH(occupancy, &per_sm, smem, &static_smem)
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "decode occupancy query: %s", cudaGetErrorString(e));
     if (per_sm < 1)
         return fail(MOE_ERR_UNSUPPORTED, "the fused decode kernel does not fit on an SM (%zu bytes of shared memory)",
                     smem);
     cudaStream_t s = to_cuda(stream);
     MOE_CUDA_TRY(cudaMemsetAsync(a.bar, 0, sizeof(unsigned), s));
-    MOE_F_DISPATCH(launch, a, grid, smem, s)
+    MOE_F_DISPATCH(launch, a, P, grid, smem, s)
 #undef MOE_F_DISPATCH
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cooperative launch of the fused decode: %s", cudaGetErrorString(e));
     return MOE_OK;
