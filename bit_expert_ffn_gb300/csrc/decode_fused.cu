@@ -29,8 +29,9 @@ namespace moe {
 namespace fused {
 
 constexpr int kMaxLayers = 64;
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+constexpr int kMaxWarps = 16;  // warps per CTA: 16 for one token, 8 for more
+template <int T>
+__host__ __device__ constexpr int warps_for() { return T == 1 ? 16 : 8; }
 constexpr int kMaxT = 4;
 constexpr int kMaxK = 16;
 constexpr int kMaxPairs = kMaxT * kMaxK;
@@ -76,8 +77,12 @@ struct Routing {
     int cand_i[kMaxT][kMaxCand];
     float sel_v[kMaxT][kMaxK];
     int sel_i[kMaxT][kMaxK];
-    float team[kWarps][kRB][2][kMaxT];  // phase-B partials of each warp
-    float wsum[kMaxT][kWarps];
+    float team[kMaxWarps][kRB][2][kMaxT];  // phase-B partials of each warp
+    float wsum[kMaxT][kMaxWarps];
+    float wmax_v[kMaxWarps];
+    int wmax_i[kMaxWarps];
+    float tau_v;
+    int tau_i, tau_all, ncand;
     float inv_rms[kMaxT];
     int b_g[kMaxChunks], b_r[kMaxChunks], b_n[kMaxChunks], nb;  // phase-B chunks: group, first row, rows
     int c_g[kMaxChunks], c_n[kMaxChunks], nc;                   // phase-C chunks: first group, groups
@@ -183,11 +188,11 @@ __device__ __forceinline__ void copy_range(void *dst, const void *src, uint32_t 
     const char *s = static_cast<const char *>(src);
     uint32_t al = (uint32_t)(reinterpret_cast<uintptr_t>(d) | reinterpret_cast<uintptr_t>(s) | bytes);
     if ((al & 15u) == 0) {
-        for (uint32_t off = threadIdx.x * 16u; off < bytes; off += kThreads * 16u) cp16(d + off, s + off);
+        for (uint32_t off = threadIdx.x * 16u; off < bytes; off += blockDim.x * 16u) cp16(d + off, s + off);
     } else if ((al & 7u) == 0) {
-        for (uint32_t off = threadIdx.x * 8u; off < bytes; off += kThreads * 8u) cp8(d + off, s + off);
+        for (uint32_t off = threadIdx.x * 8u; off < bytes; off += blockDim.x * 8u) cp8(d + off, s + off);
     } else {
-        for (uint32_t off = threadIdx.x * 4u; off < bytes; off += kThreads * 4u) cp4(d + off, s + off);
+        for (uint32_t off = threadIdx.x * 4u; off < bytes; off += blockDim.x * 4u) cp4(d + off, s + off);
     }
 }
 
@@ -284,6 +289,92 @@ __device__ bool topk_warp(const float *__restrict__ l, int E, int k, Routing &R,
         }
     }
     __syncwarp();
+    return false;
+}
+
+// Top-k of a single token's logits by the whole CTA (T = 1).  Each thread
+// holds up to two logits.  With at least k warps holding logits, the k-th
+// best warp maximum bounds the k-th best logit, so only logits at or before
+// it are candidates (otherwise every logit is); candidates are ranked exactly
+// among themselves.  Returns true for a NaN logit.
+__device__ bool topk_block(const float *__restrict__ l, int E, int k, Routing &R)
+{
+    int tid = threadIdx.x, lane = lane_id(), warp = warp_id(), nw = blockDim.x >> 5, nthr = blockDim.x;
+    int e0 = tid, e1 = tid + nthr;
+    bool h0 = e0 < E, h1 = e1 < E;
+    float v0 = h0 ? __ldcg(l + e0) : 0.f, v1 = h1 ? __ldcg(l + e1) : 0.f;
+    bool nan = (h0 && isnan(v0)) || (h1 && isnan(v1));
+    if (__syncthreads_or(nan)) {
+        if (tid < k) {
+            R.sel_i[0][tid] = tid;
+            R.sel_v[0][tid] = 0.f;
+        }
+        __syncthreads();
+        return true;
+    }
+    float mv = 0.f;
+    int mi = INT32_MAX;
+    if (h0) { mv = v0; mi = e0; }
+    if (h1 && (mi == INT32_MAX || before(v1, e1, mv, mi))) { mv = v1; mi = e1; }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, mv, o);
+        int oi = __shfl_xor_sync(0xffffffffu, mi, o);
+        if (oi != INT32_MAX && (mi == INT32_MAX || before(ov, oi, mv, mi))) { mv = ov; mi = oi; }
+    }
+    if (lane == 0) {
+        R.wmax_v[warp] = mv;
+        R.wmax_i[warp] = mi;
+    }
+    if (tid == 0) R.ncand = 0;
+    __syncthreads();
+    if (warp == 0) {
+        float wv = lane < nw ? R.wmax_v[lane] : 0.f;
+        int wi = lane < nw ? R.wmax_i[lane] : INT32_MAX;
+        int r = 0;
+        for (int q = 0; q < nw; q++) {
+            int oi = R.wmax_i[q];
+            if (oi != INT32_MAX && wi != INT32_MAX && before(R.wmax_v[q], oi, wv, wi)) r++;
+        }
+        unsigned valid = __ballot_sync(0xffffffffu, wi != INT32_MAX);
+        unsigned who = __ballot_sync(0xffffffffu, wi != INT32_MAX && r == k - 1);
+        int src = who ? __ffs(who) - 1 : 0;
+        float tv = __shfl_sync(0xffffffffu, wv, src);
+        int ti = __shfl_sync(0xffffffffu, wi, src);
+        if (lane == 0) {
+            R.tau_all = __popc(valid) < k;
+            R.tau_v = tv;
+            R.tau_i = ti;
+        }
+    }
+    __syncthreads();
+    float tv = R.tau_v;
+    int ti = R.tau_i;
+    bool all = R.tau_all;
+    float *cv = &R.cand_v[0][0];
+    int *ci = &R.cand_i[0][0];
+    if (h0 && (all || before(v0, e0, tv, ti) || (v0 == tv && e0 == ti))) {
+        int pos = atomicAdd(&R.ncand, 1);
+        cv[pos] = v0;
+        ci[pos] = e0;
+    }
+    if (h1 && (all || before(v1, e1, tv, ti) || (v1 == tv && e1 == ti))) {
+        int pos = atomicAdd(&R.ncand, 1);
+        cv[pos] = v1;
+        ci[pos] = e1;
+    }
+    __syncthreads();
+    int C = R.ncand;
+    for (int c = tid; c < C; c += nthr) {
+        float x = cv[c];
+        int e = ci[c], r = 0;
+        for (int d = 0; d < C; d++) r += before(cv[d], ci[d], x, e) ? 1 : 0;
+        if (r < k) {
+            R.sel_v[0][r] = x;
+            R.sel_i[0][r] = e;
+        }
+    }
+    __syncthreads();
     return false;
 }
 
@@ -488,7 +579,7 @@ __device__ void phase_a(const Args &a, const Plan &P, const Layer &L, const floa
     int r1 = min(hi, a.E), r0 = min(lo, a.E);
     const char *qbase = ab + (size_t)(r1 - r0) * H * 4;
     int nq = max(hi, a.E) - max(lo, a.E);
-    for (int u = lo + warp; u < hi; u += kWarps) {
+    for (int u = lo + warp; u < hi; u += (int)(blockDim.x >> 5)) {
         if (u < a.E) {
             const float4 *wr = reinterpret_cast<const float4 *>(ab + (size_t)(u - r0) * H * 4);
             float acc[T];
@@ -612,29 +703,32 @@ __device__ void issue_cr(const Args &a, const Plan &P, const Layer &L, const Rou
 
 // Phase B on one chunk in shared memory: rows r..r+nr of group g, gate and up.
 // A team of `team` warps shares each row (one 32-weight chunk per lane).
-template <int T, int BITS>
+template <int T, int BITS, int CPL>
 __device__ void phase_b_chunk(const Args &a, const Plan &P, const float *xsw, Routing &R, int i, const char *ab,
-                              float (&v)[T][32], float (&X)[T], int &cur_g)
+                              float (&v)[CPL][T][32], float (&X)[CPL][T], int &cur_g)
 {
     int lane = lane_id(), warp = warp_id();
-    int team = (P.C + 31) / 32;
-    int kw = warp % team, tid_team = warp / team, nteams = kWarps / team;
-    int chunk = kw * 32 + lane;
-    bool active = chunk < P.C;
+    int team = (P.C + 32 * CPL - 1) / (32 * CPL);
+    int kw = warp % team, tid_team = warp / team, nteams = (int)(blockDim.x >> 5) / team;
     const char *buf = ab + (size_t)(i & 1) * (P.regAB / 2);
     int g = R.b_g[i], r0 = R.b_r[i], nr = R.b_n[i];
     int n = R.g_n[g], p0 = R.g_p0[g];
     if (g != cur_g) {
         cur_g = g;
 #pragma unroll
-        for (int t = 0; t < T; t++) {
-            X[t] = 0.f;
-            int tok = t < n ? R.perm[p0 + t] / a.k : 0;
-            const float *xb = xsw + tok * 32 * P.xsw_stride + chunk;
+        for (int c = 0; c < CPL; c++) {
+            int chunk = (kw + team * c) * 32 + lane;
+            bool active = chunk < P.C;
 #pragma unroll
-            for (int q = 0; q < 32; q++) v[t][q] = (active && t < n) ? xb[q * P.xsw_stride] : 0.f;
+            for (int t = 0; t < T; t++) {
+                X[c][t] = 0.f;
+                int tok = t < n ? R.perm[p0 + t] / a.k : 0;
+                const float *xb = xsw + tok * 32 * P.xsw_stride + chunk;
 #pragma unroll
-            for (int q = 0; q < 32; q++) X[t] += v[t][q];
+                for (int q = 0; q < 32; q++) v[c][t][q] = (active && t < n) ? xb[q * P.xsw_stride] : 0.f;
+#pragma unroll
+                for (int q = 0; q < 32; q++) X[c][t] += v[c][t][q];
+            }
         }
     }
     const uint8_t *gc = reinterpret_cast<const uint8_t *>(buf);
@@ -651,11 +745,15 @@ __device__ void phase_b_chunk(const Args &a, const Plan &P, const float *xsw, Ro
             float pg[T], pu[T];
 #pragma unroll
             for (int t = 0; t < T; t++) pg[t] = pu[t] = 0.f;
-            if (active) {
-                QChunk cg = qload_s<BITS>(gc + (size_t)row * P.rb_gu, gs + (size_t)row * (P.sb_gu / 2), a.H, chunk);
-                QChunk cu = qload_s<BITS>(uc + (size_t)row * P.rb_gu, us + (size_t)row * (P.sb_gu / 2), a.H, chunk);
-                qdot<T, BITS>(cg, v, X, pg);
-                qdot<T, BITS>(cu, v, X, pu);
+#pragma unroll
+            for (int c = 0; c < CPL; c++) {
+                int chunk = (kw + team * c) * 32 + lane;
+                if (chunk < P.C) {
+                    QChunk cg = qload_s<BITS>(gc + (size_t)row * P.rb_gu, gs + (size_t)row * (P.sb_gu / 2), a.H, chunk);
+                    QChunk cu = qload_s<BITS>(uc + (size_t)row * P.rb_gu, us + (size_t)row * (P.sb_gu / 2), a.H, chunk);
+                    qdot<T, BITS>(cg, v[c], X[c], pg);
+                    qdot<T, BITS>(cu, v[c], X[c], pu);
+                }
             }
 #pragma unroll
             for (int t = 0; t < T; t++) {
@@ -694,7 +792,11 @@ __device__ void phase_c_chunk(const Args &a, const Plan &P, Routing &R, int j, c
     int np = a.T * a.k, pstride = np + a.T;
     const char *buf = cregion + P.sC + (size_t)(j & 1) * P.chC * P.gC;
     bool active = lane < a.I / 32;
-    for (int q = warp; q < R.c_n[j]; q += kWarps) {
+    int half = (nrows + 1) / 2;
+    int nw = (int)(blockDim.x >> 5);
+    for (int it = warp; it < 2 * R.c_n[j]; it += nw) {
+        int q = it >> 1;
+        int rr0 = (it & 1) ? half : 0, rr1 = (it & 1) ? nrows : half;
         int g = R.c_g[j] + q;
         int n = R.g_n[g], p0 = R.g_p0[g];
         float v[T][32];
@@ -718,7 +820,7 @@ __device__ void phase_c_chunk(const Args &a, const Plan &P, Routing &R, int j, c
         }
         const uint8_t *codes = reinterpret_cast<const uint8_t *>(buf + (size_t)q * P.gC);
         const uint16_t *scales = reinterpret_cast<const uint16_t *>(codes + (size_t)nrows * P.rb_d);
-        for (int rr = 0; rr < nrows; rr++) {
+        for (int rr = rr0; rr < rr1; rr++) {
             float p[T];
 #pragma unroll
             for (int t = 0; t < T; t++) p[t] = 0.f;
@@ -758,7 +860,7 @@ __device__ void phase_c_shared(const Args &a, const Plan &P, const char *cregion
             for (int i = 0; i < 32; i++) v[t][i] = 0.f;
         }
     }
-    for (int rr = warp; rr < nrows; rr += kWarps) {
+    for (int rr = warp; rr < nrows; rr += (int)(blockDim.x >> 5)) {
         float p[T];
 #pragma unroll
         for (int t = 0; t < T; t++) p[t] = 0.f;
@@ -788,8 +890,13 @@ __device__ void phase_c_shared(const Args &a, const Plan &P, const char *cregion
 }
 
 template <int T, int BITS>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ Args a, const __grid_constant__ Plan P)
+__global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __grid_constant__ Args a,
+                                                                         const __grid_constant__ Plan P)
 {
+    constexpr int NW = warps_for<T>();
+    constexpr int NT = NW * 32;
+    // activations of phase B held per lane: two chunks when they fit, else one chunk and a warp team
+    constexpr int CPL = T == 1 ? 2 : 1;
     extern __shared__ __align__(128) char dyn[];
     __shared__ Routing R;
     float *xs = reinterpret_cast<float *>(dyn);                 // [T][H] layer input as fp32
@@ -804,7 +911,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     int H = a.H;
     unsigned nbar = 0;
     int ncommit = 0;
-    for (int i = threadIdx.x; i < T * nrows; i += kThreads) {
+    for (int i = threadIdx.x; i < T * nrows; i += NT) {
         int t = i / nrows, rr = i % nrows;
         xown[t * nrows + rr] = __ldcg(a.x + (int64_t)t * H + o0 + rr);
     }
@@ -818,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         for (int t = 0; t < T; t++) {
             float ss = 0.f;
             const float4 *xp = reinterpret_cast<const float4 *>(a.x + (int64_t)t * H);
-            for (int i = threadIdx.x; i < (H >> 2); i += kThreads) {
+            for (int i = threadIdx.x; i < (H >> 2); i += NT) {
                 float4 v = __ldcg(xp + i);
                 ss = fmaf(v.x, v.x, ss);
                 ss = fmaf(v.y, v.y, ss);
@@ -833,13 +940,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             float inv = 1.0f;
             if (a.rms_eps >= 0.f) {
                 float tot = 0.f;
-                for (int w = 0; w < kWarps; w++) tot += R.wsum[threadIdx.x][w];
+                for (int w = 0; w < NW; w++) tot += R.wsum[threadIdx.x][w];
                 inv = 1.0f / sqrtf(tot / (float)H + a.rms_eps);
             }
             R.inv_rms[threadIdx.x] = inv;
         }
         __syncthreads();
-        for (int i = threadIdx.x; i < T * (H >> 2); i += kThreads) {
+        for (int i = threadIdx.x; i < T * (H >> 2); i += NT) {
             int t = i / (H >> 2), c4 = i % (H >> 2);
             float4 v = __ldcg(reinterpret_cast<const float4 *>(a.x + (int64_t)t * H) + c4);
             float inv = R.inv_rms[t];
@@ -860,7 +967,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         if (!grid_barrier(a, R, ++nbar)) { wait_all_copies(); return; }
         // -- routing, redundantly in every CTA
         int w = warp_id();
-        if (w < T) {
+        if (T == 1) {
+            bool nan_token = topk_block(a.logits, a.E, a.k, R);
+            if (nan_token && threadIdx.x == 0) set_status(a.status, MOE_ERR_NONFINITE);
+            if (w == 0) topk_weights(R, 0, a.k, nan_token);
+        } else if (w < T) {
             bool nan_token = topk_warp(a.logits + w * a.E, a.E, a.k, R, w);
             if (nan_token && lane_id() == 0) set_status(a.status, MOE_ERR_NONFINITE);
             topk_weights(R, w, a.k, nan_token);
@@ -886,13 +997,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         }
         // -- phase B
         {
-            float v[T][32];
-            float X[T];
+            float v[CPL][T][32];
+            float X[CPL][T];
             int cur_g = -1;
             for (int i = 0; i < R.nb; i++) {
                 wait_group_index(gi_b[i & 1], ncommit);
                 __syncthreads();
-                phase_b_chunk<T, BITS>(a, P, xsw, R, i, ab, v, X, cur_g);
+                phase_b_chunk<T, BITS, CPL>(a, P, xsw, R, i, ab, v, X, cur_g);
                 __syncthreads();
                 if (i + 2 < R.nb) {
                     issue_b<BITS>(a, P, L, R, i + 2, ab);
@@ -921,7 +1032,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             }
         }
         __syncthreads();
-        for (int i = threadIdx.x; i < nrows * T; i += kThreads) {
+        for (int i = threadIdx.x; i < nrows * T; i += NT) {
             int rr = i / T, t = i % T;
             float s = 0.f;
             for (int j = 0; j < a.k; j++) s = fmaf(R.w[t * a.k + j], part[rr * pstride + R.inv[t * a.k + j]], s);
@@ -947,7 +1058,7 @@ static cudaError_t launch(const Args &a, const Plan &P, int grid, size_t smem, c
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     void *args[] = {const_cast<Args *>(&a), const_cast<Plan *>(&P)};
-    return cudaLaunchCooperativeKernel((const void *)fn, dim3(grid), dim3(kThreads), args, smem, s);
+    return cudaLaunchCooperativeKernel((const void *)fn, dim3(grid), dim3(warps_for<T>() * 32), args, smem, s);
 }
 
 template <int T, int BITS>
@@ -959,7 +1070,7 @@ static cudaError_t occupancy(int *blocks, size_t smem, size_t *static_smem)
     *static_smem = fa.sharedSizeBytes;
     e = cudaFuncSetAttribute(decode_kernel<T, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, decode_kernel<T, BITS>, kThreads, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, decode_kernel<T, BITS>, warps_for<T>() * 32, smem);
 }
 
 struct Ws {
