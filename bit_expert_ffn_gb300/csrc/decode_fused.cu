@@ -534,8 +534,9 @@ struct Plan {
     int gC;                        // bytes of one group's phase-C rows
     int chC;                       // groups per phase-C ring buffer
     int sC;                        // bytes of the shared expert's phase-C rows
-    int off_xsw, off_part, off_xown, off_ab, off_c;  // byte offsets in dynamic shared memory
+    int off_xsw, off_part, off_xown, off_ab, off_c, off_h;  // byte offsets in dynamic shared memory
     int regAB, regC;
+    int stage_h;  // 1: phase C reads h and h_s from a padded shared-memory copy
 };
 
 // Balanced contiguous split of n items over the grid.
@@ -738,7 +739,7 @@ __device__ void phase_b_chunk(const Args &a, const Plan &P, const float *xsw, Ro
     int bar_id = 1 + tid_team;
     for (int u0 = tid_team * kRB; u0 < nr; u0 += nteams * kRB) {
         int nbt = min(kRB, nr - u0);
-#pragma unroll
+#pragma unroll 1
         for (int b = 0; b < kRB; b++) {
             if (b >= nbt) break;
             int row = u0 + b;
@@ -784,9 +785,18 @@ __device__ void phase_b_chunk(const Args &a, const Plan &P, const float *xsw, Ro
 
 // Phase C for one chunk of routed groups (weights in shared memory): each
 // warp takes whole groups, keeps their h in registers and runs all rows.
+// h vectors for phase C: a padded copy in shared memory ([vector][chunk][36]
+// floats, conflict-free 16-byte reads) or the workspace in L2.
+__device__ __forceinline__ float4 h_load(const Plan &P, const float *hsm, const float *hg, int vec, int K, int lane,
+                                         int i)
+{
+    if (P.stage_h) return *reinterpret_cast<const float4 *>(hsm + ((size_t)vec * (K / 32) + lane) * 36 + 4 * i);
+    return __ldcg(reinterpret_cast<const float4 *>(hg + (int64_t)vec * K + 32 * lane) + i);
+}
+
 template <int T, int BITS>
 __device__ void phase_c_chunk(const Args &a, const Plan &P, Routing &R, int j, const char *cregion, float *part,
-                              int nrows)
+                              int nrows, const float *hsm)
 {
     int lane = lane_id(), warp = warp_id();
     int np = a.T * a.k, pstride = np + a.T;
@@ -805,10 +815,9 @@ __device__ void phase_c_chunk(const Args &a, const Plan &P, Routing &R, int j, c
         for (int t = 0; t < T; t++) {
             X[t] = 0.f;
             if (active && t < n) {
-                const float4 *hp = reinterpret_cast<const float4 *>(a.h + (int64_t)(p0 + t) * a.I + 32 * lane);
 #pragma unroll
                 for (int i = 0; i < 8; i++) {
-                    float4 f = __ldcg(hp + i);
+                    float4 f = h_load(P, hsm, a.h, p0 + t, a.I, lane, i);
                     v[t][4 * i] = f.x; v[t][4 * i + 1] = f.y; v[t][4 * i + 2] = f.z; v[t][4 * i + 3] = f.w;
                 }
             } else {
@@ -839,7 +848,8 @@ __device__ void phase_c_chunk(const Args &a, const Plan &P, Routing &R, int j, c
 
 // Phase C for the shared expert: rows of Wd_s in shared memory, h_s from L2.
 template <int T>
-__device__ void phase_c_shared(const Args &a, const Plan &P, const char *cregion, float *part, int nrows)
+__device__ void phase_c_shared(const Args &a, const Plan &P, const char *cregion, float *part, int nrows,
+                               const float *hsm_s)
 {
     int lane = lane_id(), warp = warp_id();
     int np = a.T * a.k, pstride = np + a.T;
@@ -849,10 +859,9 @@ __device__ void phase_c_shared(const Args &a, const Plan &P, const char *cregion
 #pragma unroll
     for (int t = 0; t < T; t++) {
         if (active) {
-            const float4 *hp = reinterpret_cast<const float4 *>(a.hs + (int64_t)t * Is + 32 * lane);
 #pragma unroll
             for (int i = 0; i < 8; i++) {
-                float4 f = __ldcg(hp + i);
+                float4 f = h_load(P, hsm_s, a.hs, t, Is, lane, i);
                 v[t][4 * i] = f.x; v[t][4 * i + 1] = f.y; v[t][4 * i + 2] = f.z; v[t][4 * i + 3] = f.w;
             }
         } else {
@@ -1017,14 +1026,28 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             gi_a = ncommit++;
         }
         if (!grid_barrier(a, R, ++nbar)) { wait_all_copies(); return; }
-        // -- phase C
+        // -- phase C: stage h and h_s (one coalesced pass), then the down projections
+        float *hsm = reinterpret_cast<float *>(dyn + P.off_h);
+        float *hsm_s = hsm + (size_t)np * (a.I / 32) * 36;
+        if (P.stage_h) {
+            int n4 = np * (a.I / 4), ns4 = L.swg ? T * (a.Is / 4) : 0;
+            for (int i = threadIdx.x; i < n4 + ns4; i += NT) {
+                bool sh_ = i >= n4;
+                int ii = sh_ ? i - n4 : i;
+                int K = sh_ ? a.Is : a.I;
+                int vec = ii / (K / 4), e4 = ii % (K / 4);
+                float4 f = __ldcg(reinterpret_cast<const float4 *>(sh_ ? a.hs : a.h) + ii);
+                float *dst = (sh_ ? hsm_s : hsm) + ((size_t)vec * (K / 32) + (e4 >> 3)) * 36 + 4 * (e4 & 7);
+                *reinterpret_cast<float4 *>(dst) = f;
+            }
+        }
         wait_group_index(gi_cs, ncommit);
         __syncthreads();
-        if (L.swg) phase_c_shared<T>(a, P, cregion, part, nrows);
+        if (L.swg) phase_c_shared<T>(a, P, cregion, part, nrows, hsm_s);
         for (int j = 0; j < R.nc; j++) {
             wait_group_index(gi_c[j & 1], ncommit);
             __syncthreads();
-            phase_c_chunk<T, BITS>(a, P, R, j, cregion, part, nrows);
+            phase_c_chunk<T, BITS>(a, P, R, j, cregion, part, nrows, hsm);
             __syncthreads();
             if (j + 2 < R.nc) {
                 issue_cr<BITS>(a, P, L, R, j + 2, cregion, o0, nrows);
@@ -1108,6 +1131,9 @@ static bool make_plan(Plan &P, int T, int H, int I, int E, int k, int Is, int bi
     size_t fixed = al128((size_t)T * H * 4) + al128((size_t)T * 32 * P.xsw_stride * 4) +
                    al128((size_t)rows_per_cta * (T * k + T) * 4) + al128((size_t)T * rows_per_cta * 4);
     if (fixed + regA >= budget) return false;
+    size_t hbytes = al128(((size_t)T * k * (I / 32) + (size_t)T * (Is / 32)) * 36 * 4);
+    P.stage_h = fixed + regA + hbytes + (64u << 10) <= budget;  // keep at least 64 KiB for the rings
+    if (P.stage_h) fixed += hbytes;
     size_t left = budget - fixed;
     // phase C: shared rows + two ring buffers of up to 8 groups; phase A/B: the rest
     int chC = 8;
@@ -1127,6 +1153,7 @@ static bool make_plan(Plan &P, int T, int H, int I, int E, int k, int Is, int bi
     P.off_xown = P.off_part + (int)al128((size_t)rows_per_cta * (T * k + T) * 4);
     P.off_ab = P.off_xown + (int)al128((size_t)T * rows_per_cta * 4);
     P.off_c = P.off_ab + P.regAB;
+    P.off_h = P.off_c + P.regC;
     return true;
 }
 
@@ -1229,7 +1256,7 @@ extern "C" moe_status moe_decode_forward(const moe_layer_weights *layers, int n_
     if (!make_plan(P, T, H, I, E, k, Is, bits, grid, a.rows_per_cta, budget))
         return fail(MOE_ERR_UNSUPPORTED, "the fused decode's buffers do not fit in %zu bytes of shared memory "
                     "(T=%d H=%d I=%d E=%d k=%d shared_I=%d)", budget, T, H, I, E, k, Is);
-    size_t smem = (size_t)P.off_c + P.regC;
+    size_t smem = (size_t)P.off_h + (P.stage_h ? al128(((size_t)T * k * (I / 32) + (size_t)T * (Is / 32)) * 36 * 4) : 0);
     MOE_F_DISPATCH(occupancy, &per_sm, smem, &static_smem)
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "decode occupancy query: %s", cudaGetErrorString(e));
     if (per_sm < 1)
