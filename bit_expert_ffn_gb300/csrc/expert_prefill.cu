@@ -7,11 +7,9 @@
 // where p runs over the sorted pairs of expert e (offsets[e] .. offsets[e+1])
 // and tok(p) = perm[p] / k.
 //
-// Tiles.  The work is a list of (expert, 64-pair M tile, 64-row N tile)
-// items; a small kernel turns the per-expert pair counts into a prefix of M
-// tiles so every CTA can map a flat tile index to its expert with a binary
-// search.  The tile kernel here is the CUDA-core form (fp32 FFMA on weights
-// dequantised exactly into shared memory).
+// The tile kernel here is the CUDA-core form (fp32 FFMA on weights
+// dequantised exactly into shared memory, 64 x 64 tiles); it serves shapes
+// the tensor-core form (prefill_tc.cu) does not take.
 #include "common.cuh"
 #include "prefill.cuh"
 
@@ -21,7 +19,6 @@ constexpr int PF_BM = 64;  // pairs per tile
 constexpr int PF_BN = 64;  // weight rows per tile (SWIGLU: 32 gate + 32 up)
 constexpr int PF_BK = 32;  // one quantisation block
 
-// mt_prefix[e] = M tiles of experts < e; mt_prefix[E] = total.
 __global__ void __launch_bounds__(1024) tile_prefix_kernel(const int32_t *__restrict__ offsets, int E, int bm,
                                                            int32_t *__restrict__ mt_prefix)
 {
@@ -54,18 +51,6 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(const int32_t *__rest
     int excl = incl - v + warp_tot[warp_id()];
     if (e < E) mt_prefix[e] = excl;
     if (e == E - 1) mt_prefix[E] = excl + v;
-}
-
-// Largest e with mt_prefix[e] <= mt (experts with zero tiles are skipped).
-__device__ __forceinline__ int expert_of_tile(const int32_t *mt_prefix, int E, int mt)
-{
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (mt_prefix[mid] <= mt) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
 }
 
 struct PfArgs {
@@ -232,7 +217,11 @@ static PfWs pf_ws(const moe_expert_arena &A, int T, int k, void *base)
     return d;
 }
 
-size_t prefill_workspace_bytes(const moe_expert_arena &A, int T, int k) { return pf_ws(A, T, k, nullptr).bytes; }
+size_t prefill_workspace_bytes(const moe_expert_arena &A, int T, int k)
+{
+    if (prefill_tc_supported(A)) return prefill_tc_workspace_bytes(A, T, k);
+    return pf_ws(A, T, k, nullptr).bytes;
+}
 
 template <int BITS>
 static moe_status run_prefill(const moe_expert_arena &A, const uint16_t *x, int T, const float *w, int k,
@@ -295,7 +284,8 @@ moe_status prefill_forward(const moe_expert_arena &A, const uint16_t *x, int T, 
                            moe_dtype dt, int accumulate, void *ws, int32_t *dev_status, cudaStream_t s)
 {
     (void)ids;
-    (void)dev_status;
+    if (prefill_tc_supported(A))
+        return prefill_tc_forward(A, x, T, w, k, offsets, perm, inv, out, dt, accumulate, ws, dev_status, s);
     PfWs d = pf_ws(A, T, k, ws);
     if (A.bits == 2) return run_prefill<2>(A, x, T, w, k, offsets, perm, inv, out, dt, accumulate, d, s);
     return run_prefill<3>(A, x, T, w, k, offsets, perm, inv, out, dt, accumulate, d, s);

@@ -23,6 +23,14 @@ TOL = 1e-3
 TIGHT = 2e-5
 
 
+def prefill_tol(H, I):
+    """The tensor-core prefill (H and I multiples of 64) multiplies fp16 operands:
+    weights (c - mid) * s and h each rounded once to fp16 (relative error up to
+    2^-11), fp32 accumulation; that lands near 4e-4 relative L2, under the
+    stated 1e-3 bar.  Other shapes take the exact fp32 FFMA form."""
+    return TOL if H % 64 == 0 and I % 64 == 0 else TIGHT
+
+
 def dev_u16(a):
     return torch.from_numpy(np.ascontiguousarray(a, np.uint16).view(np.int16)).to(DEV)
 
@@ -220,7 +228,7 @@ def test_tiny_layer_matches_oracle(moe, path, bits):
     want = oracle.moe_layer(bits, x, ids, w, *arena, shared=shared)
     err = rel_l2(got, want)
     assert err <= TOL
-    assert err <= TIGHT, err
+    assert err <= (TIGHT if path == m.MOE_PATH_DECODE else prefill_tol(256, 128)), err
 
 
 @pytest.mark.parametrize("T", [1, 2, 3, 5, 8])
@@ -233,16 +241,35 @@ def test_decode_token_counts(moe, T):
     assert rel_l2(got, want) <= TIGHT
 
 
-@pytest.mark.parametrize("T,E,k", [(100, 16, 2), (257, 32, 4), (1000, 64, 8)])
-def test_prefill_ragged(moe, T, E, k):
-    L, arena, shared = make_layer(E=E, k=k, zipf=1.4, seed=T)
-    x = synth.activations(T, T, 256)
+@pytest.mark.parametrize("T,E,k,bits,H,I", [
+    (100, 16, 2, 2, 256, 128),
+    (257, 32, 4, 2, 256, 128),
+    (1000, 64, 8, 2, 256, 128),
+    (3000, 32, 10, 2, 256, 128),   # several 128-pair tiles per expert
+    (3000, 32, 10, 3, 256, 128),
+    (700, 16, 4, 2, 320, 192),     # ragged N tiles: gate/up 128 + 64 rows, down 256 + 64
+    (700, 16, 4, 3, 320, 192),
+    (300, 16, 4, 2, 224, 96),      # not multiples of 64: the FFMA form
+    (300, 16, 4, 3, 224, 96),
+])
+def test_prefill_ragged(moe, T, E, k, bits, H, I):
+    L, arena, shared = make_layer(bits=bits, H=H, I=I, E=E, k=k, Is=128, zipf=1.4, seed=T)
+    x = synth.activations(T, T, H)
     got, bufs = run_layer(L, x, T, m.MOE_PATH_PREFILL)
     counts = np.diff(bufs.offsets.cpu().numpy())
     assert counts.max() > 64 and (counts % 64 != 0).any()  # several tiles and ragged tails
-    want = oracle.moe_layer(2, x, bufs.ids.cpu().numpy(), bufs.w.cpu().numpy().astype(np.float64), *arena,
+    want = oracle.moe_layer(bits, x, bufs.ids.cpu().numpy(), bufs.w.cpu().numpy().astype(np.float64), *arena,
                             shared=shared)
-    assert rel_l2(got, want) <= TIGHT
+    assert rel_l2(got, want) <= prefill_tol(H, I)
+
+
+def test_prefill_tiles_span_several_128_pair_tiles(moe):
+    """The 3000-token case above gives experts several full 128-pair tiles plus a ragged one."""
+    L, _, _ = make_layer(E=32, k=10, zipf=1.4, seed=3000)
+    x = synth.activations(3000, 3000, 256)
+    _, bufs = run_layer(L, x, 3000, m.MOE_PATH_PREFILL)
+    counts = np.diff(bufs.offsets.cpu().numpy())
+    assert counts.max() > 3 * 128 and (counts % 128 != 0).any()
 
 
 def test_decode_batch_invariance(moe):
@@ -320,4 +347,4 @@ def test_full_size_layer_sampled(moe, T, path):
     shared = synth.shared_weights(seed, layer, s.H, s.Is)
     tokens = list(range(T)) if T <= 4 else sorted(np.random.default_rng(0).choice(T, 6, replace=False))
     want = sampled_reference(seed, layer, 2, s.H, s.I, x, ids, w, shared, tokens)
-    assert rel_l2(got[tokens], want) <= TIGHT
+    assert rel_l2(got[tokens], want) <= (TIGHT if path == m.MOE_PATH_DECODE else prefill_tol(s.H, s.I))
