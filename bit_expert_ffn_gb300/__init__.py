@@ -73,7 +73,7 @@ _SIGS = {
     "moe_packed_size": [_I32, _I64, _I64, _PSZ, _PSZ],
     "moe_pack_experts": [_I32, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P],
     "moe_unpack_experts": [_I32, _I64, _I64, _I64, _P, _P, _P],
-    "moe_router_workspace_size": [_I32, _I32, _I32, _PSZ],
+    "moe_router_workspace_size": [_I32, _I32, _I32, _I32, _PSZ],
     "moe_router_topk": [_P, _I32, _I32, _P, _P, _I32, _I32, _P, _P, _P, _P, _SZ, _P, _P],
     "moe_topk_from_logits": [_P, _I32, _I32, _I32, _P, _P, _P, _P],
     "moe_permute_workspace_size": [_I32, _I32, _I32, _PSZ],
@@ -83,7 +83,7 @@ _SIGS = {
     "moe_expert_forward": [ctypes.POINTER(moe_expert_arena), _P, _I32, _P, _P, _I32, _P, _P, _P, _P, _I32, _I32,
                            _I32, _P, _SZ, _P, _P],
     "moe_shared_expert_workspace_size": [_I32, _I32, _I32, _PSZ],
-    "moe_shared_expert": [_P, _P, _P, _I32, _I32, _P, _I32, _P, _I32, _I32, _P, _SZ, _P],
+    "moe_shared_expert": [_P, _P, _P, _I32, _I32, _P, _I32, _P, _I32, _I32, _P, _SZ, _P, _P],
     "moe_f32_to_bf16": [_P, _P, _I64, _P],
     "moe_decode_workspace_size": [_I32, _I32, _I32, _I32, _I32, _I32, _PSZ],
     "moe_decode_forward": [ctypes.POINTER(moe_layer_weights), _I32, _P, _I32, _I32, ctypes.c_float, _P, _P, _P, _SZ,
@@ -200,8 +200,8 @@ def moe_unpack_experts(bits, n_mats, rows, cols, packed_codes, codes, stream=Non
 
 # ----------------------------------------------------------------- router
 
-def moe_router_workspace_size(T, E, logits_given):
-    return _size(lib().moe_router_workspace_size, T, E, int(logits_given))
+def moe_router_workspace_size(T, H, E, logits_given):
+    return _size(lib().moe_router_workspace_size, T, H, E, int(logits_given))
 
 
 def moe_router_topk(x_bf16, T, H, w_router, bias, E, k, logits_out, topk_ids, topk_w, ws=None, ws_bytes=0,
@@ -255,9 +255,10 @@ def moe_shared_expert_workspace_size(H, I, T):
 
 
 def moe_shared_expert(wg, wu, wd, H, I, x_bf16, T, out, out_dtype=MOE_F32, accumulate=False, ws=None, ws_bytes=0,
-                      stream=None):
+                      dev_status=None, stream=None):
     _check(lib().moe_shared_expert(_ptr(wg), _ptr(wu), _ptr(wd), H, I, _ptr(x_bf16), T, _ptr(out), out_dtype,
-                                   int(accumulate), _ptr(ws), ws_bytes, _stream(stream)), "moe_shared_expert")
+                                   int(accumulate), _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)),
+           "moe_shared_expert")
 
 
 def moe_f32_to_bf16(in_f32, out_bf16, n, stream=None):

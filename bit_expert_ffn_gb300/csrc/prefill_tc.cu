@@ -28,6 +28,7 @@
 #include <cuda.h>
 
 #include "common.cuh"
+#include "dense_tc.cuh"
 #include "prefill.cuh"
 #include "tc.cuh"
 
@@ -255,6 +256,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             if (SWIGLU) {
                 for (int c = 0; c < BN / 2; c += 32) {
                     uint32_t g[32], u[32];
+                    __syncwarp();
                     tc::tmem_ld_32x32b_x32(tbase + c, g);
                     tc::tmem_ld_32x32b_x32(tbase + BN / 2 + c, u);
                     tc::tmem_ld_wait();
@@ -280,6 +282,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             } else {
                 for (int c = 0; c < BN; c += 32) {
                     uint32_t r[32];
+                    __syncwarp();
                     tc::tmem_ld_32x32b_x32(tbase + c, r);
                     tc::tmem_ld_wait();
                     int o0 = n0 + c;
@@ -386,41 +389,10 @@ __global__ void gather_x_kernel(const uint16_t *__restrict__ x, const int32_t *_
 }
 
 // ---------------------------------------------------------------- host
-typedef CUresult (*EncodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static moe_status encode_fn(EncodeTiled *fn)
-{
-    // resolved once (thread-safe static initialisation); the runtime hands
-    // out the driver's entry point, so nothing links against libcuda
-    static EncodeTiled cached = []() -> EncodeTiled {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess) return nullptr;
-        return reinterpret_cast<EncodeTiled>(p);
-    }();
-    if (!cached) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    *fn = cached;
-    return MOE_OK;
-}
-
 // Tensor map over a row-major fp16 matrix [rows][cols]: 64 x 128 boxes, 128-byte swizzle.
 static moe_status make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols)
 {
-    EncodeTiled enc;
-    moe_status st = encode_fn(&enc);
-    if (st != MOE_OK) return st;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {BK, BM};
-    cuuint32_t elem[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, elem,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return MOE_OK;
+    return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rows, cols, BK, BM);
 }
 
 static size_t smem_bytes() { return (size_t)STAGES * (A_BYTES + B_BYTES) + 1024; }

@@ -6,6 +6,7 @@
 // token ("Strata Open-Source Runtime: Running a 125B-Parameter Qwen3 Model on
 // a 12GB GPU", section "The Model Itself").
 #include "common.cuh"
+#include "dense_tc.cuh"
 
 namespace moe {
 
@@ -224,6 +225,37 @@ static moe_status launch_router_gemv(const uint16_t *x, int T, int H, const floa
     return check_launch("router_gemv");
 }
 
+// W = W1 + W2 + W3 with each piece bf16 (round to nearest even of what the
+// previous pieces leave; each difference is exact in fp32), stored side by
+// side: Ws[e][j*H + i] = piece j of W[e][i].  Three pieces carry 24
+// significant bits, so x . (W1 + W2 + W3) with exact bf16 products and fp32
+// sums keeps the fp32 router's accuracy.
+__global__ void split_router_kernel(const float *__restrict__ W, int64_t n, int H, uint16_t *__restrict__ Ws)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        int64_t e = i / H, c = i - e * H;
+        float w = W[i];
+        uint16_t a = f32_to_bf16(w);
+        float r1 = w - bf16_to_f32(a);
+        uint16_t b = f32_to_bf16(r1);
+        float r2 = r1 - bf16_to_f32(b);
+        uint16_t d = f32_to_bf16(r2);
+        uint16_t *row = Ws + e * 3 * H;
+        row[c] = a;
+        row[H + c] = b;
+        row[2 * H + c] = d;
+    }
+}
+
+static bool router_tc_shape(int T, int H) { return T > 8 && H % 64 == 0; }
+
+static size_t router_ws_bytes(int T, int H, int E, int logits_given)
+{
+    size_t b = logits_given ? 0 : align256((size_t)T * E * sizeof(float));
+    if (router_tc_shape(T, H)) b += align256((size_t)E * 3 * H * sizeof(uint16_t));
+    return b;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -238,11 +270,11 @@ extern "C" moe_status moe_topk_from_logits(const float *logits, int T, int E, in
     return launch_topk(logits, T, E, k, ids, w, dev_status, to_cuda(stream));
 }
 
-extern "C" moe_status moe_router_workspace_size(int T, int E, int logits_given, size_t *bytes)
+extern "C" moe_status moe_router_workspace_size(int T, int H, int E, int logits_given, size_t *bytes)
 {
     MOE_REQUIRE(bytes, "bytes is NULL");
-    MOE_REQUIRE(T >= 0 && E >= 1, "T >= 0 and E >= 1");
-    *bytes = logits_given ? 0 : align256((size_t)T * E * sizeof(float));
+    MOE_REQUIRE(T >= 0 && H > 0 && E >= 1, "T >= 0, H > 0 and E >= 1");
+    *bytes = router_ws_bytes(T, H, E, logits_given);
     return MOE_OK;
 }
 
@@ -256,13 +288,16 @@ extern "C" moe_status moe_router_topk(const uint16_t *x_bf16, int T, int H, cons
     if (T == 0) return MOE_OK;
     MOE_REQUIRE(x_bf16 && w_router && topk_ids && topk_w, "NULL pointer");
     MOE_REQUIRE(aligned16(w_router), "w_router must be 16-byte aligned");
+    size_t need = router_ws_bytes(T, H, E, logits_out != nullptr);
+    if (need && (!ws || ws_bytes < need))
+        return fail(MOE_ERR_WORKSPACE, "router (T=%d) needs %zu bytes (%.2f MiB) of workspace, got %zu", T, need,
+                    mib((double)need), ws ? ws_bytes : (size_t)0);
+    MOE_REQUIRE(!need || aligned16(ws), "workspace must be 16-byte aligned");
+    char *wsp = static_cast<char *>(ws);
     float *logits = logits_out;
     if (!logits) {
-        size_t need = align256((size_t)T * E * sizeof(float));
-        if (!ws || ws_bytes < need)
-            return fail(MOE_ERR_WORKSPACE, "router needs %zu bytes (%.2f MiB) of workspace for the logits, got %zu",
-                        need, mib((double)need), ws ? ws_bytes : (size_t)0);
-        logits = static_cast<float *>(ws);
+        logits = reinterpret_cast<float *>(wsp);
+        wsp += align256((size_t)T * E * sizeof(float));
     }
     cudaStream_t s = to_cuda(stream);
     if (T <= 8) {
@@ -271,9 +306,29 @@ extern "C" moe_status moe_router_topk(const uint16_t *x_bf16, int T, int H, cons
         else if (T <= 4) st = launch_router_gemv<4>(x_bf16, T, H, w_router, bias, E, logits, s);
         else st = launch_router_gemv<8>(x_bf16, T, H, w_router, bias, E, logits, s);
     } else {
-        dim3 grid((T + RG_BM - 1) / RG_BM, (E + RG_BN - 1) / RG_BN);
-        router_gemm_kernel<<<grid, 256, 0, s>>>(x_bf16, T, H, w_router, bias, E, logits);
-        st = check_launch("router_gemm");
+        DenseGemm g = {};
+        uint16_t *wsplit = reinterpret_cast<uint16_t *>(wsp);
+        g.A = x_bf16;
+        g.a_cols = H;
+        g.B0 = wsplit;
+        g.b_cols = 3 * H;
+        g.M = T;
+        g.N = E;
+        g.K = 3 * H;
+        g.bias = bias;
+        g.out = logits;
+        g.status = dev_status;
+        if (router_tc_shape(T, H) && dense_tc_supported(g, DENSE_OUT)) {
+            int64_t n = (int64_t)E * H;
+            int blocks = (int)std::min<int64_t>((n + 255) / 256, (int64_t)sm_count() * 8);
+            split_router_kernel<<<blocks, 256, 0, s>>>(w_router, n, H, wsplit);
+            st = check_launch("split_router");
+            if (st == MOE_OK) st = dense_tc_gemm(g, DENSE_OUT, s);
+        } else {
+            dim3 grid((T + RG_BM - 1) / RG_BM, (E + RG_BN - 1) / RG_BN);
+            router_gemm_kernel<<<grid, 256, 0, s>>>(x_bf16, T, H, w_router, bias, E, logits);
+            st = check_launch("router_gemm");
+        }
     }
     if (st != MOE_OK) return st;
     return launch_topk(logits, T, E, k, topk_ids, topk_w, dev_status, s);

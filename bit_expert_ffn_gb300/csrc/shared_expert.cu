@@ -5,6 +5,7 @@
 // GPU", section "The Model Itself").  T <= 8 runs the dense-mode GEMV of
 // gemv.cuh (fp32 maths on exact bf16 weights); larger T a tiled GEMM.
 #include "common.cuh"
+#include "dense_tc.cuh"
 #include "gemv.cuh"
 
 namespace moe {
@@ -118,7 +119,7 @@ extern "C" moe_status moe_shared_expert_workspace_size(int H, int I, int T, size
 
 extern "C" moe_status moe_shared_expert(const uint16_t *wg, const uint16_t *wu, const uint16_t *wd, int H, int I,
                                         const uint16_t *x_bf16, int T, void *out, moe_dtype out_dtype, int accumulate,
-                                        void *ws, size_t ws_bytes, moe_stream_t stream)
+                                        void *ws, size_t ws_bytes, int32_t *dev_status, moe_stream_t stream)
 {
     MOE_REQUIRE(H > 0 && H % 32 == 0 && I > 0 && I % 32 == 0, "H and I must be positive multiples of 32 (got H=%d I=%d)",
                 H, I);
@@ -163,6 +164,38 @@ extern "C" moe_status moe_shared_expert(const uint16_t *wg, const uint16_t *wu, 
         st = launch_bf16_gemv(false, b, T, s);
         if (st != MOE_OK) return st;
     } else {
+        // tensor cores: gate/up with exact bf16 products, h = h_hi + h_lo in
+        // two bf16 halves, down projection over [h_hi | h_lo] against the down
+        // weights read twice, accumulated straight into out
+        DenseGemm gu = {};
+        uint16_t *hs = static_cast<uint16_t *>(ws);
+        gu.A = x_bf16;
+        gu.a_cols = H;
+        gu.B0 = wg;
+        gu.B1 = wu;
+        gu.b_cols = H;
+        gu.M = T;
+        gu.N = I;
+        gu.K = H;
+        gu.hsplit = hs;
+        gu.status = dev_status;
+        DenseGemm gd = {};
+        gd.A = hs;
+        gd.a_cols = 2 * I;
+        gd.B0 = wd;
+        gd.b_cols = I;
+        gd.M = T;
+        gd.N = H;
+        gd.K = 2 * I;
+        gd.out = out;
+        gd.out_bf16 = out_dtype == MOE_BF16;
+        gd.accumulate = accumulate;
+        gd.status = dev_status;
+        if (dense_tc_supported(gu, DENSE_SWIGLU_SPLIT) && dense_tc_supported(gd, DENSE_OUT)) {
+            st = dense_tc_gemm(gu, DENSE_SWIGLU_SPLIT, s);
+            if (st != MOE_OK) return st;
+            return dense_tc_gemm(gd, DENSE_OUT, s);
+        }
         dim3 g1((T + SG_BM - 1) / SG_BM, (I + SG_BN / 2 - 1) / (SG_BN / 2));
         dense_bf16_gemm_kernel<true><<<g1, 256, 0, s>>>(x_bf16, nullptr, T, H, wg, wu, I, h);
         st = check_launch("shared_gateup");

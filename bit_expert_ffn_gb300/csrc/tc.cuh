@@ -155,13 +155,14 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t smem_addr)
     return d;
 }
 
-// Instruction descriptor, kind::f16 with fp16 A and B (K-major), fp32 D.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N)
+// Instruction descriptor, kind::f16 with fp16 (bf16 = false) or bf16 A and
+// B (both K-major), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool bf16 = false)
 {
-    return (1u << 4)                      // D format: fp32
-           | (0u << 7) | (0u << 10)       // A, B format: fp16
-           | ((uint32_t)(N >> 3) << 17)   // N / 8
-           | ((uint32_t)(M >> 4) << 24);  // M / 16
+    return (1u << 4)                                         // D format: fp32
+           | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10)  // A, B format
+           | ((uint32_t)(N >> 3) << 17)                      // N / 8
+           | ((uint32_t)(M >> 4) << 24);                     // M / 16
 }
 
 }  // namespace tc

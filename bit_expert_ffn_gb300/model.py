@@ -18,9 +18,10 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from . import (MOE_F32, MOE_PATH_AUTO, RMS_EPS, load, moe_rms_norm_bf16, make_arena, moe_expert_forward, moe_expert_forward_workspace_size,
-               moe_f32_to_bf16, moe_pack_experts, moe_permute, moe_permute_workspace_size, moe_router_topk,
-               moe_shared_expert, moe_shared_expert_workspace_size, synth, synth_lib)
+from . import (MOE_F32, MOE_PATH_AUTO, RMS_EPS, load, make_arena, moe_expert_forward, moe_expert_forward_workspace_size,
+               moe_f32_to_bf16, moe_pack_experts, moe_permute, moe_permute_workspace_size, moe_rms_norm_bf16,
+               moe_router_topk, moe_router_workspace_size, moe_shared_expert, moe_shared_expert_workspace_size, synth,
+               synth_lib)
 
 
 def _u16(a: np.ndarray, dev) -> torch.Tensor:
@@ -149,18 +150,20 @@ class MoeLayer:
                 with_shared=True):
         """out_f32 (+)= S(x) + routed(x), through the library calls only."""
         s = self.s
-        moe_router_topk(x_bf16, T, s.H, self.router_w, self.router_b, s.E, s.k, bufs.logits, bufs.ids, bufs.w,
-                        dev_status=self.status)
+        rws = moe_router_workspace_size(T, s.H, s.E, True)
         pws = moe_permute_workspace_size(T, s.k, s.E)
         ews = moe_expert_forward_workspace_size(self.arena, T, s.k, path)
         sws = moe_shared_expert_workspace_size(s.H, s.Is, T) if with_shared and self.shared is not None else 0
-        need = max(pws, ews, sws)
+        need = max(rws, pws, ews, sws)
         buf = ws.get(need)
+        moe_router_topk(x_bf16, T, s.H, self.router_w, self.router_b, s.E, s.k, bufs.logits, bufs.ids, bufs.w,
+                        buf if rws else None, rws, dev_status=self.status)
         moe_permute(bufs.ids, T, s.k, s.E, bufs.offsets, bufs.perm, bufs.inv, buf if pws else None, pws,
                     dev_status=self.status)
         acc = accumulate
         if with_shared and self.shared is not None:
-            moe_shared_expert(*self.shared, s.H, s.Is, x_bf16, T, out_f32, MOE_F32, acc, buf, sws)
+            moe_shared_expert(*self.shared, s.H, s.Is, x_bf16, T, out_f32, MOE_F32, acc, buf, sws,
+                              dev_status=self.status)
             acc = True
         moe_expert_forward(self.arena, x_bf16, T, bufs.ids, bufs.w, s.k, bufs.offsets, bufs.perm, bufs.inv, out_f32,
                            MOE_F32, acc, path, buf, ews, dev_status=self.status)

@@ -167,11 +167,18 @@ typedef struct moe_expert_arena {
  *   bias        [E] fp32, or NULL for none
  *   logits_out  [T][E] fp32, or NULL (then the workspace holds them)
  *   topk_ids    [T][k] int32,  topk_w [T][k] fp32
- * Workspace: moe_router_workspace_size (0 bytes when logits_out is given).
+ * T <= 8 runs an fp32 GEMV.  Larger T with H a multiple of 64 runs on the
+ * tensor cores: W is split into three bf16 pieces (W1 + W2 + W3 carries
+ * W's 24 significant bits), every product with the bf16 x is exact and
+ * the sums are fp32; other shapes take an fp32 FFMA GEMM.
+ * Workspace: moe_router_workspace_size (0 bytes when logits_out is given
+ * and T <= 8; the split weights, E * 3H * 2 bytes, for the tensor cores).
+ * A wait of the tensor-core kernel that runs out (about 2 s) sets
+ * *dev_status = MOE_ERR_TIMEOUT.
  * The pages: the router keeps 10 of 512 experts per token per layer
  * ("Strata Open-Source Runtime ...", section "The Model Itself").
  */
-moe_status moe_router_workspace_size(int T, int E, int logits_given, size_t *bytes);
+moe_status moe_router_workspace_size(int T, int H, int E, int logits_given, size_t *bytes);
 moe_status moe_router_topk(const uint16_t *x_bf16, int T, int H, const float *w_router,
                            const float *bias, int E, int k, float *logits_out, int32_t *topk_ids,
                            float *topk_w, void *ws, size_t ws_bytes, int32_t *dev_status,
@@ -269,14 +276,21 @@ moe_status moe_expert_forward(const moe_expert_arena *arena, const uint16_t *x_b
 /*
  * out[t] = (accumulate ? out[t] : 0) + Wd (silu(Wg x[t]) * (Wu x[t])),
  * bf16 weights wg [I][H], wu [I][H], wd [H][I] (I here is the shared
- * expert's width), fp32 accumulation.  The pages: one always-on shared
- * expert per layer ("Strata Open-Source Runtime ...", section "The Model
- * Itself").  Workspace: moe_shared_expert_workspace_size.
+ * expert's width), fp32 accumulation.  T <= 8 runs fp32 GEMVs; larger T
+ * with H and I multiples of 64 runs on the tensor cores with exact bf16
+ * products, h carried as two bf16 halves (h_hi + h_lo, 16 significant
+ * bits) into the down projection; other shapes take an fp32 FFMA GEMM.
+ * A wait of the tensor-core kernels that runs out (about 2 s) sets
+ * *dev_status = MOE_ERR_TIMEOUT (dev_status may be NULL: then it is not
+ * reported).  The pages: one always-on shared expert per layer
+ * ("Strata Open-Source Runtime ...", section "The Model Itself").
+ * Workspace: moe_shared_expert_workspace_size.
  */
 moe_status moe_shared_expert_workspace_size(int H, int I, int T, size_t *bytes);
 moe_status moe_shared_expert(const uint16_t *wg, const uint16_t *wu, const uint16_t *wd, int H,
                              int I, const uint16_t *x_bf16, int T, void *out, moe_dtype out_dtype,
-                             int accumulate, void *ws, size_t ws_bytes, moe_stream_t stream);
+                             int accumulate, void *ws, size_t ws_bytes, int32_t *dev_status,
+                             moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Fused decode over a stack of layers                                      */

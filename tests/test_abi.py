@@ -77,8 +77,11 @@ def test_workspace_rules(lib):
     assert e.status == m.MOE_ERR_WORKSPACE and str(dec) in str(e)
     assert m.moe_permute_workspace_size(1, 10, 512) == 0
     assert m.moe_permute_workspace_size(32768, 10, 512) > 0
-    assert m.moe_router_workspace_size(8, 16, 1) == 0
-    assert m.moe_router_workspace_size(8, 16, 0) >= 8 * 16 * 4
+    assert m.moe_router_workspace_size(8, 256, 16, 1) == 0
+    assert m.moe_router_workspace_size(8, 256, 16, 0) >= 8 * 16 * 4
+    # larger batches keep the three bf16 pieces of the router weights
+    assert m.moe_router_workspace_size(9, 256, 16, 1) >= 16 * 3 * 256 * 2
+    assert m.moe_router_workspace_size(9, 256, 16, 0) >= 16 * 3 * 256 * 2 + 9 * 16 * 4
     # the decode path refuses more than 8 tokens
     ws = m.moe_expert_forward_workspace_size(arena, 9, 10, m.MOE_PATH_DECODE)
     e = _err(m.moe_expert_forward, arena, 16, 9, 16, 16, 10, 16, 16, 16, 16, m.MOE_F32, 0, m.MOE_PATH_DECODE, 16, ws)

@@ -94,7 +94,10 @@ def test_device_generator_matches_host(moe):
 # ---------------------------------------------------------------- router
 
 @pytest.mark.parametrize("T,H,E,k,zipf", [(8, 256, 16, 2, 0.0), (1, 2048, 512, 10, 1.1), (4, 2048, 512, 10, 1.1),
-                                          (3, 2048, 512, 10, 0.0), (77, 2048, 512, 10, 1.1), (130, 256, 1024, 16, 0.0)])
+                                          (3, 2048, 512, 10, 0.0), (77, 2048, 512, 10, 1.1), (130, 256, 1024, 16, 0.0),
+                                          (300, 256, 33, 11, 0.0),      # N tile ragged, unaligned rows: scalar stores
+                                          (1000, 2048, 512, 10, 1.1),   # several M tiles on the tensor cores
+                                          (50, 96, 16, 4, 0.0)])        # H off the 64 grid: the fp32 FFMA GEMM
 def test_router_topk(moe, T, H, E, k, zipf):
     x = synth.activations(21, T, H)
     wr = synth.router_weights(21, 0, E, H)
@@ -103,8 +106,10 @@ def test_router_topk(moe, T, H, E, k, zipf):
     ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
     w = torch.empty(T, k, dtype=torch.float32, device=DEV)
     st = status()
+    nb = m.moe_router_workspace_size(T, H, E, True)
+    ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=DEV)
     m.moe_router_topk(dev_u16(x), T, H, torch.from_numpy(wr).to(DEV), torch.from_numpy(b).to(DEV), E, k, logits, ids,
-                      w, dev_status=st)
+                      w, ws, nb, dev_status=st)
     assert m.moe_check_status(st) == 0
     gl = logits.cpu().numpy()
     ol = oracle.router_logits(x, wr, b)
@@ -302,18 +307,38 @@ def test_zero_tokens_is_a_noop(moe):
     assert torch.all(out == 7.0)
 
 
-@pytest.mark.parametrize("T", [1, 4, 8, 9, 100])
-def test_shared_expert(moe, T):
-    H, Is = 512, 256
+@pytest.mark.parametrize("T,H,Is", [(1, 512, 256), (4, 512, 256), (8, 512, 256), (9, 512, 256), (100, 512, 256),
+                                    (700, 320, 192),   # ragged M and N tiles on the tensor cores
+                                    (60, 224, 96)])    # off the 64 grid: the fp32 FFMA GEMM
+def test_shared_expert(moe, T, H, Is):
     wg, wu, wd = synth.shared_weights(8, 0, H, Is)
     x = synth.activations(8, T, H)
     out = torch.zeros(T, H, dtype=torch.float32, device=DEV)
     nb = m.moe_shared_expert_workspace_size(H, Is, T)
     ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
-    m.moe_shared_expert(dev_u16(wg), dev_u16(wu), dev_u16(wd), H, Is, dev_u16(x), T, out, m.MOE_F32, False, ws, nb)
+    st = status()
+    m.moe_shared_expert(dev_u16(wg), dev_u16(wu), dev_u16(wd), H, Is, dev_u16(x), T, out, m.MOE_F32, False, ws, nb, st)
+    assert m.moe_check_status(st) == 0
     xf = synth.bf16_bits_to_f32(x).astype(np.float64)
     want = np.stack([oracle.shared_expert(wg, wu, wd, xf[t]) for t in range(T)])
     assert rel_l2(out.cpu().numpy(), want) <= TIGHT
+
+
+@pytest.mark.parametrize("T", [5, 300])
+def test_shared_expert_accumulates_into_bf16(moe, T):
+    """out (bf16) = RNE(old + S(x)), on the GEMV and on the tensor-core path."""
+    H, Is = 256, 128
+    wg, wu, wd = synth.shared_weights(9, 0, H, Is)
+    x = synth.activations(9, T, H)
+    old = synth.f32_to_bf16_bits(synth.normal_sigma(99, T * H, 1.0).reshape(T, H))
+    out = dev_u16(old)
+    nb = m.moe_shared_expert_workspace_size(H, Is, T)
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    m.moe_shared_expert(dev_u16(wg), dev_u16(wu), dev_u16(wd), H, Is, dev_u16(x), T, out, m.MOE_BF16, True, ws, nb)
+    ref = torch.zeros(T, H, dtype=torch.float32, device=DEV)
+    m.moe_shared_expert(dev_u16(wg), dev_u16(wu), dev_u16(wd), H, Is, dev_u16(x), T, ref, m.MOE_F32, False, ws, nb)
+    want = bf16_rne(synth.bf16_bits_to_f32(old) + ref.cpu().numpy())
+    assert np.array_equal(u16(out), want)  # one rounding of the same fp32 sum
 
 
 # ---------------------------------------------------------------- full size, sampled
