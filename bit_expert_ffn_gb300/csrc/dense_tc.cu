@@ -300,7 +300,7 @@ static moe_status encode_fn(EncodeTiled *fn)
 }
 
 moe_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes, int64_t rows,
-                        int64_t cols, int box_cols, int box_rows)
+                        int64_t cols, int box_cols, int box_rows, CUtensorMapSwizzle swizzle)
 {
     EncodeTiled enc;
     moe_status st = encode_fn(&enc);
@@ -313,7 +313,7 @@ moe_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType 
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t elem[2] = {1, 1};
     CUresult r = enc(map, dtype, 2, const_cast<void *>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return MOE_OK;
 }

@@ -47,8 +47,9 @@ bool dense_tc_supported(const DenseGemm &g, DenseEpi epi);
 
 moe_status dense_tc_gemm(const DenseGemm &g, DenseEpi epi, cudaStream_t s);
 
-// Row-major 2D tensor map with a (box_cols x box_rows) box and 128-byte swizzle.
+// Row-major 2D tensor map with a (box_cols x box_rows) box.
 moe_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes, int64_t rows,
-                        int64_t cols, int box_cols, int box_rows);
+                        int64_t cols, int box_cols, int box_rows,
+                        CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 }  // namespace moe

@@ -23,12 +23,14 @@ TOL = 1e-3
 TIGHT = 2e-5
 
 
-def prefill_tol(H, I):
-    """The tensor-core prefill (H and I multiples of 64) multiplies fp16 operands:
-    weights (c - mid) * s and h each rounded once to fp16 (relative error up to
-    2^-11), fp32 accumulation; that lands near 4e-4 relative L2, under the
-    stated 1e-3 bar.  Other shapes take the exact fp32 FFMA form."""
-    return TOL if H % 64 == 0 and I % 64 == 0 else TIGHT
+def prefill_tol(H, I, bits=2):
+    """The tensor-core prefill (H and I multiples of 64; of 128 for 3-bit)
+    multiplies fp16 operands: weights (c - mid) * s and h each rounded once to
+    fp16 (relative error up to 2^-11), fp32 accumulation; that lands near 4e-4
+    relative L2, under the stated 1e-3 bar.  Other shapes take the exact fp32
+    FFMA form."""
+    q = 64 if bits == 2 else 128
+    return TOL if H % q == 0 and I % q == 0 else TIGHT
 
 
 def dev_u16(a):
@@ -119,11 +121,15 @@ def test_router_topk(moe, T, H, E, k, zipf):
     oids, ow = oracle.topk(gl, k)
     assert np.array_equal(ids.cpu().numpy(), oids)
     np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=1e-6, atol=1e-7)
-    # (iii) ids from the oracle's own logits agree except at near-ties
+    # (iii) ids from the oracle's own logits agree except at near-ties: a
+    # token counts as near when any two of its k+1 largest logits (the kept
+    # ones, whose order is compared too, and the first one left out) lie
+    # within the logit tolerance of each other
     oids2, _ = oracle.topk(ol.astype(np.float32), k)
     srt = -np.sort(-ol, axis=1)
-    margin = srt[:, k - 1] - (srt[:, k] if k < E else -np.inf)
-    near = margin < 1e-5 * scale
+    top = srt[:, :min(k + 1, E)]
+    margin = np.min(top[:, :-1] - top[:, 1:], axis=1) if top.shape[1] > 1 else np.full(T, np.inf)
+    near = margin < 2e-5 * scale
     assert np.array_equal(oids2[~near], oids[~near])
 
 
@@ -233,7 +239,7 @@ def test_tiny_layer_matches_oracle(moe, path, bits):
     want = oracle.moe_layer(bits, x, ids, w, *arena, shared=shared)
     err = rel_l2(got, want)
     assert err <= TOL
-    assert err <= (TIGHT if path == m.MOE_PATH_DECODE else prefill_tol(256, 128)), err
+    assert err <= (TIGHT if path == m.MOE_PATH_DECODE else prefill_tol(256, 128, bits)), err
 
 
 @pytest.mark.parametrize("T", [1, 2, 3, 5, 8])
@@ -252,8 +258,9 @@ def test_decode_token_counts(moe, T):
     (1000, 64, 8, 2, 256, 128),
     (3000, 32, 10, 2, 256, 128),   # several 128-pair tiles per expert
     (3000, 32, 10, 3, 256, 128),
-    (700, 16, 4, 2, 320, 192),     # ragged N tiles: gate/up 128 + 64 rows, down 256 + 64
-    (700, 16, 4, 3, 320, 192),
+    (700, 16, 4, 2, 320, 192),     # weight rows off the tile grid (down: 2 x 128 + 64)
+    (700, 16, 4, 3, 320, 192),     # 3-bit off the 128 grid: the FFMA form
+    (700, 16, 4, 3, 384, 256),
     (300, 16, 4, 2, 224, 96),      # not multiples of 64: the FFMA form
     (300, 16, 4, 3, 224, 96),
 ])
@@ -265,7 +272,7 @@ def test_prefill_ragged(moe, T, E, k, bits, H, I):
     assert counts.max() > 64 and (counts % 64 != 0).any()  # several tiles and ragged tails
     want = oracle.moe_layer(bits, x, bufs.ids.cpu().numpy(), bufs.w.cpu().numpy().astype(np.float64), *arena,
                             shared=shared)
-    assert rel_l2(got, want) <= prefill_tol(H, I)
+    assert rel_l2(got, want) <= prefill_tol(H, I, bits)
 
 
 def test_prefill_tiles_span_several_128_pair_tiles(moe):
