@@ -5,7 +5,9 @@
 // loads both operands with TMA (128-byte swizzle, four 48 KiB stages),
 // warp 1 issues tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32 in
 // TMEM, two accumulator buffers so the epilogue of one tile overlaps the
-// next tile's MMAs), warp 2 owns the TMEM allocation and warps 4..7 move
+// next tile's MMAs), warp 2 owns the TMEM allocation and waits on the
+// barriers for warp 1 (a named barrier hands each ready step over, so the
+// issuing thread does no mbarrier waits of its own), and warps 4..7 move
 // the accumulators out (one TMEM lane quadrant each).  Every wait is
 // bounded: after about 2 s the CTA records MOE_ERR_TIMEOUT and stops.
 #include "dense_tc.cuh"
@@ -110,29 +112,34 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                 if (!tc::mbar_wait(&S.full[s], u & 1, kWaitNs)) set_status(p.status, MOE_ERR_TIMEOUT);
             }
         }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer
-            const uint32_t idesc = tc::idesc_f16_f32(BM, BN, true);
-            int it = 0, j = 0;
-            for (int tile = blockIdx.x; tile < p.total && !S.abort; tile += gridDim.x, j++) {
-                int acc = j & 1, v = j >> 1;
-                if (v > 0 && !tc::mbar_wait(&S.acc_empty[acc], (v - 1) & 1, kWaitNs)) {
-                    set_status(p.status, MOE_ERR_TIMEOUT);
-                    S.abort = 1;
+    } else if (warp == 1 || warp == 2) {
+        // ---------------- MMA: warp 2 waits on the barriers, lane 0 of warp 1 issues; they meet
+        // at named barrier 3 every step, so the issuing thread never waits on
+        // an mbarrier behind its own queued MMAs.  The OR over the barrier
+        // makes every stop decision common to both warps.
+        const bool issuer = warp == 1;
+        const uint32_t idesc = tc::idesc_f16_f32(BM, BN, true);
+        int it = 0, j = 0;
+        bool stop = false;
+        for (int tile = blockIdx.x; tile < p.total; tile += gridDim.x, j++) {
+            int acc = j & 1, v = j >> 1;
+            bool fail = false;
+            if (!issuer && lane == 0)
+                fail = S.abort || (v > 0 && !tc::mbar_wait(&S.acc_empty[acc], (v - 1) & 1, kWaitNs));
+            if (tc::named_sync_or(3, 64, fail)) {
+                stop = true;
+                break;
+            }
+            uint32_t d = tmem + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < p.nk; kb++, it++) {
+                int s = it % STAGES, u = it / STAGES;
+                fail = false;
+                if (!issuer && lane == 0) fail = !tc::mbar_wait(&S.full[s], u & 1, kWaitNs);
+                if (tc::named_sync_or(3, 64, fail)) {
+                    stop = true;
                     break;
                 }
-                tc::tc_fence_after();
-                uint32_t d = tmem + (uint32_t)(acc * BN);
-                bool ok = true;
-                for (int kb = 0; kb < p.nk; kb++, it++) {
-                    int s = it % STAGES, u = it / STAGES;
-                    if (!tc::mbar_wait(&S.full[s], u & 1, kWaitNs)) {
-                        set_status(p.status, MOE_ERR_TIMEOUT);
-                        S.abort = 1;
-                        ok = false;
-                        break;
-                    }
+                if (issuer && lane == 0) {
                     tc::tc_fence_after();
                     uint32_t abase = tc::smem_u32(sA + s * A_BYTES), bbase = tc::smem_u32(sB + s * B_BYTES);
 #pragma unroll
@@ -141,9 +148,15 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                                        idesc, (kb | k16) ? 1u : 0u);
                     tc::mma_commit(&S.empty[s]);
                 }
-                if (!ok) break;
-                tc::mma_commit(&S.acc_full[acc]);
             }
+            if (stop) break;
+            if (issuer && lane == 0) tc::mma_commit(&S.acc_full[acc]);
+        }
+        if (stop && !issuer && lane == 0) {
+            set_status(p.status, MOE_ERR_TIMEOUT);
+            S.abort = 1;
+        }
+        if (issuer && lane == 0) {
             tc::mma_commit(&S.mma_done);
             if (!tc::mbar_wait(&S.mma_done, 0, kWaitNs)) set_status(p.status, MOE_ERR_TIMEOUT);
         }

@@ -8,20 +8,31 @@
 //   combine:  out[t][o] = sum_j w[t][j] y[inv[t*k+j]][o]   (slot order)
 //
 // The weights are the MMA's M operand (128 rows per tile) and an expert's
-// sorted pairs its N operand (up to 256 per tile, in steps of 32, so an
+// sorted pairs its N operand (up to 192 per tile, in steps of 32, so an
 // expert with few pairs costs few columns).  One CTA per SM runs a
-// persistent loop over (expert, up to 256 pairs) x (128 weight rows) tiles:
-//   warp 0      TMA: the packed codes of each 64-wide K step and the pairs'
-//               fp16 rows (128-byte swizzle);
-//   warps 8-15  dequantise the codes into the swizzled K-major fp16 tile
-//               (two threads per row, one 32-weight block each);
-//   warp 1      tcgen05.mma M=128, N=32..256, K=16 into TMEM (two
-//               accumulator buffers: the epilogue of one tile overlaps the
+// persistent loop over (expert, up to 192 pairs) x (128 weight rows) tiles,
+// streaming the reduction dimension in 64-wide steps through three rings,
+// each as deep as its producer's latency asks:
+//   warp 3      TMA: packed codes and scales of each step into the code
+//               ring (shared memory, several steps ahead);
+//   warp 0      TMA: the pairs' fp16 rows of each step into the pair ring
+//               (shared memory, 128-byte swizzle);
+//   warp 24     waits for free slots of both rings and hands them to the
+//               two TMA warps (an mbarrier call right after queued copies
+//               would stall the issuing thread);
+//   warps 8-23  dequantise codes straight into the weight ring in TMEM
+//               (tcgen05.st; a warp per lane quadrant and 16-weight group);
+//   warp 1      tcgen05.mma M=128, N=32..192, K=16 with the weights read
+//               from TMEM and the pairs from shared memory, into two TMEM
+//               accumulator buffers (the epilogue of one tile overlaps the
 //               next tile's MMAs);
-//   warp 2      owns the TMEM allocation;
+//   warp 2      owns the TMEM allocation and waits on the rings' barriers
+//               for warp 1, handing each ready step over by a named barrier;
 //   warps 4-7   epilogue: TMEM -> registers, transposed through shared
 //               memory, written by TMA stores (the gate/up epilogue first
 //               hands the up rows' values to the gate rows' warps).
+// Keeping the weights out of shared memory leaves its bandwidth to the
+// pairs' rows, which the tensor cores read there.
 // Operands are fp16: x (bf16) converts exactly, the weights (c - mid) * s
 // round once to fp16, h rounds to fp16 between the two GEMMs.  Every wait is
 // bounded: after about 2 s the CTA records MOE_ERR_TIMEOUT and stops.
@@ -46,24 +57,45 @@ namespace moe {
 namespace ptc {
 
 constexpr int BM = 128;  // weight rows per tile (MMA M); gate/up: 64 gate + 64 up rows
-constexpr int BT = 256;  // sorted pairs per tile at most (MMA N, multiples of 32)
-constexpr int BK = 64;   // reduction per stage: one 128-byte swizzle row of fp16
-constexpr int STAGES = 3;
-constexpr int A_BYTES = BM * BK * 2;   // dequantised weights
-constexpr int B_BYTES = BT * BK * 2;   // pairs' rows
-constexpr int C_BYTES = BM * 16;       // 2-bit (low) codes of one stage: 16 B per row
-constexpr int HI_BYTES = BM * 16;      // 3-bit high planes of two stages: 16 B per row
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + C_BYTES + HI_BYTES;
-constexpr int XCH_BYTES = 32 * 64 * 4;  // up values: 32 pairs x 64 rows, fp32
-constexpr int STG_BYTES = 32 * 32 * 4;  // one 32 x 32 output block
-constexpr int OFF_XCH = STAGES * STAGE_BYTES;
-constexpr int OFF_STG = OFF_XCH + 2 * XCH_BYTES;
-constexpr int SMEM_BYTES = OFF_STG + 8 * STG_BYTES + 1024;
-constexpr int THREADS = 512;
-constexpr int DQ_WARP0 = 8;
+constexpr int BT = 192;  // sorted pairs per tile at most (MMA N, multiples of 32)
+constexpr int BK = 64;   // reduction per step: one 128-byte swizzle row of fp16
+constexpr int B_BYTES = BT * BK * 2;   // one step of the pairs' rows
+constexpr int C_LO = 0;                // code entry: low codes, 16 B per row
+constexpr int C_SC = BM * 16;          //             scales of four steps, 16 B per row
+constexpr int C_HI = 2 * BM * 16;      //             3-bit high planes of two steps, 16 B per row
+constexpr int NA = 4, NB = 6;          // weight ring (TMEM), pair ring (shared memory)
+// TMEM columns: two accumulators of BT fp32 columns, then the weight ring
+// (a 64-wide fp16 step is 32 columns).
+constexpr int TM_A = 2 * BT;
+static_assert(TM_A + NA * 32 <= 512, "TMEM columns");
+constexpr int XCH_BYTES = 32 * 64 * 4;  // up values of one 32-pair chunk: 64 rows, fp32
+// Epilogue area.  down: four fp32 32 x 32 staging blocks; gate/up: two fp16
+// 32 x 32 staging blocks, then two exchange buffers.
+constexpr int STG_DOWN = 32 * 32 * 4, STG_H = 32 * 32 * 2;
+constexpr int OFF_XCH = 2 * STG_H;
+constexpr int EPI_BYTES = OFF_XCH + 2 * XCH_BYTES > 4 * STG_DOWN ? OFF_XCH + 2 * XCH_BYTES : 4 * STG_DOWN;
+constexpr int THREADS = 800;
+constexpr int DQ_WARP0 = 8;  // warps 8..23 dequantise: four threads per weight row
+constexpr int DQ_WARPS = 16;
+constexpr int RING_WARP = 24;  // waits for free pair/code slots for the TMA issuers
 constexpr int EPI_WARP0 = 4;
+constexpr int NC_MAX = 8;
 constexpr unsigned long long kWaitNs = 2000000000ull;
-static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && OFF_STG % 1024 == 0, "1024-byte aligned areas");
+
+// Shared-memory plan per bit width: the code entry carries the 3-bit high
+// planes only for 3 bits, which leaves room for fewer entries.
+template <int BITS>
+struct Cfg {
+    static constexpr int C_BYTES = BITS == 2 ? 2 * BM * 16 : 3 * BM * 16;
+    static constexpr int NC = BITS == 2 ? 8 : 6;
+    static constexpr int OFF_B = 0;
+    static constexpr int OFF_C = OFF_B + NB * B_BYTES;
+    static constexpr int OFF_E = OFF_C + NC * C_BYTES;
+    static constexpr int SMEM = OFF_E + EPI_BYTES + 1024;
+    static_assert(OFF_C % 1024 == 0 && OFF_E % 1024 == 0 && B_BYTES % 1024 == 0, "1024-byte aligned areas");
+    static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
+    static_assert(NC <= NC_MAX, "code ring");
+};
 
 struct Args {
     const uint16_t *scales;
@@ -73,15 +105,16 @@ struct Args {
     int K, rows, up_rows;          // rows: output rows (I or H); up_rows: where the up rows start (I)
     int rtiles;                    // weight-row tiles per pair tile
     int hi_x;                      // byte offset of the 3-bit high plane inside a code row
-    const int32_t *offsets, *mt_prefix;
-    int E;
+    int scale_tma;                 // scales come by TMA (rows of K/32 scales are 16-byte multiples)
+    const int4 *table;          // per pair tile: expert, first pair, pair count
+    const int32_t *ntt;         // number of pair tiles
     uint16_t *h_out;  // gate/up: fp16 [pairs][I] (columns permuted within 16-groups)
     float *y_out;     // down: fp32 [pairs][H]
     int32_t *status;
 };
 
 struct Shared {
-    uint64_t tfull[STAGES], cfull[STAGES], wfull[STAGES], empty[STAGES];
+    uint64_t afull[NA], aempty[NA], bfull[NB], bempty[NB], cfull[NC_MAX], cempty[NC_MAX];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t mma_done;
     uint32_t tmem;
@@ -92,16 +125,44 @@ struct Tile {
     int e, p0, cnt, rt, n32;  // n32: 32-pair chunks (MMA N = 32 n32)
 };
 
-__device__ __forceinline__ Tile decode_tile(const Args &a, int tile)
+// A tile's entry of the pair-tile table; loaded one tile ahead of its use,
+// so the load's latency hides behind the current tile's work.
+__device__ __forceinline__ int4 tile_entry(const Args &a, int tile, int total)
+{
+    return tile < total ? __ldg(&a.table[tile / a.rtiles]) : make_int4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ Tile make_tile(const Args &a, int4 e, int tile)
 {
     Tile t;
-    int tt = tile / a.rtiles;
-    t.rt = tile - tt * a.rtiles;
-    t.e = expert_of_tile(a.mt_prefix, a.E, tt);
-    t.p0 = a.offsets[t.e] + (tt - a.mt_prefix[t.e]) * BT;
-    t.cnt = min(BT, a.offsets[t.e + 1] - t.p0);
+    t.e = e.x;
+    t.p0 = e.y;
+    t.cnt = e.z;
+    t.rt = tile % a.rtiles;
     t.n32 = (t.cnt + 31) >> 5;
     return t;
+}
+
+// table[mt_prefix[e] + j] = (e, offsets[e] + j*BT, pairs of that tile): one thread per expert.
+__global__ void tile_table_kernel(const int32_t *__restrict__ offsets, const int32_t *__restrict__ mt_prefix, int E,
+                                  int bt, int4 *__restrict__ table)
+{
+    int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    int n = offsets[e + 1] - offsets[e], base = mt_prefix[e];
+    for (int j = 0; j * bt < n; j++) table[base + j] = make_int4(e, offsets[e] + j * bt, min(bt, n - j * bt), 0);
+}
+
+// Ring slot and phase parity of step `it` in a ring of n entries.
+struct Slot {
+    int s;
+    uint32_t par;
+    bool reuse;  // the slot held an earlier step: wait until it is free
+};
+__device__ __forceinline__ Slot slot_of(int it, int n)
+{
+    int u = it / n;
+    return Slot{it - u * n, (uint32_t)(u & 1), u > 0};
 }
 
 // Stored position, inside its 16-element group, of element m.
@@ -136,47 +197,66 @@ __device__ __forceinline__ void dq_chunk(uint32_t w, uint32_t hw, __half2 s2, ui
 #undef MOE_DQ
 }
 
-// One 32-weight block (codes c0: weights 0-15, c1: 16-31; 3-bit high plane
-// word hw; fp16 scale bits sc) into the four 16-byte chunks 4*half .. 4*half+3
-// of swizzled row r.
+// One 16-weight group (codes w, 3-bit high bits hw already aligned to the
+// group, fp16 scale bits sc) as eight fp16x2 words: word m holds the stored
+// positions 2m and 2m+1 of the group (true elements m and m+8).
 template <int BITS>
-__device__ __forceinline__ void dq_block(uint32_t c0, uint32_t c1, uint32_t hw, uint32_t sc, char *rowp, int r,
-                                         int half)
+__device__ __forceinline__ void dq_group(uint32_t w, uint32_t hw, uint32_t sc, uint32_t (&v)[8])
 {
     __half2 s2 = __half2half2(__ushort_as_half((uint16_t)sc));
+    uint32_t lo4[4], hi4[4];
+    dq_chunk<BITS, 0>(w, hw, s2, lo4);
+    dq_chunk<BITS, 4>(w, hw, s2, hi4);
 #pragma unroll
-    for (int g = 0; g < 2; g++) {
-        uint32_t w = g ? c1 : c0;
-        uint32_t hword = BITS == 3 ? (g ? hw >> 8 : hw) : 0u;
-        uint32_t lo4[4], hi4[4];
-        dq_chunk<BITS, 0>(w, hword, s2, lo4);
-        dq_chunk<BITS, 4>(w, hword, s2, hi4);
-        int c = 4 * half + 2 * g;
-        *reinterpret_cast<uint4 *>(rowp + ((c ^ (r & 7)) << 4)) = make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
-        *reinterpret_cast<uint4 *>(rowp + (((c + 1) ^ (r & 7)) << 4)) = make_uint4(hi4[0], hi4[1], hi4[2], hi4[3]);
+    for (int j = 0; j < 4; j++) {
+        v[j] = lo4[j];
+        v[4 + j] = hi4[j];
     }
 }
+
+// silu with a fast division: h is rounded to fp16 right after, far coarser
+// than the approximation's couple of fp32 ulps.
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // Shared-memory reads of what TMA wrote: ordered after the mbarrier wait by
 // that wait's memory clobber.
 __device__ __forceinline__ uint32_t lds32(const void *p) { return *reinterpret_cast<const uint32_t *>(p); }
 
+// Waits for the last phase each slot of a ring was filled in (its copies
+// have landed); used before the CTA leaves, so no copy is still in flight.
+__device__ __forceinline__ void drain_ring(uint64_t *full, int n, int issued, int32_t *status)
+{
+    for (int s = 0; s < n && s < issued; s++) {
+        int last = s + n * ((issued - 1 - s) / n);
+        if (!tc::mbar_wait(&full[s], (uint32_t)((last / n) & 1), kWaitNs)) set_status(status, MOE_ERR_TIMEOUT);
+    }
+}
+
 template <int BITS, bool SWIGLU>
 __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_constant__ Args a,
                                                              const __grid_constant__ CUtensorMap tok_map,
+                                                             const __grid_constant__ CUtensorMap tok_full_map,
                                                              const __grid_constant__ CUtensorMap code_map,
+                                                             const __grid_constant__ CUtensorMap scale_map,
                                                              const __grid_constant__ CUtensorMap out_map)
 {
+    using C = Cfg<BITS>;
     extern __shared__ __align__(1024) char dyn_raw[];
     char *dyn = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
     __shared__ Shared S;
     const int warp = warp_id(), lane = lane_id();
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; s++) {
-            tc::mbar_init(&S.tfull[s], 1);
+        for (int s = 0; s < NA; s++) {
+            tc::mbar_init(&S.afull[s], DQ_WARPS);
+            tc::mbar_init(&S.aempty[s], 1);
+        }
+        for (int s = 0; s < NB; s++) {
+            tc::mbar_init(&S.bfull[s], 1);
+            tc::mbar_init(&S.bempty[s], 1);
+        }
+        for (int s = 0; s < C::NC; s++) {
             tc::mbar_init(&S.cfull[s], 1);
-            tc::mbar_init(&S.wfull[s], 8);
-            tc::mbar_init(&S.empty[s], 1);
+            tc::mbar_init(&S.cempty[s], DQ_WARPS);
         }
         for (int i = 0; i < 2; i++) {
             tc::mbar_init(&S.acc_full[i], 1);
@@ -189,91 +269,145 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     if (warp == 2) tc::tmem_alloc(&S.tmem, 512);
     if (warp == 0 && lane == 0) {
         tc::tma_prefetch_desc(&tok_map);
+        tc::tma_prefetch_desc(&tok_full_map);
         tc::tma_prefetch_desc(&code_map);
+        if (a.scale_tma) tc::tma_prefetch_desc(&scale_map);
         tc::tma_prefetch_desc(&out_map);
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = S.tmem;
-    const int total = a.mt_prefix[a.E] * a.rtiles;
+    const int total = *a.ntt * a.rtiles;
     const int nk = a.K / BK;
 
-    if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- TMA producer: codes and the pairs' rows
-            int it = 0;
-            for (int tile = blockIdx.x; tile < total && !S.abort; tile += gridDim.x) {
-                Tile t = decode_tile(a, tile);
-                int64_t base = (int64_t)t.e * a.code_rows;
-                int r0 = (int)(base + (SWIGLU ? t.rt * 64 : t.rt * 128));
-                int r1 = SWIGLU ? (int)(base + a.up_rows + t.rt * 64) : r0 + 64;
-                for (int kb = 0; kb < nk; kb++, it++) {
-                    int s = it % STAGES, u = it / STAGES;
-                    if (u > 0 && !tc::mbar_wait(&S.empty[s], (u - 1) & 1, kWaitNs)) {
-                        set_status(a.status, MOE_ERR_TIMEOUT);
-                        S.abort = 1;
+    if (warp == 0 || warp == 3 || warp == RING_WARP) {
+        // ---------------- TMA: warp 24 waits for free ring slots and posts the
+        // expected bytes; it hands each step over by named barriers 4 (pair
+        // rows, issued by warp 0) and 5 (codes and scales, issued by warp 3),
+        // so the issuing threads make no mbarrier calls between their copies.
+        // The OR over each barrier makes every stop decision common.
+        const int role = warp == RING_WARP ? 0 : warp == 0 ? 1 : 2;  // 0 waiter, 1 pairs, 2 codes
+        const uint32_t cbytes = (BITS == 3 ? 2 * BM * 16 : BM * 16) + (a.scale_tma ? BM * 16 : 0);
+        int it = 0;
+        bool stop = false;
+        int4 nxt = tile_entry(a, blockIdx.x, total);
+        for (int tile = blockIdx.x; tile < total && !stop; tile += gridDim.x) {
+            Tile t = make_tile(a, nxt, tile);
+            nxt = tile_entry(a, tile + gridDim.x, total);
+            int64_t base = (int64_t)t.e * a.code_rows;
+            int r0 = (int)(base + (SWIGLU ? t.rt * 64 : t.rt * 128));
+            int r1 = SWIGLU ? (int)(base + a.up_rows + t.rt * 64) : r0 + 64;
+            for (int kb = 0; kb < nk; kb++, it++) {
+                Slot b = slot_of(it, NB), c = slot_of(it, C::NC);
+                if (role != 2) {
+                    bool fail = false;
+                    if (role == 0 && lane == 0) {
+                        fail = S.abort || (b.reuse && !tc::mbar_wait(&S.bempty[b.s], b.par ^ 1, kWaitNs));
+                        if (!fail) tc::mbar_arrive_expect_tx(&S.bfull[b.s], t.n32 * 32 * BK * 2);
+                    }
+                    if (tc::named_sync_or(4, 64, fail)) {
+                        stop = true;
                         break;
                     }
-                    char *st = dyn + s * STAGE_BYTES;
-                    char *cs = st + A_BYTES + B_BYTES;
-                    bool hi = BITS == 3 && !(kb & 1);
-                    tc::mbar_arrive_expect_tx(&S.cfull[s], C_BYTES + (hi ? HI_BYTES : 0));
-                    tc::tma_load_2d(cs, &code_map, kb * 16, r0, &S.cfull[s]);
-                    tc::tma_load_2d(cs + C_BYTES / 2, &code_map, kb * 16, r1, &S.cfull[s]);
-                    if (hi) {
-                        tc::tma_load_2d(cs + C_BYTES, &code_map, a.hi_x + (kb >> 1) * 16, r0, &S.cfull[s]);
-                        tc::tma_load_2d(cs + C_BYTES + HI_BYTES / 2, &code_map, a.hi_x + (kb >> 1) * 16, r1,
-                                        &S.cfull[s]);
+                    if (role == 1 && lane == 0) {
+                        char *bs = dyn + C::OFF_B + b.s * B_BYTES;
+                        if (t.n32 * 32 == BT) {  // a full tile: one box of BT rows
+                            tc::tma_load_2d(bs, &tok_full_map, kb * BK, t.p0, &S.bfull[b.s]);
+                        } else {
+                            for (int i = 0; i < t.n32; i++)
+                                tc::tma_load_2d(bs + i * 32 * BK * 2, &tok_map, kb * BK, t.p0 + 32 * i, &S.bfull[b.s]);
+                        }
                     }
-                    tc::mbar_arrive_expect_tx(&S.tfull[s], t.n32 * 32 * BK * 2);
-                    for (int i = 0; i < t.n32; i++)
-                        tc::tma_load_2d(st + A_BYTES + i * 32 * BK * 2, &tok_map, kb * BK, t.p0 + 32 * i, &S.tfull[s]);
                 }
-            }
-            // no copy may still be in flight when the CTA leaves (after a timeout elsewhere)
-            for (int s = 0; s < STAGES && s < it; s++) {
-                int u = (s + STAGES * ((it - 1 - s) / STAGES)) / STAGES;
-                if (!tc::mbar_wait(&S.cfull[s], u & 1, kWaitNs) || !tc::mbar_wait(&S.tfull[s], u & 1, kWaitNs))
-                    set_status(a.status, MOE_ERR_TIMEOUT);
+                if (role != 1) {
+                    bool fail = false;
+                    if (role == 0 && lane == 0) {
+                        fail = S.abort || (c.reuse && !tc::mbar_wait(&S.cempty[c.s], c.par ^ 1, kWaitNs));
+                        if (!fail) tc::mbar_arrive_expect_tx(&S.cfull[c.s], cbytes);
+                    }
+                    if (tc::named_sync_or(5, 64, fail)) {
+                        stop = true;
+                        break;
+                    }
+                    if (role == 2 && lane == 0) {
+                        char *cs = dyn + C::OFF_C + c.s * C::C_BYTES;
+                        tc::tma_load_2d(cs + C_LO, &code_map, kb * 16, r0, &S.cfull[c.s]);
+                        tc::tma_load_2d(cs + C_LO + 64 * 16, &code_map, kb * 16, r1, &S.cfull[c.s]);
+                        if (a.scale_tma) {
+                            tc::tma_load_2d(cs + C_SC, &scale_map, (kb >> 2) * 8, r0, &S.cfull[c.s]);
+                            tc::tma_load_2d(cs + C_SC + 64 * 16, &scale_map, (kb >> 2) * 8, r1, &S.cfull[c.s]);
+                        }
+                        if (BITS == 3) {
+                            tc::tma_load_2d(cs + C_HI, &code_map, a.hi_x + (kb >> 1) * 16, r0, &S.cfull[c.s]);
+                            tc::tma_load_2d(cs + C_HI + 64 * 16, &code_map, a.hi_x + (kb >> 1) * 16, r1,
+                                            &S.cfull[c.s]);
+                        }
+                    }
+                }
             }
         }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer
-            int it = 0, j = 0;
-            for (int tile = blockIdx.x; tile < total && !S.abort; tile += gridDim.x, j++) {
-                Tile t = decode_tile(a, tile);
-                const uint32_t idesc = tc::idesc_f16_f32(BM, 32 * t.n32);
-                int acc = j & 1, v = j >> 1;
-                if (v > 0 && !tc::mbar_wait(&S.acc_empty[acc], (v - 1) & 1, kWaitNs)) {
-                    set_status(a.status, MOE_ERR_TIMEOUT);
-                    S.abort = 1;
+        if (stop && role == 0 && lane == 0) {
+            set_status(a.status, MOE_ERR_TIMEOUT);
+            S.abort = 1;
+        }
+        // no copy may still be in flight when the CTA leaves (after a timeout elsewhere);
+        // the waiter posted the bytes of every step it handed over, so each slot's
+        // last phase completes once its copies land
+        if (role == 1 && lane == 0) drain_ring(S.bfull, NB, it, a.status);
+        if (role == 2 && lane == 0) drain_ring(S.cfull, C::NC, it, a.status);
+    } else if (warp == 1 || warp == 2) {
+        // ---------------- MMA: warp 2 waits on the rings' barriers, lane 0 of warp 1 issues.
+        // They meet at named barrier 3 every step, so the issuing thread never
+        // waits on an mbarrier behind its own queued MMAs (such a wait takes
+        // longer than a step's MMAs).  The OR over the barrier makes every
+        // stop decision common to both warps.
+        const bool issuer = warp == 1;
+        int it = 0, j = 0;
+        bool stop = false;
+        int4 nxt = tile_entry(a, blockIdx.x, total);
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, j++) {
+            Tile t = make_tile(a, nxt, tile);
+            nxt = tile_entry(a, tile + gridDim.x, total);
+            int acc = j & 1, v = j >> 1;
+            bool fail = false;
+            if (!issuer && lane == 0)
+                fail = S.abort || (v > 0 && !tc::mbar_wait(&S.acc_empty[acc], (v - 1) & 1, kWaitNs));
+            if (tc::named_sync_or(3, 64, fail)) {
+                stop = true;
+                break;
+            }
+            const uint32_t idesc = tc::idesc_f16_f32(BM, 32 * t.n32);
+            uint32_t d = tmem + (uint32_t)(acc * BT);
+            for (int kb = 0; kb < nk; kb++, it++) {
+                Slot sa = slot_of(it, NA), sb = slot_of(it, NB);
+                fail = false;
+                if (!issuer && lane == 0)
+                    fail = !tc::mbar_wait(&S.afull[sa.s], sa.par, kWaitNs) || !tc::mbar_wait(&S.bfull[sb.s], sb.par, kWaitNs);
+                if (tc::named_sync_or(3, 64, fail)) {
+                    stop = true;
                     break;
                 }
-                tc::tc_fence_after();
-                uint32_t d = tmem + (uint32_t)(acc * BT);
-                bool ok = true;
-                for (int kb = 0; kb < nk; kb++, it++) {
-                    int s = it % STAGES, u = it / STAGES;
-                    if (!tc::mbar_wait(&S.wfull[s], u & 1, kWaitNs) || !tc::mbar_wait(&S.tfull[s], u & 1, kWaitNs)) {
-                        set_status(a.status, MOE_ERR_TIMEOUT);
-                        S.abort = 1;
-                        ok = false;
-                        break;
-                    }
+                if (issuer && lane == 0) {
                     tc::tc_fence_after();
-                    char *st = dyn + s * STAGE_BYTES;
-                    uint32_t abase = tc::smem_u32(st), bbase = tc::smem_u32(st + A_BYTES);
+                    uint32_t abase = tmem + (uint32_t)(TM_A + sa.s * 32);
+                    uint32_t bbase = tc::smem_u32(dyn + C::OFF_B + sb.s * B_BYTES);
 #pragma unroll
                     for (int k16 = 0; k16 < BK / 16; k16++)
-                        tc::mma_f16_ss(d, tc::desc_kmajor_sw128(abase + k16 * 32), tc::desc_kmajor_sw128(bbase + k16 * 32),
-                                       idesc, (kb | k16) ? 1u : 0u);
-                    tc::mma_commit(&S.empty[s]);
+                        tc::mma_f16_ts(d, abase + k16 * 8, tc::desc_kmajor_sw128(bbase + k16 * 32), idesc,
+                                       (kb | k16) ? 1u : 0u);
+                    tc::mma_commit(&S.aempty[sa.s]);
+                    tc::mma_commit(&S.bempty[sb.s]);
                 }
-                if (!ok) break;
-                tc::mma_commit(&S.acc_full[acc]);
             }
+            if (stop) break;
+            if (issuer && lane == 0) tc::mma_commit(&S.acc_full[acc]);
+        }
+        if (stop && !issuer && lane == 0) {
+            set_status(a.status, MOE_ERR_TIMEOUT);
+            S.abort = 1;
+        }
+        if (issuer && lane == 0) {
             // every MMA of this CTA has finished before TMEM is released
             tc::mma_commit(&S.mma_done);
             if (!tc::mbar_wait(&S.mma_done, 0, kWaitNs)) set_status(a.status, MOE_ERR_TIMEOUT);
@@ -281,14 +415,16 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + 4) {
         // ---------------- epilogue: TMEM -> registers -> shared (transposed) -> TMA store
         const int q = warp - EPI_WARP0;  // TMEM lane quadrant: weight rows 32q .. 32q+31 of the tile
-        float *xch = reinterpret_cast<float *>(dyn + OFF_XCH);
-        int nstore = 0;
+        float *xch = reinterpret_cast<float *>(dyn + C::OFF_E + OFF_XCH);
+        char *stg = dyn + C::OFF_E + q * (SWIGLU ? STG_H : STG_DOWN);  // this warp's staging block
         int j = 0;
         // the gate/up warps meet at named barriers, so they decide together
         // whether to stop (the OR over the four warps); the down warps alone
+        int4 nxt = tile_entry(a, blockIdx.x, total);
         for (int tile = blockIdx.x; tile < total && (SWIGLU || !S.abort); tile += gridDim.x, j++) {
             int acc = j & 1, v = j >> 1;
-            bool stop = !tc::mbar_wait(&S.acc_full[acc], v & 1, kWaitNs);
+            bool stop = !tc::mbar_wait_sleep(&S.acc_full[acc], v & 1, kWaitNs);
+            stop = __any_sync(0xffffffffu, stop);  // the warp's TMEM loads need all its lanes
             if (stop) {
                 if (lane == 0) set_status(a.status, MOE_ERR_TIMEOUT);
                 S.abort = 1;
@@ -297,7 +433,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             if (SWIGLU) stop = tc::named_sync_or(2, 128, stop);
             if (stop) break;
             tc::tc_fence_after();
-            Tile t = decode_tile(a, tile);
+            Tile t = make_tile(a, nxt, tile);
+            nxt = tile_entry(a, tile + gridDim.x, total);
             uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BT);
             for (int ch = 0; ch < t.n32; ch++) {
                 uint32_t r[32];
@@ -322,11 +459,11 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
 #pragma unroll
                         for (int i = 0; i < 32; i++) {
                             float g = __uint_as_float(r[i]);
-                            hv[i] = __half_as_ushort(__float2half_rn(silu(g) * xb[i * 64 + q * 32 + lane]));
+                            hv[i] = __half_as_ushort(__float2half_rn(silu_fast(g) * xb[i * 64 + q * 32 + lane]));
                         }
                         if (full) {
-                            uint16_t *sb = reinterpret_cast<uint16_t *>(dyn + OFF_STG + (q * 2 + (nstore & 1)) * STG_BYTES);
-                            if (lane == 0) tc::bulk_wait_read<1>();
+                            uint16_t *sb = reinterpret_cast<uint16_t *>(stg);
+                            if (lane == 0) tc::bulk_wait_read<0>();
                             __syncwarp();
 #pragma unroll
                             for (int i = 0; i < 32; i++) sb[i * 32 + pos] = hv[i];
@@ -336,7 +473,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                                 tc::tma_store_2d(&out_map, orow0, t.p0 + tok0, sb);
                                 tc::bulk_commit();
                             }
-                            nstore++;
                         } else {
                             uint16_t *dst = a.h_out + (int64_t)(t.p0 + tok0) * a.rows + orow0 + pos;
 #pragma unroll
@@ -348,8 +484,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                     int o0 = t.rt * 128 + q * 32;
                     if (o0 < a.rows) {
                         if (full) {
-                            float *sb = reinterpret_cast<float *>(dyn + OFF_STG + (q * 2 + (nstore & 1)) * STG_BYTES);
-                            if (lane == 0) tc::bulk_wait_read<1>();
+                            float *sb = reinterpret_cast<float *>(stg);
+                            if (lane == 0) tc::bulk_wait_read<0>();
                             __syncwarp();
 #pragma unroll
                             for (int i = 0; i < 32; i++) sb[i * 32 + lane] = __uint_as_float(r[i]);
@@ -359,7 +495,6 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                                 tc::tma_store_2d(&out_map, o0, t.p0 + tok0, sb);
                                 tc::bulk_commit();
                             }
-                            nstore++;
                         } else {
                             float *dst = a.y_out + (int64_t)(t.p0 + tok0) * a.rows + o0 + lane;
 #pragma unroll
@@ -375,70 +510,65 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         }
         if (lane == 0) tc::bulk_wait_all();
         __syncwarp();
-    } else if (warp >= DQ_WARP0) {
-        // ---------------- dequantisation: thread = (row r of the tile, 32-weight half of the stage)
-        const int d = threadIdx.x - DQ_WARP0 * 32;
-        const int r = d & (BM - 1), half = d >> 7;
-        const bool vec_scales = (a.K & 255) == 0;  // rows of scales 16-byte aligned: 8 blocks per load
+    } else if (warp >= DQ_WARP0 && warp < DQ_WARP0 + DQ_WARPS) {
+        // ---------------- dequantisation into TMEM: warp = (lane quadrant qd, 16-weight group gq of the step)
+        const int dw = warp - DQ_WARP0;
+        const int qd = warp & 3, gq = dw >> 2, bq = gq >> 1;  // bq: 32-weight block of the step (0, 1)
+        const int r = qd * 32 + lane;                         // weight row of the tile = TMEM lane
+        const uint32_t tq = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(TM_A + gq * 8);
         int it = 0;
-        for (int tile = blockIdx.x; tile < total && !S.abort; tile += gridDim.x) {
-            Tile t = decode_tile(a, tile);
+        bool aborted = false;
+        int4 nxt = tile_entry(a, blockIdx.x, total);
+        for (int tile = blockIdx.x; tile < total && !S.abort && !aborted; tile += gridDim.x) {
+            Tile t = make_tile(a, nxt, tile);
+            nxt = tile_entry(a, tile + gridDim.x, total);
             int orow = SWIGLU ? t.rt * 64 + (r & 63) : t.rt * 128 + r;
             bool valid = orow < a.rows;
             int64_t mrow = SWIGLU && r >= 64 ? (int64_t)a.up_rows + orow : orow;
+            // scales from global memory only when they cannot come by TMA
             const uint16_t *sp = a.scales + (int64_t)t.e * a.scales_expert_stride + mrow * a.scale_row;
-            uint4 cur4 = make_uint4(0, 0, 0, 0), nxt4 = cur4;
-            if (valid && vec_scales) nxt4 = __ldg(reinterpret_cast<const uint4 *>(sp));
-            uint32_t hw_next = 0;
-            bool aborted = false;
             for (int kb = 0; kb < nk; kb++, it++) {
-                int s = it % STAGES, u = it / STAGES;
+                Slot c = slot_of(it, C::NC), sa = slot_of(it, NA);
                 uint32_t sc = 0;
-                if (valid) {
-                    if (vec_scales) {
-                        if ((kb & 3) == 0) {
-                            cur4 = nxt4;
-                            if (kb + 4 < nk) nxt4 = __ldg(reinterpret_cast<const uint4 *>(sp + 8 * ((kb >> 2) + 1)));
-                        }
-                        int wsel = kb & 3;
-                        uint32_t w2 = wsel == 0 ? cur4.x : wsel == 1 ? cur4.y : wsel == 2 ? cur4.z : cur4.w;
-                        sc = half ? w2 >> 16 : w2 & 0xffffu;
-                    } else {
-                        sc = __ldg(sp + 2 * kb + half);
-                    }
-                }
-                if ((u > 0 && !tc::mbar_wait(&S.empty[s], (u - 1) & 1, kWaitNs)) ||
-                    !tc::mbar_wait(&S.cfull[s], u & 1, kWaitNs)) {
-                    if (lane == 0) set_status(a.status, MOE_ERR_TIMEOUT);
-                    S.abort = 1;
+                if (valid && !a.scale_tma) sc = __ldg(sp + 2 * kb + bq);
+                // the warp moves as one (its TMEM stores need all lanes): lane 0 waits
+                bool ok = lane == 0 ? tc::mbar_wait(&S.cfull[c.s], c.par, kWaitNs) : true;
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
                     aborted = true;
                     break;
                 }
-                char *st = dyn + s * STAGE_BYTES;
-                const char *cs = st + A_BYTES + B_BYTES;
-                char *rowp = st + r * 128;
+                // codes of this step into registers, then the code slot is free
+                const char *cs = dyn + C::OFF_C + c.s * C::C_BYTES;
+                uint32_t cw = 0, hw = 0;
                 if (valid) {
-                    uint2 cw = *reinterpret_cast<const uint2 *>(cs + r * 16 + half * 8);
-                    uint32_t hw = 0;
+                    cw = lds32(cs + C_LO + r * 16 + gq * 4);
+                    if (a.scale_tma)
+                        sc = *reinterpret_cast<const uint16_t *>(cs + C_SC + r * 16 + (2 * (kb & 3) + bq) * 2);
                     if (BITS == 3) {
-                        if (!(kb & 1)) {
-                            hw = lds32(cs + C_BYTES + r * 16 + half * 4);
-                            hw_next = lds32(cs + C_BYTES + r * 16 + 8 + half * 4);
-                        } else {
-                            hw = hw_next;
-                        }
+                        hw = lds32(cs + C_HI + r * 16 + (kb & 1) * 8 + bq * 4);
+                        if (gq & 1) hw >>= 8;  // the block's second 16 weights
                     }
-                    dq_block<BITS>(cw.x, cw.y, hw, sc, rowp, r, half);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 4; c++)
-                        *reinterpret_cast<uint4 *>(rowp + (((4 * half + c) ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
                 }
-                tc::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&S.wfull[s]);
+                if (lane == 0) tc::mbar_arrive(&S.cempty[c.s]);
+                uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                if (valid) dq_group<BITS>(cw, hw, sc, v);
+                ok = lane == 0 && sa.reuse ? tc::mbar_wait(&S.aempty[sa.s], sa.par ^ 1, kWaitNs) : true;
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    aborted = true;
+                    break;
+                }
+                tc::tc_fence_after();
+                tc::tmem_st_32x32b_x8(tq + (uint32_t)(sa.s * 32), v);
+                tc::tmem_st_wait();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&S.afull[sa.s]);
             }
-            if (aborted) break;
+        }
+        if (aborted) {
+            if (lane == 0) set_status(a.status, MOE_ERR_TIMEOUT);
+            S.abort = 1;
         }
     }
     tc::tc_fence_before();
@@ -481,13 +611,15 @@ __global__ void gather_x_kernel(const uint16_t *__restrict__ x, const int32_t *_
 }
 
 template <int BITS, bool SWIGLU>
-static moe_status launch_gemm(const Args &a, const CUtensorMap &tok, const CUtensorMap &codes,
-                              const CUtensorMap &out, int grid, cudaStream_t s)
+static moe_status launch_gemm(const Args &a, const CUtensorMap &tok, const CUtensorMap &tok_full,
+                              const CUtensorMap &codes, const CUtensorMap &scales, const CUtensorMap &out, int grid,
+                              cudaStream_t s)
 {
     auto fn = tc_gemm_kernel<BITS, SWIGLU>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    const int smem = Cfg<BITS>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "tc gemm attribute: %s", cudaGetErrorString(e));
-    fn<<<grid, THREADS, SMEM_BYTES, s>>>(a, tok, codes, out);
+    fn<<<grid, THREADS, smem, s>>>(a, tok, tok_full, codes, scales, out);
     return check_launch(SWIGLU ? "tc_gemm_gateup" : "tc_gemm_down");
 }
 
@@ -495,6 +627,7 @@ static moe_status launch_gemm(const Args &a, const CUtensorMap &tok, const CUten
 
 struct PtcWs {
     int32_t *mt_prefix;
+    int4 *table;
     uint16_t *xg, *h;
     float *y;
     size_t bytes;
@@ -505,13 +638,15 @@ static PtcWs ptc_ws(const moe_expert_arena &A, int T, int k, void *base)
     PtcWs w;
     size_t n = (size_t)T * k;
     size_t tb = align256((A.E + 1) * sizeof(int32_t));
+    size_t tab = align256((n / ptc::BT + A.E + 1) * sizeof(int4));  // pair tiles: at most n/BT + one partial per expert
     size_t xb = align256(n * A.H * 2), hb = align256(n * A.I * 2), yb = align256(n * A.H * 4);
     char *b = static_cast<char *>(base);
     w.mt_prefix = reinterpret_cast<int32_t *>(b);
-    w.xg = b ? reinterpret_cast<uint16_t *>(b + tb) : nullptr;
-    w.h = b ? reinterpret_cast<uint16_t *>(b + tb + xb) : nullptr;
-    w.y = b ? reinterpret_cast<float *>(b + tb + xb + hb) : nullptr;
-    w.bytes = tb + xb + hb + yb;
+    w.table = b ? reinterpret_cast<int4 *>(b + tb) : nullptr;
+    w.xg = b ? reinterpret_cast<uint16_t *>(b + tb + tab) : nullptr;
+    w.h = b ? reinterpret_cast<uint16_t *>(b + tb + tab + xb) : nullptr;
+    w.y = b ? reinterpret_cast<float *>(b + tb + tab + xb + hb) : nullptr;
+    w.bytes = tb + tab + xb + hb + yb;
     return w;
 }
 
@@ -537,6 +672,9 @@ static moe_status run_tc(const moe_expert_arena &A, const uint16_t *x, int T, co
     tile_prefix_kernel<<<1, 1024, 0, s>>>(offsets, A.E, BT, d.mt_prefix);
     moe_status st = check_launch("tile_prefix");
     if (st != MOE_OK) return st;
+    tile_table_kernel<<<(A.E + 255) / 256, 256, 0, s>>>(offsets, d.mt_prefix, A.E, BT, d.table);
+    st = check_launch("tile_table");
+    if (st != MOE_OK) return st;
     int64_t gthreads = n * (A.H / 16);
     int gblocks = (int)std::min<int64_t>((gthreads + 255) / 256, (int64_t)sm_count() * 16);
     gather_x_kernel<<<gblocks, 256, 0, s>>>(x, perm, offsets, A.E, k, A.H, d.xg);
@@ -547,14 +685,21 @@ static moe_status run_tc(const moe_expert_arena &A, const uint16_t *x, int T, co
     int grid = sm_count();
     const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     // gate/up: codes [E * 2I][rbH], pairs' rows xg [n][H] -> h [n][I]
-    CUtensorMap mtok, mcode, mout;
+    CUtensorMap mtok, mtokf, mcode, mscale, mout;
     st = make_tmap_2d(&mtok, d.xg, F16, 2, n, A.H, BK, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == MOE_OK) st = make_tmap_2d(&mtokf, d.xg, F16, 2, n, A.H, BK, BT, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st == MOE_OK)
         st = make_tmap_2d(&mcode, A.gu_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (int64_t)A.E * 2 * A.I, rbH, 16, 64,
                           CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st == MOE_OK) st = make_tmap_2d(&mout, d.h, F16, 2, n, A.I, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+    bool sc_gu = A.H % 256 == 0;  // scale rows (H/32 fp16) are 16-byte multiples
+    mscale = mcode;
+    if (st == MOE_OK && sc_gu)
+        st = make_tmap_2d(&mscale, A.gu_scales, F16, 2, (int64_t)A.E * 2 * A.I, A.H / 32, 8, 64,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != MOE_OK) return st;
     Args a = {};
+    a.scale_tma = sc_gu;
     a.scales = A.gu_scales;
     a.scales_expert_stride = (int64_t)2 * A.I * (A.H / 32);
     a.code_rows = (int64_t)2 * A.I;
@@ -564,22 +709,27 @@ static moe_status run_tc(const moe_expert_arena &A, const uint16_t *x, int T, co
     a.up_rows = A.I;
     a.rtiles = (A.I + 63) / 64;
     a.hi_x = A.H / 4;
-    a.offsets = offsets;
-    a.mt_prefix = d.mt_prefix;
-    a.E = A.E;
+    a.table = d.table;
+    a.ntt = d.mt_prefix + A.E;
     a.h_out = d.h;
     a.status = status;
-    st = launch_gemm<BITS, true>(a, mtok, mcode, mout, grid, s);
+    st = launch_gemm<BITS, true>(a, mtok, mtokf, mcode, mscale, mout, grid, s);
     if (st != MOE_OK) return st;
     // down: codes [E * H][rbI], h [n][I] -> y [n][H]
     st = make_tmap_2d(&mtok, d.h, F16, 2, n, A.I, BK, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == MOE_OK) st = make_tmap_2d(&mtokf, d.h, F16, 2, n, A.I, BK, BT, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st == MOE_OK)
         st = make_tmap_2d(&mcode, A.d_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (int64_t)A.E * A.H, rbI, 16, 64,
                           CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st == MOE_OK)
         st = make_tmap_2d(&mout, d.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, n, A.H, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+    bool sc_d = A.I % 256 == 0;
+    mscale = mcode;
+    if (st == MOE_OK && sc_d)
+        st = make_tmap_2d(&mscale, A.d_scales, F16, 2, (int64_t)A.E * A.H, A.I / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != MOE_OK) return st;
     Args b = a;
+    b.scale_tma = sc_d;
     b.scales = A.d_scales;
     b.scales_expert_stride = (int64_t)A.H * (A.I / 32);
     b.code_rows = A.H;
@@ -591,7 +741,7 @@ static moe_status run_tc(const moe_expert_arena &A, const uint16_t *x, int T, co
     b.hi_x = A.I / 4;
     b.h_out = nullptr;
     b.y_out = d.y;
-    st = launch_gemm<BITS, false>(b, mtok, mcode, mout, grid, s);
+    st = launch_gemm<BITS, false>(b, mtok, mtokf, mcode, mscale, mout, grid, s);
     if (st != MOE_OK) return st;
     return launch_combine(d.y, w, inv, T, k, A.H, out, dt, accumulate, s);
 }
