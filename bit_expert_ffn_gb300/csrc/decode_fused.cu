@@ -1,16 +1,20 @@
 // decode_fused.cu -- moe_decode_forward: a stack of MoE layers for up to four
-// tokens in one persistent cooperative kernel.
+// tokens in one persistent cooperative kernel (one CTA per SM).
 //
-// Per layer, with a residual stream x (fp32) and xb = bf16(x):
-//   phase A  router logits W_r xb + b, shared gate/up h_s = silu(Wg xb)*(Wu xb)
-//   -- grid barrier --
-//   phase B  top-k + renormalised softmax (every CTA, redundantly, from the
-//            logits), grouping of the (token, slot) pairs by expert, routed
-//            gate/up h_p = silu(dq(Wg_e) xb_t) * dq(Wu_e) xb_t
-//   -- grid barrier --
-//   phase C  routed down dq(Wd_e) h_p and shared down Wd_s h_s for this CTA's
-//            output rows, then x[t][o] += sum_j w_tj y_j[o] + S[o] (slot order)
-//   -- grid barrier --
+// Per layer, with a residual stream x (fp32) and u = bf16(x / rms(x)):
+//   gather   every CTA reads the whole x (tagged words written by the owners
+//            of its rows in the previous layer), normalises it and keeps u in
+//            shared memory, both in natural order and as MMA operand pairs
+//   A        router logits W_r u + b of this CTA's router rows -> tagged words
+//   A'       shared gate/up h_s = silu(Wg u) * (Wu u) of this CTA's rows
+//   routing  every CTA reads all logits (tagged words), takes the top-k of
+//            each token, the renormalised softmax weights and the groups of
+//            (token, slot) pairs that share an expert
+//   B        routed gate/up: this CTA's share of the (group, 16-row tile)
+//            units, h = silu(dq(Wg_e) u) * dq(Wu_e) u, on the tensor cores
+//   -- h counter barrier --
+//   C        routed down dq(Wd_e) h and shared down Wd_s h_s of this CTA's
+//            output rows, then x[t][o] += sum_j w_tj y_j[o] + S[o]
 // The pages put a router, ten of 512 experts and an always-on shared expert
 // in each of 48 layers ("Strata Open-Source Runtime: Running a 125B-Parameter
 // Qwen3 Model on a 12GB GPU", section "The Model Itself") and sum the expert
@@ -18,28 +22,37 @@
 // Step 2); verify windows hold up to four tokens ("Strata serves a 125B MoE
 // ...", section "Six billion active parameters per token").
 //
-// Every CTA is resident (cooperative launch); the barriers are a counter in
-// the workspace with acquire/release ordering and a %globaltimer deadline
-// after which the kernel records MOE_ERR_TIMEOUT and returns.  A token's
-// result is computed with a fixed split and reduction order that does not
-// depend on the other tokens of the call.
+// Weights move by bulk asynchronous copies (TMA, one row per copy into padded
+// shared-memory slots) completing on mbarriers; the next layer's router and
+// shared-expert rows are fetched while this layer finishes.  Routed products
+// run on mma.sync bf16 tensor-core instructions: a 2-/3-bit code c is turned
+// into the exact bf16 value c (one LOP3 + one HFMA2 per pair of weights), the
+// MMA sums c*u exactly per 32-weight block (one block per accumulator
+// column), and the block scale and the code offset are applied in fp32:
+// sum_i (c_i - mid) u_i s = s * (sum_i c_i u_i - mid * sum_i u_i).  The down
+// projection's fp32 h enters as two bf16 parts (h = hi + lo to 2^-17), so no
+// operand is rounded beyond fp32 accumulation.  Every wait (mbarrier, counter,
+// tagged word) gives up after about 2 s, records MOE_ERR_TIMEOUT and raises an
+// abort flag that the other CTAs check.  A token's result is computed by the
+// same instruction sequence whatever the other tokens of the call are.
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace moe {
 namespace fused {
 
 constexpr int kMaxLayers = 64;
-constexpr int kMaxWarps = 16;  // warps per CTA: 16 for one token, 8 for more
-template <int T>
-__host__ __device__ constexpr int warps_for() { return T == 1 ? 16 : 8; }
 constexpr int kMaxT = 4;
 constexpr int kMaxK = 16;
 constexpr int kMaxPairs = kMaxT * kMaxK;
-constexpr int kMaxCand = 512;  // k lanes x 32 values per lane at most
-constexpr int kRB = 4;         // units per phase-B batch (team partial sums)
-constexpr int kMaxChunks = 128;  // phase-B / phase-C chunk list entries per CTA
-constexpr unsigned long long kBarrierTimeoutNs = 2000000000ull;
+constexpr int kMaxUnitSlots = 16;
+constexpr int kMaxDownSlots = kMaxPairs;
+constexpr int kRedV = 256;  // fixed number of partial sums in the RMS reduction
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr unsigned kAbort = 0x80000000u;
+
+template <int T>
+__host__ __device__ constexpr int warps_for() { return T == 1 ? 16 : 8; }
 
 struct Layer {
     const uint8_t *gu_codes;
@@ -54,16 +67,32 @@ struct Layer {
 struct Args {
     Layer L[kMaxLayers];
     int n_layers, T, H, I, E, k, Is, bits;
-    int rows_per_cta;
+    int rpc;           // output rows per CTA (even, <= 16)
     float rms_eps;     // < 0: no normalisation in front of each layer
-    float *x;          // [T][H] residual stream, in/out
-    float *logits;     // [T][E]
-    float *h;          // [T*k][I] routed h in sorted pair order
+    float *x;          // [T][H] residual stream, in/out (read at layer 0, written after the last)
+    uint64_t *xll;     // [2][T][H] tagged x between layers
+    uint64_t *lgll;    // [2][T][E] tagged router logits
+    uint32_t *hop;     // [T*k][I/32][2][16] routed h as bf16 operand pairs (high, low parts), sorted pair order
+    float *hsum;       // [T*k][I/16] sums of 16 consecutive h values
     float *hs;         // [T][Is] shared h
-    unsigned *bar;     // barrier counter (zero at launch)
+    unsigned *cnt;     // [0] h counter, [1] h_s counter, [2] abort word
     int32_t *ids_out;  // [n_layers][T][k] or NULL
     float *w_out;
     int32_t *status;
+};
+
+// Shared-memory plan (host-computed): strides, slot sizes, byte offsets.
+struct Plan {
+    int cb_gu, sb_gu;                // gate/up code and scale row bytes
+    int cb_d, sb_d;                  // down code and scale row bytes
+    int unitB, nsu;                  // bytes per unit slot (16 gate + 16 up rows), number of slots
+    int downB, nsd;                  // bytes per down slot (16 code rows + scales), number of slots
+    int NST, NSD2;                   // gate/up super-tiles (256 wide), down super-tiles (128 wide)
+    int rA, sA;                      // max router rows, max shared rows per CTA
+    int xp_stride;                   // bytes per block of operand pairs (80: conflict-free 16-byte reads)
+    int off_xb, off_xp, off_xs, off_lg, off_r1, off_r2, off_r3, off_hs, off_pgu, off_pd, off_xown, off_hop, off_hsum;
+    int stage_h;                     // h's operand words staged in shared memory for the down items
+    int r1B, smem;
 };
 
 struct Routing {
@@ -73,21 +102,27 @@ struct Routing {
     int inv[kMaxPairs];   // flat -> sorted position
     int g_e[kMaxPairs], g_p0[kMaxPairs], g_n[kMaxPairs];
     int ngroups;
-    float cand_v[kMaxT][kMaxCand];
-    int cand_i[kMaxT][kMaxCand];
-    float sel_v[kMaxT][kMaxK];
     int sel_i[kMaxT][kMaxK];
-    float team[kMaxWarps][kRB][2][kMaxT];  // phase-B partials of each warp
-    float wsum[kMaxT][kMaxWarps];
-    float wmax_v[kMaxWarps];
-    int wmax_i[kMaxWarps];
+    float sel_v[kMaxT][kMaxK];
+    float inv_rms[kMaxT];
+    float wred[kMaxT][8];
+    float gmax_v[32];
+    int gmax_i[32];
     float tau_v;
     int tau_i, tau_all, ncand;
-    float inv_rms[kMaxT];
-    int b_g[kMaxChunks], b_r[kMaxChunks], b_n[kMaxChunks], nb;  // phase-B chunks: group, first row, rows
-    int c_g[kMaxChunks], c_n[kMaxChunks], nc;                   // phase-C chunks: first group, groups
+    int u0, nu;                     // this CTA's units [u0, u0 + nu)
+    int fills_u[kMaxUnitSlots];     // completed fills per unit slot before this layer
+    int fills_d[kMaxDownSlots];
+    int ucnt[kMaxUnitSlots];        // finished items of the unit in each slot
+    int dcnt[kMaxDownSlots];
+    int fillsA, fillsS;             // fills of the router/shared-rows and shared-down barriers
     int abort;
+    uint64_t fullU[kMaxUnitSlots];
+    uint64_t fullD[kMaxDownSlots];
+    uint64_t fullA, fullS;
 };
+
+// ------------------------------------------------------------ memory helpers
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
 {
@@ -101,31 +136,97 @@ __device__ __forceinline__ void red_release_add(unsigned *p, unsigned v)
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ unsigned long long globaltimer()
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t *p)
 {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
 }
 
-// Grid-wide barrier: every CTA adds one to *bar and waits until it reaches
-// `target`.  Gives up after timeout_ns (recording MOE_ERR_TIMEOUT and setting
-// the abort bit so the other CTAs stop waiting too).  Returns false when the
-// barrier failed; `flag` is a shared-memory word for the CTA-wide answer.
-__device__ bool barrier_wait(unsigned *bar, unsigned target, unsigned long long timeout_ns, int32_t *status,
-                             int &flag)
+__device__ __forceinline__ void st_relaxed_u64(uint64_t *p, uint64_t v)
 {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t tagged(float v, unsigned tag)
+{
+    return (uint64_t)__float_as_uint(v) | ((uint64_t)tag << 32);
+}
+
+// One bulk asynchronous copy global -> shared completing on `bar` (16-byte
+// aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     tc::smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool aborted(const Args &a) { return (ld_acquire(a.cnt + 2) & kAbort) != 0; }
+
+__device__ __forceinline__ void raise_abort(const Args &a)
+{
+    set_status(a.status, MOE_ERR_TIMEOUT);
+    atomicOr(a.cnt + 2, kAbort);
+}
+
+// Wait (one thread) until *c >= target; false on timeout or abort.
+__device__ bool wait_counter(const Args &a, const unsigned *c, unsigned target)
+{
+    unsigned long long t0 = tc::now_ns();
+    for (;;) {
+        if (ld_acquire(c) >= target) return true;
+        if (ld_acquire(a.cnt + 2) & kAbort) return false;
+        if (tc::now_ns() - t0 > kTimeoutNs) {
+            raise_abort(a);
+            return false;
+        }
+    }
+}
+
+// Wait for a tagged word; false on timeout or abort (checked every 64 polls).
+__device__ __forceinline__ bool wait_tagged(const Args &a, const uint64_t *p, unsigned tag, float &v)
+{
+    uint64_t w = ld_relaxed_u64(p);
+    if ((unsigned)(w >> 32) == tag) {
+        v = __uint_as_float((unsigned)w);
+        return true;
+    }
+    unsigned long long t0 = tc::now_ns();
+    for (int it = 1;; it++) {
+        w = ld_relaxed_u64(p);
+        if ((unsigned)(w >> 32) == tag) {
+            v = __uint_as_float((unsigned)w);
+            return true;
+        }
+        if ((it & 63) == 0) {
+            if (ld_acquire(a.cnt + 2) & kAbort) return false;
+            if (tc::now_ns() - t0 > kTimeoutNs) {
+                raise_abort(a);
+                return false;
+            }
+        }
+    }
+}
+
+// Barrier-style self-test used by moe_selftest_barrier: one counter barrier
+// whose target exceeds the number of CTAs by `extra`.
+__global__ void barrier_probe_kernel(unsigned *bar, unsigned extra, unsigned long long timeout_ns, int32_t *status,
+                                     int32_t *passed)
+{
+    __shared__ int flag;
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
         red_release_add(bar, 1u);
-        unsigned long long t0 = globaltimer();
+        unsigned long long t0 = tc::now_ns();
         int ab = 0;
         for (;;) {
             unsigned v = ld_acquire(bar);
             if (v & kAbort) { ab = 1; break; }
-            if (v >= target) break;
-            if (globaltimer() - t0 > timeout_ns) {
+            if (v >= gridDim.x + extra) break;
+            if (tc::now_ns() - t0 > timeout_ns) {
                 set_status(status, MOE_ERR_TIMEOUT);
                 atomicOr(bar, kAbort);
                 ab = 1;
@@ -135,23 +236,7 @@ __device__ bool barrier_wait(unsigned *bar, unsigned target, unsigned long long 
         flag = ab;
     }
     __syncthreads();
-    return flag == 0;
-}
-
-// Barrier number n (1-based) of the decode kernel.
-__device__ __forceinline__ bool grid_barrier(const Args &a, Routing &R, unsigned n)
-{
-    return barrier_wait(a.bar, n * gridDim.x, kBarrierTimeoutNs, a.status, R.abort);
-}
-
-// Self-test of the barrier's time limit: one barrier whose target exceeds the
-// number of CTAs by `extra`, so for extra > 0 it can only end by timing out.
-__global__ void barrier_probe_kernel(unsigned *bar, unsigned extra, unsigned long long timeout_ns, int32_t *status,
-                                     int32_t *passed)
-{
-    __shared__ int flag;
-    bool ok = barrier_wait(bar, gridDim.x + extra, timeout_ns, status, flag);
-    if (ok && threadIdx.x == 0) atomicAdd(passed, 1);
+    if (flag == 0 && threadIdx.x == 0) atomicAdd(passed, 1);
 }
 
 __device__ __forceinline__ bool before(float av, int ai, float bv, int bi)
@@ -159,188 +244,73 @@ __device__ __forceinline__ bool before(float av, int ai, float bv, int bi)
     return av > bv || (av == bv && ai < bi);
 }
 
-// ------------------------------------------------------------ async copies
-// Every thread copies its share of a contiguous range in 16-byte pieces
-// (cp.async, L2-only); a commit group then covers one logical transfer.
-__device__ __forceinline__ void cp16(void *dst, const void *src)
+__device__ __forceinline__ float warp_sum(float v)
 {
-    uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
 }
-
-__device__ __forceinline__ void cp8(void *dst, const void *src)
-{
-    uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp4(void *dst, const void *src)
-{
-    uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
-}
-
-// Pieces of 16, 8 or 4 bytes, the largest that the addresses and length allow
-// (the host only admits shapes whose rows are multiples of 4 bytes).
-__device__ __forceinline__ void copy_range(void *dst, const void *src, uint32_t bytes)
-{
-    char *d = static_cast<char *>(dst);
-    const char *s = static_cast<const char *>(src);
-    uint32_t al = (uint32_t)(reinterpret_cast<uintptr_t>(d) | reinterpret_cast<uintptr_t>(s) | bytes);
-    if ((al & 15u) == 0) {
-        for (uint32_t off = threadIdx.x * 16u; off < bytes; off += blockDim.x * 16u) cp16(d + off, s + off);
-    } else if ((al & 7u) == 0) {
-        for (uint32_t off = threadIdx.x * 8u; off < bytes; off += blockDim.x * 8u) cp8(d + off, s + off);
-    } else {
-        for (uint32_t off = threadIdx.x * 4u; off < bytes; off += blockDim.x * 4u) cp4(d + off, s + off);
-    }
-}
-
-__device__ __forceinline__ void commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
-// Wait until commit group number `gi` (0-based, in commit order) has landed,
-// given that `ncommit` groups have been committed.  Waiting for more groups
-// than needed is always safe, so larger distances are clamped.
-__device__ __forceinline__ void wait_group_index(int gi, int ncommit)
-{
-    int n = ncommit - 1 - gi;
-    if (n <= 0) asm volatile("cp.async.wait_group 0;" ::: "memory");
-    else if (n == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
-    else if (n == 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
-    else if (n == 3) asm volatile("cp.async.wait_group 3;" ::: "memory");
-    else if (n == 4) asm volatile("cp.async.wait_group 4;" ::: "memory");
-    else if (n == 5) asm volatile("cp.async.wait_group 5;" ::: "memory");
-    else if (n == 6) asm volatile("cp.async.wait_group 6;" ::: "memory");
-    else asm volatile("cp.async.wait_group 7;" ::: "memory");
-}
-
-__device__ __forceinline__ void wait_all_copies() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // ------------------------------------------------------------ routing
 
-// Top-k of one token's logits by one warp.  Every logit is loaded once into
-// registers.  The k-th best of the 32 lane maxima bounds the k-th best
-// overall, so only values at or before it are candidates, and candidates are
-// ranked exactly among themselves.  Returns true for a NaN logit.
-__device__ bool topk_warp(const float *__restrict__ l, int E, int k, Routing &R, int t)
+// Top-k of one token's logits (in shared memory) by the whole CTA.  The
+// logits are cut into groups of 16 threads' elements; at least k groups hold
+// an element no worse than the k-th best group maximum tau, so the k best
+// logits are all at or before tau (otherwise, with fewer than k non-empty
+// groups, every logit is a candidate).  Candidates are ranked exactly among
+// themselves by (value desc, id asc).  `cv`, `ci` hold up to E candidates.
+// Returns true for a NaN logit (the token then gets ids 0..k-1).
+__device__ bool topk_cta(const float *l, int E, int k, Routing &R, int t, float *cv, int *ci)
 {
-    int lane = lane_id();
-    float v[32];
-#pragma unroll
-    for (int q = 0; q < 32; q++) {
-        int e = lane + 32 * q;
-        v[q] = (e < E) ? __ldcg(l + e) : 0.f;
-    }
-    float mv = 0.f;
-    int mi = INT32_MAX;
+    const int tid = threadIdx.x, nthr = blockDim.x, lane = lane_id();
+    float bv = 0.f;
+    int bi = INT32_MAX;
     bool nan = false;
-#pragma unroll
-    for (int q = 0; q < 32; q++) {
-        int e = lane + 32 * q;
-        if (e < E) {
-            nan |= isnan(v[q]);
-            if (mi == INT32_MAX || before(v[q], e, mv, mi)) {
-                mv = v[q];
-                mi = e;
-            }
+    for (int e = tid; e < E; e += nthr) {
+        const float v = l[e];
+        nan |= isnan(v);
+        if (bi == INT32_MAX || before(v, e, bv, bi)) {
+            bv = v;
+            bi = e;
         }
     }
-    if (__any_sync(0xffffffffu, nan)) {
-        if (lane < k) {
-            R.sel_i[t][lane] = lane;
-            R.sel_v[t][lane] = 0.f;
-        }
-        __syncwarp();
-        return true;
-    }
-    int rank = 0;
-    for (int s = 0; s < 32; s++) {
-        float ov = __shfl_sync(0xffffffffu, mv, s);
-        int oi = __shfl_sync(0xffffffffu, mi, s);
-        if (oi != INT32_MAX && mi != INT32_MAX && before(ov, oi, mv, mi)) rank++;
-    }
-    unsigned who = __ballot_sync(0xffffffffu, mi != INT32_MAX && rank == k - 1);
-    int src = __ffs(who) - 1;  // min(E, 32) >= k valid lane maxima: exactly one has rank k-1
-    float tv = __shfl_sync(0xffffffffu, mv, src);
-    int ti = __shfl_sync(0xffffffffu, mi, src);
-    int base = 0;
-#pragma unroll
-    for (int q = 0; q < 32; q++) {
-        int e = lane + 32 * q;
-        bool c = e < E && (before(v[q], e, tv, ti) || (v[q] == tv && e == ti));
-        unsigned m = __ballot_sync(0xffffffffu, c);
-        if (c) {
-            int pos = base + __popc(m & ((1u << lane) - 1u));
-            R.cand_v[t][pos] = v[q];
-            R.cand_i[t][pos] = e;
-        }
-        base += __popc(m);
-    }
-    __syncwarp();
-    int C = base;
-    for (int c = lane; c < C; c += 32) {
-        float cv = R.cand_v[t][c];
-        int ce = R.cand_i[t][c];
-        int r = 0;
-        for (int d = 0; d < C; d++) r += before(R.cand_v[t][d], R.cand_i[t][d], cv, ce) ? 1 : 0;
-        if (r < k) {
-            R.sel_v[t][r] = cv;
-            R.sel_i[t][r] = ce;
-        }
-    }
-    __syncwarp();
-    return false;
-}
-
-// Top-k of a single token's logits by the whole CTA (T = 1).  Each thread
-// holds up to two logits.  With at least k warps holding logits, the k-th
-// best warp maximum bounds the k-th best logit, so only logits at or before
-// it are candidates (otherwise every logit is); candidates are ranked exactly
-// among themselves.  Returns true for a NaN logit.
-__device__ bool topk_block(const float *__restrict__ l, int E, int k, Routing &R)
-{
-    int tid = threadIdx.x, lane = lane_id(), warp = warp_id(), nw = blockDim.x >> 5, nthr = blockDim.x;
-    int e0 = tid, e1 = tid + nthr;
-    bool h0 = e0 < E, h1 = e1 < E;
-    float v0 = h0 ? __ldcg(l + e0) : 0.f, v1 = h1 ? __ldcg(l + e1) : 0.f;
-    bool nan = (h0 && isnan(v0)) || (h1 && isnan(v1));
     if (__syncthreads_or(nan)) {
         if (tid < k) {
-            R.sel_i[0][tid] = tid;
-            R.sel_v[0][tid] = 0.f;
+            R.sel_i[t][tid] = tid;
+            R.sel_v[t][tid] = 0.f;
         }
         __syncthreads();
         return true;
     }
-    float mv = 0.f;
-    int mi = INT32_MAX;
-    if (h0) { mv = v0; mi = e0; }
-    if (h1 && (mi == INT32_MAX || before(v1, e1, mv, mi))) { mv = v1; mi = e1; }
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, mv, o);
-        int oi = __shfl_xor_sync(0xffffffffu, mi, o);
-        if (oi != INT32_MAX && (mi == INT32_MAX || before(ov, oi, mv, mi))) { mv = ov; mi = oi; }
+    for (int o = 8; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (oi != INT32_MAX && (bi == INT32_MAX || before(ov, oi, bv, bi))) {
+            bv = ov;
+            bi = oi;
+        }
     }
-    if (lane == 0) {
-        R.wmax_v[warp] = mv;
-        R.wmax_i[warp] = mi;
+    const int ngrp = nthr / 16;
+    if ((lane & 15) == 0) {
+        R.gmax_v[tid >> 4] = bv;
+        R.gmax_i[tid >> 4] = bi;
     }
     if (tid == 0) R.ncand = 0;
     __syncthreads();
-    if (warp == 0) {
-        float wv = lane < nw ? R.wmax_v[lane] : 0.f;
-        int wi = lane < nw ? R.wmax_i[lane] : INT32_MAX;
+    if (tid < 32) {
+        const float gv = lane < ngrp ? R.gmax_v[lane] : 0.f;
+        const int gi = lane < ngrp ? R.gmax_i[lane] : INT32_MAX;
         int r = 0;
-        for (int q = 0; q < nw; q++) {
-            int oi = R.wmax_i[q];
-            if (oi != INT32_MAX && wi != INT32_MAX && before(R.wmax_v[q], oi, wv, wi)) r++;
+        for (int q = 0; q < ngrp; q++) {
+            const int oi = R.gmax_i[q];
+            if (oi != INT32_MAX && gi != INT32_MAX && before(R.gmax_v[q], oi, gv, gi)) r++;
         }
-        unsigned valid = __ballot_sync(0xffffffffu, wi != INT32_MAX);
-        unsigned who = __ballot_sync(0xffffffffu, wi != INT32_MAX && r == k - 1);
-        int src = who ? __ffs(who) - 1 : 0;
-        float tv = __shfl_sync(0xffffffffu, wv, src);
-        int ti = __shfl_sync(0xffffffffu, wi, src);
+        const unsigned valid = __ballot_sync(0xffffffffu, gi != INT32_MAX);
+        const unsigned who = __ballot_sync(0xffffffffu, gi != INT32_MAX && r == k - 1);
+        const int src = who ? __ffs(who) - 1 : 0;
+        const float tv = __shfl_sync(0xffffffffu, gv, src);
+        const int ti = __shfl_sync(0xffffffffu, gi, src);
         if (lane == 0) {
             R.tau_all = __popc(valid) < k;
             R.tau_v = tv;
@@ -348,30 +318,27 @@ __device__ bool topk_block(const float *__restrict__ l, int E, int k, Routing &R
         }
     }
     __syncthreads();
-    float tv = R.tau_v;
-    int ti = R.tau_i;
-    bool all = R.tau_all;
-    float *cv = &R.cand_v[0][0];
-    int *ci = &R.cand_i[0][0];
-    if (h0 && (all || before(v0, e0, tv, ti) || (v0 == tv && e0 == ti))) {
-        int pos = atomicAdd(&R.ncand, 1);
-        cv[pos] = v0;
-        ci[pos] = e0;
-    }
-    if (h1 && (all || before(v1, e1, tv, ti) || (v1 == tv && e1 == ti))) {
-        int pos = atomicAdd(&R.ncand, 1);
-        cv[pos] = v1;
-        ci[pos] = e1;
+    const float tv = R.tau_v;
+    const int ti = R.tau_i;
+    const bool all = R.tau_all;
+    for (int e = tid; e < E; e += nthr) {
+        const float v = l[e];
+        if (all || before(v, e, tv, ti) || (v == tv && e == ti)) {
+            const int pos = atomicAdd(&R.ncand, 1);
+            cv[pos] = v;
+            ci[pos] = e;
+        }
     }
     __syncthreads();
-    int C = R.ncand;
+    const int C = R.ncand;
     for (int c = tid; c < C; c += nthr) {
-        float x = cv[c];
-        int e = ci[c], r = 0;
+        const float x = cv[c];
+        const int e = ci[c];
+        int r = 0;
         for (int d = 0; d < C; d++) r += before(cv[d], ci[d], x, e) ? 1 : 0;
         if (r < k) {
-            R.sel_v[0][r] = x;
-            R.sel_i[0][r] = e;
+            R.sel_v[t][r] = x;
+            R.sel_i[t][r] = e;
         }
     }
     __syncthreads();
@@ -399,7 +366,7 @@ __device__ void topk_weights(Routing &R, int t, int k, bool nan_token)
     }
 }
 
-// Sort the T*k pairs by (expert, flat index) and cut them into groups.
+// Sort the T*k pairs by (expert, flat index) and cut them into groups (one warp).
 __device__ void build_groups(Routing &R, int n)
 {
     int lane = lane_id();
@@ -436,467 +403,335 @@ __device__ void build_groups(Routing &R, int n)
     __syncwarp();
 }
 
-// ------------------------------------------------------------ chunk dots
-// (exact dequantisation through fp16x2 words with exponent of 1.0, then the
-// block-sum identity sum (c - mid) v = 2^B sum (1 + c/2^B) v - (2^B + mid) sum v)
+// ------------------------------------------------------------ tensor-core pieces
 
-__device__ __forceinline__ float2 h2f(uint32_t b)
+// D += A * B for one m16n8k16 tile, bf16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t hfma2_bf16(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Codes of a 16-weight word: weight j at bits 2j..2j+1 (low plane).  Pair M
+// (weights M and M+8, bits 2M and 2M+16) becomes the bf16x2 (c_M, c_{M+8})
+// exactly: the codes are OR-ed into the mantissa of 128.0 at bit 2M' (M' =
+// M mod 3 after a shift of the word by 0, 6 or 12 bits), giving 128 + c*4^M',
+// and one fma with (4^-M', -128*4^-M') leaves c.  For 3 bits the high bit of
+// each weight (the word `hw`, bit M+8w and M+8w+16 for word w of the block)
+// joins at bit 2M'+2: 128 + (lo + 4 hi)*4^M' stays below 256, so exact too.
+template <int M, int BITS, int W>
+__device__ __forceinline__ uint32_t dq_pair(uint32_t w0, uint32_t w6, uint32_t w12, uint32_t hw)
+{
+    constexpr int MP = M < 3 ? M : (M < 6 ? M - 3 : M - 6);
+    const uint32_t src = M < 3 ? w0 : (M < 6 ? w6 : w12);
+    uint32_t v = src & (0x00030003u << (2 * MP));
+    if constexpr (BITS == 3) {
+        constexpr int SH = 8 * W + M - 2 * MP - 2;  // bring bit (8W+M) to bit 2MP+2
+        uint32_t hb = SH >= 0 ? (hw >> (SH >= 0 ? SH : 0)) : (hw << (SH < 0 ? -SH : 0));
+        v |= hb & (0x00010001u << (2 * MP + 2));
+    }
+    v |= 0x43004300u;
+    constexpr uint32_t kMul = MP == 0 ? 0x3F803F80u : (MP == 1 ? 0x3E803E80u : 0x3D803D80u);
+    constexpr uint32_t kAdd = MP == 0 ? 0xC300C300u : (MP == 1 ? 0xC200C200u : 0xC100C100u);
+    return hfma2_bf16(v, kMul, kAdd);
+}
+
+__device__ __forceinline__ float2 h2f2(uint32_t b)
 {
     __half2 h = *reinterpret_cast<__half2 *>(&b);
     return __half22float2(h);
 }
 
-template <int S>
-__device__ __forceinline__ uint32_t sh(uint32_t w)
-{
-    if constexpr (S > 0) return w << S;
-    else if constexpr (S < 0) return w >> (-S);
-    else return w;
-}
+__device__ __forceinline__ uint32_t pack_bf16(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
 
-template <int NV, int BITS>
-__device__ __forceinline__ void dot_word(uint32_t w, uint32_t hw, const float (&v)[NV][32], int off,
-                                         float (&acc)[NV][2])
-{
-#define MOE_F_PAIR(M)                                                                                  \
-    {                                                                                                  \
-        uint32_t b;                                                                                    \
-        if (BITS == 2) b = (sh<8 - 2 * (M)>(w) & 0x03000300u) | 0x3C003C00u;                           \
-        else b = (sh<7 - 2 * (M)>(w) & 0x01800180u) | (sh<9 - (M)>(hw) & 0x02000200u) | 0x3C003C00u;  \
-        float2 f = h2f(b);                                                                             \
-        _Pragma("unroll") for (int t = 0; t < NV; t++) {                                               \
-            acc[t][0] = fmaf(f.x, v[t][off + (M)], acc[t][0]);                                         \
-            acc[t][1] = fmaf(f.y, v[t][off + (M) + 8], acc[t][1]);                                     \
-        }                                                                                              \
-    }
-    MOE_F_PAIR(0) MOE_F_PAIR(1) MOE_F_PAIR(2) MOE_F_PAIR(3)
-    MOE_F_PAIR(4) MOE_F_PAIR(5) MOE_F_PAIR(6) MOE_F_PAIR(7)
-#undef MOE_F_PAIR
-}
-
-struct QChunk {
-    uint32_t lo0, lo1, hi;
-    uint16_t s;
+// Per-token operand pairs of one 256-wide super-tile: word i = w*8+m of the
+// thread's block (block 8s+tig for gid == tig, 8s+tig+4 for gid == tig+4).
+template <int T>
+struct XFrag {
+    uint32_t r[T][16];
 };
 
-// One 32-weight chunk of a packed row that sits in shared memory.
-template <int BITS>
-__device__ __forceinline__ QChunk qload_s(const uint8_t *rowc, const uint16_t *rows, int cols, int chunk)
+// One gate/up work item: matrix `mtx` (0 gate, 1 up) of the unit in `slot`,
+// super-tile s (columns 256s .. 256s+255), for the n tokens of the unit's
+// group.  MMA k-pair j (j < 4) carries block 8s+2j and k-pair j+4 block
+// 8s+2j+1, so a thread's A operand is one 16-byte read per row; accumulator
+// column c sums block 8s+c.  Writes per-row partial sums (over the
+// super-tile's 8 blocks) of sum_i (c_i - mid) u_i s_block to `pgu`
+// [2][NST][16][T].
+template <int T, int BITS>
+__device__ __forceinline__ void gu_item(const Plan &P, const char *slot, int mtx, int s, int n, const int (&tok)[kMaxT],
+                                        const char *xp, const float *xs, int H, float *pgu)
 {
-    QChunk c;
-    if (BITS == 2) {
-        uint2 lo = *reinterpret_cast<const uint2 *>(rowc + 8 * chunk);
-        c.lo0 = lo.x;
-        c.lo1 = lo.y;
-        c.hi = 0;
-    } else {
-        const uint32_t *lo = reinterpret_cast<const uint32_t *>(rowc + 8 * chunk);
-        c.lo0 = lo[0];
-        c.lo1 = lo[1];
-        c.hi = *reinterpret_cast<const uint32_t *>(rowc + (cols / 4) + 4 * chunk);
+    const int lane = lane_id(), gid = lane >> 2, tig = lane & 3;
+    const int cbr = P.cb_gu;
+    const uint8_t *cb = reinterpret_cast<const uint8_t *>(slot) + (size_t)mtx * 16 * cbr;
+    const char *sb = slot + 32 * cbr + (size_t)mtx * 16 * P.sb_gu;
+    const int bA = 8 * s + 2 * tig;  // blocks bA (k-pair tig) and bA + 1 (k-pair tig + 4)
+    const uint4 q0 = *reinterpret_cast<const uint4 *>(cb + (size_t)gid * cbr + bA * 8);
+    const uint4 q1 = *reinterpret_cast<const uint4 *>(cb + (size_t)(gid + 8) * cbr + bA * 8);
+    uint2 hq0 = make_uint2(0u, 0u), hq1 = make_uint2(0u, 0u);
+    if constexpr (BITS == 3) {
+        hq0 = *reinterpret_cast<const uint2 *>(cb + (size_t)gid * cbr + H / 4 + bA * 4);
+        hq1 = *reinterpret_cast<const uint2 *>(cb + (size_t)(gid + 8) * cbr + H / 4 + bA * 4);
     }
-    c.s = rows[chunk];
-    return c;
+    const uint32_t h00 = hq0.x, h10 = hq1.x, h01 = hq0.y, h11 = hq1.y;
+    const uint2 q00 = make_uint2(q0.x, q0.y), q10 = make_uint2(q1.x, q1.y);
+    const uint2 q01 = make_uint2(q0.z, q0.w), q11 = make_uint2(q1.z, q1.w);
+    // operand column gid is block 8s+gid: held by the thread whose k-pair carries that block
+    const uint32_t mA = gid == 2 * tig ? 0xffffffffu : 0u, mB = gid == 2 * tig + 1 ? 0xffffffffu : 0u;
+    const int bx = 8 * s + gid;
+    XFrag<T> X;
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        if (t < n) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(xp + (size_t)tok[t] * (H / 32) * P.xp_stride +
+                                                               (size_t)bx * P.xp_stride);
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                uint4 v = src[j];
+                X.r[t][4 * j] = v.x;
+                X.r[t][4 * j + 1] = v.y;
+                X.r[t][4 * j + 2] = v.z;
+                X.r[t][4 * j + 3] = v.w;
+            }
+        }
+    }
+    float acc[T][2][4];
+#pragma unroll
+    for (int t = 0; t < T; t++)
+#pragma unroll
+        for (int w = 0; w < 2; w++) acc[t][w][0] = acc[t][w][1] = acc[t][w][2] = acc[t][w][3] = 0.f;
+#define MOE_GU_STEP(Wn, Mn)                                                                               \
+    {                                                                                                     \
+        uint32_t a0 = dq_pair<Mn, BITS, Wn>(W0, W0s6, W0s12, H0);                                         \
+        uint32_t a1 = dq_pair<Mn, BITS, Wn>(W1, W1s6, W1s12, H1);                                         \
+        uint32_t a2 = dq_pair<Mn, BITS, Wn>(W2, W2s6, W2s12, H2);                                         \
+        uint32_t a3 = dq_pair<Mn, BITS, Wn>(W3, W3s6, W3s12, H3);                                         \
+        _Pragma("unroll") for (int t = 0; t < T; t++) if (t < n)                                          \
+            mma16816(acc[t][Wn], a0, a1, a2, a3, X.r[t][8 * Wn + Mn] & mA, X.r[t][8 * Wn + Mn] & mB);     \
+    }
+#define MOE_GU_WORD(Wn)                                                                                   \
+    {                                                                                                     \
+        const uint32_t W0 = Wn ? q00.y : q00.x, W1 = Wn ? q10.y : q10.x;                                  \
+        const uint32_t W2 = Wn ? q01.y : q01.x, W3 = Wn ? q11.y : q11.x;                                  \
+        const uint32_t W0s6 = W0 >> 6, W1s6 = W1 >> 6, W2s6 = W2 >> 6, W3s6 = W3 >> 6;                    \
+        const uint32_t W0s12 = W0 >> 12, W1s12 = W1 >> 12, W2s12 = W2 >> 12, W3s12 = W3 >> 12;            \
+        const uint32_t H0 = h00, H1 = h10, H2 = h01, H3 = h11;                                            \
+        MOE_GU_STEP(Wn, 0) MOE_GU_STEP(Wn, 1) MOE_GU_STEP(Wn, 2) MOE_GU_STEP(Wn, 3)                        \
+        MOE_GU_STEP(Wn, 4) MOE_GU_STEP(Wn, 5) MOE_GU_STEP(Wn, 6) MOE_GU_STEP(Wn, 7)                        \
+    }
+    MOE_GU_WORD(0)
+    MOE_GU_WORD(1)
+#undef MOE_GU_WORD
+#undef MOE_GU_STEP
+    constexpr float mid = BITS == 2 ? 1.5f : 3.5f;
+    const int bs = 8 * s + 2 * tig;
+    const float2 sa = h2f2(*reinterpret_cast<const uint32_t *>(sb + (size_t)gid * P.sb_gu + bs * 2));
+    const float2 sc = h2f2(*reinterpret_cast<const uint32_t *>(sb + (size_t)(gid + 8) * P.sb_gu + bs * 2));
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        if (t < n) {
+            const float2 xv = *reinterpret_cast<const float2 *>(xs + (size_t)tok[t] * (H / 32) + bs);
+            float c0 = acc[t][0][0] + acc[t][1][0], c1 = acc[t][0][1] + acc[t][1][1];
+            float c2 = acc[t][0][2] + acc[t][1][2], c3 = acc[t][0][3] + acc[t][1][3];
+            float p0 = sa.x * fmaf(-mid, xv.x, c0);
+            p0 = fmaf(sa.y, fmaf(-mid, xv.y, c1), p0);
+            float p1 = sc.x * fmaf(-mid, xv.x, c2);
+            p1 = fmaf(sc.y, fmaf(-mid, xv.y, c3), p1);
+            p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+            p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+            p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+            p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+            if (tig == 0) {
+                const int NST = H / 256;
+                pgu[((mtx * NST + s) * 16 + gid) * T + t] = p0;
+                pgu[((mtx * NST + s) * 16 + gid + 8) * T + t] = p1;
+            }
+        }
+    }
 }
 
-template <int NV, int BITS>
-__device__ __forceinline__ void qdot(const QChunk &c, const float (&v)[NV][32], const float (&X)[NV], float (&part)[NV])
+// One down work item: super-tile s2 (columns 128 s2 .. 128 s2 + 127 of h) of
+// the group in `slot` (16 code rows of Wd_e, the CTA's output rows, and their
+// scales), for the n tokens of the group.  Accumulator columns are (part,
+// block): 0..3 the bf16 high parts of h in the super-tile's four blocks, 4..7
+// the low parts, so both parts share one dequantised A operand.  `hop`, `hs16`
+// (shared memory if `staged`, else global) hold h's operand words and half-
+// block sums.  Writes per-row partial sums to pd[(p0 + t) * NSD2 + s2][16].
+template <int T, int BITS>
+__device__ __forceinline__ void down_item(const Plan &P, const char *slot, int s2, int n, int p0, const uint32_t *hop,
+                                          const float *hs16, bool staged, int I, float *pd)
 {
-    float acc[NV][2];
+    const int lane = lane_id(), gid = lane >> 2, tig = lane & 3;
+    const uint8_t *cb = reinterpret_cast<const uint8_t *>(slot);
+    const char *sb = slot + 16 * P.cb_d;
+    const int bt = 4 * s2 + tig;  // the block of this thread's A operand
+    const uint2 q0 = *reinterpret_cast<const uint2 *>(cb + (size_t)gid * P.cb_d + bt * 8);
+    const uint2 q1 = *reinterpret_cast<const uint2 *>(cb + (size_t)(gid + 8) * P.cb_d + bt * 8);
+    uint32_t hw0 = 0, hw1 = 0;
+    if constexpr (BITS == 3) {
+        hw0 = *reinterpret_cast<const uint32_t *>(cb + (size_t)gid * P.cb_d + I / 4 + bt * 4);
+        hw1 = *reinterpret_cast<const uint32_t *>(cb + (size_t)(gid + 8) * P.cb_d + I / 4 + bt * 4);
+    }
+    const uint32_t mA = gid == tig ? 0xffffffffu : 0u, mB = gid == tig + 4 ? 0xffffffffu : 0u;
+    const bool act = (mA | mB) != 0;
+    // operands: the high (gid == tig) or low (gid == tig + 4) bf16 part of h
+    // over block bt as pairs (16w+m, 16w+m+8), made by the gate/up epilogue;
+    // the block sum of h from its two 16-value halves
+    uint32_t B[T][16];
+    float hsum[T];
 #pragma unroll
-    for (int t = 0; t < NV; t++) acc[t][0] = acc[t][1] = 0.f;
-    dot_word<NV, BITS>(c.lo0, c.hi, v, 0, acc);
-    dot_word<NV, BITS>(c.lo1, c.hi >> 8, v, 16, acc);
-    float s = fp16_to_f32(c.s);
-    constexpr float kMul = BITS == 2 ? 4.f : 8.f;
-    constexpr float kOff = BITS == 2 ? 5.5f : 11.5f;
+    for (int t = 0; t < T; t++) {
+        hsum[t] = 0.f;
 #pragma unroll
-    for (int t = 0; t < NV; t++) part[t] = fmaf(s, fmaf(kMul, acc[t][0] + acc[t][1], -kOff * X[t]), part[t]);
+        for (int i = 0; i < 16; i++) B[t][i] = 0u;
+        if (t < n && act) {
+            const size_t pb = (size_t)(p0 + t) * (I / 32) + bt;
+            const uint4 *src = reinterpret_cast<const uint4 *>(hop + pb * 32 + (mB ? 16 : 0));
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const uint4 v = staged ? src[j] : __ldcg(src + j);
+                B[t][4 * j] = v.x; B[t][4 * j + 1] = v.y; B[t][4 * j + 2] = v.z; B[t][4 * j + 3] = v.w;
+            }
+            const float2 hh = staged ? *reinterpret_cast<const float2 *>(hs16 + 2 * pb)
+                                     : __ldcg(reinterpret_cast<const float2 *>(hs16 + 2 * pb));
+            hsum[t] = hh.x + hh.y;
+        }
+    }
+    float acc[T][2][4];
+#pragma unroll
+    for (int t = 0; t < T; t++)
+#pragma unroll
+        for (int w = 0; w < 2; w++) acc[t][w][0] = acc[t][w][1] = acc[t][w][2] = acc[t][w][3] = 0.f;
+#define MOE_D_STEP(Wn, Mn)                                                                                \
+    {                                                                                                     \
+        uint32_t a0 = dq_pair<Mn, BITS, Wn>(W0, W0s6, W0s12, hw0);                                        \
+        uint32_t a1 = dq_pair<Mn, BITS, Wn>(W1, W1s6, W1s12, hw1);                                        \
+        _Pragma("unroll") for (int t = 0; t < T; t++) if (t < n)                                          \
+            mma16816(acc[t][Wn], a0, a1, a0, a1, B[t][8 * Wn + Mn] & mA, B[t][8 * Wn + Mn] & mB);         \
+    }
+#define MOE_D_WORD(Wn)                                                                                    \
+    {                                                                                                     \
+        const uint32_t W0 = Wn ? q0.y : q0.x, W1 = Wn ? q1.y : q1.x;                                      \
+        const uint32_t W0s6 = W0 >> 6, W1s6 = W1 >> 6, W0s12 = W0 >> 12, W1s12 = W1 >> 12;                \
+        MOE_D_STEP(Wn, 0) MOE_D_STEP(Wn, 1) MOE_D_STEP(Wn, 2) MOE_D_STEP(Wn, 3)                            \
+        MOE_D_STEP(Wn, 4) MOE_D_STEP(Wn, 5) MOE_D_STEP(Wn, 6) MOE_D_STEP(Wn, 7)                            \
+    }
+    MOE_D_WORD(0)
+    MOE_D_WORD(1)
+#undef MOE_D_WORD
+#undef MOE_D_STEP
+    constexpr float mid = BITS == 2 ? 1.5f : 3.5f;
+    const int bb = 4 * s2 + 2 * (tig & 1);  // blocks of accumulator columns 2 tig, 2 tig + 1
+    const bool hi_cols = tig < 2;           // columns of the high parts carry the offset term
+    const float2 sa = h2f2(*reinterpret_cast<const uint32_t *>(sb + (size_t)gid * P.sb_d + bb * 2));
+    const float2 sc = h2f2(*reinterpret_cast<const uint32_t *>(sb + (size_t)(gid + 8) * P.sb_d + bb * 2));
+    const int src0 = 5 * (2 * (tig & 1)), src1 = src0 + 5;  // lanes that summed blocks bb, bb+1
+    const int NSD2 = I / 128;
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        if (t < n) {
+            float H0 = __shfl_sync(0xffffffffu, hsum[t], src0);
+            float H1 = __shfl_sync(0xffffffffu, hsum[t], src1);
+            float o0 = hi_cols ? -mid * H0 : 0.f, o1 = hi_cols ? -mid * H1 : 0.f;
+            float c0 = acc[t][0][0] + acc[t][1][0], c1 = acc[t][0][1] + acc[t][1][1];
+            float c2 = acc[t][0][2] + acc[t][1][2], c3 = acc[t][0][3] + acc[t][1][3];
+            float r0 = sa.x * (c0 + o0);
+            r0 = fmaf(sa.y, c1 + o1, r0);
+            float r1 = sc.x * (c2 + o0);
+            r1 = fmaf(sc.y, c3 + o1, r1);
+            r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
+            r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
+            r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
+            r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
+            if (tig == 0) {
+                pd[((size_t)(p0 + t) * NSD2 + s2) * 16 + gid] = r0;
+                pd[((size_t)(p0 + t) * NSD2 + s2) * 16 + gid + 8] = r1;
+            }
+        }
+    }
 }
 
-__device__ __forceinline__ float warp_sum(float v)
-{
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
+// ------------------------------------------------------------ copies (warp-collective issue)
 
-__device__ __forceinline__ float bf16_round(float f) { return bf16_to_f32(f32_to_bf16(f)); }
-
-// ------------------------------------------------------------ per-CTA plan
-// Shapes and shared-memory layout, computed on the host and passed in Args.
-struct Plan {
-    int rb_gu, sb_gu, rb_d, sb_d;  // bytes per row: codes / scales of gate||up and down
-    int C;                         // chunks of 32 along H
-    int xsw_stride;                // C + 1 (padding keeps the interleaved copy conflict-free)
-    int uB;                        // bytes of one phase-B unit (gate+up row codes and scales)
-    int chB;                       // phase-B units per ring buffer
-    int gC;                        // bytes of one group's phase-C rows
-    int chC;                       // groups per phase-C ring buffer
-    int sC;                        // bytes of the shared expert's phase-C rows
-    int off_xsw, off_part, off_xown, off_ab, off_c, off_h;  // byte offsets in dynamic shared memory
-    int regAB, regC;
-    int stage_h;  // 1: phase C reads h and h_s from a padded shared-memory copy
-};
-
-// Balanced contiguous split of n items over the grid.
 __device__ __forceinline__ void split_range(int n, int c, int G, int &lo, int &hi)
 {
     lo = (int)((int64_t)n * c / G);
     hi = (int)((int64_t)n * (c + 1) / G);
 }
 
-// Phase A units: router rows [0, E) then shared gate/up row pairs [E, E+Is).
-__device__ void issue_a(const Args &a, const Plan &P, const Layer &L, char *ab)
+// Router rows and shared gate/up rows of layer L into region r1 (one thread).
+__device__ void issue_a(const Args &a, const Plan &P, const Layer &L, char *r1, uint64_t *bar)
 {
-    int lo, hi;
-    split_range(a.E + (L.swg ? a.Is : 0), blockIdx.x, gridDim.x, lo, hi);
-    int r0 = min(lo, a.E), r1 = min(hi, a.E);
-    uint32_t rbytes = (uint32_t)(r1 - r0) * a.H * 4u;
-    if (r1 > r0) copy_range(ab, L.w_router + (int64_t)r0 * a.H, rbytes);
-    int q0 = max(lo, a.E) - a.E, q1 = max(hi, a.E) - a.E;
-    if (q1 > q0) {
-        uint32_t qb = (uint32_t)(q1 - q0) * a.H * 2u;
-        copy_range(ab + rbytes, L.swg + (int64_t)q0 * a.H, qb);
-        copy_range(ab + rbytes + qb, L.swu + (int64_t)q0 * a.H, qb);
-    }
-    commit();
-}
-
-// Phase C shared-expert rows [o0, o0+nrows) of Wd_s.
-__device__ void issue_cs(const Args &a, const Plan &P, const Layer &L, char *cregion, int o0, int nrows)
-{
-    if (L.swg && nrows > 0) copy_range(cregion, L.swd + (int64_t)o0 * a.Is, (uint32_t)nrows * a.Is * 2u);
-    commit();
-}
-
-template <int T>
-__device__ void phase_a(const Args &a, const Plan &P, const Layer &L, const float *xs, const char *ab)
-{
-    int lane = lane_id(), warp = warp_id();
-    int lo, hi;
-    split_range(a.E + (L.swg ? a.Is : 0), blockIdx.x, gridDim.x, lo, hi);
-    int H = a.H;
-    int r1 = min(hi, a.E), r0 = min(lo, a.E);
-    const char *qbase = ab + (size_t)(r1 - r0) * H * 4;
-    int nq = max(hi, a.E) - max(lo, a.E);
-    for (int u = lo + warp; u < hi; u += (int)(blockDim.x >> 5)) {
-        if (u < a.E) {
-            const float4 *wr = reinterpret_cast<const float4 *>(ab + (size_t)(u - r0) * H * 4);
-            float acc[T];
-#pragma unroll
-            for (int t = 0; t < T; t++) acc[t] = 0.f;
-#pragma unroll 4
-            for (int c = lane; c < (H >> 2); c += 32) {
-                float4 w = wr[c];
-#pragma unroll
-                for (int t = 0; t < T; t++) {
-                    float4 xv = *reinterpret_cast<const float4 *>(xs + t * H + 4 * c);
-                    acc[t] = fmaf(w.x, xv.x, acc[t]);
-                    acc[t] = fmaf(w.y, xv.y, acc[t]);
-                    acc[t] = fmaf(w.z, xv.z, acc[t]);
-                    acc[t] = fmaf(w.w, xv.w, acc[t]);
-                }
-            }
-            float b = L.bias ? L.bias[u] : 0.f;
-#pragma unroll
-            for (int t = 0; t < T; t++) {
-                float s = warp_sum(acc[t]);
-                if (lane == 0) a.logits[t * a.E + u] = s + b;
-            }
-        } else {
-            int q = u - max(lo, a.E);
-            int r = u - a.E;
-            const uint4 *wg = reinterpret_cast<const uint4 *>(qbase + (size_t)q * H * 2);
-            const uint4 *wu = reinterpret_cast<const uint4 *>(qbase + (size_t)(nq + q) * H * 2);
-            float g[T], uu[T];
-#pragma unroll
-            for (int t = 0; t < T; t++) g[t] = uu[t] = 0.f;
-#pragma unroll 2
-            for (int c = lane; c < (H >> 3); c += 32) {
-                uint4 qg = wg[c], qu = wu[c];
-                uint32_t G[4] = {qg.x, qg.y, qg.z, qg.w}, U[4] = {qu.x, qu.y, qu.z, qu.w};
-#pragma unroll
-                for (int t = 0; t < T; t++) {
-                    const float4 *xp = reinterpret_cast<const float4 *>(xs + t * H + 8 * c);
-                    float4 x0 = xp[0], x1 = xp[1];
-                    float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        g[t] = fmaf(__uint_as_float(G[j] << 16), xv[2 * j], g[t]);
-                        g[t] = fmaf(__uint_as_float(G[j] & 0xffff0000u), xv[2 * j + 1], g[t]);
-                        uu[t] = fmaf(__uint_as_float(U[j] << 16), xv[2 * j], uu[t]);
-                        uu[t] = fmaf(__uint_as_float(U[j] & 0xffff0000u), xv[2 * j + 1], uu[t]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int t = 0; t < T; t++) {
-                float gs = warp_sum(g[t]), us = warp_sum(uu[t]);
-                if (lane == 0) a.hs[t * a.Is + r] = silu(gs) * us;
-            }
-        }
+    int r0, rh, q0, qh;
+    split_range(a.E, blockIdx.x, gridDim.x, r0, rh);
+    split_range(a.Is, blockIdx.x, gridDim.x, q0, qh);
+    if (!L.swg) qh = q0;
+    uint32_t rb = (uint32_t)(rh - r0) * a.H * 4u, qb = (uint32_t)(qh - q0) * a.H * 2u;
+    tc::mbar_arrive_expect_tx(bar, rb + 2 * qb);
+    if (rb) bulk_g2s(r1, L.w_router + (size_t)r0 * a.H, rb, bar);
+    if (qb) {
+        bulk_g2s(r1 + rb, L.swg + (size_t)q0 * a.H, qb, bar);
+        bulk_g2s(r1 + rb + qb, L.swu + (size_t)q0 * a.H, qb, bar);
     }
 }
 
-// Phase-B chunk list: the CTA's range of (group, row) units cut at group
-// boundaries and at chB units.
-__device__ void plan_b(const Args &a, const Plan &P, Routing &R)
+// Shared down rows [o0, o0 + nrows) of layer L into region r3 (one thread).
+__device__ void issue_s(const Args &a, const Layer &L, char *r3, int o0, int nrows, uint64_t *bar)
 {
-    if (threadIdx.x != 0) return;
-    int lo, hi;
-    split_range(R.ngroups * a.I, blockIdx.x, gridDim.x, lo, hi);
-    int n = 0;
-    for (int u = lo; u < hi && n < kMaxChunks;) {
-        int g = u / a.I, r = u % a.I;
-        int nr = min(P.chB, min(hi - u, a.I - r));
-        R.b_g[n] = g;
-        R.b_r[n] = r;
-        R.b_n[n] = nr;
-        n++;
-        u += nr;
-    }
-    R.nb = n;
-    int covered = n ? (R.b_g[n - 1] * a.I + R.b_r[n - 1] + R.b_n[n - 1]) : lo;
-    int nc = 0, gdone = 0;
-    for (int g = 0; g < R.ngroups && nc < kMaxChunks; g += P.chC) {
-        R.c_g[nc] = g;
-        R.c_n[nc] = min(P.chC, R.ngroups - g);
-        gdone = g + R.c_n[nc];
-        nc++;
-    }
-    R.nc = nc;
-    if (covered < hi || gdone < R.ngroups) set_status(a.status, MOE_ERR_UNSUPPORTED);  // never drop work silently
+    uint32_t b = (L.swg && nrows > 0) ? (uint32_t)nrows * a.Is * 2u : 0u;
+    tc::mbar_arrive_expect_tx(bar, b);
+    if (b) bulk_g2s(r3, L.swd + (size_t)o0 * a.Is, b, bar);
 }
 
-template <int BITS>
-__device__ void issue_b(const Args &a, const Plan &P, const Layer &L, const Routing &R, int i, char *ab)
+// Unit u (group u / (I/16), rows 16 rt .. 16 rt + 15 of gate and of up) into
+// a unit slot, as four contiguous copies: gate codes, up codes (16 rows each),
+// gate scales, up scales.  One thread.
+__device__ void issue_unit(const Args &a, const Plan &P, const Layer &L, const Routing &R, int u, char *slot,
+                           uint64_t *bar)
 {
-    char *buf = ab + (size_t)(i & 1) * (P.regAB / 2);
-    int e = R.g_e[R.b_g[i]], r = R.b_r[i], nr = R.b_n[i];
-    const uint8_t *codes = L.gu_codes + (int64_t)e * 2 * a.I * P.rb_gu;
-    const char *scales = reinterpret_cast<const char *>(L.gu_scales) + (int64_t)e * 2 * a.I * P.sb_gu;
-    uint32_t cb = (uint32_t)nr * P.rb_gu, sb = (uint32_t)nr * P.sb_gu;
-    copy_range(buf, codes + (int64_t)r * P.rb_gu, cb);
-    copy_range(buf + cb, codes + (int64_t)(a.I + r) * P.rb_gu, cb);
-    copy_range(buf + 2 * cb, scales + (int64_t)r * P.sb_gu, sb);
-    copy_range(buf + 2 * cb + sb, scales + (int64_t)(a.I + r) * P.sb_gu, sb);
-    commit();
+    const int tiles = a.I / 16;
+    const int g = u / tiles, rt = u % tiles, e = R.g_e[g];
+    const size_t rg = (size_t)e * 2 * a.I + 16 * (size_t)rt, ru = rg + a.I;  // first gate row, first up row
+    const uint32_t cb = 16u * P.cb_gu, sb = 16u * P.sb_gu;
+    const char *sc = reinterpret_cast<const char *>(L.gu_scales);
+    tc::fence_proxy_async_smem();
+    tc::mbar_arrive_expect_tx(bar, 2 * (cb + sb));
+    bulk_g2s(slot, L.gu_codes + rg * P.cb_gu, cb, bar);
+    bulk_g2s(slot + cb, L.gu_codes + ru * P.cb_gu, cb, bar);
+    bulk_g2s(slot + 2 * cb, sc + rg * P.sb_gu, sb, bar);
+    bulk_g2s(slot + 2 * cb + sb, sc + ru * P.sb_gu, sb, bar);
 }
 
-template <int BITS>
-__device__ void issue_cr(const Args &a, const Plan &P, const Layer &L, const Routing &R, int j, char *cregion,
-                         int o0, int nrows)
+// Down rows [o0, o0 + nrows) of group g's expert into a down slot: the code
+// rows (contiguous) and their scales, two copies.  One thread.
+__device__ void issue_down(const Args &a, const Plan &P, const Layer &L, const Routing &R, int g, int o0, int nrows,
+                           char *slot, uint64_t *bar)
 {
-    char *buf = cregion + P.sC + (size_t)(j & 1) * P.chC * P.gC;
-    if (nrows > 0) {
-        for (int q = 0; q < R.c_n[j]; q++) {
-            int e = R.g_e[R.c_g[j] + q];
-            const uint8_t *codes = L.d_codes + (int64_t)e * a.H * P.rb_d + (int64_t)o0 * P.rb_d;
-            const char *scales = reinterpret_cast<const char *>(L.d_scales) + (int64_t)e * a.H * P.sb_d + (int64_t)o0 * P.sb_d;
-            char *d = buf + (size_t)q * P.gC;
-            copy_range(d, codes, (uint32_t)nrows * P.rb_d);
-            copy_range(d + (size_t)nrows * P.rb_d, scales, (uint32_t)nrows * P.sb_d);
-        }
-    }
-    commit();
+    const size_t row0 = (size_t)R.g_e[g] * a.H + o0;
+    tc::fence_proxy_async_smem();
+    tc::mbar_arrive_expect_tx(bar, (uint32_t)nrows * (P.cb_d + P.sb_d));
+    bulk_g2s(slot, L.d_codes + row0 * P.cb_d, (uint32_t)nrows * P.cb_d, bar);
+    bulk_g2s(slot + 16 * P.cb_d, reinterpret_cast<const char *>(L.d_scales) + row0 * P.sb_d, (uint32_t)nrows * P.sb_d,
+             bar);
 }
 
-// Phase B on one chunk in shared memory: rows r..r+nr of group g, gate and up.
-// A team of `team` warps shares each row (one 32-weight chunk per lane).
-template <int T, int BITS, int CPL>
-__device__ void phase_b_chunk(const Args &a, const Plan &P, const float *xsw, Routing &R, int i, const char *ab,
-                              float (&v)[CPL][T][32], float (&X)[CPL][T], int &cur_g)
-{
-    int lane = lane_id(), warp = warp_id();
-    int team = (P.C + 32 * CPL - 1) / (32 * CPL);
-    int kw = warp % team, tid_team = warp / team, nteams = (int)(blockDim.x >> 5) / team;
-    const char *buf = ab + (size_t)(i & 1) * (P.regAB / 2);
-    int g = R.b_g[i], r0 = R.b_r[i], nr = R.b_n[i];
-    int n = R.g_n[g], p0 = R.g_p0[g];
-    if (g != cur_g) {
-        cur_g = g;
-#pragma unroll
-        for (int c = 0; c < CPL; c++) {
-            int chunk = (kw + team * c) * 32 + lane;
-            bool active = chunk < P.C;
-#pragma unroll
-            for (int t = 0; t < T; t++) {
-                X[c][t] = 0.f;
-                int tok = t < n ? R.perm[p0 + t] / a.k : 0;
-                const float *xb = xsw + tok * 32 * P.xsw_stride + chunk;
-#pragma unroll
-                for (int q = 0; q < 32; q++) v[c][t][q] = (active && t < n) ? xb[q * P.xsw_stride] : 0.f;
-#pragma unroll
-                for (int q = 0; q < 32; q++) X[c][t] += v[c][t][q];
-            }
-        }
-    }
-    const uint8_t *gc = reinterpret_cast<const uint8_t *>(buf);
-    const uint8_t *uc = gc + (size_t)nr * P.rb_gu;
-    const uint16_t *gs = reinterpret_cast<const uint16_t *>(uc + (size_t)nr * P.rb_gu);
-    const uint16_t *us = gs + (size_t)nr * (P.sb_gu / 2);
-    int bar_id = 1 + tid_team;
-    for (int u0 = tid_team * kRB; u0 < nr; u0 += nteams * kRB) {
-        int nbt = min(kRB, nr - u0);
-#pragma unroll 1
-        for (int b = 0; b < kRB; b++) {
-            if (b >= nbt) break;
-            int row = u0 + b;
-            float pg[T], pu[T];
-#pragma unroll
-            for (int t = 0; t < T; t++) pg[t] = pu[t] = 0.f;
-#pragma unroll
-            for (int c = 0; c < CPL; c++) {
-                int chunk = (kw + team * c) * 32 + lane;
-                if (chunk < P.C) {
-                    QChunk cg = qload_s<BITS>(gc + (size_t)row * P.rb_gu, gs + (size_t)row * (P.sb_gu / 2), a.H, chunk);
-                    QChunk cu = qload_s<BITS>(uc + (size_t)row * P.rb_gu, us + (size_t)row * (P.sb_gu / 2), a.H, chunk);
-                    qdot<T, BITS>(cg, v[c], X[c], pg);
-                    qdot<T, BITS>(cu, v[c], X[c], pu);
-                }
-            }
-#pragma unroll
-            for (int t = 0; t < T; t++) {
-                float sg = warp_sum(pg[t]), su = warp_sum(pu[t]);
-                if (lane == 0) {
-                    R.team[warp][b][0][t] = sg;
-                    R.team[warp][b][1][t] = su;
-                }
-            }
-        }
-        if (team > 1) asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(team * 32) : "memory");
-        else __syncwarp();
-        if (kw == 0 && lane < nbt * T) {
-            int b = lane / T, t = lane % T;
-            if (t < n) {
-                float sg = 0.f, su = 0.f;
-                for (int q = 0; q < team; q++) {
-                    sg += R.team[warp + q][b][0][t];
-                    su += R.team[warp + q][b][1][t];
-                }
-                a.h[(int64_t)(p0 + t) * a.I + r0 + u0 + b] = silu(sg) * su;
-            }
-        }
-        if (team > 1) asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(team * 32) : "memory");
-        else __syncwarp();
-    }
-}
+// The number of fills a ring slot s receives when n items go through nslot slots.
+__device__ __forceinline__ int fills_of(int s, int n, int nslot) { return s < n ? (n - 1 - s) / nslot + 1 : 0; }
 
-// Phase C for one chunk of routed groups (weights in shared memory): each
-// warp takes whole groups, keeps their h in registers and runs all rows.
-// h vectors for phase C: a padded copy in shared memory ([vector][chunk][36]
-// floats, conflict-free 16-byte reads) or the workspace in L2.
-__device__ __forceinline__ float4 h_load(const Plan &P, const float *hsm, const float *hg, int vec, int K, int lane,
-                                         int i)
-{
-    if (P.stage_h) return *reinterpret_cast<const float4 *>(hsm + ((size_t)vec * (K / 32) + lane) * 36 + 4 * i);
-    return __ldcg(reinterpret_cast<const float4 *>(hg + (int64_t)vec * K + 32 * lane) + i);
-}
+__device__ __forceinline__ float bf16r(float f) { return bf16_to_f32(f32_to_bf16(f)); }
 
-template <int T, int BITS>
-__device__ void phase_c_chunk(const Args &a, const Plan &P, Routing &R, int j, const char *cregion, float *part,
-                              int nrows, const float *hsm)
-{
-    int lane = lane_id(), warp = warp_id();
-    int np = a.T * a.k, pstride = np + a.T;
-    const char *buf = cregion + P.sC + (size_t)(j & 1) * P.chC * P.gC;
-    bool active = lane < a.I / 32;
-    int half = (nrows + 1) / 2;
-    int nw = (int)(blockDim.x >> 5);
-    for (int it = warp; it < 2 * R.c_n[j]; it += nw) {
-        int q = it >> 1;
-        int rr0 = (it & 1) ? half : 0, rr1 = (it & 1) ? nrows : half;
-        int g = R.c_g[j] + q;
-        int n = R.g_n[g], p0 = R.g_p0[g];
-        float v[T][32];
-        float X[T];
-#pragma unroll
-        for (int t = 0; t < T; t++) {
-            X[t] = 0.f;
-            if (active && t < n) {
-#pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    float4 f = h_load(P, hsm, a.h, p0 + t, a.I, lane, i);
-                    v[t][4 * i] = f.x; v[t][4 * i + 1] = f.y; v[t][4 * i + 2] = f.z; v[t][4 * i + 3] = f.w;
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; i++) v[t][i] = 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < 32; i++) X[t] += v[t][i];
-        }
-        const uint8_t *codes = reinterpret_cast<const uint8_t *>(buf + (size_t)q * P.gC);
-        const uint16_t *scales = reinterpret_cast<const uint16_t *>(codes + (size_t)nrows * P.rb_d);
-        for (int rr = rr0; rr < rr1; rr++) {
-            float p[T];
-#pragma unroll
-            for (int t = 0; t < T; t++) p[t] = 0.f;
-            if (active) {
-                QChunk c = qload_s<BITS>(codes + (size_t)rr * P.rb_d, scales + (size_t)rr * (P.sb_d / 2), a.I, lane);
-                qdot<T, BITS>(c, v, X, p);
-            }
-#pragma unroll
-            for (int t = 0; t < T; t++) {
-                float s = warp_sum(p[t]);
-                if (lane == 0 && t < n) part[rr * pstride + p0 + t] = s;
-            }
-        }
-    }
-}
-
-// Phase C for the shared expert: rows of Wd_s in shared memory, h_s from L2.
-template <int T>
-__device__ void phase_c_shared(const Args &a, const Plan &P, const char *cregion, float *part, int nrows,
-                               const float *hsm_s)
-{
-    int lane = lane_id(), warp = warp_id();
-    int np = a.T * a.k, pstride = np + a.T;
-    int Is = a.Is;
-    bool active = lane < Is / 32;
-    float v[T][32];
-#pragma unroll
-    for (int t = 0; t < T; t++) {
-        if (active) {
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-                float4 f = h_load(P, hsm_s, a.hs, t, Is, lane, i);
-                v[t][4 * i] = f.x; v[t][4 * i + 1] = f.y; v[t][4 * i + 2] = f.z; v[t][4 * i + 3] = f.w;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; i++) v[t][i] = 0.f;
-        }
-    }
-    for (int rr = warp; rr < nrows; rr += (int)(blockDim.x >> 5)) {
-        float p[T];
-#pragma unroll
-        for (int t = 0; t < T; t++) p[t] = 0.f;
-        if (active) {
-            const uint4 *wp = reinterpret_cast<const uint4 *>(cregion + (size_t)rr * Is * 2) + 4 * lane;
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                uint4 q = wp[j];
-                uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    float lo = __uint_as_float(w4[i] << 16), hi = __uint_as_float(w4[i] & 0xffff0000u);
-#pragma unroll
-                    for (int t = 0; t < T; t++) {
-                        p[t] = fmaf(lo, v[t][8 * j + 2 * i], p[t]);
-                        p[t] = fmaf(hi, v[t][8 * j + 2 * i + 1], p[t]);
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int t = 0; t < T; t++) {
-            float s = warp_sum(p[t]);
-            if (lane == 0) part[rr * pstride + np + t] = s;
-        }
-    }
-}
+// ------------------------------------------------------------ the kernel
 
 template <int T, int BITS>
 __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __grid_constant__ Args a,
@@ -904,257 +739,569 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
 {
     constexpr int NW = warps_for<T>();
     constexpr int NT = NW * 32;
-    // activations of phase B held per lane: two chunks when they fit, else one chunk and a warp team
-    constexpr int CPL = T == 1 ? 2 : 1;
+    constexpr int kQ = 10;  // H / 256 <= 9 (at most 16 output rows per CTA)
     extern __shared__ __align__(128) char dyn[];
     __shared__ Routing R;
-    float *xs = reinterpret_cast<float *>(dyn);                 // [T][H] layer input as fp32
-    float *xsw = reinterpret_cast<float *>(dyn + P.off_xsw);    // [T][32][C+1] the same, chunk-interleaved
-    float *part = reinterpret_cast<float *>(dyn + P.off_part);  // [rows][T*k + T]
-    float *xown = reinterpret_cast<float *>(dyn + P.off_xown);  // [T][rows] this CTA's rows of x
-    char *ab = dyn + P.off_ab;                                  // phase A data / phase B ring
-    char *cregion = dyn + P.off_c;                              // phase C shared rows + ring
-    int o0 = blockIdx.x * a.rows_per_cta;
-    int nrows = max(0, min(a.H, o0 + a.rows_per_cta) - o0);
-    int np = T * a.k, pstride = np + T;
-    int H = a.H;
-    unsigned nbar = 0;
-    int ncommit = 0;
-    for (int i = threadIdx.x; i < T * nrows; i += NT) {
-        int t = i / nrows, rr = i % nrows;
-        xown[t * nrows + rr] = __ldcg(a.x + (int64_t)t * H + o0 + rr);
+    __shared__ int iss_u[kMaxUnitSlots], iss_d[kMaxDownSlots], iss_a, iss_s;  // fills issued per barrier
+    const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
+    const int G = gridDim.x, cta = blockIdx.x;
+    const int H = a.H, I = a.I, E = a.E, k = a.k, Is = a.Is;
+    const int o0 = cta * a.rpc, nrows = max(0, min(H, o0 + a.rpc) - o0);
+    const int NST = H / 256, NSD2 = I / 128, tiles = I / 16, per_unit = 2 * NST;
+    uint16_t *xb = reinterpret_cast<uint16_t *>(dyn + P.off_xb);  // [T][H] u (bf16)
+    char *xp = dyn + P.off_xp;                                     // [T][H/32] blocks of operand pairs
+    float *xs = reinterpret_cast<float *>(dyn + P.off_xs);         // [T][H/32] block sums of u
+    float *lg = reinterpret_cast<float *>(dyn + P.off_lg);         // [T][E] logits
+    char *r1 = dyn + P.off_r1;                                     // router/shared rows, then unit slots
+    char *r2 = dyn + P.off_r2;                                     // down slots
+    char *r3 = dyn + P.off_r3;                                     // shared down rows
+    float *hsm = reinterpret_cast<float *>(dyn + P.off_hs);        // [T][Is] shared h
+    float *pgu = reinterpret_cast<float *>(dyn + P.off_pgu);       // [nsu][2][NST][16][T]
+    float *pd = reinterpret_cast<float *>(dyn + P.off_pd);         // [T*k][NSD2][16]
+    float *xown = reinterpret_cast<float *>(dyn + P.off_xown);     // [T][16] own rows of x
+    float *sdn = xown + T * 16;                                    // [T][16] shared down outputs
+
+    if (tid == 0) {
+        for (int s = 0; s < P.nsu; s++) {
+            tc::mbar_init(&R.fullU[s], 1);
+            R.fills_u[s] = 0;
+            R.ucnt[s] = 0;
+            iss_u[s] = 0;
+        }
+        for (int s = 0; s < P.nsd; s++) {
+            tc::mbar_init(&R.fullD[s], 1);
+            R.fills_d[s] = 0;
+            R.dcnt[s] = 0;
+            iss_d[s] = 0;
+        }
+        tc::mbar_init(&R.fullA, 1);
+        tc::mbar_init(&R.fullS, 1);
+        tc::fence_mbar_init();
+        issue_a(a, P, a.L[0], r1, &R.fullA);
+        issue_s(a, a.L[0], r3, o0, nrows, &R.fullS);
+        iss_a = 1;
+        iss_s = 1;
     }
-    issue_a(a, P, a.L[0], ab);
-    int gi_a = ncommit++;
-    issue_cs(a, P, a.L[0], cregion, o0, nrows);
-    int gi_cs = ncommit++;
+    __syncthreads();
+    int fillsA = 0, fillsS = 0;
+    bool ok = true;
     for (int l = 0; l < a.n_layers; l++) {
         const Layer &L = a.L[l];
-        // -- layer input: bf16(x / rms(x)) per token; sums of squares in a fixed order
-        for (int t = 0; t < T; t++) {
-            float ss = 0.f;
-            const float4 *xp = reinterpret_cast<const float4 *>(a.x + (int64_t)t * H);
-            for (int i = threadIdx.x; i < (H >> 2); i += NT) {
-                float4 v = __ldcg(xp + i);
-                ss = fmaf(v.x, v.x, ss);
-                ss = fmaf(v.y, v.y, ss);
-                ss = fmaf(v.z, v.z, ss);
-                ss = fmaf(v.w, v.w, ss);
+        bool fail = false;
+        // ---- gather x_l (every CTA, all of it), u = bf16(x * inv_rms)
+        const int nq = H / 256;
+        float xr[T][kQ];
+        if (tid < kRedV) {
+            // all of this thread's words are requested before any is checked
+            // (one round trip when they are ready), then late ones are polled
+            if (l == 0) {
+#pragma unroll
+                for (int t = 0; t < T; t++)
+#pragma unroll
+                    for (int q = 0; q < kQ; q++)
+                        xr[t][q] = q < nq ? __ldcg(a.x + (size_t)t * H + tid + 256 * q) : 0.f;
+            } else {
+                const uint64_t *src = a.xll + (size_t)(l & 1) * T * H + tid;
+                uint64_t wv[T][kQ];
+#pragma unroll
+                for (int t = 0; t < T; t++)
+#pragma unroll
+                    for (int q = 0; q < kQ; q++) wv[t][q] = q < nq ? ld_relaxed_u64(src + (size_t)t * H + 256 * q) : 0;
+#pragma unroll
+                for (int t = 0; t < T; t++)
+#pragma unroll
+                    for (int q = 0; q < kQ; q++) {
+                        xr[t][q] = 0.f;
+                        if (q < nq && !fail) {
+                            float v = __uint_as_float((unsigned)wv[t][q]);
+                            if ((unsigned)(wv[t][q] >> 32) != (unsigned)l)
+                                fail |= !wait_tagged(a, src + (size_t)t * H + 256 * q, (unsigned)l, v);
+                            xr[t][q] = v;
+                        }
+                    }
             }
-            ss = warp_sum(ss);
-            if (lane_id() == 0) R.wsum[t][warp_id()] = ss;
+#pragma unroll
+            for (int t = 0; t < T; t++) {
+                float ss = 0.f;
+#pragma unroll
+                for (int q = 0; q < kQ; q++) {
+                    if (q < nq) {
+                        const int idx = tid + 256 * q;
+                        if (idx >= o0 && idx < o0 + nrows) xown[t * 16 + idx - o0] = xr[t][q];
+                        ss = fmaf(xr[t][q], xr[t][q], ss);
+                    }
+                }
+                ss = warp_sum(ss);
+                if (lane == 0) R.wred[t][warp] = ss;
+            }
         }
-        __syncthreads();
-        if (threadIdx.x < T) {
+        if (__syncthreads_or(fail)) { ok = false; break; }
+        if (tid < T) {
             float inv = 1.0f;
             if (a.rms_eps >= 0.f) {
                 float tot = 0.f;
-                for (int w = 0; w < NW; w++) tot += R.wsum[threadIdx.x][w];
+                for (int w = 0; w < kRedV / 32; w++) tot += R.wred[tid][w];
                 inv = 1.0f / sqrtf(tot / (float)H + a.rms_eps);
             }
-            R.inv_rms[threadIdx.x] = inv;
+            R.inv_rms[tid] = inv;
         }
         __syncthreads();
-        for (int i = threadIdx.x; i < T * (H >> 2); i += NT) {
-            int t = i / (H >> 2), c4 = i % (H >> 2);
-            float4 v = __ldcg(reinterpret_cast<const float4 *>(a.x + (int64_t)t * H) + c4);
-            float inv = R.inv_rms[t];
-            float4 o = make_float4(bf16_round(v.x * inv), bf16_round(v.y * inv), bf16_round(v.z * inv),
-                                   bf16_round(v.w * inv));
-            reinterpret_cast<float4 *>(xs + t * H)[c4] = o;
-            int r = 4 * c4;
-            float *dst = xsw + t * 32 * P.xsw_stride;
-            dst[((r + 0) & 31) * P.xsw_stride + ((r + 0) >> 5)] = o.x;
-            dst[((r + 1) & 31) * P.xsw_stride + ((r + 1) >> 5)] = o.y;
-            dst[((r + 2) & 31) * P.xsw_stride + ((r + 2) >> 5)] = o.z;
-            dst[((r + 3) & 31) * P.xsw_stride + ((r + 3) >> 5)] = o.w;
-        }
-        // -- phase A from the prefetched rows
-        wait_group_index(gi_a, ncommit);
-        __syncthreads();
-        phase_a<T>(a, P, L, xs, ab);
-        if (!grid_barrier(a, R, ++nbar)) { wait_all_copies(); return; }
-        // -- routing, redundantly in every CTA
-        int w = warp_id();
-        if (T == 1) {
-            bool nan_token = topk_block(a.logits, a.E, a.k, R);
-            if (nan_token && threadIdx.x == 0) set_status(a.status, MOE_ERR_NONFINITE);
-            if (w == 0) topk_weights(R, 0, a.k, nan_token);
-        } else if (w < T) {
-            bool nan_token = topk_warp(a.logits + w * a.E, a.E, a.k, R, w);
-            if (nan_token && lane_id() == 0) set_status(a.status, MOE_ERR_NONFINITE);
-            topk_weights(R, w, a.k, nan_token);
+        if (tid < kRedV) {
+#pragma unroll
+            for (int t = 0; t < T; t++)
+#pragma unroll
+                for (int q = 0; q < kQ; q++)
+                    if (q < nq) xb[(size_t)t * H + tid + 256 * q] = f32_to_bf16(xr[t][q] * R.inv_rms[t]);
         }
         __syncthreads();
-        if (w == 0) build_groups(R, np);
-        __syncthreads();
-        if (blockIdx.x == 0 && a.ids_out && threadIdx.x < np) {
-            a.ids_out[(int64_t)l * np + threadIdx.x] = R.ids[threadIdx.x];
-            a.w_out[(int64_t)l * np + threadIdx.x] = R.w[threadIdx.x];
+        for (int i = warp; i < T * (H / 32); i += NW) {  // token i / (H/32), block i % (H/32)
+            const uint16_t uv = xb[(size_t)i * 32 + lane];
+            const float sum = warp_sum(bf16_to_f32(uv));
+            const uint16_t up = (uint16_t)__shfl_down_sync(0xffffffffu, (unsigned)uv, 8);
+            if (lane == 0) xs[i] = sum;
+            if ((lane & 8) == 0)  // lane 16w + m holds position 16w+m, pairs with 16w+m+8
+                reinterpret_cast<uint32_t *>(xp + (size_t)i * P.xp_stride)[8 * (lane >> 4) + (lane & 7)] =
+                    pack_bf16(uv, up);
         }
-        plan_b(a, P, R);
-        __syncthreads();
-        // -- prefetch phase B chunks 0,1 and phase C routed chunks 0,1
-        int gi_b[2] = {-1, -1}, gi_c[2] = {-1, -1};
-        for (int i = 0; i < 2 && i < R.nb; i++) {
-            issue_b<BITS>(a, P, L, R, i, ab);
-            gi_b[i] = ncommit++;
+        // ---- A: router rows (fp32 weights) -> tagged logits
+        int r0, rh, q0, qh;
+        split_range(E, cta, G, r0, rh);
+        split_range(Is, cta, G, q0, qh);
+        if (!L.swg) qh = q0;
+        bool okA = tc::mbar_wait(&R.fullA, (uint32_t)(fillsA & 1), kTimeoutNs);
+        fillsA++;
+        if (__syncthreads_or(!okA)) {
+            if (tid == 0) raise_abort(a);
+            ok = false;
+            break;
         }
-        for (int j = 0; j < 2 && j < R.nc; j++) {
-            issue_cr<BITS>(a, P, L, R, j, cregion, o0, nrows);
-            gi_c[j] = ncommit++;
-        }
-        // -- phase B
-        {
-            float v[CPL][T][32];
-            float X[CPL][T];
-            int cur_g = -1;
-            for (int i = 0; i < R.nb; i++) {
-                wait_group_index(gi_b[i & 1], ncommit);
-                __syncthreads();
-                phase_b_chunk<T, BITS, CPL>(a, P, xsw, R, i, ab, v, X, cur_g);
-                __syncthreads();
-                if (i + 2 < R.nb) {
-                    issue_b<BITS>(a, P, L, R, i + 2, ab);
-                    gi_b[i & 1] = ncommit++;
+        // items: this CTA's router rows, then its shared gate/up rows (A'),
+        // spread over the warps; A' overlaps the wait for the other CTAs' logits
+        const int nra = rh - r0, nqa = qh - q0;
+        for (int item = warp; item < nra + nqa; item += NW) {
+            if (item < nra) {
+                const float4 *wr = reinterpret_cast<const float4 *>(r1 + (size_t)item * H * 4);
+                float acc[T];
+#pragma unroll
+                for (int t = 0; t < T; t++) acc[t] = 0.f;
+#pragma unroll 4
+                for (int cc = lane; cc < (H >> 2); cc += 32) {
+                    const float4 w = wr[cc];
+#pragma unroll
+                    for (int t = 0; t < T; t++) {
+                        const uint2 ub = *reinterpret_cast<const uint2 *>(xb + (size_t)t * H + 4 * cc);
+                        acc[t] = fmaf(w.x, __uint_as_float(ub.x << 16), acc[t]);
+                        acc[t] = fmaf(w.y, __uint_as_float(ub.x & 0xffff0000u), acc[t]);
+                        acc[t] = fmaf(w.z, __uint_as_float(ub.y << 16), acc[t]);
+                        acc[t] = fmaf(w.w, __uint_as_float(ub.y & 0xffff0000u), acc[t]);
+                    }
+                }
+                const float b = L.bias ? L.bias[r0 + item] : 0.f;
+#pragma unroll
+                for (int t = 0; t < T; t++) {
+                    const float sv = warp_sum(acc[t]);
+                    if (lane == 0)
+                        st_relaxed_u64(a.lgll + ((size_t)(l & 1) * T + t) * E + r0 + item,
+                                       tagged(sv + b, (unsigned)(l + 1)));
+                }
+            } else {
+                const int q = item - nra;
+                const char *qg = r1 + (size_t)nra * H * 4;
+                const uint4 *wg = reinterpret_cast<const uint4 *>(qg + (size_t)q * H * 2);
+                const uint4 *wu = reinterpret_cast<const uint4 *>(qg + (size_t)(nqa + q) * H * 2);
+                float gg[T], uu[T];
+#pragma unroll
+                for (int t = 0; t < T; t++) gg[t] = uu[t] = 0.f;
+#pragma unroll 2
+                for (int cc = lane; cc < (H >> 3); cc += 32) {
+                    const uint4 Gv = wg[cc], Uv = wu[cc];
+                    const uint32_t Gw[4] = {Gv.x, Gv.y, Gv.z, Gv.w}, Uw[4] = {Uv.x, Uv.y, Uv.z, Uv.w};
+#pragma unroll
+                    for (int t = 0; t < T; t++) {
+                        const uint4 Xv = *reinterpret_cast<const uint4 *>(xb + (size_t)t * H + 8 * cc);
+                        const uint32_t Xw[4] = {Xv.x, Xv.y, Xv.z, Xv.w};
+#pragma unroll
+                        for (int j = 0; j < 4; j++) {
+                            const float x0 = __uint_as_float(Xw[j] << 16), x1 = __uint_as_float(Xw[j] & 0xffff0000u);
+                            gg[t] = fmaf(__uint_as_float(Gw[j] << 16), x0, gg[t]);
+                            gg[t] = fmaf(__uint_as_float(Gw[j] & 0xffff0000u), x1, gg[t]);
+                            uu[t] = fmaf(__uint_as_float(Uw[j] << 16), x0, uu[t]);
+                            uu[t] = fmaf(__uint_as_float(Uw[j] & 0xffff0000u), x1, uu[t]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < T; t++) {
+                    const float gs = warp_sum(gg[t]), us = warp_sum(uu[t]);
+                    if (lane == 0) __stcg(a.hs + (size_t)t * Is + q0 + q, silu(gs) * us);
                 }
             }
         }
-        // -- prefetch the next layer's phase A rows (the ring is free now)
-        if (l + 1 < a.n_layers) {
-            issue_a(a, P, a.L[l + 1], ab);
-            gi_a = ncommit++;
-        }
-        if (!grid_barrier(a, R, ++nbar)) { wait_all_copies(); return; }
-        // -- phase C: stage h and h_s (one coalesced pass), then the down projections
-        float *hsm = reinterpret_cast<float *>(dyn + P.off_h);
-        float *hsm_s = hsm + (size_t)np * (a.I / 32) * 36;
-        if (P.stage_h) {
-            int n4 = np * (a.I / 4), ns4 = L.swg ? T * (a.Is / 4) : 0;
-            for (int i = threadIdx.x; i < n4 + ns4; i += NT) {
-                bool sh_ = i >= n4;
-                int ii = sh_ ? i - n4 : i;
-                int K = sh_ ? a.Is : a.I;
-                int vec = ii / (K / 4), e4 = ii % (K / 4);
-                float4 f = __ldcg(reinterpret_cast<const float4 *>(sh_ ? a.hs : a.h) + ii);
-                float *dst = (sh_ ? hsm_s : hsm) + ((size_t)vec * (K / 32) + (e4 >> 3)) * 36 + 4 * (e4 & 7);
-                *reinterpret_cast<float4 *>(dst) = f;
+        __syncthreads();
+        if (tid == 0) red_release_add(a.cnt + 1, 1u);
+        // ---- routing: all logits, top-k per token, groups of pairs
+        {
+            // all requests first (one round trip when the logits are ready), then late ones
+            constexpr int kL = (kMaxT * 1024 + NT - 1) / NT;
+            const uint64_t *src = a.lgll + (size_t)(l & 1) * T * E;
+            uint64_t wv[kL];
+#pragma unroll
+            for (int j = 0; j < kL; j++) {
+                const int i = tid + NT * j;
+                wv[j] = i < T * E ? ld_relaxed_u64(src + i) : 0;
+            }
+#pragma unroll
+            for (int j = 0; j < kL; j++) {
+                const int i = tid + NT * j;
+                if (i < T * E && !fail) {
+                    float v = __uint_as_float((unsigned)wv[j]);
+                    if ((unsigned)(wv[j] >> 32) != (unsigned)(l + 1)) fail |= !wait_tagged(a, src + i, (unsigned)(l + 1), v);
+                    lg[i] = v;
+                }
             }
         }
-        wait_group_index(gi_cs, ncommit);
+        if (__syncthreads_or(fail)) { ok = false; break; }
+        unsigned nan_mask = 0;
+        for (int t = 0; t < T; t++)
+            if (topk_cta(lg + (size_t)t * E, E, k, R, t, reinterpret_cast<float *>(r1),
+                         reinterpret_cast<int *>(r1) + E))
+                nan_mask |= 1u << t;
+        if (nan_mask && tid == 0) set_status(a.status, MOE_ERR_NONFINITE);
+        if (warp < T) topk_weights(R, warp, k, (nan_mask >> warp) & 1u);
         __syncthreads();
-        if (L.swg) phase_c_shared<T>(a, P, cregion, part, nrows, hsm_s);
-        for (int j = 0; j < R.nc; j++) {
-            wait_group_index(gi_c[j & 1], ncommit);
-            __syncthreads();
-            phase_c_chunk<T, BITS>(a, P, R, j, cregion, part, nrows, hsm);
-            __syncthreads();
-            if (j + 2 < R.nc) {
-                issue_cr<BITS>(a, P, L, R, j + 2, cregion, o0, nrows);
-                gi_c[j & 1] = ncommit++;
+        if (warp == 0) build_groups(R, T * k);
+        __syncthreads();
+        if (cta == 0 && a.ids_out && tid < T * k) {
+            a.ids_out[(size_t)l * T * k + tid] = R.ids[tid];
+            a.w_out[(size_t)l * T * k + tid] = R.w[tid];
+        }
+        const int ng = R.ngroups, NU = ng * tiles;
+        int u0, u1;
+        split_range(NU, cta, G, u0, u1);
+        const int nu = u1 - u0;
+        if (warp == 0) {  // one lane per unit slot and per down slot
+            const int nui = min(nu, P.nsu), ndi = nrows > 0 ? min(ng, P.nsd) : 0;
+            for (int j = lane; j < nui + ndi; j += 32) {
+                if (j < nui) {
+                    issue_unit(a, P, L, R, u0 + j, r1 + (size_t)j * P.unitB, &R.fullU[j]);
+                    iss_u[j]++;
+                } else {
+                    const int g = j - nui;
+                    issue_down(a, P, L, R, g, o0, nrows, r2 + (size_t)g * P.downB, &R.fullD[g]);
+                    iss_d[g]++;
+                }
             }
         }
-        __syncthreads();
-        for (int i = threadIdx.x; i < nrows * T; i += NT) {
-            int rr = i / T, t = i % T;
-            float s = 0.f;
-            for (int j = 0; j < a.k; j++) s = fmaf(R.w[t * a.k + j], part[rr * pstride + R.inv[t * a.k + j]], s);
-            if (L.swg) s += part[rr * pstride + np + t];
-            float nx = xown[t * nrows + rr] + s;
-            xown[t * nrows + rr] = nx;
-            a.x[(int64_t)t * H + o0 + rr] = nx;
+        // ---- B: routed gate/up on the tensor cores
+        for (int j = warp; j < nu * per_unit; j += NW) {
+            const int ul = j / per_unit, it = j % per_unit, mtx = it / NST, s = it % NST;
+            const int slot = ul % P.nsu, fill = R.fills_u[slot] + ul / P.nsu;
+            if (!tc::mbar_wait(&R.fullU[slot], (uint32_t)(fill & 1), kTimeoutNs)) {
+                fail = true;
+                break;
+            }
+            const int u = u0 + ul, g = u / tiles, rt = u % tiles;
+            const int n = R.g_n[g], p0 = R.g_p0[g];
+            int tok[kMaxT];
+#pragma unroll
+            for (int t = 0; t < kMaxT; t++) tok[t] = t < n ? R.perm[p0 + t] / k : 0;
+            float *pslot = pgu + (size_t)slot * per_unit * 16 * T;
+            gu_item<T, BITS>(P, r1 + (size_t)slot * P.unitB, mtx, s, n, tok, xp, xs, H, pslot);
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                last = atomicAdd(&R.ucnt[slot], 1) == per_unit - 1;
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                // h = silu(g) * u for the unit's 16 rows, stored as the down
+                // projection's operand words: bf16 high and low parts paired
+                // (16w+m, 16w+m+8) in block rt/2, word half w = rt&1, and the
+                // fp32 sum of the 16 values
+                __threadfence_block();
+                for (int tb = 0; tb < n; tb += 2) {
+                    const int t = tb + (lane >> 4), r = lane & 15;
+                    float hv = 0.f;
+                    if (t < n) {
+                        float gs = 0.f, us = 0.f;
+                        for (int s2 = 0; s2 < NST; s2++) {
+                            gs += pslot[((size_t)s2 * 16 + r) * T + t];
+                            us += pslot[((size_t)(NST + s2) * 16 + r) * T + t];
+                        }
+                        hv = silu(gs) * us;
+                    }
+                    const uint16_t hi = f32_to_bf16(hv);
+                    const uint16_t lo = f32_to_bf16(hv - bf16_to_f32(hi));
+                    const uint16_t hi8 = (uint16_t)__shfl_down_sync(0xffffffffu, (unsigned)hi, 8);
+                    const uint16_t lo8 = (uint16_t)__shfl_down_sync(0xffffffffu, (unsigned)lo, 8);
+                    float s16 = hv;
+#pragma unroll
+                    for (int o = 8; o; o >>= 1) s16 += __shfl_xor_sync(0xffffffffu, s16, o);
+                    if (t < n) {
+                        const size_t pb = (size_t)(p0 + t) * (I / 32) + (rt >> 1);
+                        if (r < 8) {
+                            __stcg(a.hop + pb * 32 + 8 * (rt & 1) + r, pack_bf16(hi, hi8));
+                            __stcg(a.hop + pb * 32 + 16 + 8 * (rt & 1) + r, pack_bf16(lo, lo8));
+                        }
+                        if (r == 0) __stcg(a.hsum + (size_t)(p0 + t) * (I / 16) + rt, s16);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    atomicExch(&R.ucnt[slot], 0);
+                    if (ul + P.nsu < nu) {
+                        issue_unit(a, P, L, R, u + P.nsu, r1 + (size_t)slot * P.unitB, &R.fullU[slot]);
+                        iss_u[slot]++;
+                    }
+                }
+            }
+        }
+        if (__syncthreads_or(fail)) {
+            if (tid == 0) raise_abort(a);
+            ok = false;
+            break;
+        }
+        if (tid == 0) {
+            for (int s = 0; s < P.nsu; s++) R.fills_u[s] += fills_of(s, nu, P.nsu);
+            red_release_add(a.cnt + 0, 1u);
+            if (l + 1 < a.n_layers) {
+                tc::fence_proxy_async_smem();
+                issue_a(a, P, a.L[l + 1], r1, &R.fullA);
+                iss_a++;
+            }
+        }
+        // ---- shared down (while the other CTAs finish their h)
+        if (tid == 0) fail = !wait_counter(a, a.cnt + 1, (unsigned)(l + 1) * (unsigned)G);
+        if (__syncthreads_or(fail)) { ok = false; break; }
+        for (int i = tid; i < T * Is; i += NT) hsm[i] = __ldcg(a.hs + i);
+        const bool okS = tc::mbar_wait(&R.fullS, (uint32_t)(fillsS & 1), kTimeoutNs);
+        fillsS++;
+        if (__syncthreads_or(!okS)) {
+            if (tid == 0) raise_abort(a);
+            ok = false;
+            break;
+        }
+        if (L.swg) {
+            for (int rr = warp; rr < nrows; rr += NW) {
+                const uint4 *wd = reinterpret_cast<const uint4 *>(r3 + (size_t)rr * Is * 2);
+                float p[T];
+#pragma unroll
+                for (int t = 0; t < T; t++) p[t] = 0.f;
+                for (int cc = lane; cc < Is / 8; cc += 32) {
+                    const uint4 Wv = wd[cc];
+                    const uint32_t Ww[4] = {Wv.x, Wv.y, Wv.z, Wv.w};
+#pragma unroll
+                    for (int t = 0; t < T; t++) {
+                        const float4 h0 = *reinterpret_cast<const float4 *>(hsm + (size_t)t * Is + 8 * cc);
+                        const float4 h1 = *reinterpret_cast<const float4 *>(hsm + (size_t)t * Is + 8 * cc + 4);
+                        const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+                        for (int j = 0; j < 4; j++) {
+                            p[t] = fmaf(__uint_as_float(Ww[j] << 16), hv[2 * j], p[t]);
+                            p[t] = fmaf(__uint_as_float(Ww[j] & 0xffff0000u), hv[2 * j + 1], p[t]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < T; t++) {
+                    const float s = warp_sum(p[t]);
+                    if (lane == 0) sdn[t * 16 + rr] = s;
+                }
+            }
+        }
+        // ---- every CTA's h
+        if (tid == 0) fail = !wait_counter(a, a.cnt + 0, (unsigned)(l + 1) * (unsigned)G);
+        if (__syncthreads_or(fail)) { ok = false; break; }
+        if (tid == 0 && l + 1 < a.n_layers) {  // the shared down rows are consumed: fetch the next layer's
+            tc::fence_proxy_async_smem();
+            issue_s(a, a.L[l + 1], r3, o0, nrows, &R.fullS);
+            iss_s++;
+        }
+        const uint32_t *hop = a.hop;
+        const float *hs16 = a.hsum;
+        if (P.stage_h && nrows > 0) {  // h's operand words and half-block sums into shared memory, once
+            uint4 *dst = reinterpret_cast<uint4 *>(dyn + P.off_hop);
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.hop);
+            const int n4 = T * k * I / 4;
+            for (int i = tid; i < n4; i += NT) dst[i] = __ldcg(src + i);
+            float *hsd = reinterpret_cast<float *>(dyn + P.off_hsum);
+            for (int i = tid; i < T * k * (I / 16); i += NT) hsd[i] = __ldcg(a.hsum + i);
+            __syncthreads();
+            hop = reinterpret_cast<const uint32_t *>(dst);
+            hs16 = hsd;
+        }
+        // ---- C: routed down on the tensor cores
+        if (nrows > 0) {
+            for (int j = warp; j < ng * NSD2; j += NW) {
+                const int g = j / NSD2, s2 = j % NSD2, slot = g % P.nsd, fill = R.fills_d[slot] + g / P.nsd;
+                if (!tc::mbar_wait(&R.fullD[slot], (uint32_t)(fill & 1), kTimeoutNs)) {
+                    fail = true;
+                    break;
+                }
+                down_item<T, BITS>(P, r2 + (size_t)slot * P.downB, s2, R.g_n[g], R.g_p0[g], hop, hs16, P.stage_h != 0, I,
+                                   pd);
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) {
+                    __threadfence_block();
+                    last = atomicAdd(&R.dcnt[slot], 1) == NSD2 - 1;
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last && lane == 0) {
+                    atomicExch(&R.dcnt[slot], 0);
+                    if (g + P.nsd < ng) {
+                        issue_down(a, P, L, R, g + P.nsd, o0, nrows, r2 + (size_t)slot * P.downB, &R.fullD[slot]);
+                        iss_d[slot]++;
+                    }
+                }
+            }
+        }
+        if (__syncthreads_or(fail)) {
+            if (tid == 0) raise_abort(a);
+            ok = false;
+            break;
+        }
+        // ---- combine in slot order, residual update, x_{l+1} out
+        for (int i = tid; i < T * k * nrows; i += NT) {  // y of pair p, row rr: its super-tiles in order
+            const int p = i / nrows, rr = i % nrows;
+            float y = 0.f;
+            for (int s2 = 0; s2 < NSD2; s2++) y += pd[((size_t)p * NSD2 + s2) * 16 + rr];
+            pd[(size_t)p * NSD2 * 16 + rr] = y;
         }
         __syncthreads();
-        if (l + 1 < a.n_layers) {
-            issue_cs(a, P, a.L[l + 1], cregion, o0, nrows);
-            gi_cs = ncommit++;
+        for (int i = tid; i < nrows * T; i += NT) {
+            const int rr = i / T, t = i % T;
+            float sum = 0.f;
+            for (int j = 0; j < k; j++) sum = fmaf(R.w[t * k + j], pd[(size_t)R.inv[t * k + j] * NSD2 * 16 + rr], sum);
+            if (L.swg) sum += sdn[t * 16 + rr];
+            const float nx = xown[t * 16 + rr] + sum;
+            if (l + 1 < a.n_layers)
+                st_relaxed_u64(a.xll + ((size_t)((l + 1) & 1) * T + t) * H + o0 + rr, tagged(nx, (unsigned)(l + 1)));
+            else
+                a.x[(size_t)t * H + o0 + rr] = nx;
         }
-        if (!grid_barrier(a, R, ++nbar)) { wait_all_copies(); return; }
+        if (tid == 0 && nrows > 0)
+            for (int s = 0; s < P.nsd; s++) R.fills_d[s] += fills_of(s, ng, P.nsd);
+        __syncthreads();
     }
-    wait_all_copies();
+    // ---- on an early exit, let every copy in flight land before the CTA ends
+    if (!ok && tid == 0) {
+        constexpr unsigned long long kDrainNs = 100000000ull;
+        for (int s = 0; s < P.nsu; s++)
+            if (iss_u[s]) tc::mbar_wait(&R.fullU[s], (uint32_t)((iss_u[s] - 1) & 1), kDrainNs);
+        for (int s = 0; s < P.nsd; s++)
+            if (iss_d[s]) tc::mbar_wait(&R.fullD[s], (uint32_t)((iss_d[s] - 1) & 1), kDrainNs);
+        tc::mbar_wait(&R.fullA, (uint32_t)((iss_a - 1) & 1), kDrainNs);
+        tc::mbar_wait(&R.fullS, (uint32_t)((iss_s - 1) & 1), kDrainNs);
+    }
 }
 
+// ------------------------------------------------------------ host side
+
 template <int T, int BITS>
-static cudaError_t launch(const Args &a, const Plan &P, int grid, size_t smem, cudaStream_t s)
+static cudaError_t launch(const Args &a, const Plan &P, int grid, cudaStream_t s)
 {
     auto fn = decode_kernel<T, BITS>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, P.smem);
     if (e != cudaSuccess) return e;
     void *args[] = {const_cast<Args *>(&a), const_cast<Plan *>(&P)};
-    return cudaLaunchCooperativeKernel((const void *)fn, dim3(grid), dim3(warps_for<T>() * 32), args, smem, s);
+    return cudaLaunchCooperativeKernel((const void *)fn, dim3(grid), dim3(warps_for<T>() * 32), args, (size_t)P.smem, s);
 }
 
 template <int T, int BITS>
-static cudaError_t occupancy(int *blocks, size_t smem, size_t *static_smem)
+static cudaError_t attributes(size_t *static_smem)
 {
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, decode_kernel<T, BITS>);
-    if (e != cudaSuccess) return e;
-    *static_smem = fa.sharedSizeBytes;
-    e = cudaFuncSetAttribute(decode_kernel<T, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) *static_smem = fa.sharedSizeBytes;
+    return e;
+}
+
+template <int T, int BITS>
+static cudaError_t occupancy(int *blocks, int smem)
+{
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, decode_kernel<T, BITS>, warps_for<T>() * 32, smem);
 }
 
 struct Ws {
-    size_t bar, logits, h, hs, total;
+    size_t cnt, xll, lgll, hop, hsum, hs, zero_end, total;
 };
 
 static Ws ws_layout(int T, int H, int I, int E, int k, int Is)
 {
     Ws w;
-    w.bar = 0;
-    w.logits = 256;
-    w.h = w.logits + align256((size_t)T * E * 4);
-    w.hs = w.h + align256((size_t)T * k * I * 4);
+    w.cnt = 0;
+    w.xll = 256;
+    w.lgll = w.xll + align256((size_t)2 * T * H * 8);
+    w.zero_end = w.lgll + align256((size_t)2 * T * E * 8);
+    w.hop = w.zero_end;
+    w.hsum = w.hop + align256((size_t)T * k * I * 4);
+    w.hs = w.hsum + align256((size_t)T * k * (I / 16) * 4);
     w.total = w.hs + align256((size_t)T * std::max(Is, 1) * 4);
     return w;
 }
 
-static size_t al128(size_t n) { return (n + 127) & ~size_t(127); }
+static int al128(long n) { return (int)((n + 127) & ~127L); }
 
-// Shared-memory plan; returns false if the shapes do not fit.
-static bool make_plan(Plan &P, int T, int H, int I, int E, int k, int Is, int bits, int grid, int rows_per_cta,
-                      size_t budget)
+// Shared-memory plan; false if the shapes do not fit in `budget` bytes.
+static bool make_plan(Plan &P, int T, int H, int I, int E, int k, int Is, int bits, int G, int rpc, long budget,
+                      bool stage_h)
 {
-    P.rb_gu = bits == 2 ? H / 4 : H / 4 + H / 8;
+    memset(&P, 0, sizeof P);
+    P.cb_gu = bits == 2 ? H / 4 : 3 * H / 8;
     P.sb_gu = H / 16;
-    P.rb_d = bits == 2 ? I / 4 : I / 4 + I / 8;
+    P.cb_d = bits == 2 ? I / 4 : 3 * I / 8;
     P.sb_d = I / 16;
-    P.C = H / 32;
-    P.xsw_stride = P.C + 1;
-    P.uB = 2 * (P.rb_gu + P.sb_gu);
-    P.gC = (rows_per_cta * (P.rb_d + P.sb_d) + 15) & ~15;  // ring slots stay 16-byte aligned
-    P.sC = (int)al128((size_t)rows_per_cta * Is * 2);
-    int unitsA = (E + Is + grid - 1) / grid;
-    size_t regA = al128((size_t)unitsA * H * 4);
-    size_t fixed = al128((size_t)T * H * 4) + al128((size_t)T * 32 * P.xsw_stride * 4) +
-                   al128((size_t)rows_per_cta * (T * k + T) * 4) + al128((size_t)T * rows_per_cta * 4);
-    if (fixed + regA >= budget) return false;
-    size_t hbytes = al128(((size_t)T * k * (I / 32) + (size_t)T * (Is / 32)) * 36 * 4);
-    P.stage_h = fixed + regA + hbytes + (64u << 10) <= budget;  // keep at least 64 KiB for the rings
-    if (P.stage_h) fixed += hbytes;
-    size_t left = budget - fixed;
-    // phase C: shared rows + two ring buffers of up to 8 groups; phase A/B: the rest
-    int chC = 8;
-    while (chC > 1 && (size_t)P.sC + 2 * (size_t)chC * P.gC > left / 3) chC--;
-    size_t regC = al128((size_t)P.sC + 2 * (size_t)chC * P.gC);
-    if (regC + regA > left) return false;
-    size_t regAB = std::max(regA, (size_t)2 * P.uB);
-    regAB = std::min(left - regC, std::max(regAB, (size_t)2 * 32 * P.uB));  // room for 32 units per ring half
-    regAB &= ~size_t(255);
-    if (regAB < regA || regAB < (size_t)2 * P.uB) return false;
-    P.chB = (int)std::min<size_t>((regAB / 2) / P.uB, (size_t)1 << 20);
-    P.chC = chC;
-    P.regAB = (int)regAB;
-    P.regC = (int)regC;
-    P.off_xsw = (int)al128((size_t)T * H * 4);
-    P.off_part = P.off_xsw + (int)al128((size_t)T * 32 * P.xsw_stride * 4);
-    P.off_xown = P.off_part + (int)al128((size_t)rows_per_cta * (T * k + T) * 4);
-    P.off_ab = P.off_xown + (int)al128((size_t)T * rows_per_cta * 4);
-    P.off_c = P.off_ab + P.regAB;
-    P.off_h = P.off_c + P.regC;
-    return true;
+    P.unitB = al128(32L * (P.cb_gu + P.sb_gu));
+    P.downB = al128(16L * (P.cb_d + P.sb_d));
+    P.NST = H / 256;
+    P.NSD2 = I / 128;
+    P.rA = (E + G - 1) / G;
+    P.sA = (Is + G - 1) / G;
+    P.xp_stride = 80;
+    const int np = T * k;
+    const long aBytes = std::max((long)P.rA * H * 4 + 2L * P.sA * H * 2, 8L * E);  // also the top-k candidates
+    long off = 0;
+    P.off_xb = (int)off;   off += al128((long)T * H * 2);
+    P.off_xp = (int)off;   off += al128((long)T * (H / 32) * P.xp_stride);
+    P.off_xs = (int)off;   off += al128((long)T * (H / 32) * 4);
+    P.off_lg = (int)off;   off += al128((long)T * E * 4);
+    P.off_hs = (int)off;   off += al128((long)T * std::max(Is, 1) * 4);
+    P.off_pd = (int)off;   off += al128((long)np * P.NSD2 * 16 * 4);
+    P.off_xown = (int)off; off += al128((long)2 * T * 16 * 4);
+    P.off_r3 = (int)off;   off += al128((long)rpc * std::max(Is, 1) * 2);
+    P.stage_h = stage_h;
+    if (stage_h) {
+        P.off_hop = (int)off;  off += al128((long)np * I * 4);
+        P.off_hsum = (int)off; off += al128((long)np * (I / 16) * 4);
+    }
+    const long fixed = off;
+    const long pguPer = (long)2 * P.NST * 16 * T * 4;
+    const int nsuMax = std::min(kMaxUnitSlots, std::max(1, (np * (I / 16) + G - 1) / G));
+    const int nsdMax = np;
+    // the most unit slots that still leave room for min(np, 4) down slots
+    for (int nsu = nsuMax; nsu >= 1; nsu--) {
+        const long r1 = al128(std::max(aBytes, (long)nsu * P.unitB));
+        const long base = fixed + al128(nsu * pguPer) + r1;
+        if (base > budget) continue;
+        const int nsd = (int)std::min<long>(nsdMax, (budget - base) / P.downB);
+        if (nsd < std::min(nsdMax, 4)) continue;
+        P.nsu = nsu;
+        P.nsd = nsd;
+        P.r1B = (int)r1;
+        P.off_pgu = (int)off;
+        off += al128(nsu * pguPer);
+        P.off_r1 = (int)off;
+        off += r1;
+        P.off_r2 = (int)off;
+        off += (long)nsd * P.downB;
+        P.smem = (int)off;
+        return true;
+    }
+    return false;
 }
 
 }  // namespace fused
@@ -1162,11 +1309,24 @@ static bool make_plan(Plan &P, int T, int H, int I, int E, int k, int Is, int bi
 
 using namespace moe;
 
+// Shape checks shared by the workspace query and the launch.
+static moe_status decode_shapes_ok(int T, int H, int I, int E, int k, int Is)
+{
+    using namespace fused;
+    MOE_REQUIRE(T >= 1 && T <= kMaxT, "T must be in [1, %d] (got %d)", kMaxT, T);
+    MOE_REQUIRE(H >= 256 && H % 256 == 0, "the fused decode takes H a multiple of 256 (got %d)", H);
+    MOE_REQUIRE(I >= 128 && I % 128 == 0 && I <= 4096, "the fused decode takes I a multiple of 128 up to 4096 (got %d)",
+                I);
+    MOE_REQUIRE(E >= 1 && E <= 1024 && k >= 1 && k <= kMaxK && k <= E, "1 <= k <= min(E, 16), E <= 1024");
+    MOE_REQUIRE(Is >= 0 && Is % 64 == 0 && Is <= 4096, "shared_I must be a multiple of 64 up to 4096 (got %d)", Is);
+    return MOE_OK;
+}
+
 extern "C" moe_status moe_decode_workspace_size(int T, int H, int I, int E, int k, int shared_I, size_t *bytes)
 {
     MOE_REQUIRE(bytes, "bytes is NULL");
-    MOE_REQUIRE(T >= 1 && T <= fused::kMaxT, "T must be in [1, %d] (got %d)", fused::kMaxT, T);
-    MOE_REQUIRE(H > 0 && I > 0 && E > 0 && k > 0 && shared_I >= 0, "positive shapes required");
+    moe_status st = decode_shapes_ok(T, H, I, E, k, shared_I);
+    if (st != MOE_OK) return st;
     *bytes = fused::ws_layout(T, H, I, E, k, shared_I).total;
     return MOE_OK;
 }
@@ -1181,13 +1341,10 @@ extern "C" moe_status moe_decode_forward(const moe_layer_weights *layers, int n_
     MOE_REQUIRE(T >= 1 && T <= kMaxT, "T must be in [1, %d] (got %d)", kMaxT, T);
     if (n_layers == 0) return MOE_OK;
     const moe_expert_arena &A0 = layers[0].experts;
-    int H = A0.H, I = A0.I, E = A0.E, bits = A0.bits, Is = layers[0].shared_I;
+    const int H = A0.H, I = A0.I, E = A0.E, bits = A0.bits, Is = layers[0].shared_I;
     MOE_REQUIRE(bits == 2 || bits == 3, "bits must be 2 or 3 (got %d)", bits);
-    MOE_REQUIRE(H % 64 == 0 && H >= 64 && (H <= 1024 || H == 2048 || H == 4096),
-                "the fused decode takes H a multiple of 64 up to 1024, or 2048 or 4096 (got %d)", H);
-    MOE_REQUIRE(I % 64 == 0 && I >= 64 && I <= 1024, "the fused decode takes I a multiple of 64 up to 1024 (got %d)", I);
-    MOE_REQUIRE(E >= 1 && E <= 1024 && k >= 1 && k <= kMaxK && k <= E, "1 <= k <= min(E, 16), E <= 1024");
-    MOE_REQUIRE(Is >= 0 && Is % 64 == 0 && Is <= 1024, "shared_I must be a multiple of 64 up to 1024 (got %d)", Is);
+    moe_status st = decode_shapes_ok(T, H, I, E, k, Is);
+    if (st != MOE_OK) return st;
     MOE_REQUIRE(x && aligned16(x), "x must be a 16-byte aligned device pointer");
     MOE_REQUIRE(!ids_out == !w_out, "ids_out and w_out must both be given or both be NULL");
     Args a;
@@ -1200,18 +1357,25 @@ extern "C" moe_status moe_decode_forward(const moe_layer_weights *layers, int n_
         MOE_REQUIRE(A.gu_codes && A.gu_scales && A.d_codes && A.d_scales && W.w_router,
                     "layer %d: NULL weight pointer", l);
         MOE_REQUIRE(aligned16(A.gu_codes) && aligned16(A.gu_scales) && aligned16(A.d_codes) && aligned16(A.d_scales) &&
-                    aligned16(W.w_router), "layer %d: weight pointers must be 16-byte aligned", l);
+                        aligned16(W.w_router),
+                    "layer %d: weight pointers must be 16-byte aligned", l);
         MOE_REQUIRE(!Is || (W.shared_wg && W.shared_wu && W.shared_wd && aligned16(W.shared_wg) &&
                             aligned16(W.shared_wu) && aligned16(W.shared_wd)),
                     "layer %d: shared expert pointers must be 16-byte aligned and non-NULL", l);
         a.L[l] = {A.gu_codes, A.gu_scales, A.d_codes, A.d_scales, W.w_router, W.bias,
                   Is ? W.shared_wg : nullptr, Is ? W.shared_wu : nullptr, Is ? W.shared_wd : nullptr};
     }
-    Ws lay = ws_layout(T, H, I, E, k, Is);
+    const Ws lay = ws_layout(T, H, I, E, k, Is);
     if (!ws || ws_bytes < lay.total)
         return fail(MOE_ERR_WORKSPACE, "moe_decode_forward needs %zu bytes (%.2f MiB) of workspace, got %zu", lay.total,
                     mib((double)lay.total), ws ? ws_bytes : (size_t)0);
     MOE_REQUIRE(aligned16(ws), "workspace must be 16-byte aligned");
+    const int grid = sm_count();
+    int rpc = (H + grid - 1) / grid;
+    rpc += rpc & 1;
+    if (rpc > 16)
+        return fail(MOE_ERR_UNSUPPORTED, "the fused decode gives each of the %d SMs at most 16 output rows (H=%d)", grid,
+                    H);
     char *wb = static_cast<char *>(ws);
     a.n_layers = n_layers;
     a.T = T;
@@ -1221,50 +1385,53 @@ extern "C" moe_status moe_decode_forward(const moe_layer_weights *layers, int n_
     a.k = k;
     a.Is = Is;
     a.bits = bits;
-    a.x = x;
+    a.rpc = rpc;
     a.rms_eps = rms_eps;
-    a.logits = reinterpret_cast<float *>(wb + lay.logits);
-    a.h = reinterpret_cast<float *>(wb + lay.h);
+    a.x = x;
+    a.cnt = reinterpret_cast<unsigned *>(wb + lay.cnt);
+    a.xll = reinterpret_cast<uint64_t *>(wb + lay.xll);
+    a.lgll = reinterpret_cast<uint64_t *>(wb + lay.lgll);
+    a.hop = reinterpret_cast<uint32_t *>(wb + lay.hop);
+    a.hsum = reinterpret_cast<float *>(wb + lay.hsum);
     a.hs = reinterpret_cast<float *>(wb + lay.hs);
-    a.bar = reinterpret_cast<unsigned *>(wb + lay.bar);
     a.ids_out = ids_out;
     a.w_out = w_out;
     a.status = dev_status;
-    int grid = sm_count();
-    a.rows_per_cta = (H + grid - 1) / grid;
-    int per_sm = 0;
-    size_t static_smem = 0;
     cudaError_t e = cudaSuccess;
-#define MOE_F_DISPATCH(FN, ...)                                           \
-    switch (T * 10 + bits) {                                              \
-    case 12: e = FN<1, 2>(__VA_ARGS__); break;                            \
-    case 13: e = FN<1, 3>(__VA_ARGS__); break;                            \
-    case 22: e = FN<2, 2>(__VA_ARGS__); break;                            \
-    case 23: e = FN<2, 3>(__VA_ARGS__); break;                            \
-    case 32: e = FN<3, 2>(__VA_ARGS__); break;                            \
-    case 33: e = FN<3, 3>(__VA_ARGS__); break;                            \
-    case 42: e = FN<4, 2>(__VA_ARGS__); break;                            \
-    default: e = FN<4, 3>(__VA_ARGS__); break;                            \
+    size_t static_smem = 0;
+#define MOE_F_DISPATCH(FN, ...)                       \
+    switch (T * 10 + bits) {                          \
+    case 12: e = FN<1, 2>(__VA_ARGS__); break;        \
+    case 13: e = FN<1, 3>(__VA_ARGS__); break;        \
+    case 22: e = FN<2, 2>(__VA_ARGS__); break;        \
+    case 23: e = FN<2, 3>(__VA_ARGS__); break;        \
+    case 32: e = FN<3, 2>(__VA_ARGS__); break;        \
+    case 33: e = FN<3, 3>(__VA_ARGS__); break;        \
+    case 42: e = FN<4, 2>(__VA_ARGS__); break;        \
+    default: e = FN<4, 3>(__VA_ARGS__); break;        \
     }
-    MOE_F_DISPATCH(occupancy, &per_sm, 0, &static_smem)
+    MOE_F_DISPATCH(attributes, &static_smem)
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "decode kernel attributes: %s", cudaGetErrorString(e));
     int dev = 0, optin = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     MOE_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
-    size_t budget = (size_t)optin > static_smem + 1024 ? (size_t)optin - static_smem - 1024 : 0;
+    const long budget = (long)optin - (long)static_smem - 1024;
     Plan P;
-    if (!make_plan(P, T, H, I, E, k, Is, bits, grid, a.rows_per_cta, budget))
-        return fail(MOE_ERR_UNSUPPORTED, "the fused decode's buffers do not fit in %zu bytes of shared memory "
-                    "(T=%d H=%d I=%d E=%d k=%d shared_I=%d)", budget, T, H, I, E, k, Is);
-    size_t smem = (size_t)P.off_h + (P.stage_h ? al128(((size_t)T * k * (I / 32) + (size_t)T * (Is / 32)) * 36 * 4) : 0);
-    MOE_F_DISPATCH(occupancy, &per_sm, smem, &static_smem)
+    if (!make_plan(P, T, H, I, E, k, Is, bits, grid, rpc, budget, true) &&
+        !make_plan(P, T, H, I, E, k, Is, bits, grid, rpc, budget, false))
+        return fail(MOE_ERR_UNSUPPORTED,
+                    "the fused decode's buffers do not fit in %ld bytes of shared memory "
+                    "(T=%d H=%d I=%d E=%d k=%d shared_I=%d)",
+                    budget, T, H, I, E, k, Is);
+    int per_sm = 0;
+    MOE_F_DISPATCH(occupancy, &per_sm, P.smem)
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "decode occupancy query: %s", cudaGetErrorString(e));
     if (per_sm < 1)
-        return fail(MOE_ERR_UNSUPPORTED, "the fused decode kernel does not fit on an SM (%zu bytes of shared memory)",
-                    smem);
+        return fail(MOE_ERR_UNSUPPORTED, "the fused decode kernel does not fit on an SM (%d bytes of shared memory)",
+                    P.smem);
     cudaStream_t s = to_cuda(stream);
-    MOE_CUDA_TRY(cudaMemsetAsync(a.bar, 0, sizeof(unsigned), s));
-    MOE_F_DISPATCH(launch, a, P, grid, smem, s)
+    MOE_CUDA_TRY(cudaMemsetAsync(ws, 0, lay.zero_end, s));
+    MOE_F_DISPATCH(launch, a, P, grid, s)
 #undef MOE_F_DISPATCH
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cooperative launch of the fused decode: %s", cudaGetErrorString(e));
     return MOE_OK;
