@@ -25,13 +25,14 @@
 // Weights move by bulk asynchronous copies (TMA, one row per copy into padded
 // shared-memory slots) completing on mbarriers; the next layer's router and
 // shared-expert rows are fetched while this layer finishes.  Routed products
-// run on mma.sync bf16 tensor-core instructions: a 2-/3-bit code c is turned
-// into the exact bf16 value c (one LOP3 + one HFMA2 per pair of weights), the
+// run on mma.sync fp16 tensor-core instructions: a 2-/3-bit code c is turned
+// into the exact fp16 value c (one LOP3 + one HFMA2 per pair of weights), the
 // MMA sums c*u exactly per 32-weight block (one block per accumulator
 // column), and the block scale and the code offset are applied in fp32:
 // sum_i (c_i - mid) u_i s = s * (sum_i c_i u_i - mid * sum_i u_i).  The down
-// projection's fp32 h enters as two bf16 parts (h = hi + lo to 2^-17), so no
-// operand is rounded beyond fp32 accumulation.  Every wait (mbarrier, counter,
+// projection's fp32 h enters as two fp16 parts (h = hi + lo to 2^-22), and u
+// (bf16) converts to fp16 exactly down to 2^-17, so no operand is rounded
+// beyond fp32 accumulation (below 2^-17 by at most 2^-25).  Every wait (mbarrier, counter,
 // tagged word) gives up after about 2 s, records MOE_ERR_TIMEOUT and raises an
 // abort flag that the other CTAs check.  A token's result is computed by the
 // same instruction sequence whatever the other tokens of the call are.
@@ -72,7 +73,7 @@ struct Args {
     float *x;          // [T][H] residual stream, in/out (read at layer 0, written after the last)
     uint64_t *xll;     // [2][T][H] tagged x between layers
     uint64_t *lgll;    // [2][T][E] tagged router logits
-    uint32_t *hop;     // [T*k][I/32][2][16] routed h as bf16 operand pairs (high, low parts), sorted pair order
+    uint32_t *hop;     // [T*k][I/32][2][16] routed h as fp16 operand pairs (high, low parts), sorted pair order
     float *hsum;       // [T*k][I/16] sums of 16 consecutive h values
     float *hs;         // [T][Is] shared h
     unsigned *cnt;     // [0] h counter, [1] h_s counter, [2] abort word
@@ -101,6 +102,7 @@ struct Routing {
     int perm[kMaxPairs];  // sorted position -> flat t*k+j
     int inv[kMaxPairs];   // flat -> sorted position
     int g_e[kMaxPairs], g_p0[kMaxPairs], g_n[kMaxPairs];
+    int tok_of[kMaxPairs];  // sorted position -> token
     int ngroups;
     int sel_i[kMaxT][kMaxK];
     float sel_v[kMaxT][kMaxK];
@@ -186,18 +188,13 @@ __device__ bool wait_counter(const Args &a, const unsigned *c, unsigned target)
 }
 
 // Wait for a tagged word; false on timeout or abort (checked every 64 polls).
-__device__ __forceinline__ bool wait_tagged(const Args &a, const uint64_t *p, unsigned tag, float &v)
+__device__ __noinline__ bool wait_word(const Args &a, const uint64_t *p, unsigned tag, uint32_t &v)
 {
-    uint64_t w = ld_relaxed_u64(p);
-    if ((unsigned)(w >> 32) == tag) {
-        v = __uint_as_float((unsigned)w);
-        return true;
-    }
     unsigned long long t0 = tc::now_ns();
     for (int it = 1;; it++) {
-        w = ld_relaxed_u64(p);
+        const uint64_t w = ld_relaxed_u64(p);
         if ((unsigned)(w >> 32) == tag) {
-            v = __uint_as_float((unsigned)w);
+            v = (uint32_t)w;
             return true;
         }
         if ((it & 63) == 0) {
@@ -208,6 +205,14 @@ __device__ __forceinline__ bool wait_tagged(const Args &a, const uint64_t *p, un
             }
         }
     }
+}
+
+__device__ __forceinline__ bool wait_tagged(const Args &a, const uint64_t *p, unsigned tag, float &v)
+{
+    uint32_t u;
+    if (!wait_word(a, p, tag, u)) return false;
+    v = __uint_as_float(u);
+    return true;
 }
 
 // Barrier-style self-test used by moe_selftest_barrier: one counter barrier
@@ -403,48 +408,71 @@ __device__ void build_groups(Routing &R, int n)
     __syncwarp();
 }
 
+// Token of each sorted pair (k pairs per token).
+__device__ void pair_tokens(Routing &R, int n, int k)
+{
+    for (int p = lane_id(); p < n; p += 32) R.tok_of[p] = R.perm[p] / k;
+    __syncwarp();
+}
+
 // ------------------------------------------------------------ tensor-core pieces
 
-// D += A * B for one m16n8k16 tile, bf16 operands, fp32 accumulators.
+// D += A * B for one m16n8k16 tile, fp16 operands, fp32 accumulators.
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1)
 {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t hfma2_bf16(uint32_t a, uint32_t b, uint32_t c)
+__device__ __forceinline__ uint32_t hfma2_f16(uint32_t a, uint32_t b, uint32_t c)
 {
     uint32_t d;
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// (a & b) | c in one instruction.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
 
 // Codes of a 16-weight word: weight j at bits 2j..2j+1 (low plane).  Pair M
-// (weights M and M+8, bits 2M and 2M+16) becomes the bf16x2 (c_M, c_{M+8})
-// exactly: the codes are OR-ed into the mantissa of 128.0 at bit 2M' (M' =
-// M mod 3 after a shift of the word by 0, 6 or 12 bits), giving 128 + c*4^M',
-// and one fma with (4^-M', -128*4^-M') leaves c.  For 3 bits the high bit of
-// each weight (the word `hw`, bit M+8w and M+8w+16 for word w of the block)
-// joins at bit 2M'+2: 128 + (lo + 4 hi)*4^M' stays below 256, so exact too.
+// (weights M and M+8, bits 2M and 2M+16) becomes the fp16x2 (c_M, c_{M+8})
+// exactly: the codes are OR-ed into the mantissa of 1024.0 at bit 2M' (M' =
+// M for the first pairs, M - Q after a shift of the word by 2Q bits), giving
+// 1024 + c*4^M' (< 2048, so exact), and one fma with (4^-M', -1024*4^-M')
+// leaves c.  2 bits: Q = 5 (M' <= 4); 3 bits: Q = 4 (M' <= 3), and the high
+// bit of each weight (word `hw`, bit M+8w and M+8w+16 for word w of the
+// block) joins at bit 2M'+2.
 template <int M, int BITS, int W>
-__device__ __forceinline__ uint32_t dq_pair(uint32_t w0, uint32_t w6, uint32_t w12, uint32_t hw)
+__device__ __forceinline__ uint32_t dq_pair(uint32_t w0, uint32_t wq, uint32_t hw)
 {
-    constexpr int MP = M < 3 ? M : (M < 6 ? M - 3 : M - 6);
-    const uint32_t src = M < 3 ? w0 : (M < 6 ? w6 : w12);
-    uint32_t v = src & (0x00030003u << (2 * MP));
-    if constexpr (BITS == 3) {
+    constexpr int Q = BITS == 2 ? 5 : 4;
+    constexpr int MP = M < Q ? M : M - Q;
+    const uint32_t src = M < Q ? w0 : wq;
+    uint32_t v;
+    if constexpr (BITS == 2) {
+        v = and_or(src, 0x00030003u << (2 * MP), 0x64006400u);
+    } else {
         constexpr int SH = 8 * W + M - 2 * MP - 2;  // bring bit (8W+M) to bit 2MP+2
-        uint32_t hb = SH >= 0 ? (hw >> (SH >= 0 ? SH : 0)) : (hw << (SH < 0 ? -SH : 0));
-        v |= hb & (0x00010001u << (2 * MP + 2));
+        const uint32_t hb = SH >= 0 ? (hw >> (SH >= 0 ? SH : 0)) : (hw << (SH < 0 ? -SH : 0));
+        v = and_or(src, 0x00030003u << (2 * MP), 0x64006400u);
+        v = and_or(hb, 0x00010001u << (2 * MP + 2), v);
     }
-    v |= 0x43004300u;
-    constexpr uint32_t kMul = MP == 0 ? 0x3F803F80u : (MP == 1 ? 0x3E803E80u : 0x3D803D80u);
-    constexpr uint32_t kAdd = MP == 0 ? 0xC300C300u : (MP == 1 ? 0xC200C200u : 0xC100C100u);
-    return hfma2_bf16(v, kMul, kAdd);
+    constexpr uint32_t kMul[5] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u, 0x1C001C00u};
+    constexpr uint32_t kAdd[5] = {0xE400E400u, 0xDC00DC00u, 0xD400D400u, 0xCC00CC00u, 0xC400C400u};
+    return hfma2_f16(v, kMul[MP], kAdd[MP]);
 }
+
+// Shift of a code word that brings pairs Q.. down to bit 0 (see dq_pair).
+template <int BITS>
+__device__ __forceinline__ uint32_t dq_shift(uint32_t w) { return w >> (BITS == 2 ? 10 : 8); }
 
 __device__ __forceinline__ float2 h2f2(uint32_t b)
 {
@@ -452,14 +480,53 @@ __device__ __forceinline__ float2 h2f2(uint32_t b)
     return __half22float2(h);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
+__device__ __forceinline__ uint32_t pack16(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
 
-// Per-token operand pairs of one 256-wide super-tile: word i = w*8+m of the
-// thread's block (block 8s+tig for gid == tig, 8s+tig+4 for gid == tig+4).
+__device__ __forceinline__ uint16_t f16_bits(float f) { return __half_as_ushort(__float2half_rn(f)); }
+__device__ __forceinline__ float f16_val(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+// B operands of one 256-wide super-tile for the n tokens of a group: word
+// i = 8w+m of block 8s+gid as fp16 pairs (16w+m, 16w+m+8).  For T <= 2 two
+// copies, one per B register of the MMA, each zero in the lanes that do not
+// supply it (loaded from a zero area, so no per-MMA masking); for more tokens
+// one copy, masked per MMA.
 template <int T>
-struct XFrag {
-    uint32_t r[T][16];
+struct GuOps {
+    static constexpr bool kPre = T <= 2;
+    uint32_t A[kPre ? T : 1][16], B[kPre ? T : 1][16];
+    uint32_t X[kPre ? 1 : T][16];
 };
+
+template <int T>
+__device__ __forceinline__ void gu_load_ops(GuOps<T> &O, int s, int n, const int (&tok)[kMaxT], const char *xp, int H,
+                                            int xp_stride, const uint32_t *zero16)
+{
+    const int lane = lane_id(), gid = lane >> 2, tig = lane & 3;
+    const bool isA = gid == 2 * tig, isB = gid == 2 * tig + 1;
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        if (t < n) {
+            const char *src = xp + ((size_t)tok[t] * (H / 32) + 8 * s + gid) * xp_stride;
+            if constexpr (GuOps<T>::kPre) {
+                const uint4 *pa = reinterpret_cast<const uint4 *>(isA ? src : reinterpret_cast<const char *>(zero16));
+                const uint4 *pb = reinterpret_cast<const uint4 *>(isB ? src : reinterpret_cast<const char *>(zero16));
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const uint4 va = pa[j], vb = pb[j];
+                    O.A[t][4 * j] = va.x; O.A[t][4 * j + 1] = va.y; O.A[t][4 * j + 2] = va.z; O.A[t][4 * j + 3] = va.w;
+                    O.B[t][4 * j] = vb.x; O.B[t][4 * j + 1] = vb.y; O.B[t][4 * j + 2] = vb.z; O.B[t][4 * j + 3] = vb.w;
+                }
+            } else {
+                const uint4 *px = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const uint4 v = px[j];
+                    O.X[t][4 * j] = v.x; O.X[t][4 * j + 1] = v.y; O.X[t][4 * j + 2] = v.z; O.X[t][4 * j + 3] = v.w;
+                }
+            }
+        }
+    }
+}
 
 // One gate/up work item: matrix `mtx` (0 gate, 1 up) of the unit in `slot`,
 // super-tile s (columns 256s .. 256s+255), for the n tokens of the unit's
@@ -469,8 +536,8 @@ struct XFrag {
 // super-tile's 8 blocks) of sum_i (c_i - mid) u_i s_block to `pgu`
 // [2][NST][16][T].
 template <int T, int BITS>
-__device__ __forceinline__ void gu_item(const Plan &P, const char *slot, int mtx, int s, int n, const int (&tok)[kMaxT],
-                                        const char *xp, const float *xs, int H, float *pgu)
+__device__ __forceinline__ void gu_item(const Plan &P, const char *slot, int mtx, int s, int n, const GuOps<T> &O,
+                                        const int (&tok)[kMaxT], const float *xs, int H, float *pgu)
 {
     const int lane = lane_id(), gid = lane >> 2, tig = lane & 3;
     const int cbr = P.cb_gu;
@@ -484,28 +551,8 @@ __device__ __forceinline__ void gu_item(const Plan &P, const char *slot, int mtx
         hq0 = *reinterpret_cast<const uint2 *>(cb + (size_t)gid * cbr + H / 4 + bA * 4);
         hq1 = *reinterpret_cast<const uint2 *>(cb + (size_t)(gid + 8) * cbr + H / 4 + bA * 4);
     }
-    const uint32_t h00 = hq0.x, h10 = hq1.x, h01 = hq0.y, h11 = hq1.y;
-    const uint2 q00 = make_uint2(q0.x, q0.y), q10 = make_uint2(q1.x, q1.y);
-    const uint2 q01 = make_uint2(q0.z, q0.w), q11 = make_uint2(q1.z, q1.w);
-    // operand column gid is block 8s+gid: held by the thread whose k-pair carries that block
+    // operand column gid is block 8s+gid: held by the lane whose k-pair carries that block
     const uint32_t mA = gid == 2 * tig ? 0xffffffffu : 0u, mB = gid == 2 * tig + 1 ? 0xffffffffu : 0u;
-    const int bx = 8 * s + gid;
-    XFrag<T> X;
-#pragma unroll
-    for (int t = 0; t < T; t++) {
-        if (t < n) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(xp + (size_t)tok[t] * (H / 32) * P.xp_stride +
-                                                               (size_t)bx * P.xp_stride);
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                uint4 v = src[j];
-                X.r[t][4 * j] = v.x;
-                X.r[t][4 * j + 1] = v.y;
-                X.r[t][4 * j + 2] = v.z;
-                X.r[t][4 * j + 3] = v.w;
-            }
-        }
-    }
     float acc[T][2][4];
 #pragma unroll
     for (int t = 0; t < T; t++)
@@ -513,25 +560,28 @@ __device__ __forceinline__ void gu_item(const Plan &P, const char *slot, int mtx
         for (int w = 0; w < 2; w++) acc[t][w][0] = acc[t][w][1] = acc[t][w][2] = acc[t][w][3] = 0.f;
 #define MOE_GU_STEP(Wn, Mn)                                                                               \
     {                                                                                                     \
-        uint32_t a0 = dq_pair<Mn, BITS, Wn>(W0, W0s6, W0s12, H0);                                         \
-        uint32_t a1 = dq_pair<Mn, BITS, Wn>(W1, W1s6, W1s12, H1);                                         \
-        uint32_t a2 = dq_pair<Mn, BITS, Wn>(W2, W2s6, W2s12, H2);                                         \
-        uint32_t a3 = dq_pair<Mn, BITS, Wn>(W3, W3s6, W3s12, H3);                                         \
-        _Pragma("unroll") for (int t = 0; t < T; t++) if (t < n)                                          \
-            mma16816(acc[t][Wn], a0, a1, a2, a3, X.r[t][8 * Wn + Mn] & mA, X.r[t][8 * Wn + Mn] & mB);     \
+        const uint32_t a0 = dq_pair<Mn, BITS, Wn>(W0, W0q, H0);                                           \
+        const uint32_t a1 = dq_pair<Mn, BITS, Wn>(W1, W1q, H1);                                           \
+        const uint32_t a2 = dq_pair<Mn, BITS, Wn>(W2, W2q, H2);                                           \
+        const uint32_t a3 = dq_pair<Mn, BITS, Wn>(W3, W3q, H3);                                           \
+        _Pragma("unroll") for (int t = 0; t < T; t++) if (t < n) {                                        \
+            if constexpr (GuOps<T>::kPre)                                                                 \
+                mma16816(acc[t][Wn], a0, a1, a2, a3, O.A[t][8 * Wn + Mn], O.B[t][8 * Wn + Mn]);           \
+            else                                                                                          \
+                mma16816(acc[t][Wn], a0, a1, a2, a3, O.X[t][8 * Wn + Mn] & mA, O.X[t][8 * Wn + Mn] & mB); \
+        }                                                                                                 \
     }
-#define MOE_GU_WORD(Wn)                                                                                   \
+#define MOE_GU_WORD(Wn, X0, X1, X2, X3)                                                                   \
     {                                                                                                     \
-        const uint32_t W0 = Wn ? q00.y : q00.x, W1 = Wn ? q10.y : q10.x;                                  \
-        const uint32_t W2 = Wn ? q01.y : q01.x, W3 = Wn ? q11.y : q11.x;                                  \
-        const uint32_t W0s6 = W0 >> 6, W1s6 = W1 >> 6, W2s6 = W2 >> 6, W3s6 = W3 >> 6;                    \
-        const uint32_t W0s12 = W0 >> 12, W1s12 = W1 >> 12, W2s12 = W2 >> 12, W3s12 = W3 >> 12;            \
-        const uint32_t H0 = h00, H1 = h10, H2 = h01, H3 = h11;                                            \
+        const uint32_t W0 = X0, W1 = X1, W2 = X2, W3 = X3;                                                \
+        const uint32_t W0q = dq_shift<BITS>(W0), W1q = dq_shift<BITS>(W1);                                \
+        const uint32_t W2q = dq_shift<BITS>(W2), W3q = dq_shift<BITS>(W3);                                \
+        const uint32_t H0 = hq0.x, H1 = hq1.x, H2 = hq0.y, H3 = hq1.y;                                    \
         MOE_GU_STEP(Wn, 0) MOE_GU_STEP(Wn, 1) MOE_GU_STEP(Wn, 2) MOE_GU_STEP(Wn, 3)                        \
         MOE_GU_STEP(Wn, 4) MOE_GU_STEP(Wn, 5) MOE_GU_STEP(Wn, 6) MOE_GU_STEP(Wn, 7)                        \
     }
-    MOE_GU_WORD(0)
-    MOE_GU_WORD(1)
+    MOE_GU_WORD(0, q0.x, q1.x, q0.z, q1.z)
+    MOE_GU_WORD(1, q0.y, q1.y, q0.w, q1.w)
 #undef MOE_GU_WORD
 #undef MOE_GU_STEP
     constexpr float mid = BITS == 2 ? 1.5f : 3.5f;
@@ -564,13 +614,14 @@ __device__ __forceinline__ void gu_item(const Plan &P, const char *slot, int mtx
 // One down work item: super-tile s2 (columns 128 s2 .. 128 s2 + 127 of h) of
 // the group in `slot` (16 code rows of Wd_e, the CTA's output rows, and their
 // scales), for the n tokens of the group.  Accumulator columns are (part,
-// block): 0..3 the bf16 high parts of h in the super-tile's four blocks, 4..7
-// the low parts, so both parts share one dequantised A operand.  `hop`, `hs16`
-// (shared memory if `staged`, else global) hold h's operand words and half-
-// block sums.  Writes per-row partial sums to pd[(p0 + t) * NSD2 + s2][16].
+// block): 0..3 the fp16 high parts of h in the super-tile's four blocks, 4..7
+// the low parts, so both parts share one dequantised A operand.  h's operand
+// words and half-block sums come from `hop`, `hs16` (shared memory if
+// `staged`, else global).  Writes per-row partial sums to
+// pd[(p0 + t) * NSD2 + s2][16].
 template <int T, int BITS>
 __device__ __forceinline__ void down_item(const Plan &P, const char *slot, int s2, int n, int p0, const uint32_t *hop,
-                                          const float *hs16, bool staged, int I, float *pd)
+                                          const float *hs16, bool staged, const uint32_t *zero16, int I, float *pd)
 {
     const int lane = lane_id(), gid = lane >> 2, tig = lane & 3;
     const uint8_t *cb = reinterpret_cast<const uint8_t *>(slot);
@@ -583,29 +634,58 @@ __device__ __forceinline__ void down_item(const Plan &P, const char *slot, int s
         hw0 = *reinterpret_cast<const uint32_t *>(cb + (size_t)gid * P.cb_d + I / 4 + bt * 4);
         hw1 = *reinterpret_cast<const uint32_t *>(cb + (size_t)(gid + 8) * P.cb_d + I / 4 + bt * 4);
     }
-    const uint32_t mA = gid == tig ? 0xffffffffu : 0u, mB = gid == tig + 4 ? 0xffffffffu : 0u;
-    const bool act = (mA | mB) != 0;
-    // operands: the high (gid == tig) or low (gid == tig + 4) bf16 part of h
-    // over block bt as pairs (16w+m, 16w+m+8), made by the gate/up epilogue;
-    // the block sum of h from its two 16-value halves
-    uint32_t B[T][16];
+    const bool isA = gid == tig, isB = gid == tig + 4;
+    const uint32_t mA = isA ? 0xffffffffu : 0u, mB = isB ? 0xffffffffu : 0u;
+    // B operands: the high (isA lanes) or low (isB lanes) fp16 part of h over
+    // block bt as pairs (16w+m, 16w+m+8), made by the gate/up epilogue; the
+    // block sum of h from its two 16-value halves
+    constexpr bool kPre = T <= 2;
+    uint32_t BA[kPre ? T : 1][16], BB[kPre ? T : 1][16], BX[kPre ? 1 : T][16];
     float hsum[T];
 #pragma unroll
     for (int t = 0; t < T; t++) {
         hsum[t] = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; i++) B[t][i] = 0u;
-        if (t < n && act) {
+        if (t < n) {
             const size_t pb = (size_t)(p0 + t) * (I / 32) + bt;
-            const uint4 *src = reinterpret_cast<const uint4 *>(hop + pb * 32 + (mB ? 16 : 0));
+            const uint32_t *wa = hop + pb * 32, *wb = wa + 16;
+            if (kPre && staged) {
+                const uint4 *pa = reinterpret_cast<const uint4 *>(isA ? wa : zero16);
+                const uint4 *pq = reinterpret_cast<const uint4 *>(isB ? wb : zero16);
 #pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const uint4 v = staged ? src[j] : __ldcg(src + j);
-                B[t][4 * j] = v.x; B[t][4 * j + 1] = v.y; B[t][4 * j + 2] = v.z; B[t][4 * j + 3] = v.w;
+                for (int j = 0; j < 4; j++) {
+                    const uint4 va = pa[j], vb = pq[j];
+                    BA[kPre ? t : 0][4 * j] = va.x; BA[kPre ? t : 0][4 * j + 1] = va.y;
+                    BA[kPre ? t : 0][4 * j + 2] = va.z; BA[kPre ? t : 0][4 * j + 3] = va.w;
+                    BB[kPre ? t : 0][4 * j] = vb.x; BB[kPre ? t : 0][4 * j + 1] = vb.y;
+                    BB[kPre ? t : 0][4 * j + 2] = vb.z; BB[kPre ? t : 0][4 * j + 3] = vb.w;
+                }
+            } else {
+                uint32_t v[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) v[i] = 0u;
+                if (isA || isB) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(isB ? wb : wa);
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const uint4 q = staged ? src[j] : __ldcg(src + j);
+                        v[4 * j] = q.x; v[4 * j + 1] = q.y; v[4 * j + 2] = q.z; v[4 * j + 3] = q.w;
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    if constexpr (kPre) {
+                        BA[t][i] = v[i] & mA;
+                        BB[t][i] = v[i] & mB;
+                    } else {
+                        BX[kPre ? 0 : t][i] = v[i];
+                    }
+                }
             }
-            const float2 hh = staged ? *reinterpret_cast<const float2 *>(hs16 + 2 * pb)
-                                     : __ldcg(reinterpret_cast<const float2 *>(hs16 + 2 * pb));
-            hsum[t] = hh.x + hh.y;
+            if (isA) {
+                const float2 hh = staged ? *reinterpret_cast<const float2 *>(hs16 + 2 * pb)
+                                         : __ldcg(reinterpret_cast<const float2 *>(hs16 + 2 * pb));
+                hsum[t] = hh.x + hh.y;
+            }
         }
     }
     float acc[T][2][4];
@@ -615,15 +695,19 @@ __device__ __forceinline__ void down_item(const Plan &P, const char *slot, int s
         for (int w = 0; w < 2; w++) acc[t][w][0] = acc[t][w][1] = acc[t][w][2] = acc[t][w][3] = 0.f;
 #define MOE_D_STEP(Wn, Mn)                                                                                \
     {                                                                                                     \
-        uint32_t a0 = dq_pair<Mn, BITS, Wn>(W0, W0s6, W0s12, hw0);                                        \
-        uint32_t a1 = dq_pair<Mn, BITS, Wn>(W1, W1s6, W1s12, hw1);                                        \
-        _Pragma("unroll") for (int t = 0; t < T; t++) if (t < n)                                          \
-            mma16816(acc[t][Wn], a0, a1, a0, a1, B[t][8 * Wn + Mn] & mA, B[t][8 * Wn + Mn] & mB);         \
+        const uint32_t a0 = dq_pair<Mn, BITS, Wn>(W0, W0q, hw0);                                          \
+        const uint32_t a1 = dq_pair<Mn, BITS, Wn>(W1, W1q, hw1);                                          \
+        _Pragma("unroll") for (int t = 0; t < T; t++) if (t < n) {                                        \
+            if constexpr (kPre)                                                                           \
+                mma16816(acc[t][Wn], a0, a1, a0, a1, BA[t][8 * Wn + Mn], BB[t][8 * Wn + Mn]);             \
+            else                                                                                          \
+                mma16816(acc[t][Wn], a0, a1, a0, a1, BX[t][8 * Wn + Mn] & mA, BX[t][8 * Wn + Mn] & mB);   \
+        }                                                                                                 \
     }
 #define MOE_D_WORD(Wn)                                                                                    \
     {                                                                                                     \
         const uint32_t W0 = Wn ? q0.y : q0.x, W1 = Wn ? q1.y : q1.x;                                      \
-        const uint32_t W0s6 = W0 >> 6, W1s6 = W1 >> 6, W0s12 = W0 >> 12, W1s12 = W1 >> 12;                \
+        const uint32_t W0q = dq_shift<BITS>(W0), W1q = dq_shift<BITS>(W1);                                \
         MOE_D_STEP(Wn, 0) MOE_D_STEP(Wn, 1) MOE_D_STEP(Wn, 2) MOE_D_STEP(Wn, 3)                            \
         MOE_D_STEP(Wn, 4) MOE_D_STEP(Wn, 5) MOE_D_STEP(Wn, 6) MOE_D_STEP(Wn, 7)                            \
     }
@@ -641,11 +725,11 @@ __device__ __forceinline__ void down_item(const Plan &P, const char *slot, int s
 #pragma unroll
     for (int t = 0; t < T; t++) {
         if (t < n) {
-            float H0 = __shfl_sync(0xffffffffu, hsum[t], src0);
-            float H1 = __shfl_sync(0xffffffffu, hsum[t], src1);
-            float o0 = hi_cols ? -mid * H0 : 0.f, o1 = hi_cols ? -mid * H1 : 0.f;
-            float c0 = acc[t][0][0] + acc[t][1][0], c1 = acc[t][0][1] + acc[t][1][1];
-            float c2 = acc[t][0][2] + acc[t][1][2], c3 = acc[t][0][3] + acc[t][1][3];
+            const float H0 = __shfl_sync(0xffffffffu, hsum[t], src0);
+            const float H1 = __shfl_sync(0xffffffffu, hsum[t], src1);
+            const float o0 = hi_cols ? -mid * H0 : 0.f, o1 = hi_cols ? -mid * H1 : 0.f;
+            const float c0 = acc[t][0][0] + acc[t][1][0], c1 = acc[t][0][1] + acc[t][1][1];
+            const float c2 = acc[t][0][2] + acc[t][1][2], c3 = acc[t][0][3] + acc[t][1][3];
             float r0 = sa.x * (c0 + o0);
             r0 = fmaf(sa.y, c1 + o1, r0);
             float r1 = sc.x * (c2 + o0);
@@ -729,7 +813,44 @@ __device__ void issue_down(const Args &a, const Plan &P, const Layer &L, const R
 // The number of fills a ring slot s receives when n items go through nslot slots.
 __device__ __forceinline__ int fills_of(int s, int n, int nslot) { return s < n ? (n - 1 - s) / nslot + 1 : 0; }
 
-__device__ __forceinline__ float bf16r(float f) { return bf16_to_f32(f32_to_bf16(f)); }
+
+// h = silu(g) * u for the 16 rows of unit row tile rt (n tokens, sorted pairs
+// p0..p0+n-1) from its per-super-tile partial sums, stored as the down
+// projection's operand words: fp16 high and low parts paired (16w+m,
+// 16w+m+8) in block rt/2, word half w = rt&1, and the fp32 sum of the 16
+// values.  One warp.
+template <int T>
+__device__ __forceinline__ void finalize_unit(const Args &a, const float *pslot, int n, int p0, int rt, int I, int NST)
+{
+    const int lane = lane_id();
+    for (int tb = 0; tb < n; tb += 2) {
+        const int t = tb + (lane >> 4), r = lane & 15;
+        float hv = 0.f;
+        if (t < n) {
+            float gs = 0.f, us = 0.f;
+            for (int s2 = 0; s2 < NST; s2++) {
+                gs += pslot[((size_t)s2 * 16 + r) * T + t];
+                us += pslot[((size_t)(NST + s2) * 16 + r) * T + t];
+            }
+            hv = silu(gs) * us;
+        }
+        const uint16_t hi = f16_bits(hv);
+        const uint16_t lo = f16_bits(hv - f16_val(hi));
+        const uint16_t hi8 = (uint16_t)__shfl_down_sync(0xffffffffu, (unsigned)hi, 8);
+        const uint16_t lo8 = (uint16_t)__shfl_down_sync(0xffffffffu, (unsigned)lo, 8);
+        float s16 = hv;
+#pragma unroll
+        for (int o = 8; o; o >>= 1) s16 += __shfl_xor_sync(0xffffffffu, s16, o);
+        if (t < n) {
+            const size_t pb = (size_t)(p0 + t) * (I / 32) + (rt >> 1);
+            if (r < 8) {
+                __stcg(a.hop + pb * 32 + 8 * (rt & 1) + r, pack16(hi, hi8));
+                __stcg(a.hop + pb * 32 + 16 + 8 * (rt & 1) + r, pack16(lo, lo8));
+            }
+            if (r == 0) __stcg(a.hsum + (size_t)(p0 + t) * (I / 16) + rt, s16);
+        }
+    }
+}
 
 // ------------------------------------------------------------ the kernel
 
@@ -742,6 +863,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
     constexpr int kQ = 10;  // H / 256 <= 9 (at most 16 output rows per CTA)
     extern __shared__ __align__(128) char dyn[];
     __shared__ Routing R;
+    __shared__ __align__(16) uint32_t zero16[16];  // B operands of lanes that supply none
     __shared__ int iss_u[kMaxUnitSlots], iss_d[kMaxDownSlots], iss_a, iss_s;  // fills issued per barrier
     const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
     const int G = gridDim.x, cta = blockIdx.x;
@@ -761,6 +883,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
     float *xown = reinterpret_cast<float *>(dyn + P.off_xown);     // [T][16] own rows of x
     float *sdn = xown + T * 16;                                    // [T][16] shared down outputs
 
+    if (tid < 16) zero16[tid] = 0u;
     if (tid == 0) {
         for (int s = 0; s < P.nsu; s++) {
             tc::mbar_init(&R.fullU[s], 1);
@@ -788,6 +911,12 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
     for (int l = 0; l < a.n_layers; l++) {
         const Layer &L = a.L[l];
         bool fail = false;
+        int r0, rh, q0, qh;
+        split_range(E, cta, G, r0, rh);
+        split_range(Is, cta, G, q0, qh);
+        if (!L.swg) qh = q0;
+        // the bias of router row r0 + warp, requested now and used in phase A
+        const float bias_w = (L.bias && warp < rh - r0) ? __ldg(L.bias + r0 + warp) : 0.f;
         // ---- gather x_l (every CTA, all of it), u = bf16(x * inv_rms)
         const int nq = H / 256;
         float xr[T][kQ];
@@ -847,27 +976,26 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
         }
         __syncthreads();
         if (tid < kRedV) {
+            // warp w holds block 8q+w of every token for each q: u, its block
+            // sum and its MMA operand pairs (16w+m, 16w+m+8) straight from here
 #pragma unroll
             for (int t = 0; t < T; t++)
 #pragma unroll
                 for (int q = 0; q < kQ; q++)
-                    if (q < nq) xb[(size_t)t * H + tid + 256 * q] = f32_to_bf16(xr[t][q] * R.inv_rms[t]);
-        }
-        __syncthreads();
-        for (int i = warp; i < T * (H / 32); i += NW) {  // token i / (H/32), block i % (H/32)
-            const uint16_t uv = xb[(size_t)i * 32 + lane];
-            const float sum = warp_sum(bf16_to_f32(uv));
-            const uint16_t up = (uint16_t)__shfl_down_sync(0xffffffffu, (unsigned)uv, 8);
-            if (lane == 0) xs[i] = sum;
-            if ((lane & 8) == 0)  // lane 16w + m holds position 16w+m, pairs with 16w+m+8
-                reinterpret_cast<uint32_t *>(xp + (size_t)i * P.xp_stride)[8 * (lane >> 4) + (lane & 7)] =
-                    pack_bf16(uv, up);
+                    if (q < nq) {
+                        const int b = 8 * q + warp;
+                        const uint16_t uv = f32_to_bf16(xr[t][q] * R.inv_rms[t]);
+                        xb[(size_t)t * H + tid + 256 * q] = uv;
+                        const float sum = warp_sum(bf16_to_f32(uv));
+                        const uint16_t uh = f16_bits(bf16_to_f32(uv));  // exact for |u| >= 2^-17
+                        const uint16_t up = (uint16_t)__shfl_down_sync(0xffffffffu, (unsigned)uh, 8);
+                        if (lane == 0) xs[t * (H / 32) + b] = sum;
+                        if ((lane & 8) == 0)
+                            reinterpret_cast<uint32_t *>(xp + ((size_t)t * (H / 32) + b) * P.xp_stride)
+                                [8 * (lane >> 4) + (lane & 7)] = pack16(uh, up);
+                    }
         }
         // ---- A: router rows (fp32 weights) -> tagged logits
-        int r0, rh, q0, qh;
-        split_range(E, cta, G, r0, rh);
-        split_range(Is, cta, G, q0, qh);
-        if (!L.swg) qh = q0;
         bool okA = tc::mbar_wait(&R.fullA, (uint32_t)(fillsA & 1), kTimeoutNs);
         fillsA++;
         if (__syncthreads_or(!okA)) {
@@ -896,7 +1024,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                         acc[t] = fmaf(w.w, __uint_as_float(ub.y & 0xffff0000u), acc[t]);
                     }
                 }
-                const float b = L.bias ? L.bias[r0 + item] : 0.f;
+                const float b = item < NW ? bias_w : (L.bias ? L.bias[r0 + item] : 0.f);
 #pragma unroll
                 for (int t = 0; t < T; t++) {
                     const float sv = warp_sum(acc[t]);
@@ -969,7 +1097,10 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
         if (nan_mask && tid == 0) set_status(a.status, MOE_ERR_NONFINITE);
         if (warp < T) topk_weights(R, warp, k, (nan_mask >> warp) & 1u);
         __syncthreads();
-        if (warp == 0) build_groups(R, T * k);
+        if (warp == 0) {
+            build_groups(R, T * k);
+            pair_tokens(R, T * k, k);
+        }
         __syncthreads();
         if (cta == 0 && a.ids_out && tid < T * k) {
             a.ids_out[(size_t)l * T * k + tid] = R.ids[tid];
@@ -993,68 +1124,70 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             }
         }
         // ---- B: routed gate/up on the tensor cores
-        for (int j = warp; j < nu * per_unit; j += NW) {
-            const int ul = j / per_unit, it = j % per_unit, mtx = it / NST, s = it % NST;
-            const int slot = ul % P.nsu, fill = R.fills_u[slot] + ul / P.nsu;
+        const bool ring = nu > P.nsu;
+        // item j = ul * per_unit + it for j = warp, warp + NW, ...: the unit ul
+        // (its slot, fill, group and row tile) and the item it advance by
+        // counting, without divisions
+        int ul = 0, it = warp, slot = 0, fq = 0, g = u0 / tiles, rt = u0 % tiles;
+        while (it >= per_unit) {
+            it -= per_unit;
+            ul++;
+            if (++slot == P.nsu) { slot = 0; fq++; }
+            if (++rt == tiles) { rt = 0; g++; }
+        }
+        for (; ul < nu;) {
+            const int mtx = it >= NST, s = it - mtx * NST;
+            const int fill = R.fills_u[slot] + fq;
             if (!tc::mbar_wait(&R.fullU[slot], (uint32_t)(fill & 1), kTimeoutNs)) {
                 fail = true;
                 break;
             }
-            const int u = u0 + ul, g = u / tiles, rt = u % tiles;
+            const int u = u0 + ul;
             const int n = R.g_n[g], p0 = R.g_p0[g];
             int tok[kMaxT];
 #pragma unroll
-            for (int t = 0; t < kMaxT; t++) tok[t] = t < n ? R.perm[p0 + t] / k : 0;
+            for (int t = 0; t < kMaxT; t++) tok[t] = t < n ? R.tok_of[p0 + t] : 0;
             float *pslot = pgu + (size_t)slot * per_unit * 16 * T;
-            gu_item<T, BITS>(P, r1 + (size_t)slot * P.unitB, mtx, s, n, tok, xp, xs, H, pslot);
-            __syncwarp();
-            int last = 0;
-            if (lane == 0) {
-                __threadfence_block();
-                last = atomicAdd(&R.ucnt[slot], 1) == per_unit - 1;
-            }
-            last = __shfl_sync(0xffffffffu, last, 0);
-            if (last) {
-                // h = silu(g) * u for the unit's 16 rows, stored as the down
-                // projection's operand words: bf16 high and low parts paired
-                // (16w+m, 16w+m+8) in block rt/2, word half w = rt&1, and the
-                // fp32 sum of the 16 values
-                __threadfence_block();
-                for (int tb = 0; tb < n; tb += 2) {
-                    const int t = tb + (lane >> 4), r = lane & 15;
-                    float hv = 0.f;
-                    if (t < n) {
-                        float gs = 0.f, us = 0.f;
-                        for (int s2 = 0; s2 < NST; s2++) {
-                            gs += pslot[((size_t)s2 * 16 + r) * T + t];
-                            us += pslot[((size_t)(NST + s2) * 16 + r) * T + t];
-                        }
-                        hv = silu(gs) * us;
-                    }
-                    const uint16_t hi = f32_to_bf16(hv);
-                    const uint16_t lo = f32_to_bf16(hv - bf16_to_f32(hi));
-                    const uint16_t hi8 = (uint16_t)__shfl_down_sync(0xffffffffu, (unsigned)hi, 8);
-                    const uint16_t lo8 = (uint16_t)__shfl_down_sync(0xffffffffu, (unsigned)lo, 8);
-                    float s16 = hv;
-#pragma unroll
-                    for (int o = 8; o; o >>= 1) s16 += __shfl_xor_sync(0xffffffffu, s16, o);
-                    if (t < n) {
-                        const size_t pb = (size_t)(p0 + t) * (I / 32) + (rt >> 1);
-                        if (r < 8) {
-                            __stcg(a.hop + pb * 32 + 8 * (rt & 1) + r, pack_bf16(hi, hi8));
-                            __stcg(a.hop + pb * 32 + 16 + 8 * (rt & 1) + r, pack_bf16(lo, lo8));
-                        }
-                        if (r == 0) __stcg(a.hsum + (size_t)(p0 + t) * (I / 16) + rt, s16);
-                    }
-                }
+            GuOps<T> ops;
+            gu_load_ops<T>(ops, s, n, tok, xp, H, P.xp_stride, zero16);
+            gu_item<T, BITS>(P, r1 + (size_t)slot * P.unitB, mtx, s, n, ops, tok, xs, H, pslot);
+            if (ring) {  // slots are reused: the last item of a unit finalises it and refills the slot
                 __syncwarp();
+                int last = 0;
                 if (lane == 0) {
-                    atomicExch(&R.ucnt[slot], 0);
-                    if (ul + P.nsu < nu) {
-                        issue_unit(a, P, L, R, u + P.nsu, r1 + (size_t)slot * P.unitB, &R.fullU[slot]);
-                        iss_u[slot]++;
+                    __threadfence_block();
+                    last = atomicAdd(&R.ucnt[slot], 1) == per_unit - 1;
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence_block();
+                    finalize_unit<T>(a, pslot, n, p0, rt, I, NST);
+                    __syncwarp();
+                    if (lane == 0) {
+                        atomicExch(&R.ucnt[slot], 0);
+                        if (ul + P.nsu < nu) {
+                            issue_unit(a, P, L, R, u + P.nsu, r1 + (size_t)slot * P.unitB, &R.fullU[slot]);
+                            iss_u[slot]++;
+                        }
                     }
                 }
+            }
+            for (it += NW; it >= per_unit;) {
+                it -= per_unit;
+                ul++;
+                if (++slot == P.nsu) { slot = 0; fq++; }
+                if (++rt == tiles) { rt = 0; g++; }
+            }
+        }
+        if (!ring) {  // every unit had its own slot: finalise them all once every item is done
+            if (__syncthreads_or(fail)) {
+                if (tid == 0) raise_abort(a);
+                ok = false;
+                break;
+            }
+            for (int ul = warp; ul < nu; ul += NW) {
+                const int u = u0 + ul, g = u / tiles;
+                finalize_unit<T>(a, pgu + (size_t)ul * per_unit * 16 * T, R.g_n[g], R.g_p0[g], u % tiles, I, NST);
             }
         }
         if (__syncthreads_or(fail)) {
@@ -1110,7 +1243,8 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                 }
             }
         }
-        // ---- every CTA's h
+        // ---- every CTA's h: its operand words and half-block sums, staged in
+        // shared memory when they fit, else read by each down item
         if (tid == 0) fail = !wait_counter(a, a.cnt + 0, (unsigned)(l + 1) * (unsigned)G);
         if (__syncthreads_or(fail)) { ok = false; break; }
         if (tid == 0 && l + 1 < a.n_layers) {  // the shared down rows are consumed: fetch the next layer's
@@ -1120,11 +1254,10 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
         }
         const uint32_t *hop = a.hop;
         const float *hs16 = a.hsum;
-        if (P.stage_h && nrows > 0) {  // h's operand words and half-block sums into shared memory, once
+        if (P.stage_h && nrows > 0) {
             uint4 *dst = reinterpret_cast<uint4 *>(dyn + P.off_hop);
             const uint4 *src = reinterpret_cast<const uint4 *>(a.hop);
-            const int n4 = T * k * I / 4;
-            for (int i = tid; i < n4; i += NT) dst[i] = __ldcg(src + i);
+            for (int i = tid; i < T * k * I / 4; i += NT) dst[i] = __ldcg(src + i);
             float *hsd = reinterpret_cast<float *>(dyn + P.off_hsum);
             for (int i = tid; i < T * k * (I / 16); i += NT) hsd[i] = __ldcg(a.hsum + i);
             __syncthreads();
@@ -1133,27 +1266,40 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
         }
         // ---- C: routed down on the tensor cores
         if (nrows > 0) {
-            for (int j = warp; j < ng * NSD2; j += NW) {
-                const int g = j / NSD2, s2 = j % NSD2, slot = g % P.nsd, fill = R.fills_d[slot] + g / P.nsd;
+            int g = 0, s2 = warp, slot = 0, fq = 0;
+            while (s2 >= NSD2) {
+                s2 -= NSD2;
+                g++;
+                if (++slot == P.nsd) { slot = 0; fq++; }
+            }
+            for (; g < ng;) {
+                const int fill = R.fills_d[slot] + fq;
                 if (!tc::mbar_wait(&R.fullD[slot], (uint32_t)(fill & 1), kTimeoutNs)) {
                     fail = true;
                     break;
                 }
-                down_item<T, BITS>(P, r2 + (size_t)slot * P.downB, s2, R.g_n[g], R.g_p0[g], hop, hs16, P.stage_h != 0, I,
-                                   pd);
-                __syncwarp();
-                int last = 0;
-                if (lane == 0) {
-                    __threadfence_block();
-                    last = atomicAdd(&R.dcnt[slot], 1) == NSD2 - 1;
-                }
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (last && lane == 0) {
-                    atomicExch(&R.dcnt[slot], 0);
-                    if (g + P.nsd < ng) {
-                        issue_down(a, P, L, R, g + P.nsd, o0, nrows, r2 + (size_t)slot * P.downB, &R.fullD[slot]);
-                        iss_d[slot]++;
+                down_item<T, BITS>(P, r2 + (size_t)slot * P.downB, s2, R.g_n[g], R.g_p0[g], hop, hs16, P.stage_h != 0,
+                                   zero16, I, pd);
+                if (ng > P.nsd) {  // slots are reused: the last item of a group refills its slot
+                    __syncwarp();
+                    int last = 0;
+                    if (lane == 0) {
+                        __threadfence_block();
+                        last = atomicAdd(&R.dcnt[slot], 1) == NSD2 - 1;
                     }
+                    last = __shfl_sync(0xffffffffu, last, 0);
+                    if (last && lane == 0) {
+                        atomicExch(&R.dcnt[slot], 0);
+                        if (g + P.nsd < ng) {
+                            issue_down(a, P, L, R, g + P.nsd, o0, nrows, r2 + (size_t)slot * P.downB, &R.fullD[slot]);
+                            iss_d[slot]++;
+                        }
+                    }
+                }
+                for (s2 += NW; s2 >= NSD2;) {
+                    s2 -= NSD2;
+                    g++;
+                    if (++slot == P.nsd) { slot = 0; fq++; }
                 }
             }
         }
@@ -1233,7 +1379,7 @@ struct Ws {
 static Ws ws_layout(int T, int H, int I, int E, int k, int Is)
 {
     Ws w;
-    w.cnt = 0;
+    w.cnt = 0;  // counters and tagged words: zeroed before each launch
     w.xll = 256;
     w.lgll = w.xll + align256((size_t)2 * T * H * 8);
     w.zero_end = w.lgll + align256((size_t)2 * T * E * 8);
