@@ -11,8 +11,13 @@ expert_forward.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Prints one JSON line.  ``--impl reference`` times the oracle (plain scalar
-CPU code) on a bounded sample of the same workload instead.  Under torchrun
+Prints one JSON line.  Besides the headline (one-token decode) it carries
+``verify_4tok`` (4-token verify windows through the same 48-layer stack) and
+``prefill_32k`` (one layer over a 32,768-token prompt: router, permutation,
+shared expert and the grouped expert GEMMs, with the tensor roofline of the
+expert call); ``--no-extra`` skips those two.  ``--impl reference`` times the
+oracle (plain scalar CPU code) on a bounded sample of the same workload
+instead.  Under torchrun
 every rank runs an independent replica (the layer does not shard across GPUs
 here); rank 0 prints the whole-job throughput.
 """
@@ -48,6 +53,15 @@ def peaks():
         d = json.load(open(p))
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def peaks_bf16():
+    """Dense bf16 tensor peak (TFLOP/s), burst: the prefill GEMMs are timed alone."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
 
 
 class ClockSampler:
@@ -199,6 +213,117 @@ def run_reference(args, world, rank):
 
 # ---------------------------------------------------------------- our leg
 
+def bench_verify(m, lib, layers, descs, dev, stream, steps: int, warmup: int):
+    """4-token verify windows through the same stack (moe_decode_forward, T=4).
+
+    Bytes per step are counted from the routing the kernel reports: the union
+    of the 4 tokens' experts in every layer, plus every layer's router and
+    shared expert.
+    """
+    import ctypes
+
+    import torch
+
+    from bit_expert_ffn_gb300 import synth
+
+    T, NL = 4, len(layers)
+    nb = m.moe_decode_workspace_size(T, H, I, E, K_TOP, IS)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ids = torch.empty(NL, T, K_TOP, dtype=torch.int32, device=dev)
+    wts = torch.empty(NL, T, K_TOP, dtype=torch.float32, device=dev)
+    n_steps = warmup + steps
+    X = torch.stack([torch.from_numpy(synth.bf16_bits_to_f32(synth.verify_window(100 + i, T, H))) for i in range(n_steps)]).to(dev)
+    x = torch.zeros(T, H, dtype=torch.float32, device=dev)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    unions = []
+
+    def call(with_ids):
+        r = lib.moe_decode_forward(descs, NL, x.data_ptr(), T, K_TOP, m.RMS_EPS,
+                                   ids.data_ptr() if with_ids else None, wts.data_ptr() if with_ids else None,
+                                   ws.data_ptr(), nb, st.data_ptr(), sptr)
+        if r:
+            raise m.MoeError(r, m.moe_last_error())
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            x.copy_(X[i])
+            call(True)
+            stream.synchronize()
+            unions.append(sum(len(set(ids[l].flatten().tolist())) for l in range(NL)))
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(warmup, n_steps):
+            x.copy_(X[i])
+            call(False)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    assert m.moe_check_status(st) == 0, m.moe_last_error()
+    ms = e0.elapsed_time(e1) / steps
+    u = float(np.mean(unions))
+    bytes_step = u * EXPERT_BYTES + NL * (ROUTER_BYTES + SHARED_BYTES)
+    return {"workload": f"verify window: 4 tokens x {NL} layers, same stack (c + N(0, 0.3^2) per token)",
+            "value": T / (ms / 1000.0), "unit": "tokens/s", "ms_per_step": ms,
+            "mean_experts_per_step": u, "bytes_per_step": bytes_step,
+            "achieved_gbs": bytes_step / (ms / 1000.0) / 1e9}
+
+
+def bench_prefill(m, dev, reps: int = 3, T: int = 32768):
+    """One routed-expert layer over a 32,768-token prompt: router_topk ->
+    permute -> shared_expert -> expert_forward (prefill path), CUDA events
+    around each call."""
+    import torch
+
+    from bit_expert_ffn_gb300 import synth
+    from bit_expert_ffn_gb300.model import LayerShape, MoeLayer, StepBuffers, Workspace
+
+    s = LayerShape(bits=2)
+    L = MoeLayer(s, dev)
+    L.fill_device(seed=1, layer=0, zipf_s=1.1)
+    x = torch.from_numpy(synth.activations(1, T, s.H).view(np.int16)).to(dev)
+    bufs = StepBuffers(T, s.E, s.k, dev)
+    wsp = Workspace(dev)
+    out = torch.zeros(T, s.H, dtype=torch.float32, device=dev)
+    pws = m.moe_permute_workspace_size(T, s.k, s.E)
+    ews = m.moe_expert_forward_workspace_size(L.arena, T, s.k, m.MOE_PATH_PREFILL)
+    sws = m.moe_shared_expert_workspace_size(s.H, s.Is, T)
+    rws = m.moe_router_workspace_size(T, s.H, s.E, True)
+    buf = wsp.get(max(pws, ews, sws, rws))
+    res = {}
+    for r in range(reps + 2):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev[0].record()
+        m.moe_router_topk(x, T, s.H, L.router_w, L.router_b, s.E, s.k, bufs.logits, bufs.ids, bufs.w, buf, rws,
+                          dev_status=L.status)
+        ev[1].record()
+        m.moe_permute(bufs.ids, T, s.k, s.E, bufs.offsets, bufs.perm, bufs.inv, buf, pws, dev_status=L.status)
+        ev[2].record()
+        m.moe_shared_expert(*L.shared, s.H, s.Is, x, T, out, m.MOE_F32, False, buf, sws, L.status)
+        ev[3].record()
+        m.moe_expert_forward(L.arena, x, T, bufs.ids, bufs.w, s.k, bufs.offsets, bufs.perm, bufs.inv, out, m.MOE_F32,
+                             True, m.MOE_PATH_PREFILL, buf, ews, dev_status=L.status)
+        ev[4].record()
+        torch.cuda.synchronize()
+        if r >= 2:
+            for name, i0, i1 in (("router", 0, 1), ("permute", 1, 2), ("shared", 2, 3), ("experts", 3, 4),
+                                 ("total", 0, 4)):
+                res.setdefault(name, []).append(ev[i0].elapsed_time(ev[i1]))
+    assert m.moe_check_status(L.status) == 0, m.moe_last_error()
+    assert bool(torch.isfinite(out).all()), "prefill output is not finite"
+    ms = {k: float(np.median(v)) for k, v in res.items()}
+    flop = 2.0 * T * s.k * 3 * s.H * s.I  # routed experts: gate, up, down
+    tflops = flop / (ms["experts"] / 1000.0) / 1e12
+    peak = peaks_bf16()
+    return {"workload": f"prefill: {T} tokens x 1 layer, H=2048, E=512, I=768, top-10, 2-bit, Zipf(1.1)",
+            "value": T / (ms["total"] / 1000.0), "unit": "tokens/s", "ms": ms,
+            "experts_tflops": tflops, "experts_flop": flop,
+            "tensor_roofline": {"kernel": "moe_expert_forward prefill (gather, gate/up GEMM, down GEMM, combine)",
+                                "bound": "tensor", "achieved": tflops, "peak": peak[0], "unit": "TFLOP/s",
+                                "frac": tflops / peak[0], "peak_kind": peak[1],
+                                "note": "fp16 operands (kind::f16, the bf16 rate)"}}
+
+
 def run_ours(args, world, rank, local):
     import ctypes
 
@@ -323,6 +448,12 @@ def run_ours(args, world, rank, local):
     e2e = {"value": world * n_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 4 * H,
            "d2h_bytes_per_step": 4 * H}
 
+    extra = {}
+    if args.path == "fused" and not args.no_extra and NL == LAYERS:
+        extra["verify_4tok"] = bench_verify(m, lib, layers, descs, dev, stream, steps=min(args.steps, 50), warmup=3)
+    if not args.no_extra:  # the decode stack stays resident (36 GB of 288 GB)
+        extra["prefill_32k"] = bench_prefill(m, dev)
+
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline:
@@ -352,6 +483,7 @@ def run_ours(args, world, rank, local):
             "gpu_launches": kernels_per_step * args.steps,
             "cpu_baseline": cpu,
         }
+        line.update(extra)
         print(json.dumps(line), flush=True)
 
 
@@ -362,6 +494,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the verify-window and 32K-prefill measurements")
+    ap.add_argument("--only-prefill", action="store_true", help="run only the 32K-prefill measurement (profiling)")
     ap.add_argument("--path", default="fused", choices=["fused", "modular"])
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (48 is the workload; fewer only "
                     "for profiling captures)")
@@ -369,6 +503,15 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_setup()
+    if args.only_prefill:
+        import torch
+
+        import bit_expert_ffn_gb300 as m
+
+        torch.cuda.set_device(local)
+        m.load()
+        print(json.dumps(bench_prefill(m, torch.device("cuda", local))), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args, world, rank)
     else:

@@ -319,9 +319,13 @@ typedef struct moe_layer_weights {
  *   x        [T][H] fp32, device, 16-byte aligned, in/out
  *   ids_out, w_out  [n_layers][T][k] device outputs of the routing, or both NULL
  * A token's result does not depend on the other tokens of the call.  Shapes:
- * H a multiple of 32 up to 1024, or 2048 or 4096; I and shared_I multiples
- * of 32 up to 1024.  The kernel's grid barriers give up after about 2 s and
- * report MOE_ERR_TIMEOUT through dev_status.  The pages: 48 layers of a
+ * H a multiple of 256 with at most 16 output rows per SM (H <= 2432 on 152
+ * SMs), I a multiple of 128 up to 4096, shared_I a multiple of 64 up to 4096,
+ * E <= 1024, k <= 16; MOE_ERR_UNSUPPORTED when the buffers do not fit in
+ * shared memory.  The workspace (moe_decode_workspace_size) holds counters and
+ * tagged exchange words that the call zeroes on the stream before its launch.
+ * Every wait in the kernel gives up after about 2 s and reports
+ * MOE_ERR_TIMEOUT through dev_status.  The pages: 48 layers of a
  * router, ten of 512 experts and a shared expert, verify windows of up to
  * four tokens ("Strata serves a 125B MoE ...", section "Six billion active
  * parameters per token").
