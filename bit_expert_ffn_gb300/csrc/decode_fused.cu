@@ -26,10 +26,9 @@
 // shared-memory slots) completing on mbarriers; the next layer's router and
 // shared-expert rows are fetched while this layer finishes.  Routed products
 // run on mma.sync fp16 tensor-core instructions: a 2-/3-bit code c is turned
-// into the exact fp16 value c (one LOP3 + one HFMA2 per pair of weights), the
-// MMA sums c*u exactly per 32-weight block (one block per accumulator
-// column), and the block scale and the code offset are applied in fp32:
-// sum_i (c_i - mid) u_i s = s * (sum_i c_i u_i - mid * sum_i u_i).  The down
+// into the exact fp16 value c - mid (one LOP3 + one HFMA2 per pair), the
+// MMA sums (c - mid)*u exactly per 32-weight block (one block per
+// accumulator column), and the block scale is applied in fp32.  The down
 // projection's fp32 h enters as two fp16 parts (h = hi + lo to 2^-22), and u
 // (bf16) converts to fp16 exactly down to 2^-17, so no operand is rounded
 // beyond fp32 accumulation (below 2^-17 by at most 2^-25).  Every wait (mbarrier, counter,
@@ -74,7 +73,6 @@ struct Args {
     uint64_t *xll;     // [2][T][H] tagged x between layers
     uint64_t *lgll;    // [2][T][E] tagged router logits
     uint32_t *hop;     // [T*k][I/32][2][16] routed h as fp16 operand pairs (high, low parts), sorted pair order
-    float *hsum;       // [T*k][I/16] sums of 16 consecutive h values
     float *hs;         // [T][Is] shared h
     unsigned *cnt;     // [0] h counter, [1] h_s counter, [2] abort word
     int32_t *ids_out;  // [n_layers][T][k] or NULL
@@ -91,7 +89,7 @@ struct Plan {
     int NST, NSD2;                   // gate/up super-tiles (256 wide), down super-tiles (128 wide)
     int rA, sA;                      // max router rows, max shared rows per CTA
     int xp_stride;                   // bytes per block of operand pairs (80: conflict-free 16-byte reads)
-    int off_xb, off_xp, off_xs, off_lg, off_r1, off_r2, off_r3, off_hs, off_pgu, off_pd, off_xown, off_hop, off_hsum;
+    int off_xb, off_xp, off_lg, off_r1, off_r2, off_r3, off_hs, off_pgu, off_pd, off_xown, off_hop;
     int stage_h;                     // h's operand words staged in shared memory for the down items
     int r1B, smem;
 };
@@ -108,10 +106,6 @@ struct Routing {
     float sel_v[kMaxT][kMaxK];
     float inv_rms[kMaxT];
     float wred[kMaxT][8];
-    float gmax_v[32];
-    int gmax_i[32];
-    float tau_v;
-    int tau_i, tau_all, ncand;
     int u0, nu;                     // this CTA's units [u0, u0 + nu)
     int fills_u[kMaxUnitSlots];     // completed fills per unit slot before this layer
     int fills_d[kMaxDownSlots];
@@ -258,25 +252,45 @@ __device__ __forceinline__ float warp_sum(float v)
 
 // ------------------------------------------------------------ routing
 
-// Top-k of one token's logits (in shared memory) by the whole CTA.  The
-// logits are cut into groups of 16 threads' elements; at least k groups hold
-// an element no worse than the k-th best group maximum tau, so the k best
-// logits are all at or before tau (otherwise, with fewer than k non-empty
-// groups, every logit is a candidate).  Candidates are ranked exactly among
-// themselves by (value desc, id asc).  `cv`, `ci` hold up to E candidates.
-// Returns true for a NaN logit (the token then gets ids 0..k-1).
-__device__ bool topk_cta(const float *l, int E, int k, Routing &R, int t, float *cv, int *ci)
+// Order-preserving 32-bit key of a logit (a larger key is a larger logit;
+// -0 counts as +0; every logit's key is >= 0x007FFFFF, so 0 means "none").
+__device__ __forceinline__ uint32_t order_key(float v)
 {
-    const int tid = threadIdx.x, nthr = blockDim.x, lane = lane_id();
-    float bv = 0.f;
-    int bi = INT32_MAX;
+    if (v == 0.f) v = 0.f;
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Top-k of one token's logits (in shared memory) by the whole CTA, in two
+// passes of warp reductions (redux.sync): every warp pops the k best of each
+// 32-logit chunk it holds in order (max of the keys; among equal keys the
+// lowest lane, which is the lowest id), then one warp merges the sorted
+// lists (max of the list heads; among equal heads the lowest id).  Order:
+// (value desc, id asc).  `ck`, `ci` hold ceil(E/threads) x warps x k
+// entries.  Returns true for a NaN logit (the token then gets ids 0..k-1).
+__device__ __noinline__ bool topk_cta(const float *l, int E, int k, Routing &R, int t, uint32_t *ck, int *ci)
+{
+    const int tid = threadIdx.x, nthr = blockDim.x, lane = lane_id(), warp = warp_id(), nw = nthr >> 5;
+    const int nch = (E + nthr - 1) / nthr;
     bool nan = false;
-    for (int e = tid; e < E; e += nthr) {
-        const float v = l[e];
-        nan |= isnan(v);
-        if (bi == INT32_MAX || before(v, e, bv, bi)) {
-            bv = v;
-            bi = e;
+    for (int c = 0; c < nch; c++) {
+        const int e = c * nthr + tid;
+        uint32_t key = 0;
+        if (e < E) {
+            const float v = l[e];
+            nan |= isnan(v);
+            key = order_key(v);
+        }
+        const int list = c * nw + warp;
+        for (int r = 0; r < k; r++) {
+            const uint32_t m = __reduce_max_sync(0xffffffffu, key);
+            const unsigned who = __ballot_sync(0xffffffffu, key == m && m != 0u);
+            const int w = who ? __ffs(who) - 1 : 0;
+            if (lane == w) key = 0u;
+            if (lane == 0) {
+                ck[list * k + r] = m;
+                ci[list * k + r] = who ? c * nthr + warp * 32 + w : INT32_MAX;
+            }
         }
     }
     if (__syncthreads_or(nan)) {
@@ -287,63 +301,20 @@ __device__ bool topk_cta(const float *l, int E, int k, Routing &R, int t, float 
         __syncthreads();
         return true;
     }
-#pragma unroll
-    for (int o = 8; o; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (oi != INT32_MAX && (bi == INT32_MAX || before(ov, oi, bv, bi))) {
-            bv = ov;
-            bi = oi;
-        }
-    }
-    const int ngrp = nthr / 16;
-    if ((lane & 15) == 0) {
-        R.gmax_v[tid >> 4] = bv;
-        R.gmax_i[tid >> 4] = bi;
-    }
-    if (tid == 0) R.ncand = 0;
-    __syncthreads();
-    if (tid < 32) {
-        const float gv = lane < ngrp ? R.gmax_v[lane] : 0.f;
-        const int gi = lane < ngrp ? R.gmax_i[lane] : INT32_MAX;
-        int r = 0;
-        for (int q = 0; q < ngrp; q++) {
-            const int oi = R.gmax_i[q];
-            if (oi != INT32_MAX && gi != INT32_MAX && before(R.gmax_v[q], oi, gv, gi)) r++;
-        }
-        const unsigned valid = __ballot_sync(0xffffffffu, gi != INT32_MAX);
-        const unsigned who = __ballot_sync(0xffffffffu, gi != INT32_MAX && r == k - 1);
-        const int src = who ? __ffs(who) - 1 : 0;
-        const float tv = __shfl_sync(0xffffffffu, gv, src);
-        const int ti = __shfl_sync(0xffffffffu, gi, src);
-        if (lane == 0) {
-            R.tau_all = __popc(valid) < k;
-            R.tau_v = tv;
-            R.tau_i = ti;
-        }
-    }
-    __syncthreads();
-    const float tv = R.tau_v;
-    const int ti = R.tau_i;
-    const bool all = R.tau_all;
-    for (int e = tid; e < E; e += nthr) {
-        const float v = l[e];
-        if (all || before(v, e, tv, ti) || (v == tv && e == ti)) {
-            const int pos = atomicAdd(&R.ncand, 1);
-            cv[pos] = v;
-            ci[pos] = e;
-        }
-    }
-    __syncthreads();
-    const int C = R.ncand;
-    for (int c = tid; c < C; c += nthr) {
-        const float x = cv[c];
-        const int e = ci[c];
-        int r = 0;
-        for (int d = 0; d < C; d++) r += before(cv[d], ci[d], x, e) ? 1 : 0;
-        if (r < k) {
-            R.sel_v[t][r] = x;
-            R.sel_i[t][r] = e;
+    if (warp == 0) {
+        const int nl = nch * nw;  // <= 32 lists, one per lane
+        int p = 0;
+        for (int r = 0; r < k; r++) {
+            const bool live = lane < nl && p < k;
+            const uint32_t hk = live ? ck[lane * k + p] : 0u;
+            const int hi = live ? ci[lane * k + p] : INT32_MAX;
+            const uint32_t m = __reduce_max_sync(0xffffffffu, hk);
+            const int idx = (int)__reduce_min_sync(0xffffffffu, (unsigned)(hk == m ? hi : INT32_MAX));
+            if (hk == m && hi == idx) p++;
+            if (lane == 0) {
+                R.sel_i[t][r] = idx;
+                R.sel_v[t][r] = l[idx];
+            }
         }
     }
     __syncthreads();
@@ -371,32 +342,49 @@ __device__ void topk_weights(Routing &R, int t, int k, bool nan_token)
     }
 }
 
-// Sort the T*k pairs by (expert, flat index) and cut them into groups (one warp).
+// Sort the T*k pairs by (expert, flat index) and cut them into groups (one
+// warp; n <= 64 pairs, two per lane, ranks by shuffles).
 __device__ void build_groups(Routing &R, int n)
 {
-    int lane = lane_id();
-    for (int f = lane; f < n; f += 32) {
-        int e = R.ids[f], r = 0;
-        for (int g = 0; g < n; g++) {
-            int eg = R.ids[g];
-            r += (eg < e || (eg == e && g < f)) ? 1 : 0;
+    const int lane = lane_id();
+    const int e0 = lane < n ? R.ids[lane] : INT32_MAX, e1 = lane + 32 < n ? R.ids[lane + 32] : INT32_MAX;
+    int r0 = 0, r1 = 0;
+    const int n0 = n < 32 ? n : 32;
+#pragma unroll 4
+    for (int g = 0; g < n0; g++) {
+        const int eg = __shfl_sync(0xffffffffu, e0, g);
+        r0 += (eg < e0 || (eg == e0 && g < lane)) ? 1 : 0;
+        r1 += (eg <= e1) ? 1 : 0;  // g < lane + 32 always
+    }
+    if (n > 32) {
+#pragma unroll 4
+        for (int g = 0; g < n - 32; g++) {
+            const int eg = __shfl_sync(0xffffffffu, e1, g);
+            r0 += (eg < e0) ? 1 : 0;  // g + 32 > lane always
+            r1 += (eg < e1 || (eg == e1 && g < lane)) ? 1 : 0;
         }
-        R.perm[r] = f;
-        R.inv[f] = r;
+    }
+    if (lane < n) {
+        R.perm[r0] = lane;
+        R.inv[lane] = r0;
+    }
+    if (lane + 32 < n) {
+        R.perm[r1] = lane + 32;
+        R.inv[lane + 32] = r1;
     }
     __syncwarp();
     int seen = 0;
     for (int b = 0; b < n; b += 32) {
-        int p = b + lane;
+        const int p = b + lane;
         bool start = false;
         int e = 0;
         if (p < n) {
             e = R.ids[R.perm[p]];
             start = p == 0 || R.ids[R.perm[p - 1]] != e;
         }
-        unsigned m = __ballot_sync(0xffffffffu, start);
+        const unsigned m = __ballot_sync(0xffffffffu, start);
         if (start) {
-            int g = seen + __popc(m & ((1u << lane) - 1u));
+            const int g = seen + __popc(m & ((1u << lane) - 1u));
             R.g_e[g] = e;
             R.g_p0[g] = p;
         }
@@ -443,36 +431,51 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c)
 }
 
 // Codes of a 16-weight word: weight j at bits 2j..2j+1 (low plane).  Pair M
-// (weights M and M+8, bits 2M and 2M+16) becomes the fp16x2 (c_M, c_{M+8})
-// exactly: the codes are OR-ed into the mantissa of 1024.0 at bit 2M' (M' =
-// M for the first pairs, M - Q after a shift of the word by 2Q bits), giving
-// 1024 + c*4^M' (< 2048, so exact), and one fma with (4^-M', -1024*4^-M')
-// leaves c.  2 bits: Q = 5 (M' <= 4); 3 bits: Q = 4 (M' <= 3), and the high
-// bit of each weight (word `hw`, bit M+8w and M+8w+16 for word w of the
-// block) joins at bit 2M'+2.
-template <int M, int BITS, int W>
-__device__ __forceinline__ uint32_t dq_pair(uint32_t w0, uint32_t wq, uint32_t hw)
+// (weights M and M+8, bits 2M and 2M+16) becomes the fp16x2 of the centred
+// codes (c_M - mid, c_{M+8} - mid) exactly: the codes are OR-ed into the
+// mantissa of 1024.0 at bit 2M' with M' in 1..4 (2 bits) or 1..3 (3 bits),
+// giving 1024 + c*4^M' (< 2048, so exact), and one fma with 4^-M' and
+// -(1024*4^-M' + mid) (both fp16 values) yields c - mid, also exact.  Which
+// shift of the word puts pair M at M' is in dq_src; for 3 bits the high bit
+// of each weight (word `hw`, bits M+8w and M+8w+16 for word w of the block)
+// joins at bit 2M'+2.
+template <int BITS>
+struct DqWord {
+    uint32_t w0, wl2, wr;   // the word, << 2, >> 8 (2 bits) or >> 6 (3 bits)
+    uint32_t wr12;          // >> 12 (3 bits)
+};
+
+template <int BITS>
+__device__ __forceinline__ DqWord<BITS> dq_word(uint32_t w)
 {
-    constexpr int Q = BITS == 2 ? 5 : 4;
-    constexpr int MP = M < Q ? M : M - Q;
-    const uint32_t src = M < Q ? w0 : wq;
-    uint32_t v;
-    if constexpr (BITS == 2) {
-        v = and_or(src, 0x00030003u << (2 * MP), 0x64006400u);
-    } else {
-        constexpr int SH = 8 * W + M - 2 * MP - 2;  // bring bit (8W+M) to bit 2MP+2
-        const uint32_t hb = SH >= 0 ? (hw >> (SH >= 0 ? SH : 0)) : (hw << (SH < 0 ? -SH : 0));
-        v = and_or(src, 0x00030003u << (2 * MP), 0x64006400u);
-        v = and_or(hb, 0x00010001u << (2 * MP + 2), v);
-    }
-    constexpr uint32_t kMul[5] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u, 0x1C001C00u};
-    constexpr uint32_t kAdd[5] = {0xE400E400u, 0xDC00DC00u, 0xD400D400u, 0xCC00CC00u, 0xC400C400u};
-    return hfma2_f16(v, kMul[MP], kAdd[MP]);
+    DqWord<BITS> d;
+    d.w0 = w;
+    d.wl2 = w << 2;
+    d.wr = w >> (BITS == 2 ? 8 : 6);
+    d.wr12 = BITS == 2 ? 0u : w >> 12;
+    return d;
 }
 
-// Shift of a code word that brings pairs Q.. down to bit 0 (see dq_pair).
-template <int BITS>
-__device__ __forceinline__ uint32_t dq_shift(uint32_t w) { return w >> (BITS == 2 ? 10 : 8); }
+template <int M, int BITS, int W>
+__device__ __forceinline__ uint32_t dq_pair(const DqWord<BITS> &d, uint32_t hw)
+{
+    // pair M sits at bit 2*MP of: the word (M 1..4 | 1..3), the word << 2 (M 0), the word >> 8 (M 5..7, 2 bits),
+    // >> 6 (M 4..6, 3 bits), >> 12 (M 7, 3 bits)
+    constexpr int MP = M == 0 ? 1 : (BITS == 2 ? (M <= 4 ? M : M - 4) : (M <= 3 ? M : (M <= 6 ? M - 3 : 1)));
+    const uint32_t src = M == 0 ? d.wl2
+                                : (BITS == 2 ? (M <= 4 ? d.w0 : d.wr) : (M <= 3 ? d.w0 : (M <= 6 ? d.wr : d.wr12)));
+    uint32_t v = and_or(src, 0x00030003u << (2 * MP), 0x64006400u);
+    if constexpr (BITS == 3) {
+        constexpr int SH = 8 * W + M - 2 * MP - 2;  // bring bit (8W+M) to bit 2MP+2
+        const uint32_t hb = SH >= 0 ? (hw >> (SH >= 0 ? SH : 0)) : (hw << (SH < 0 ? -SH : 0));
+        v = and_or(hb, 0x00010001u << (2 * MP + 2), v);
+    }
+    // 4^-MP and -(1024 * 4^-MP + mid) as fp16 pairs, MP = 1..4
+    constexpr uint32_t kMul[5] = {0u, 0x34003400u, 0x2C002C00u, 0x24002400u, 0x1C001C00u};
+    constexpr uint32_t kAdd2[5] = {0u, 0xDC06DC06u, 0xD418D418u, 0xCC60CC60u, 0xC580C580u};  // mid 1.5
+    constexpr uint32_t kAdd3[4] = {0u, 0xDC0EDC0Eu, 0xD438D438u, 0xCCE0CCE0u};               // mid 3.5
+    return hfma2_f16(v, kMul[MP], BITS == 2 ? kAdd2[MP] : kAdd3[MP < 4 ? MP : 1]);
+}
 
 __device__ __forceinline__ float2 h2f2(uint32_t b)
 {
@@ -533,11 +536,11 @@ __device__ __forceinline__ void gu_load_ops(GuOps<T> &O, int s, int n, const int
 // group.  MMA k-pair j (j < 4) carries block 8s+2j and k-pair j+4 block
 // 8s+2j+1, so a thread's A operand is one 16-byte read per row; accumulator
 // column c sums block 8s+c.  Writes per-row partial sums (over the
-// super-tile's 8 blocks) of sum_i (c_i - mid) u_i s_block to `pgu`
+// super-tile's 8 blocks) of s_block * sum_i (c_i - mid) u_i to `pgu`
 // [2][NST][16][T].
 template <int T, int BITS>
 __device__ __forceinline__ void gu_item(const Plan &P, const char *slot, int mtx, int s, int n, const GuOps<T> &O,
-                                        const int (&tok)[kMaxT], const float *xs, int H, float *pgu)
+                                        int H, float *pgu)
 {
     const int lane = lane_id(), gid = lane >> 2, tig = lane & 3;
     const int cbr = P.cb_gu;
@@ -560,10 +563,10 @@ __device__ __forceinline__ void gu_item(const Plan &P, const char *slot, int mtx
         for (int w = 0; w < 2; w++) acc[t][w][0] = acc[t][w][1] = acc[t][w][2] = acc[t][w][3] = 0.f;
 #define MOE_GU_STEP(Wn, Mn)                                                                               \
     {                                                                                                     \
-        const uint32_t a0 = dq_pair<Mn, BITS, Wn>(W0, W0q, H0);                                           \
-        const uint32_t a1 = dq_pair<Mn, BITS, Wn>(W1, W1q, H1);                                           \
-        const uint32_t a2 = dq_pair<Mn, BITS, Wn>(W2, W2q, H2);                                           \
-        const uint32_t a3 = dq_pair<Mn, BITS, Wn>(W3, W3q, H3);                                           \
+        const uint32_t a0 = dq_pair<Mn, BITS, Wn>(D0, H0);                                                \
+        const uint32_t a1 = dq_pair<Mn, BITS, Wn>(D1, H1);                                                \
+        const uint32_t a2 = dq_pair<Mn, BITS, Wn>(D2, H2);                                                \
+        const uint32_t a3 = dq_pair<Mn, BITS, Wn>(D3, H3);                                                \
         _Pragma("unroll") for (int t = 0; t < T; t++) if (t < n) {                                        \
             if constexpr (GuOps<T>::kPre)                                                                 \
                 mma16816(acc[t][Wn], a0, a1, a2, a3, O.A[t][8 * Wn + Mn], O.B[t][8 * Wn + Mn]);           \
@@ -573,9 +576,8 @@ __device__ __forceinline__ void gu_item(const Plan &P, const char *slot, int mtx
     }
 #define MOE_GU_WORD(Wn, X0, X1, X2, X3)                                                                   \
     {                                                                                                     \
-        const uint32_t W0 = X0, W1 = X1, W2 = X2, W3 = X3;                                                \
-        const uint32_t W0q = dq_shift<BITS>(W0), W1q = dq_shift<BITS>(W1);                                \
-        const uint32_t W2q = dq_shift<BITS>(W2), W3q = dq_shift<BITS>(W3);                                \
+        const DqWord<BITS> D0 = dq_word<BITS>(X0), D1 = dq_word<BITS>(X1);                                \
+        const DqWord<BITS> D2 = dq_word<BITS>(X2), D3 = dq_word<BITS>(X3);                                \
         const uint32_t H0 = hq0.x, H1 = hq1.x, H2 = hq0.y, H3 = hq1.y;                                    \
         MOE_GU_STEP(Wn, 0) MOE_GU_STEP(Wn, 1) MOE_GU_STEP(Wn, 2) MOE_GU_STEP(Wn, 3)                        \
         MOE_GU_STEP(Wn, 4) MOE_GU_STEP(Wn, 5) MOE_GU_STEP(Wn, 6) MOE_GU_STEP(Wn, 7)                        \
@@ -584,20 +586,18 @@ __device__ __forceinline__ void gu_item(const Plan &P, const char *slot, int mtx
     MOE_GU_WORD(1, q0.y, q1.y, q0.w, q1.w)
 #undef MOE_GU_WORD
 #undef MOE_GU_STEP
-    constexpr float mid = BITS == 2 ? 1.5f : 3.5f;
     const int bs = 8 * s + 2 * tig;
     const float2 sa = h2f2(*reinterpret_cast<const uint32_t *>(sb + (size_t)gid * P.sb_gu + bs * 2));
     const float2 sc = h2f2(*reinterpret_cast<const uint32_t *>(sb + (size_t)(gid + 8) * P.sb_gu + bs * 2));
 #pragma unroll
     for (int t = 0; t < T; t++) {
         if (t < n) {
-            const float2 xv = *reinterpret_cast<const float2 *>(xs + (size_t)tok[t] * (H / 32) + bs);
-            float c0 = acc[t][0][0] + acc[t][1][0], c1 = acc[t][0][1] + acc[t][1][1];
-            float c2 = acc[t][0][2] + acc[t][1][2], c3 = acc[t][0][3] + acc[t][1][3];
-            float p0 = sa.x * fmaf(-mid, xv.x, c0);
-            p0 = fmaf(sa.y, fmaf(-mid, xv.y, c1), p0);
-            float p1 = sc.x * fmaf(-mid, xv.x, c2);
-            p1 = fmaf(sc.y, fmaf(-mid, xv.y, c3), p1);
+            const float c0 = acc[t][0][0] + acc[t][1][0], c1 = acc[t][0][1] + acc[t][1][1];
+            const float c2 = acc[t][0][2] + acc[t][1][2], c3 = acc[t][0][3] + acc[t][1][3];
+            float p0 = sa.x * c0;
+            p0 = fmaf(sa.y, c1, p0);
+            float p1 = sc.x * c2;
+            p1 = fmaf(sc.y, c3, p1);
             p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
             p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
             p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
@@ -616,12 +616,11 @@ __device__ __forceinline__ void gu_item(const Plan &P, const char *slot, int mtx
 // scales), for the n tokens of the group.  Accumulator columns are (part,
 // block): 0..3 the fp16 high parts of h in the super-tile's four blocks, 4..7
 // the low parts, so both parts share one dequantised A operand.  h's operand
-// words and half-block sums come from `hop`, `hs16` (shared memory if
-// `staged`, else global).  Writes per-row partial sums to
-// pd[(p0 + t) * NSD2 + s2][16].
+// words come from `hop` (shared memory if `staged`, else global).  Writes
+// per-row partial sums to pd[(p0 + t) * NSD2 + s2][16].
 template <int T, int BITS>
 __device__ __forceinline__ void down_item(const Plan &P, const char *slot, int s2, int n, int p0, const uint32_t *hop,
-                                          const float *hs16, bool staged, const uint32_t *zero16, int I, float *pd)
+                                          bool staged, const uint32_t *zero16, int I, float *pd)
 {
     const int lane = lane_id(), gid = lane >> 2, tig = lane & 3;
     const uint8_t *cb = reinterpret_cast<const uint8_t *>(slot);
@@ -637,14 +636,11 @@ __device__ __forceinline__ void down_item(const Plan &P, const char *slot, int s
     const bool isA = gid == tig, isB = gid == tig + 4;
     const uint32_t mA = isA ? 0xffffffffu : 0u, mB = isB ? 0xffffffffu : 0u;
     // B operands: the high (isA lanes) or low (isB lanes) fp16 part of h over
-    // block bt as pairs (16w+m, 16w+m+8), made by the gate/up epilogue; the
-    // block sum of h from its two 16-value halves
+    // block bt as pairs (16w+m, 16w+m+8), made by the gate/up epilogue
     constexpr bool kPre = T <= 2;
     uint32_t BA[kPre ? T : 1][16], BB[kPre ? T : 1][16], BX[kPre ? 1 : T][16];
-    float hsum[T];
 #pragma unroll
     for (int t = 0; t < T; t++) {
-        hsum[t] = 0.f;
         if (t < n) {
             const size_t pb = (size_t)(p0 + t) * (I / 32) + bt;
             const uint32_t *wa = hop + pb * 32, *wb = wa + 16;
@@ -681,11 +677,6 @@ __device__ __forceinline__ void down_item(const Plan &P, const char *slot, int s
                     }
                 }
             }
-            if (isA) {
-                const float2 hh = staged ? *reinterpret_cast<const float2 *>(hs16 + 2 * pb)
-                                         : __ldcg(reinterpret_cast<const float2 *>(hs16 + 2 * pb));
-                hsum[t] = hh.x + hh.y;
-            }
         }
     }
     float acc[T][2][4];
@@ -695,8 +686,8 @@ __device__ __forceinline__ void down_item(const Plan &P, const char *slot, int s
         for (int w = 0; w < 2; w++) acc[t][w][0] = acc[t][w][1] = acc[t][w][2] = acc[t][w][3] = 0.f;
 #define MOE_D_STEP(Wn, Mn)                                                                                \
     {                                                                                                     \
-        const uint32_t a0 = dq_pair<Mn, BITS, Wn>(W0, W0q, hw0);                                          \
-        const uint32_t a1 = dq_pair<Mn, BITS, Wn>(W1, W1q, hw1);                                          \
+        const uint32_t a0 = dq_pair<Mn, BITS, Wn>(D0, hw0);                                               \
+        const uint32_t a1 = dq_pair<Mn, BITS, Wn>(D1, hw1);                                               \
         _Pragma("unroll") for (int t = 0; t < T; t++) if (t < n) {                                        \
             if constexpr (kPre)                                                                           \
                 mma16816(acc[t][Wn], a0, a1, a0, a1, BA[t][8 * Wn + Mn], BB[t][8 * Wn + Mn]);             \
@@ -706,8 +697,7 @@ __device__ __forceinline__ void down_item(const Plan &P, const char *slot, int s
     }
 #define MOE_D_WORD(Wn)                                                                                    \
     {                                                                                                     \
-        const uint32_t W0 = Wn ? q0.y : q0.x, W1 = Wn ? q1.y : q1.x;                                      \
-        const uint32_t W0q = dq_shift<BITS>(W0), W1q = dq_shift<BITS>(W1);                                \
+        const DqWord<BITS> D0 = dq_word<BITS>(Wn ? q0.y : q0.x), D1 = dq_word<BITS>(Wn ? q1.y : q1.x);      \
         MOE_D_STEP(Wn, 0) MOE_D_STEP(Wn, 1) MOE_D_STEP(Wn, 2) MOE_D_STEP(Wn, 3)                            \
         MOE_D_STEP(Wn, 4) MOE_D_STEP(Wn, 5) MOE_D_STEP(Wn, 6) MOE_D_STEP(Wn, 7)                            \
     }
@@ -715,25 +705,19 @@ __device__ __forceinline__ void down_item(const Plan &P, const char *slot, int s
     MOE_D_WORD(1)
 #undef MOE_D_WORD
 #undef MOE_D_STEP
-    constexpr float mid = BITS == 2 ? 1.5f : 3.5f;
     const int bb = 4 * s2 + 2 * (tig & 1);  // blocks of accumulator columns 2 tig, 2 tig + 1
-    const bool hi_cols = tig < 2;           // columns of the high parts carry the offset term
     const float2 sa = h2f2(*reinterpret_cast<const uint32_t *>(sb + (size_t)gid * P.sb_d + bb * 2));
     const float2 sc = h2f2(*reinterpret_cast<const uint32_t *>(sb + (size_t)(gid + 8) * P.sb_d + bb * 2));
-    const int src0 = 5 * (2 * (tig & 1)), src1 = src0 + 5;  // lanes that summed blocks bb, bb+1
     const int NSD2 = I / 128;
 #pragma unroll
     for (int t = 0; t < T; t++) {
         if (t < n) {
-            const float H0 = __shfl_sync(0xffffffffu, hsum[t], src0);
-            const float H1 = __shfl_sync(0xffffffffu, hsum[t], src1);
-            const float o0 = hi_cols ? -mid * H0 : 0.f, o1 = hi_cols ? -mid * H1 : 0.f;
             const float c0 = acc[t][0][0] + acc[t][1][0], c1 = acc[t][0][1] + acc[t][1][1];
             const float c2 = acc[t][0][2] + acc[t][1][2], c3 = acc[t][0][3] + acc[t][1][3];
-            float r0 = sa.x * (c0 + o0);
-            r0 = fmaf(sa.y, c1 + o1, r0);
-            float r1 = sc.x * (c2 + o0);
-            r1 = fmaf(sc.y, c3 + o1, r1);
+            float r0 = sa.x * c0;
+            r0 = fmaf(sa.y, c1, r0);
+            float r1 = sc.x * c2;
+            r1 = fmaf(sc.y, c3, r1);
             r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
             r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
             r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
@@ -817,8 +801,7 @@ __device__ __forceinline__ int fills_of(int s, int n, int nslot) { return s < n 
 // h = silu(g) * u for the 16 rows of unit row tile rt (n tokens, sorted pairs
 // p0..p0+n-1) from its per-super-tile partial sums, stored as the down
 // projection's operand words: fp16 high and low parts paired (16w+m,
-// 16w+m+8) in block rt/2, word half w = rt&1, and the fp32 sum of the 16
-// values.  One warp.
+// 16w+m+8) in block rt/2, word half w = rt&1.  One warp.
 template <int T>
 __device__ __forceinline__ void finalize_unit(const Args &a, const float *pslot, int n, int p0, int rt, int I, int NST)
 {
@@ -838,16 +821,12 @@ __device__ __forceinline__ void finalize_unit(const Args &a, const float *pslot,
         const uint16_t lo = f16_bits(hv - f16_val(hi));
         const uint16_t hi8 = (uint16_t)__shfl_down_sync(0xffffffffu, (unsigned)hi, 8);
         const uint16_t lo8 = (uint16_t)__shfl_down_sync(0xffffffffu, (unsigned)lo, 8);
-        float s16 = hv;
-#pragma unroll
-        for (int o = 8; o; o >>= 1) s16 += __shfl_xor_sync(0xffffffffu, s16, o);
         if (t < n) {
             const size_t pb = (size_t)(p0 + t) * (I / 32) + (rt >> 1);
             if (r < 8) {
                 __stcg(a.hop + pb * 32 + 8 * (rt & 1) + r, pack16(hi, hi8));
                 __stcg(a.hop + pb * 32 + 16 + 8 * (rt & 1) + r, pack16(lo, lo8));
             }
-            if (r == 0) __stcg(a.hsum + (size_t)(p0 + t) * (I / 16) + rt, s16);
         }
     }
 }
@@ -872,7 +851,6 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
     const int NST = H / 256, NSD2 = I / 128, tiles = I / 16, per_unit = 2 * NST;
     uint16_t *xb = reinterpret_cast<uint16_t *>(dyn + P.off_xb);  // [T][H] u (bf16)
     char *xp = dyn + P.off_xp;                                     // [T][H/32] blocks of operand pairs
-    float *xs = reinterpret_cast<float *>(dyn + P.off_xs);         // [T][H/32] block sums of u
     float *lg = reinterpret_cast<float *>(dyn + P.off_lg);         // [T][E] logits
     char *r1 = dyn + P.off_r1;                                     // router/shared rows, then unit slots
     char *r2 = dyn + P.off_r2;                                     // down slots
@@ -976,8 +954,8 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
         }
         __syncthreads();
         if (tid < kRedV) {
-            // warp w holds block 8q+w of every token for each q: u, its block
-            // sum and its MMA operand pairs (16w+m, 16w+m+8) straight from here
+            // warp w holds block 8q+w of every token for each q: u and its MMA
+            // operand pairs (16w+m, 16w+m+8) straight from here
 #pragma unroll
             for (int t = 0; t < T; t++)
 #pragma unroll
@@ -986,10 +964,8 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                         const int b = 8 * q + warp;
                         const uint16_t uv = f32_to_bf16(xr[t][q] * R.inv_rms[t]);
                         xb[(size_t)t * H + tid + 256 * q] = uv;
-                        const float sum = warp_sum(bf16_to_f32(uv));
                         const uint16_t uh = f16_bits(bf16_to_f32(uv));  // exact for |u| >= 2^-17
                         const uint16_t up = (uint16_t)__shfl_down_sync(0xffffffffu, (unsigned)uh, 8);
-                        if (lane == 0) xs[t * (H / 32) + b] = sum;
                         if ((lane & 8) == 0)
                             reinterpret_cast<uint32_t *>(xp + ((size_t)t * (H / 32) + b) * P.xp_stride)
                                 [8 * (lane >> 4) + (lane & 7)] = pack16(uh, up);
@@ -1091,8 +1067,8 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
         if (__syncthreads_or(fail)) { ok = false; break; }
         unsigned nan_mask = 0;
         for (int t = 0; t < T; t++)
-            if (topk_cta(lg + (size_t)t * E, E, k, R, t, reinterpret_cast<float *>(r1),
-                         reinterpret_cast<int *>(r1) + E))
+            if (topk_cta(lg + (size_t)t * E, E, k, R, t, reinterpret_cast<uint32_t *>(r1),
+                         reinterpret_cast<int *>(r1) + ((E + 255) / 256) * 16 * kMaxK))
                 nan_mask |= 1u << t;
         if (nan_mask && tid == 0) set_status(a.status, MOE_ERR_NONFINITE);
         if (warp < T) topk_weights(R, warp, k, (nan_mask >> warp) & 1u);
@@ -1150,7 +1126,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             float *pslot = pgu + (size_t)slot * per_unit * 16 * T;
             GuOps<T> ops;
             gu_load_ops<T>(ops, s, n, tok, xp, H, P.xp_stride, zero16);
-            gu_item<T, BITS>(P, r1 + (size_t)slot * P.unitB, mtx, s, n, ops, tok, xs, H, pslot);
+            gu_item<T, BITS>(P, r1 + (size_t)slot * P.unitB, mtx, s, n, ops, H, pslot);
             if (ring) {  // slots are reused: the last item of a unit finalises it and refills the slot
                 __syncwarp();
                 int last = 0;
@@ -1253,16 +1229,12 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             iss_s++;
         }
         const uint32_t *hop = a.hop;
-        const float *hs16 = a.hsum;
         if (P.stage_h && nrows > 0) {
             uint4 *dst = reinterpret_cast<uint4 *>(dyn + P.off_hop);
             const uint4 *src = reinterpret_cast<const uint4 *>(a.hop);
             for (int i = tid; i < T * k * I / 4; i += NT) dst[i] = __ldcg(src + i);
-            float *hsd = reinterpret_cast<float *>(dyn + P.off_hsum);
-            for (int i = tid; i < T * k * (I / 16); i += NT) hsd[i] = __ldcg(a.hsum + i);
             __syncthreads();
             hop = reinterpret_cast<const uint32_t *>(dst);
-            hs16 = hsd;
         }
         // ---- C: routed down on the tensor cores
         if (nrows > 0) {
@@ -1278,8 +1250,8 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                     fail = true;
                     break;
                 }
-                down_item<T, BITS>(P, r2 + (size_t)slot * P.downB, s2, R.g_n[g], R.g_p0[g], hop, hs16, P.stage_h != 0,
-                                   zero16, I, pd);
+                down_item<T, BITS>(P, r2 + (size_t)slot * P.downB, s2, R.g_n[g], R.g_p0[g], hop, P.stage_h != 0, zero16,
+                                   I, pd);
                 if (ng > P.nsd) {  // slots are reused: the last item of a group refills its slot
                     __syncwarp();
                     int last = 0;
@@ -1373,7 +1345,7 @@ static cudaError_t occupancy(int *blocks, int smem)
 }
 
 struct Ws {
-    size_t cnt, xll, lgll, hop, hsum, hs, zero_end, total;
+    size_t cnt, xll, lgll, hop, hs, zero_end, total;
 };
 
 static Ws ws_layout(int T, int H, int I, int E, int k, int Is)
@@ -1384,8 +1356,7 @@ static Ws ws_layout(int T, int H, int I, int E, int k, int Is)
     w.lgll = w.xll + align256((size_t)2 * T * H * 8);
     w.zero_end = w.lgll + align256((size_t)2 * T * E * 8);
     w.hop = w.zero_end;
-    w.hsum = w.hop + align256((size_t)T * k * I * 4);
-    w.hs = w.hsum + align256((size_t)T * k * (I / 16) * 4);
+    w.hs = w.hop + align256((size_t)T * k * I * 4);
     w.total = w.hs + align256((size_t)T * std::max(Is, 1) * 4);
     return w;
 }
@@ -1409,11 +1380,11 @@ static bool make_plan(Plan &P, int T, int H, int I, int E, int k, int Is, int bi
     P.sA = (Is + G - 1) / G;
     P.xp_stride = 80;
     const int np = T * k;
-    const long aBytes = std::max((long)P.rA * H * 4 + 2L * P.sA * H * 2, 8L * E);  // also the top-k candidates
+    const long aBytes = std::max((long)P.rA * H * 4 + 2L * P.sA * H * 2,
+                                 8L * ((E + 255) / 256) * 16 * kMaxK);  // also the top-k lists
     long off = 0;
     P.off_xb = (int)off;   off += al128((long)T * H * 2);
     P.off_xp = (int)off;   off += al128((long)T * (H / 32) * P.xp_stride);
-    P.off_xs = (int)off;   off += al128((long)T * (H / 32) * 4);
     P.off_lg = (int)off;   off += al128((long)T * E * 4);
     P.off_hs = (int)off;   off += al128((long)T * std::max(Is, 1) * 4);
     P.off_pd = (int)off;   off += al128((long)np * P.NSD2 * 16 * 4);
@@ -1422,7 +1393,6 @@ static bool make_plan(Plan &P, int T, int H, int I, int E, int k, int Is, int bi
     P.stage_h = stage_h;
     if (stage_h) {
         P.off_hop = (int)off;  off += al128((long)np * I * 4);
-        P.off_hsum = (int)off; off += al128((long)np * (I / 16) * 4);
     }
     const long fixed = off;
     const long pguPer = (long)2 * P.NST * 16 * T * 4;
@@ -1538,7 +1508,6 @@ extern "C" moe_status moe_decode_forward(const moe_layer_weights *layers, int n_
     a.xll = reinterpret_cast<uint64_t *>(wb + lay.xll);
     a.lgll = reinterpret_cast<uint64_t *>(wb + lay.lgll);
     a.hop = reinterpret_cast<uint32_t *>(wb + lay.hop);
-    a.hsum = reinterpret_cast<float *>(wb + lay.hsum);
     a.hs = reinterpret_cast<float *>(wb + lay.hs);
     a.ids_out = ids_out;
     a.w_out = w_out;
