@@ -45,6 +45,51 @@ moe_status launch_combine(const float *y, const float *w, const int32_t *inv, in
     return check_launch("combine");
 }
 
+// As combine_kernel for fp16 rows of y (the prefill GEMM's output): eight
+// consecutive outputs per thread, 16-byte loads of y; same slot order.
+__global__ void combine_f16_kernel(const uint16_t *__restrict__ y, const float *__restrict__ w,
+                                   const int32_t *__restrict__ inv, int T, int k, int H, void *out, int out_bf16,
+                                   int accumulate)
+{
+    const int H8 = H / 8;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)T * H8) return;
+    const int t = (int)(i / H8), o = 8 * (int)(i - (int64_t)t * H8);
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; j++) {
+        const int p = inv[t * k + j];
+        if (p < 0) continue;
+        const float wj = w[t * k + j];
+        const uint4 q = __ldg(reinterpret_cast<const uint4 *>(y + (int64_t)p * H + o));
+        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int m = 0; m < 4; m++) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&qw[m]));
+            s[2 * m] = fmaf(wj, f.x, s[2 * m]);
+            s[2 * m + 1] = fmaf(wj, f.y, s[2 * m + 1]);
+        }
+    }
+    const int64_t b = (int64_t)t * H + o;
+    if (out_bf16) {
+        uint16_t *ob = static_cast<uint16_t *>(out) + b;
+#pragma unroll
+        for (int m = 0; m < 8; m++) ob[m] = f32_to_bf16((accumulate ? bf16_to_f32(ob[m]) : 0.f) + s[m]);
+    } else {
+        float *of = static_cast<float *>(out) + b;  // the caller's buffer: no alignment beyond 4 bytes assumed
+#pragma unroll
+        for (int m = 0; m < 8; m++) of[m] = (accumulate ? of[m] : 0.f) + s[m];
+    }
+}
+
+moe_status launch_combine_f16(const uint16_t *y, const float *w, const int32_t *inv, int T, int k, int H, void *out,
+                              moe_dtype dt, int accumulate, cudaStream_t s)
+{
+    int64_t n = (int64_t)T * (H / 8);
+    combine_f16_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(y, w, inv, T, k, H, out, dt == MOE_BF16,
+                                                                     accumulate);
+    return check_launch("combine_f16");
+}
+
 template <class W, bool SWIGLU>
 static moe_status launch_gemv(const GemvArgs &a, int groups, int nvmax, cudaStream_t s)
 {

@@ -42,5 +42,8 @@ moe_status prefill_tc_forward(const moe_expert_arena &A, const uint16_t *x, int 
 
 moe_status launch_combine(const float *y, const float *w, const int32_t *inv, int T, int k, int H, void *out,
                           moe_dtype dt, int accumulate, cudaStream_t s);
+// fp16 rows of y (16-byte aligned, H a multiple of 8).
+moe_status launch_combine_f16(const uint16_t *y, const float *w, const int32_t *inv, int T, int k, int H, void *out,
+                              moe_dtype dt, int accumulate, cudaStream_t s);
 
 }  // namespace moe

@@ -4,7 +4,7 @@
 //
 //   gate/up:  D[r][p] = sum_i dq(W_e[r][i]) * x[tok(p)][i]   for 64 gate rows r
 //             and the 64 matching up rows, then h[p][r] = silu(g) * u   (fp16)
-//   down:     y[p][o] = sum_r dq(Wd_e[o][r]) * h[p][r]                  (fp32)
+//   down:     y[p][o] = sum_r dq(Wd_e[o][r]) * h[p][r]   (fp32 accumulate, stored fp16)
 //   combine:  out[t][o] = sum_j w[t][j] y[inv[t*k+j]][o]   (slot order)
 //
 // The weights are the MMA's M operand (128 rows per tile) and an expert's
@@ -34,7 +34,9 @@
 // Keeping the weights out of shared memory leaves its bandwidth to the
 // pairs' rows, which the tensor cores read there.
 // Operands are fp16: x (bf16) converts exactly, the weights (c - mid) * s
-// round once to fp16, h rounds to fp16 between the two GEMMs.  Every wait is
+// round once to fp16, h rounds to fp16 between the two GEMMs, and each pair's
+// down output y (fp32 accumulated) is stored as fp16 for the combine, which
+// halves the bytes of the layer's largest intermediate.  Every wait is
 // bounded: after about 2 s the CTA records MOE_ERR_TIMEOUT and stops.
 //
 // Inside every 16-element group of the reduction dimension the operands are
@@ -109,7 +111,7 @@ struct Args {
     const int4 *table;          // per pair tile: expert, first pair, pair count
     const int32_t *ntt;         // number of pair tiles
     uint16_t *h_out;  // gate/up: fp16 [pairs][I] (columns permuted within 16-groups)
-    float *y_out;     // down: fp32 [pairs][H]
+    uint16_t *y_out;  // down: fp16 [pairs][H]
     int32_t *status;
 };
 
@@ -484,11 +486,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                     int o0 = t.rt * 128 + q * 32;
                     if (o0 < a.rows) {
                         if (full) {
-                            float *sb = reinterpret_cast<float *>(stg);
+                            uint16_t *sb = reinterpret_cast<uint16_t *>(stg);
                             if (lane == 0) tc::bulk_wait_read<0>();
                             __syncwarp();
 #pragma unroll
-                            for (int i = 0; i < 32; i++) sb[i * 32 + lane] = __uint_as_float(r[i]);
+                            for (int i = 0; i < 32; i++)
+                                sb[i * 32 + lane] = __half_as_ushort(__float2half_rn(__uint_as_float(r[i])));
                             tc::fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
@@ -496,10 +499,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                                 tc::bulk_commit();
                             }
                         } else {
-                            float *dst = a.y_out + (int64_t)(t.p0 + tok0) * a.rows + o0 + lane;
+                            uint16_t *dst = a.y_out + (int64_t)(t.p0 + tok0) * a.rows + o0 + lane;
 #pragma unroll
                             for (int i = 0; i < 32; i++)
-                                if (i < nv) dst[(int64_t)i * a.rows] = __uint_as_float(r[i]);
+                                if (i < nv) dst[(int64_t)i * a.rows] = __half_as_ushort(__float2half_rn(__uint_as_float(r[i])));
                         }
                     }
                 }
@@ -628,8 +631,7 @@ static moe_status launch_gemm(const Args &a, const CUtensorMap &tok, const CUten
 struct PtcWs {
     int32_t *mt_prefix;
     int4 *table;
-    uint16_t *xg, *h;
-    float *y;
+    uint16_t *xg, *h, *y;
     size_t bytes;
 };
 
@@ -639,13 +641,13 @@ static PtcWs ptc_ws(const moe_expert_arena &A, int T, int k, void *base)
     size_t n = (size_t)T * k;
     size_t tb = align256((A.E + 1) * sizeof(int32_t));
     size_t tab = align256((n / ptc::BT + A.E + 1) * sizeof(int4));  // pair tiles: at most n/BT + one partial per expert
-    size_t xb = align256(n * A.H * 2), hb = align256(n * A.I * 2), yb = align256(n * A.H * 4);
+    size_t xb = align256(n * A.H * 2), hb = align256(n * A.I * 2), yb = align256(n * A.H * 2);
     char *b = static_cast<char *>(base);
     w.mt_prefix = reinterpret_cast<int32_t *>(b);
     w.table = b ? reinterpret_cast<int4 *>(b + tb) : nullptr;
     w.xg = b ? reinterpret_cast<uint16_t *>(b + tb + tab) : nullptr;
     w.h = b ? reinterpret_cast<uint16_t *>(b + tb + tab + xb) : nullptr;
-    w.y = b ? reinterpret_cast<float *>(b + tb + tab + xb + hb) : nullptr;
+    w.y = b ? reinterpret_cast<uint16_t *>(b + tb + tab + xb + hb) : nullptr;
     w.bytes = tb + tab + xb + hb + yb;
     return w;
 }
@@ -722,7 +724,7 @@ static moe_status run_tc(const moe_expert_arena &A, const uint16_t *x, int T, co
         st = make_tmap_2d(&mcode, A.d_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (int64_t)A.E * A.H, rbI, 16, 64,
                           CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st == MOE_OK)
-        st = make_tmap_2d(&mout, d.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, n, A.H, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+        st = make_tmap_2d(&mout, d.y, F16, 2, n, A.H, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
     bool sc_d = A.I % 256 == 0;
     mscale = mcode;
     if (st == MOE_OK && sc_d)
@@ -743,7 +745,7 @@ static moe_status run_tc(const moe_expert_arena &A, const uint16_t *x, int T, co
     b.y_out = d.y;
     st = launch_gemm<BITS, false>(b, mtok, mtokf, mcode, mscale, mout, grid, s);
     if (st != MOE_OK) return st;
-    return launch_combine(d.y, w, inv, T, k, A.H, out, dt, accumulate, s);
+    return launch_combine_f16(d.y, w, inv, T, k, A.H, out, dt, accumulate, s);
 }
 
 moe_status prefill_tc_forward(const moe_expert_arena &A, const uint16_t *x, int T, const float *w, int k,
