@@ -12,7 +12,7 @@
 //            (token, slot) pairs that share an expert
 //   B        routed gate/up: this CTA's share of the (group, 16-row tile)
 //            units, h = silu(dq(Wg_e) u) * dq(Wu_e) u, on the tensor cores
-//   -- h counter barrier --
+//   -- h counter barrier (also covers h_s) --
 //   C        routed down dq(Wd_e) h and shared down Wd_s h_s of this CTA's
 //            output rows, then x[t][o] += sum_j w_tj y_j[o] + S[o]
 // The pages put a router, ten of 512 experts and an always-on shared expert
@@ -74,7 +74,7 @@ struct Args {
     uint64_t *lgll;    // [2][T][E] tagged router logits
     uint32_t *hop;     // [T*k][I/32][2][16] routed h as fp16 operand pairs (high, low parts), sorted pair order
     float *hs;         // [T][Is] shared h
-    unsigned *cnt;     // [0] h counter, [1] h_s counter, [2] abort word
+    unsigned *cnt;     // [0] h (and h_s) counter, [2] abort word
     int32_t *ids_out;  // [n_layers][T][k] or NULL
     float *w_out;
     int32_t *status;
@@ -980,7 +980,8 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             break;
         }
         // items: this CTA's router rows, then its shared gate/up rows (A'),
-        // spread over the warps; A' overlaps the wait for the other CTAs' logits
+        // spread over the warps; A' overlaps the wait for the other CTAs' logits,
+        // and the h counter after phase B also covers h_s
         const int nra = rh - r0, nqa = qh - q0;
         for (int item = warp; item < nra + nqa; item += NW) {
             if (item < nra) {
@@ -1041,8 +1042,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                 }
             }
         }
-        __syncthreads();
-        if (tid == 0) red_release_add(a.cnt + 1, 1u);
+        __syncthreads();  // poll only once this CTA's own rows are done (fewer spinning requests in L2)
         // ---- routing: all logits, top-k per token, groups of pairs
         {
             // all requests first (one round trip when the logits are ready), then late ones
@@ -1180,61 +1180,25 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                 iss_a++;
             }
         }
-        // ---- shared down (while the other CTAs finish their h)
-        if (tid == 0) fail = !wait_counter(a, a.cnt + 1, (unsigned)(l + 1) * (unsigned)G);
+        // ---- every CTA's h (and h_s): the routed h's operand words staged in
+        // shared memory when they fit (else read by each down item), h_s always
+        if (tid == 0) fail = !wait_counter(a, a.cnt + 0, (unsigned)(l + 1) * (unsigned)G);
         if (__syncthreads_or(fail)) { ok = false; break; }
-        for (int i = tid; i < T * Is; i += NT) hsm[i] = __ldcg(a.hs + i);
+        const uint32_t *hop = a.hop;
+        if (P.stage_h && nrows > 0) {
+            uint4 *dst = reinterpret_cast<uint4 *>(dyn + P.off_hop);
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.hop);
+            for (int i = tid; i < T * k * I / 4; i += NT) dst[i] = __ldcg(src + i);
+            hop = reinterpret_cast<const uint32_t *>(dst);
+        }
+        if (L.swg && nrows > 0)
+            for (int i = tid; i < T * Is; i += NT) hsm[i] = __ldcg(a.hs + i);
         const bool okS = tc::mbar_wait(&R.fullS, (uint32_t)(fillsS & 1), kTimeoutNs);
         fillsS++;
         if (__syncthreads_or(!okS)) {
             if (tid == 0) raise_abort(a);
             ok = false;
             break;
-        }
-        if (L.swg) {
-            for (int rr = warp; rr < nrows; rr += NW) {
-                const uint4 *wd = reinterpret_cast<const uint4 *>(r3 + (size_t)rr * Is * 2);
-                float p[T];
-#pragma unroll
-                for (int t = 0; t < T; t++) p[t] = 0.f;
-                for (int cc = lane; cc < Is / 8; cc += 32) {
-                    const uint4 Wv = wd[cc];
-                    const uint32_t Ww[4] = {Wv.x, Wv.y, Wv.z, Wv.w};
-#pragma unroll
-                    for (int t = 0; t < T; t++) {
-                        const float4 h0 = *reinterpret_cast<const float4 *>(hsm + (size_t)t * Is + 8 * cc);
-                        const float4 h1 = *reinterpret_cast<const float4 *>(hsm + (size_t)t * Is + 8 * cc + 4);
-                        const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-#pragma unroll
-                        for (int j = 0; j < 4; j++) {
-                            p[t] = fmaf(__uint_as_float(Ww[j] << 16), hv[2 * j], p[t]);
-                            p[t] = fmaf(__uint_as_float(Ww[j] & 0xffff0000u), hv[2 * j + 1], p[t]);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int t = 0; t < T; t++) {
-                    const float s = warp_sum(p[t]);
-                    if (lane == 0) sdn[t * 16 + rr] = s;
-                }
-            }
-        }
-        // ---- every CTA's h: its operand words and half-block sums, staged in
-        // shared memory when they fit, else read by each down item
-        if (tid == 0) fail = !wait_counter(a, a.cnt + 0, (unsigned)(l + 1) * (unsigned)G);
-        if (__syncthreads_or(fail)) { ok = false; break; }
-        if (tid == 0 && l + 1 < a.n_layers) {  // the shared down rows are consumed: fetch the next layer's
-            tc::fence_proxy_async_smem();
-            issue_s(a, a.L[l + 1], r3, o0, nrows, &R.fullS);
-            iss_s++;
-        }
-        const uint32_t *hop = a.hop;
-        if (P.stage_h && nrows > 0) {
-            uint4 *dst = reinterpret_cast<uint4 *>(dyn + P.off_hop);
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.hop);
-            for (int i = tid; i < T * k * I / 4; i += NT) dst[i] = __ldcg(src + i);
-            __syncthreads();
-            hop = reinterpret_cast<const uint32_t *>(dst);
         }
         // ---- C: routed down on the tensor cores
         if (nrows > 0) {
@@ -1275,10 +1239,45 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                 }
             }
         }
+        // shared down rows: one per warp, handed out from the last warp backwards
+        // (the warps with one routed item fewer)
+        if (L.swg && !fail) {
+            for (int rr = NW - 1 - warp; rr < nrows; rr += NW) {
+                const uint4 *wd = reinterpret_cast<const uint4 *>(r3 + (size_t)rr * Is * 2);
+                float p[T];
+#pragma unroll
+                for (int t = 0; t < T; t++) p[t] = 0.f;
+                for (int cc = lane; cc < Is / 8; cc += 32) {
+                    const uint4 Wv = wd[cc];
+                    const uint32_t Ww[4] = {Wv.x, Wv.y, Wv.z, Wv.w};
+#pragma unroll
+                    for (int t = 0; t < T; t++) {
+                        const float4 h0 = *reinterpret_cast<const float4 *>(hsm + (size_t)t * Is + 8 * cc);
+                        const float4 h1 = *reinterpret_cast<const float4 *>(hsm + (size_t)t * Is + 8 * cc + 4);
+                        const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+                        for (int j = 0; j < 4; j++) {
+                            p[t] = fmaf(__uint_as_float(Ww[j] << 16), hv[2 * j], p[t]);
+                            p[t] = fmaf(__uint_as_float(Ww[j] & 0xffff0000u), hv[2 * j + 1], p[t]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < T; t++) {
+                    const float sv = warp_sum(p[t]);
+                    if (lane == 0) sdn[t * 16 + rr] = sv;
+                }
+            }
+        }
         if (__syncthreads_or(fail)) {
             if (tid == 0) raise_abort(a);
             ok = false;
             break;
+        }
+        if (tid == 0 && l + 1 < a.n_layers) {  // the shared down rows are consumed: fetch the next layer's
+            tc::fence_proxy_async_smem();
+            issue_s(a, a.L[l + 1], r3, o0, nrows, &R.fullS);
+            iss_s++;
         }
         // ---- combine in slot order, residual update, x_{l+1} out
         for (int i = tid; i < T * k * nrows; i += NT) {  // y of pair p, row rr: its super-tiles in order
