@@ -45,6 +45,8 @@ constexpr int kMaxLayers = 64;
 constexpr int kMaxT = 4;
 constexpr int kMaxK = 16;
 constexpr int kMaxPairs = kMaxT * kMaxK;
+constexpr int kMaxCand = 64;   // top-k logits ranked by one warp
+constexpr int kMaxChunks = 4;  // top-k: E <= 1024 logits over >= 256 threads
 constexpr int kMaxUnitSlots = 16;
 constexpr int kMaxDownSlots = kMaxPairs;
 constexpr int kRedV = 256;  // fixed number of partial sums in the RMS reduction
@@ -104,6 +106,10 @@ struct Routing {
     int ngroups;
     int sel_i[kMaxT][kMaxK];
     float sel_v[kMaxT][kMaxK];
+    uint32_t lmax[32];              // top-k: maximum of each 32-logit list
+    uint32_t cand_k[kMaxCand];      // top-k: logits at or above the threshold
+    int cand_i[kMaxCand];
+    int ncand;
     float inv_rms[kMaxT];
     float wred[kMaxT][8];
     int u0, nu;                     // this CTA's units [u0, u0 + nu)
@@ -261,38 +267,39 @@ __device__ __forceinline__ uint32_t order_key(float v)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Top-k of one token's logits (in shared memory) by the whole CTA, in two
-// passes of warp reductions (redux.sync): every warp pops the k best of each
-// 32-logit chunk it holds in order (max of the keys; among equal keys the
-// lowest lane, which is the lowest id), then one warp merges the sorted
-// lists (max of the list heads; among equal heads the lowest id).  Order:
-// (value desc, id asc).  `ck`, `ci` hold ceil(E/threads) x warps x k
-// entries.  Returns true for a NaN logit (the token then gets ids 0..k-1).
+// Top-k of one token's logits (in shared memory) by the whole CTA.  The
+// logits fall into 32-entry lists (one per warp and chunk of `threads`
+// logits).  The k-th largest list maximum tau is a lower bound of the k-th
+// largest logit (the k lists holding the k largest maxima hold k distinct
+// logits >= tau), so only logits >= tau can be kept.  When at most
+// kMaxCand of them remain, one warp ranks them by (value desc, id asc);
+// otherwise every warp pops the k best of each of its lists in order (max
+// of the keys; among equal keys the lowest lane, which is the lowest id) and
+// one warp merges the sorted lists (max of the heads; among equal heads the
+// lowest id).  `ck`, `ci` hold ceil(E/threads) x warps x k entries.  Needs
+// E <= 32 * 32 lists.  Returns true for a NaN logit (the token then gets ids
+// 0..k-1).
 __device__ __noinline__ bool topk_cta(const float *l, int E, int k, Routing &R, int t, uint32_t *ck, int *ci)
 {
     const int tid = threadIdx.x, nthr = blockDim.x, lane = lane_id(), warp = warp_id(), nw = nthr >> 5;
-    const int nch = (E + nthr - 1) / nthr;
+    const int nch = (E + nthr - 1) / nthr, nl = nch * nw;
     bool nan = false;
-    for (int c = 0; c < nch; c++) {
-        const int e = c * nthr + tid;
-        uint32_t key = 0;
-        if (e < E) {
-            const float v = l[e];
-            nan |= isnan(v);
-            key = order_key(v);
-        }
-        const int list = c * nw + warp;
-        for (int r = 0; r < k; r++) {
-            const uint32_t m = __reduce_max_sync(0xffffffffu, key);
-            const unsigned who = __ballot_sync(0xffffffffu, key == m && m != 0u);
-            const int w = who ? __ffs(who) - 1 : 0;
-            if (lane == w) key = 0u;
-            if (lane == 0) {
-                ck[list * k + r] = m;
-                ci[list * k + r] = who ? c * nthr + warp * 32 + w : INT32_MAX;
+    uint32_t key[kMaxChunks];
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; c++) {
+        key[c] = 0u;
+        if (c < nch) {
+            const int e = c * nthr + tid;
+            if (e < E) {
+                const float v = l[e];
+                nan |= isnan(v);
+                key[c] = order_key(v);
             }
+            const uint32_t m = __reduce_max_sync(0xffffffffu, key[c]);
+            if (lane == 0) R.lmax[c * nw + warp] = m;
         }
     }
+    if (tid == 0) R.ncand = 0;
     if (__syncthreads_or(nan)) {
         if (tid < k) {
             R.sel_i[t][tid] = tid;
@@ -301,8 +308,82 @@ __device__ __noinline__ bool topk_cta(const float *l, int E, int k, Routing &R, 
         __syncthreads();
         return true;
     }
+    // tau: the list maximum of rank k-1 under (key desc, list asc); 1 (every
+    // logit) when there are fewer than k lists
+    uint32_t tau = 1u;
+    if (nl >= k) {
+        const uint32_t mj = lane < nl ? R.lmax[lane] : 0u;
+        int rank = 0;
+        for (int i = 0; i < nl; i++) {
+            const uint32_t mi = R.lmax[i];
+            rank += (mi > mj) || (mi == mj && i < lane);
+        }
+        const unsigned at = __ballot_sync(0xffffffffu, lane < nl && rank == k - 1);
+        tau = max(__shfl_sync(0xffffffffu, mj, __ffs(at) - 1), 1u);
+    }
+    const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; c++) {
+        if (c < nch) {
+            const bool p = key[c] >= tau;
+            const unsigned b = __ballot_sync(0xffffffffu, p);
+            if (b) {
+                int base = 0;
+                if (lane == 0) base = atomicAdd(&R.ncand, __popc(b));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                const int pos = base + __popc(b & below);
+                if (p && pos < kMaxCand) {
+                    R.cand_k[pos] = key[c];
+                    R.cand_i[pos] = c * nthr + tid;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    const int N = R.ncand;
+    if (N <= kMaxCand) {
+        if (warp == 0) {
+            const bool va = lane < N, vb = lane + 32 < N;
+            const uint32_t ka = va ? R.cand_k[lane] : 0u, kb = vb ? R.cand_k[lane + 32] : 0u;
+            const int ia = va ? R.cand_i[lane] : INT32_MAX, ib = vb ? R.cand_i[lane + 32] : INT32_MAX;
+            int ra = 0, rb = 0;
+            for (int i = 0; i < N; i++) {
+                const uint32_t ki = R.cand_k[i];
+                const int ii = R.cand_i[i];
+                ra += (ki > ka) || (ki == ka && ii < ia);
+                rb += (ki > kb) || (ki == kb && ii < ib);
+            }
+            if (va && ra < k) {
+                R.sel_i[t][ra] = ia;
+                R.sel_v[t][ra] = l[ia];
+            }
+            if (vb && rb < k) {
+                R.sel_i[t][rb] = ib;
+                R.sel_v[t][rb] = l[ib];
+            }
+        }
+        __syncthreads();
+        return false;
+    }
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; c++) {
+        if (c < nch) {
+            uint32_t kc = key[c];
+            const int list = c * nw + warp;
+            for (int r = 0; r < k; r++) {
+                const uint32_t m = __reduce_max_sync(0xffffffffu, kc);
+                const unsigned who = __ballot_sync(0xffffffffu, kc == m && m != 0u);
+                const int w = who ? __ffs(who) - 1 : 0;
+                if (lane == w) kc = 0u;
+                if (lane == 0) {
+                    ck[list * k + r] = m;
+                    ci[list * k + r] = who ? c * nthr + warp * 32 + w : INT32_MAX;
+                }
+            }
+        }
+    }
+    __syncthreads();
     if (warp == 0) {
-        const int nl = nch * nw;  // <= 32 lists, one per lane
         int p = 0;
         for (int r = 0; r < k; r++) {
             const bool live = lane < nl && p < k;

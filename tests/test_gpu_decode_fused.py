@@ -125,6 +125,55 @@ def test_full_size_two_layers_sampled(moe):
         shared = synth.shared_weights(seed, l, s.H, s.Is)
         xr = xr + oracle.moe_layer(2, layer_input(xr), cids, w[l].astype(np.float64), *arena, shared=shared)
     assert rel_l2(x2 - x0, xr - x0) <= 1e-4
+    # layer 0's selection is the oracle's top-10 of its own logits, up to
+    # near-ties that fp32 summation order may flip
+    lg = oracle.router_logits(layer_input(x0), synth.router_weights(seed, 0, s.E, s.H),
+                              synth.zipf_bias(seed, 0, s.E, 1.1))
+    oids, _ = oracle.topk(lg.astype(np.float32), 10)
+    for t in range(4):
+        if set(ids[0][t]) != set(oids[t]):
+            kth = np.sort(lg[t])[::-1][9]
+            assert all(abs(lg[t][e] - kth) <= 1e-5 * max(1.0, abs(kth)) for e in set(ids[0][t]) ^ set(oids[t]))
+
+
+def tie_layer(bias, E=512, H=256, I=128, Is=128):
+    """One small-expert layer whose router weights are zero, so the logits are the bias exactly."""
+    arena, _, _, shared = host_layer(seed=60, layer=0, bits=2, H=H, I=I, E=E, Is=Is)
+    wr = np.zeros((E, H), np.float32)
+    b = np.asarray(bias, np.float32)
+    L = MoeLayer(LayerShape(H=H, I=I, E=E, k=10, Is=Is, bits=2), DEV)
+    L.load_host(arena[0], arena[1], arena[2], arena[3], arena[4], arena[5], wr, b, shared)
+    return L, (arena, wr, b, shared)
+
+
+def _ties_case(name, E=512):
+    b = np.full(E, -1.0, np.float32)
+    if name == "spread":    # 12 equal logits in 12 lists of 32: 12 survive the threshold
+        b[[3, 40, 77, 100, 150, 200, 260, 300, 333, 401, 450, 500]] = 1.0
+    elif name == "cluster":  # 9 lists led by 2.0, one list of twenty 1.0s: 29 survive
+        b[[45, 90, 130, 170, 210, 250, 290, 330, 370]] = 2.0
+        b[0:20] = 1.0
+    elif name == "all":      # every logit equal: all survive, so the list merge decides
+        b[:] = 0.5
+    elif name == "dense":    # 70 top logits in 3 lists: more than 64 survive
+        b[100:170] = 3.0 + np.arange(70, dtype=np.float32) % 3
+    return b
+
+
+@pytest.mark.parametrize("case", ["spread", "cluster", "all", "dense"])
+@pytest.mark.parametrize("T", [1, 4])
+def test_topk_ties_lower_id_first(moe, case, T):
+    """Exact ties at E=512, k=10 are broken by the lower expert id, on both the
+    threshold-filtered path and the list merge it falls back to."""
+    b = _ties_case(case)
+    L, host = tie_layer(b)
+    x0 = synth.bf16_bits_to_f32(synth.verify_window(9, T, 256))
+    x1, ids, w = run_fused([L], x0, 10)
+    oids, ow = oracle.topk(np.tile(b, (T, 1)), 10)
+    assert np.array_equal(ids[0], oids)
+    np.testing.assert_allclose(w[0], ow, rtol=2e-6, atol=1e-7)
+    want = oracle_stack(2, x0, ids, w, [host])
+    assert rel_l2(x1 - x0, want - x0) <= 2e-5
 
 
 def test_barrier_completes_and_times_out(moe):
