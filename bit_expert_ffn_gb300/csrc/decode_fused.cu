@@ -207,11 +207,15 @@ __device__ __noinline__ bool wait_word(const Args &a, const uint64_t *p, unsigne
     }
 }
 
-__device__ __forceinline__ bool wait_tagged(const Args &a, const uint64_t *p, unsigned tag, float &v)
+// Wait until the n words p[0], p[stride], ... all carry `tag` (the slow
+// path of a batched poll: the caller then reads them again).
+__device__ __noinline__ bool wait_tags(const Args &a, const uint64_t *p, int n, int stride, unsigned tag)
 {
-    uint32_t u;
-    if (!wait_word(a, p, tag, u)) return false;
-    v = __uint_as_float(u);
+#pragma unroll 1
+    for (int j = 0; j < n; j++) {
+        uint32_t v;
+        if (!wait_word(a, p + (size_t)j * stride, tag, v)) return false;
+    }
     return true;
 }
 
@@ -314,6 +318,7 @@ __device__ __noinline__ bool topk_cta(const float *l, int E, int k, Routing &R, 
     if (nl >= k) {
         const uint32_t mj = lane < nl ? R.lmax[lane] : 0u;
         int rank = 0;
+#pragma unroll 4
         for (int i = 0; i < nl; i++) {
             const uint32_t mi = R.lmax[i];
             rank += (mi > mj) || (mi == mj && i < lane);
@@ -347,6 +352,7 @@ __device__ __noinline__ bool topk_cta(const float *l, int E, int k, Routing &R, 
             const uint32_t ka = va ? R.cand_k[lane] : 0u, kb = vb ? R.cand_k[lane + 32] : 0u;
             const int ia = va ? R.cand_i[lane] : INT32_MAX, ib = vb ? R.cand_i[lane + 32] : INT32_MAX;
             int ra = 0, rb = 0;
+#pragma unroll 4
             for (int i = 0; i < N; i++) {
                 const uint32_t ki = R.cand_k[i];
                 const int ii = R.cand_i[i];
@@ -370,6 +376,7 @@ __device__ __noinline__ bool topk_cta(const float *l, int E, int k, Routing &R, 
         if (c < nch) {
             uint32_t kc = key[c];
             const int list = c * nw + warp;
+#pragma unroll 1
             for (int r = 0; r < k; r++) {
                 const uint32_t m = __reduce_max_sync(0xffffffffu, kc);
                 const unsigned who = __ballot_sync(0xffffffffu, kc == m && m != 0u);
@@ -385,6 +392,7 @@ __device__ __noinline__ bool topk_cta(const float *l, int E, int k, Routing &R, 
     __syncthreads();
     if (warp == 0) {
         int p = 0;
+#pragma unroll 1
         for (int r = 0; r < k; r++) {
             const bool live = lane < nl && p < k;
             const uint32_t hk = live ? ck[lane * k + p] : 0u;
@@ -455,6 +463,7 @@ __device__ void build_groups(Routing &R, int n)
     }
     __syncwarp();
     int seen = 0;
+#pragma unroll 1
     for (int b = 0; b < n; b += 32) {
         const int p = b + lane;
         bool start = false;
@@ -472,6 +481,7 @@ __device__ void build_groups(Routing &R, int n)
         seen += __popc(m);
     }
     __syncwarp();
+#pragma unroll 1
     for (int g = lane; g < seen; g += 32) R.g_n[g] = (g + 1 < seen ? R.g_p0[g + 1] : n) - R.g_p0[g];
     if (lane == 0) R.ngroups = seen;
     __syncwarp();
@@ -480,6 +490,7 @@ __device__ void build_groups(Routing &R, int n)
 // Token of each sorted pair (k pairs per token).
 __device__ void pair_tokens(Routing &R, int n, int k)
 {
+#pragma unroll 1
     for (int p = lane_id(); p < n; p += 32) R.tok_of[p] = R.perm[p] / k;
     __syncwarp();
 }
@@ -991,22 +1002,29 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             } else {
                 const uint64_t *src = a.xll + (size_t)(l & 1) * T * H + tid;
                 uint64_t wv[T][kQ];
+#pragma unroll 1
+                for (;;) {  // read every word; while one is late, wait for it and read them all again
 #pragma unroll
-                for (int t = 0; t < T; t++)
+                    for (int t = 0; t < T; t++)
 #pragma unroll
-                    for (int q = 0; q < kQ; q++) wv[t][q] = q < nq ? ld_relaxed_u64(src + (size_t)t * H + 256 * q) : 0;
+                        for (int q = 0; q < kQ; q++)
+                            wv[t][q] = q < nq ? ld_relaxed_u64(src + (size_t)t * H + 256 * q) : 0;
+                    const uint64_t *lp = nullptr;
 #pragma unroll
-                for (int t = 0; t < T; t++)
+                    for (int t = 0; t < T; t++)
 #pragma unroll
-                    for (int q = 0; q < kQ; q++) {
-                        xr[t][q] = 0.f;
-                        if (q < nq && !fail) {
-                            float v = __uint_as_float((unsigned)wv[t][q]);
-                            if ((unsigned)(wv[t][q] >> 32) != (unsigned)l)
-                                fail |= !wait_tagged(a, src + (size_t)t * H + 256 * q, (unsigned)l, v);
-                            xr[t][q] = v;
-                        }
+                        for (int q = 0; q < kQ; q++)
+                            if (!lp && q < nq && (unsigned)(wv[t][q] >> 32) != (unsigned)l) lp = src + (size_t)t * H + 256 * q;
+                    if (!lp) break;
+                    if (!wait_tags(a, lp, 1, 0, (unsigned)l)) {
+                        fail = true;
+                        break;
                     }
+                }
+#pragma unroll
+                for (int t = 0; t < T; t++)
+#pragma unroll
+                    for (int q = 0; q < kQ; q++) xr[t][q] = q < nq ? __uint_as_float((unsigned)wv[t][q]) : 0.f;
             }
 #pragma unroll
             for (int t = 0; t < T; t++) {
@@ -1130,19 +1148,27 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             constexpr int kL = (kMaxT * 1024 + NT - 1) / NT;
             const uint64_t *src = a.lgll + (size_t)(l & 1) * T * E;
             uint64_t wv[kL];
+#pragma unroll 1
+            for (;;) {  // read every word; while one is late, wait for it and read them all again
 #pragma unroll
-            for (int j = 0; j < kL; j++) {
-                const int i = tid + NT * j;
-                wv[j] = i < T * E ? ld_relaxed_u64(src + i) : 0;
+                for (int j = 0; j < kL; j++) {
+                    const int i = tid + NT * j;
+                    wv[j] = i < T * E ? ld_relaxed_u64(src + i) : 0;
+                }
+                const uint64_t *lp = nullptr;
+#pragma unroll
+                for (int j = 0; j < kL; j++)
+                    if (!lp && tid + NT * j < T * E && (unsigned)(wv[j] >> 32) != (unsigned)(l + 1)) lp = src + tid + NT * j;
+                if (!lp) break;
+                if (!wait_tags(a, lp, 1, 0, (unsigned)(l + 1))) {
+                    fail = true;
+                    break;
+                }
             }
 #pragma unroll
             for (int j = 0; j < kL; j++) {
                 const int i = tid + NT * j;
-                if (i < T * E && !fail) {
-                    float v = __uint_as_float((unsigned)wv[j]);
-                    if ((unsigned)(wv[j] >> 32) != (unsigned)(l + 1)) fail |= !wait_tagged(a, src + i, (unsigned)(l + 1), v);
-                    lg[i] = v;
-                }
+                if (i < T * E) lg[i] = __uint_as_float((unsigned)wv[j]);
             }
         }
         if (__syncthreads_or(fail)) { ok = false; break; }
