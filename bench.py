@@ -37,6 +37,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 LAYERS, H, E, I, K_TOP, IS = 48, 2048, 512, 768, 10, 768
+# DRAM bytes (read + write) of one 48-layer fused decode launch, median of five
+# launches of an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
+# valid for the decode source with this SHA-256 prefix; reported as null once
+# that source changes, until it is captured again.
+DECODE_TRAFFIC = (1_363_556_352, "35001529e193df76")
 EXPERT_BYTES = 1_474_560
 ROUTER_BYTES = E * H * 4
 SHARED_BYTES = 3 * H * IS * 2
@@ -476,7 +481,7 @@ def run_ours(args, world, rank, local):
                              "achieved_gbs": bytes_per_token * tok_s / world / 1e9,
                              "frac_of_measured": bytes_per_token * tok_s / world / 1e9 / peak},
             "roofline": {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                         "frac": achieved / peak, "traffic": decode_traffic(args.path, NL), "peak_kind": peak_kind,
                          "bytes_per_launch": bytes_per_token, "avg_launch_ms": call_ms},
             "clocks": clocks,
             "e2e": e2e,
@@ -485,6 +490,17 @@ def run_ours(args, world, rank, local):
         }
         line.update(extra)
         print(json.dumps(line), flush=True)
+
+
+def decode_traffic(path: str, n_layers: int):
+    """The captured DRAM bytes of the timed launch, if they belong to the current source."""
+    if path != "fused" or n_layers != LAYERS:
+        return None
+    import hashlib
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "bit_expert_ffn_gb300", "csrc", "decode_fused.cu")
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    return DECODE_TRAFFIC[0] if digest.startswith(DECODE_TRAFFIC[1]) else None
 
 
 def main():
