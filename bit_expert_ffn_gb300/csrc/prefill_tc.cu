@@ -41,8 +41,8 @@
 //
 // Inside every 16-element group of the reduction dimension the operands are
 // stored in the order 0,8,1,9,...,7,15 (both x/h and the weights, so the
-// product is unchanged): a 2-bit code word then dequantises with one shift
-// and one mask per pair of weights.
+// product is unchanged): a code word then dequantises with one LOP3 and one
+// fp16 FMA per pair of weights.
 //
 // The pages place the routed experts' FFN on the GPU and add their outputs
 // ("How Strata runs a 125-billion-parameter model on a single 12 GB to 24 GB
@@ -52,6 +52,7 @@
 
 #include "common.cuh"
 #include "dense_tc.cuh"
+#include "dequant.cuh"
 #include "prefill.cuh"
 #include "tc.cuh"
 
@@ -170,50 +171,24 @@ __device__ __forceinline__ Slot slot_of(int it, int n)
 // Stored position, inside its 16-element group, of element m.
 __host__ __device__ __forceinline__ int perm16(int m) { return m < 8 ? 2 * m : 2 * (m - 8) + 1; }
 
-template <int S>
-__device__ __forceinline__ uint32_t shx(uint32_t w)
-{
-    if constexpr (S > 0) return w << S;
-    else if constexpr (S < 0) return w >> (-S);
-    else return w;
-}
-
-// Four fp16x2 words (k pairs (m, m+8), m = M0..M0+3) of one 16-code word:
-// values (c - mid) * s.  The code lands in mantissa bits 1-2 (and bit 3 for
-// the 3-bit high plane) of 512.0, so 512 + c is exact; subtracting 512 + mid
-// is exact too and the product with s rounds once.
-template <int BITS, int M0>
-__device__ __forceinline__ void dq_chunk(uint32_t w, uint32_t hw, __half2 s2, uint32_t (&o)[4])
-{
-    const __half2 off = BITS == 2 ? __halves2half2(__ushort_as_half(0x6003), __ushort_as_half(0x6003))   // 513.5
-                                  : __halves2half2(__ushort_as_half(0x6007), __ushort_as_half(0x6007));  // 515.5
-#define MOE_DQ(J)                                                                                       \
-    {                                                                                                   \
-        constexpr int m = M0 + (J);                                                                     \
-        uint32_t b = (shx<1 - 2 * m>(w) & 0x00060006u) | 0x60006000u;                                   \
-        if (BITS == 3) b |= shx<3 - m>(hw) & 0x00080008u;                                               \
-        __half2 v = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&b), off), s2);                        \
-        o[J] = *reinterpret_cast<uint32_t *>(&v);                                                       \
-    }
-    MOE_DQ(0) MOE_DQ(1) MOE_DQ(2) MOE_DQ(3)
-#undef MOE_DQ
-}
-
 // One 16-weight group (codes w, 3-bit high bits hw already aligned to the
 // group, fp16 scale bits sc) as eight fp16x2 words: word m holds the stored
-// positions 2m and 2m+1 of the group (true elements m and m+8).
+// positions 2m and 2m+1 of the group (true elements m and m+8), the values
+// (c - mid) * s.  The centred codes come out exact (one LOP3 and one fp16 FMA
+// per word, see dq_pair); the product with s rounds once.
 template <int BITS>
 __device__ __forceinline__ void dq_group(uint32_t w, uint32_t hw, uint32_t sc, uint32_t (&v)[8])
 {
-    __half2 s2 = __half2half2(__ushort_as_half((uint16_t)sc));
-    uint32_t lo4[4], hi4[4];
-    dq_chunk<BITS, 0>(w, hw, s2, lo4);
-    dq_chunk<BITS, 4>(w, hw, s2, hi4);
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-        v[j] = lo4[j];
-        v[4 + j] = hi4[j];
+    const __half2 s2 = __half2half2(__ushort_as_half((uint16_t)sc));
+    const DqWord<BITS> d = dq_word<BITS>(w);
+#define MOE_DQ(M)                                                                                       \
+    {                                                                                                   \
+        uint32_t c = dq_pair<M, BITS, 0>(d, hw);                                                        \
+        __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&c), s2);                                      \
+        v[M] = *reinterpret_cast<uint32_t *>(&r);                                                       \
     }
+    MOE_DQ(0) MOE_DQ(1) MOE_DQ(2) MOE_DQ(3) MOE_DQ(4) MOE_DQ(5) MOE_DQ(6) MOE_DQ(7)
+#undef MOE_DQ
 }
 
 // silu with a fast division: h is rounded to fp16 right after, far coarser
