@@ -17,9 +17,9 @@
 //               ring (shared memory, several steps ahead);
 //   warp 0      TMA: the pairs' fp16 rows of each step into the pair ring
 //               (shared memory, 128-byte swizzle);
-//   warp 24     waits for free slots of both rings and hands them to the
-//               two TMA warps (an mbarrier call right after queued copies
-//               would stall the issuing thread);
+//   warps 24-25 wait for free slots of the pair and code rings and hand
+//               them to the two TMA warps (an mbarrier call right after
+//               queued copies would stall the issuing thread);
 //   warps 8-23  dequantise codes straight into the weight ring in TMEM
 //               (tcgen05.st; a warp per lane quadrant and 16-weight group);
 //   warp 1      tcgen05.mma M=128, N=32..192, K=16 with the weights read
@@ -77,10 +77,11 @@ constexpr int XCH_BYTES = 32 * 64 * 4;  // up values of one 32-pair chunk: 64 ro
 constexpr int STG_DOWN = 32 * 32 * 4, STG_H = 32 * 32 * 2;
 constexpr int OFF_XCH = 2 * STG_H;
 constexpr int EPI_BYTES = OFF_XCH + 2 * XCH_BYTES > 4 * STG_DOWN ? OFF_XCH + 2 * XCH_BYTES : 4 * STG_DOWN;
-constexpr int THREADS = 800;
+constexpr int THREADS = 832;
 constexpr int DQ_WARP0 = 8;  // warps 8..23 dequantise: four threads per weight row
 constexpr int DQ_WARPS = 16;
-constexpr int RING_WARP = 24;  // waits for free pair/code slots for the TMA issuers
+constexpr int RING_WARP = 24;  // waits for free pair slots for the pair TMA issuer
+constexpr int CODE_WARP = 25;  // waits for free code slots for the code TMA issuer
 constexpr int EPI_WARP0 = 4;
 constexpr int NC_MAX = 8;
 constexpr unsigned long long kWaitNs = 2000000000ull;
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     const int warp = warp_id(), lane = lane_id();
     if (threadIdx.x == 0) {
         for (int s = 0; s < NA; s++) {
-            tc::mbar_init(&S.afull[s], DQ_WARPS);
+            tc::mbar_init(&S.afull[s], DQ_WARPS / 4);
             tc::mbar_init(&S.aempty[s], 1);
         }
         for (int s = 0; s < NB; s++) {
@@ -233,7 +234,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         }
         for (int s = 0; s < C::NC; s++) {
             tc::mbar_init(&S.cfull[s], 1);
-            tc::mbar_init(&S.cempty[s], DQ_WARPS);
+            tc::mbar_init(&S.cempty[s], DQ_WARPS / 4);
         }
         for (int i = 0; i < 2; i++) {
             tc::mbar_init(&S.acc_full[i], 1);
@@ -258,13 +259,16 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     const int total = *a.ntt * a.rtiles;
     const int nk = a.K / BK;
 
-    if (warp == 0 || warp == 3 || warp == RING_WARP) {
-        // ---------------- TMA: warp 24 waits for free ring slots and posts the
-        // expected bytes; it hands each step over by named barriers 4 (pair
-        // rows, issued by warp 0) and 5 (codes and scales, issued by warp 3),
+    if (warp == 0 || warp == 3 || warp == RING_WARP || warp == CODE_WARP) {
+        // ---------------- TMA: warps 24 and 25 wait for free pair and code slots and
+        // post the expected bytes; they hand each step over by named barriers 4
+        // (pair rows, issued by warp 0) and 5 (codes and scales, issued by warp 3),
         // so the issuing threads make no mbarrier calls between their copies.
-        // The OR over each barrier makes every stop decision common.
-        const int role = warp == RING_WARP ? 0 : warp == 0 ? 1 : 2;  // 0 waiter, 1 pairs, 2 codes
+        // The two rings run independently, each as far ahead as its own slots
+        // allow.  The OR over each barrier makes the stop decision common to a
+        // waiter and its issuer.
+        // roles: 0 pair waiter, 1 pair issuer, 2 code issuer, 3 code waiter
+        const int role = warp == RING_WARP ? 0 : warp == 0 ? 1 : warp == 3 ? 2 : 3;
         const uint32_t cbytes = (BITS == 3 ? 2 * BM * 16 : BM * 16) + (a.scale_tma ? BM * 16 : 0);
         int it = 0;
         bool stop = false;
@@ -277,7 +281,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             int r1 = SWIGLU ? (int)(base + a.up_rows + t.rt * 64) : r0 + 64;
             for (int kb = 0; kb < nk; kb++, it++) {
                 Slot b = slot_of(it, NB), c = slot_of(it, C::NC);
-                if (role != 2) {
+                if (role <= 1) {
                     bool fail = false;
                     if (role == 0 && lane == 0) {
                         fail = S.abort || (b.reuse && !tc::mbar_wait(&S.bempty[b.s], b.par ^ 1, kWaitNs));
@@ -297,9 +301,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                         }
                     }
                 }
-                if (role != 1) {
+                if (role >= 2) {
                     bool fail = false;
-                    if (role == 0 && lane == 0) {
+                    if (role == 3 && lane == 0) {
                         fail = S.abort || (c.reuse && !tc::mbar_wait(&S.cempty[c.s], c.par ^ 1, kWaitNs));
                         if (!fail) tc::mbar_arrive_expect_tx(&S.cfull[c.s], cbytes);
                     }
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                 }
             }
         }
-        if (stop && role == 0 && lane == 0) {
+        if (stop && (role == 0 || role == 3) && lane == 0) {
             set_status(a.status, MOE_ERR_TIMEOUT);
             S.abort = 1;
         }
@@ -489,12 +493,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         if (lane == 0) tc::bulk_wait_all();
         __syncwarp();
     } else if (warp >= DQ_WARP0 && warp < DQ_WARP0 + DQ_WARPS) {
-        // ---------------- dequantisation into TMEM: warp = (lane quadrant qd, 16-weight group gq of the step)
+        // ---------------- dequantisation into TMEM: warp = (lane quadrant qd, step group jg); the
+        // four warps of group jg take every fourth step, each a whole 64-wide step of its 32 rows
+        // (one 16-byte read of the row's codes, four 16-weight groups, one store wait per step)
         const int dw = warp - DQ_WARP0;
-        const int qd = warp & 3, gq = dw >> 2, bq = gq >> 1;  // bq: 32-weight block of the step (0, 1)
-        const int r = qd * 32 + lane;                         // weight row of the tile = TMEM lane
-        const uint32_t tq = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(TM_A + gq * 8);
-        int it = 0;
+        const int qd = warp & 3, jg = dw >> 2;
+        const int r = qd * 32 + lane;  // weight row of the tile = TMEM lane
+        const uint32_t tq = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)TM_A;
+        int base = 0;  // steps of the earlier tiles
         bool aborted = false;
         int4 nxt = tile_entry(a, blockIdx.x, total);
         for (int tile = blockIdx.x; tile < total && !S.abort && !aborted; tile += gridDim.x) {
@@ -505,10 +511,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             int64_t mrow = SWIGLU && r >= 64 ? (int64_t)a.up_rows + orow : orow;
             // scales from global memory only when they cannot come by TMA
             const uint16_t *sp = a.scales + (int64_t)t.e * a.scales_expert_stride + mrow * a.scale_row;
-            for (int kb = 0; kb < nk; kb++, it++) {
+            // the steps of this tile that belong to group jg: global step index = jg (mod 4)
+            for (int kb = (jg - base) & 3; kb < nk; kb += 4) {
+                const int it = base + kb;
                 Slot c = slot_of(it, C::NC), sa = slot_of(it, NA);
-                uint32_t sc = 0;
-                if (valid && !a.scale_tma) sc = __ldg(sp + 2 * kb + bq);
+                uint32_t sc = 0;  // the step's two block scales (low half: first block)
+                if (valid && !a.scale_tma) sc = (uint32_t)__ldg(sp + 2 * kb) | ((uint32_t)__ldg(sp + 2 * kb + 1) << 16);
                 // the warp moves as one (its TMEM stores need all lanes): lane 0 waits
                 bool ok = lane == 0 ? tc::mbar_wait(&S.cfull[c.s], c.par, kWaitNs) : true;
                 if (!__shfl_sync(0xffffffffu, ok, 0)) {
@@ -517,32 +525,35 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                 }
                 // codes of this step into registers, then the code slot is free
                 const char *cs = dyn + C::OFF_C + c.s * C::C_BYTES;
-                uint32_t cw = 0, hw = 0;
+                uint4 cw = make_uint4(0u, 0u, 0u, 0u);
+                uint2 hw = make_uint2(0u, 0u);
                 if (valid) {
-                    cw = lds32(cs + C_LO + r * 16 + gq * 4);
-                    if (a.scale_tma)
-                        sc = *reinterpret_cast<const uint16_t *>(cs + C_SC + r * 16 + (2 * (kb & 3) + bq) * 2);
-                    if (BITS == 3) {
-                        hw = lds32(cs + C_HI + r * 16 + (kb & 1) * 8 + bq * 4);
-                        if (gq & 1) hw >>= 8;  // the block's second 16 weights
-                    }
+                    cw = *reinterpret_cast<const uint4 *>(cs + C_LO + r * 16);
+                    if (a.scale_tma) sc = lds32(cs + C_SC + r * 16 + (kb & 3) * 4);
+                    if (BITS == 3) hw = *reinterpret_cast<const uint2 *>(cs + C_HI + r * 16 + (kb & 1) * 8);
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&S.cempty[c.s]);
-                uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                if (valid) dq_group<BITS>(cw, hw, sc, v);
                 ok = lane == 0 && sa.reuse ? tc::mbar_wait(&S.aempty[sa.s], sa.par ^ 1, kWaitNs) : true;
                 if (!__shfl_sync(0xffffffffu, ok, 0)) {
                     aborted = true;
                     break;
                 }
                 tc::tc_fence_after();
-                tc::tmem_st_32x32b_x8(tq + (uint32_t)(sa.s * 32), v);
+                const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                for (int gq = 0; gq < 4; gq++) {  // 16-weight group gq of block gq / 2
+                    uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                    const uint32_t hb = gq < 2 ? hw.x : hw.y;
+                    if (valid) dq_group<BITS>(words[gq], (gq & 1) ? hb >> 8 : hb, gq < 2 ? sc & 0xffffu : sc >> 16, v);
+                    tc::tmem_st_32x32b_x8(tq + (uint32_t)(sa.s * 32 + gq * 8), v);
+                }
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&S.afull[sa.s]);
             }
+            base += nk;
         }
         if (aborted) {
             if (lane == 0) set_status(a.status, MOE_ERR_TIMEOUT);
