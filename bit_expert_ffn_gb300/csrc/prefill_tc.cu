@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                 if (role <= 1) {
                     bool fail = false;
                     if (role == 0 && lane == 0) {
-                        fail = S.abort || (b.reuse && !tc::mbar_wait(&S.bempty[b.s], b.par ^ 1, kWaitNs));
+                        fail = S.abort || (b.reuse && !tc::mbar_wait_sleep(&S.bempty[b.s], b.par ^ 1, kWaitNs));
                         if (!fail) tc::mbar_arrive_expect_tx(&S.bfull[b.s], t.n32 * 32 * BK * 2);
                     }
                     if (tc::named_sync_or(4, 64, fail)) {
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                 if (role >= 2) {
                     bool fail = false;
                     if (role == 3 && lane == 0) {
-                        fail = S.abort || (c.reuse && !tc::mbar_wait(&S.cempty[c.s], c.par ^ 1, kWaitNs));
+                        fail = S.abort || (c.reuse && !tc::mbar_wait_sleep(&S.cempty[c.s], c.par ^ 1, kWaitNs));
                         if (!fail) tc::mbar_arrive_expect_tx(&S.cfull[c.s], cbytes);
                     }
                     if (tc::named_sync_or(5, 64, fail)) {
@@ -360,26 +360,36 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             }
             const uint32_t idesc = tc::idesc_f16_f32(BM, 32 * t.n32);
             uint32_t d = tmem + (uint32_t)(acc * BT);
-            for (int kb = 0; kb < nk; kb++, it++) {
-                Slot sa = slot_of(it, NA), sb = slot_of(it, NB);
+            // two steps per hand-over (one named barrier for eight MMAs)
+            for (int kb = 0; kb < nk; kb += 2) {
+                const int ns = kb + 1 < nk ? 2 : 1;
                 fail = false;
-                if (!issuer && lane == 0)
-                    fail = !tc::mbar_wait(&S.afull[sa.s], sa.par, kWaitNs) || !tc::mbar_wait(&S.bfull[sb.s], sb.par, kWaitNs);
+                if (!issuer && lane == 0) {
+                    for (int j = 0; j < ns && !fail; j++) {
+                        const Slot sa = slot_of(it + j, NA), sb = slot_of(it + j, NB);
+                        fail = !tc::mbar_wait(&S.afull[sa.s], sa.par, kWaitNs) ||
+                               !tc::mbar_wait(&S.bfull[sb.s], sb.par, kWaitNs);
+                    }
+                }
                 if (tc::named_sync_or(3, 64, fail)) {
                     stop = true;
                     break;
                 }
                 if (issuer && lane == 0) {
                     tc::tc_fence_after();
-                    uint32_t abase = tmem + (uint32_t)(TM_A + sa.s * 32);
-                    uint32_t bbase = tc::smem_u32(dyn + C::OFF_B + sb.s * B_BYTES);
+                    for (int j = 0; j < ns; j++) {
+                        const Slot sa = slot_of(it + j, NA), sb = slot_of(it + j, NB);
+                        const uint32_t abase = tmem + (uint32_t)(TM_A + sa.s * 32);
+                        const uint32_t bbase = tc::smem_u32(dyn + C::OFF_B + sb.s * B_BYTES);
 #pragma unroll
-                    for (int k16 = 0; k16 < BK / 16; k16++)
-                        tc::mma_f16_ts(d, abase + k16 * 8, tc::desc_kmajor_sw128(bbase + k16 * 32), idesc,
-                                       (kb | k16) ? 1u : 0u);
-                    tc::mma_commit(&S.aempty[sa.s]);
-                    tc::mma_commit(&S.bempty[sb.s]);
+                        for (int k16 = 0; k16 < BK / 16; k16++)
+                            tc::mma_f16_ts(d, abase + k16 * 8, tc::desc_kmajor_sw128(bbase + k16 * 32), idesc,
+                                           ((kb + j) | k16) ? 1u : 0u);
+                        tc::mma_commit(&S.aempty[sa.s]);
+                        tc::mma_commit(&S.bempty[sb.s]);
+                    }
                 }
+                it += ns;
             }
             if (stop) break;
             if (issuer && lane == 0) tc::mma_commit(&S.acc_full[acc]);
@@ -534,7 +544,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&S.cempty[c.s]);
-                ok = lane == 0 && sa.reuse ? tc::mbar_wait(&S.aempty[sa.s], sa.par ^ 1, kWaitNs) : true;
+                ok = lane == 0 && sa.reuse ? tc::mbar_wait_sleep(&S.aempty[sa.s], sa.par ^ 1, kWaitNs) : true;  // usually ahead
                 if (!__shfl_sync(0xffffffffu, ok, 0)) {
                     aborted = true;
                     break;
