@@ -15,7 +15,9 @@ Prints one JSON line.  Besides the headline (one-token decode) it carries
 ``verify_4tok`` (4-token verify windows through the same 48-layer stack) and
 ``prefill_32k`` (one layer over a 32,768-token prompt: router, permutation,
 shared expert and the grouped expert GEMMs, with the tensor roofline of the
-expert call); ``--no-extra`` skips those two.  ``--impl reference`` times the
+expert call) and ``prefill_3bit_4k`` (4,096 tokens through a 48-layer stack
+of 3-bit experts, uniform and Zipf(1.4) routing reported separately, with
+both the tensor and the HBM fraction); ``--no-extra`` skips those three.  ``--impl reference`` times the
 oracle (plain scalar CPU code) on a bounded sample of the same workload
 instead.  Under torchrun
 every rank runs an independent replica (the layer does not shard across GPUs
@@ -329,6 +331,82 @@ def bench_prefill(m, dev, reps: int = 3, T: int = 32768):
                                 "note": "fp16 operands (kind::f16, the bf16 rate)"}}
 
 
+def bench_prefill3(m, dev, T: int = 4096, n_layers: int = LAYERS, reps: int = 3):
+    """3-bit prefill: T tokens through the 48-layer residual stack (RMS-normalised bf16 input to each
+    layer, fp32 residual stream), prefill path, with uniform and with Zipf(1.4) routing (the same weights,
+    only the router bias changes).  CUDA events around each full 48-layer pass."""
+    import torch
+
+    from bit_expert_ffn_gb300 import synth
+    from bit_expert_ffn_gb300.model import LayerShape, MoeLayer, StepBuffers, Workspace
+
+    s = LayerShape(bits=3)
+    layers = []
+    for l in range(n_layers):
+        L = MoeLayer(s, dev)
+        L.fill_device(seed=4, layer=l, zipf_s=0.0)
+        layers.append(L)
+    x0 = torch.from_numpy(synth.bf16_bits_to_f32(synth.activations(4, T, s.H))).to(dev)
+    x = torch.empty_like(x0)
+    xb = torch.empty(T, s.H, dtype=torch.int16, device=dev)
+    wsp = Workspace(dev)
+    bufs = StepBuffers(T, s.E, s.k, dev)
+    cgu, sgu = m.moe_packed_size(3, 2 * s.I, s.H)
+    cd, sd = m.moe_packed_size(3, s.H, s.I)
+    expert_bytes = cgu + sgu + cd + sd  # 2,064,384 for H=2048, I=768
+    fixed_bytes = s.E * s.H * 4 + 3 * s.Is * s.H * 2  # router fp32 + shared bf16, every layer
+    flop_layer = 2.0 * T * s.k * 3 * s.H * s.I
+    peak_t, kind_t = peaks_bf16()
+    peak_b, kind_b = peaks()
+
+    def one_pass():
+        for L in layers:
+            m.moe_rms_norm_bf16(x, xb, T, s.H, m.RMS_EPS)
+            L.forward(xb, T, x, wsp, bufs, accumulate=True, path=m.MOE_PATH_PREFILL)
+
+    res = {}
+    for name, zs in (("uniform", 0.0), ("zipf_1.4", 1.4)):
+        for l, L in enumerate(layers):
+            L.router_b.copy_(torch.from_numpy(synth.zipf_bias(4, l, s.E, zs)))
+        # experts touched per layer (untimed pass, layer by layer)
+        x.copy_(x0)
+        used = 0
+        for L in layers:
+            m.moe_rms_norm_bf16(x, xb, T, s.H, m.RMS_EPS)
+            L.forward(xb, T, x, wsp, bufs, accumulate=True, path=m.MOE_PATH_PREFILL)
+            used += int((torch.diff(bufs.offsets) > 0).sum().item())
+        times = []
+        for r in range(reps + 2):
+            x.copy_(x0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            one_pass()
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 2:
+                times.append(e0.elapsed_time(e1))
+        for L in layers:
+            assert m.moe_check_status(L.status) == 0, m.moe_last_error()
+        assert bool(torch.isfinite(x).all()), "3-bit prefill output is not finite"
+        ms = float(np.median(times))
+        nbytes = used * expert_bytes + n_layers * fixed_bytes
+        tfl = flop_layer * n_layers / (ms / 1000.0) / 1e12
+        gbs = nbytes / (ms / 1000.0) / 1e9
+        res[name] = {"value": T / (ms / 1000.0), "unit": "tokens/s", "ms_per_pass": ms,
+                     "experts_used_per_layer": used / n_layers,
+                     "tensor": {"achieved": tfl, "peak": peak_t, "unit": "TFLOP/s", "frac": tfl / peak_t,
+                                "peak_kind": kind_t, "flop": flop_layer * n_layers,
+                                "note": "routed expert FLOP only"},
+                     "hbm": {"achieved": gbs, "peak": peak_b, "unit": "GB/s", "frac": gbs / peak_b,
+                             "peak_kind": kind_b, "bytes": nbytes,
+                             "note": "touched experts + router + shared expert, each read once"}}
+    del layers
+    torch.cuda.empty_cache()
+    return {"workload": f"3-bit prefill: {T} tokens x {n_layers} layers (residual stack), H=2048, E=512, I=768, "
+                        "top-10, 3-bit experts (8 levels, 32-weight blocks, fp16 scales), bf16 shared expert",
+            **res}
+
+
 def run_ours(args, world, rank, local):
     import ctypes
 
@@ -458,6 +536,7 @@ def run_ours(args, world, rank, local):
         extra["verify_4tok"] = bench_verify(m, lib, layers, descs, dev, stream, steps=min(args.steps, 50), warmup=3)
     if not args.no_extra:  # the decode stack stays resident (36 GB of 288 GB)
         extra["prefill_32k"] = bench_prefill(m, dev)
+        extra["prefill_3bit_4k"] = bench_prefill3(m, dev)
 
     if rank == 0:
         cpu = None
@@ -510,8 +589,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extra", action="store_true", help="skip the verify-window and 32K-prefill measurements")
+    ap.add_argument("--no-extra", action="store_true", help="skip the verify-window and prefill measurements")
     ap.add_argument("--only-prefill", action="store_true", help="run only the 32K-prefill measurement (profiling)")
+    ap.add_argument("--only-prefill3", action="store_true",
+                    help="run only the 3-bit 4,096-token 48-layer prefill measurement (profiling)")
     ap.add_argument("--path", default="fused", choices=["fused", "modular"])
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (48 is the workload; fewer only "
                     "for profiling captures)")
@@ -519,6 +600,15 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_setup()
+    if args.only_prefill3:
+        import torch
+
+        import bit_expert_ffn_gb300 as m
+
+        torch.cuda.set_device(local)
+        m.load()
+        print(json.dumps(bench_prefill3(m, torch.device("cuda", local))), flush=True)
+        return
     if args.only_prefill:
         import torch
 

@@ -380,3 +380,23 @@ def test_full_size_layer_sampled(moe, T, path):
     tokens = list(range(T)) if T <= 4 else sorted(np.random.default_rng(0).choice(T, 6, replace=False))
     want = sampled_reference(seed, layer, 2, s.H, s.I, x, ids, w, shared, tokens)
     assert rel_l2(got[tokens], want) <= (TIGHT if path == m.MOE_PATH_DECODE else prefill_tol(s.H, s.I))
+
+
+@pytest.mark.parametrize("zipf", [0.0, 1.4])
+def test_full_size_3bit_prefill_sampled(moe, zipf):
+    """4,096 tokens, H=2048, E=512, I=768, top-10, 3-bit experts, uniform or Zipf(1.4) routing, bf16 shared
+    expert, weights drawn on the GPU: sampled tokens against the oracle."""
+    seed, layer, T = 4, 0, 4096
+    s = LayerShape(bits=3)
+    L = MoeLayer(s, DEV)
+    L.fill_device(seed, layer, zipf_s=zipf)
+    x = synth.activations(seed, T, s.H)
+    got, bufs = run_layer(L, x, T, m.MOE_PATH_PREFILL)
+    ids = bufs.ids.cpu().numpy()
+    w = bufs.w.cpu().numpy()
+    counts = np.diff(bufs.offsets.cpu().numpy())
+    assert counts.sum() == T * s.k and (counts % 32 != 0).any()  # ragged pair tiles
+    shared = synth.shared_weights(seed, layer, s.H, s.Is)
+    tokens = sorted(np.random.default_rng(1).choice(T, 6, replace=False))
+    want = sampled_reference(seed, layer, 3, s.H, s.I, x, ids, w, shared, tokens)
+    assert rel_l2(got[tokens], want) <= prefill_tol(s.H, s.I, 3)
