@@ -122,7 +122,7 @@ struct Routing {
     int abort;
     uint64_t fullU[kMaxUnitSlots];
     uint64_t fullD[kMaxDownSlots];
-    uint64_t fullA, fullS;
+    uint64_t fullA, fullS, fullH;   // router/shared rows, shared down rows, staged h
 };
 
 // ------------------------------------------------------------ memory helpers
@@ -874,7 +874,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
     extern __shared__ __align__(128) char dyn[];
     __shared__ Routing R;
     __shared__ __align__(16) uint32_t zero16[16];  // B operands of lanes that supply none
-    __shared__ int iss_u[kMaxUnitSlots], iss_d[kMaxDownSlots], iss_a, iss_s;  // fills issued per barrier
+    __shared__ int iss_u[kMaxUnitSlots], iss_d[kMaxDownSlots], iss_a, iss_s, iss_h;  // fills issued per barrier
     const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
     const int G = gridDim.x, cta = blockIdx.x;
     const int H = a.H, I = a.I, E = a.E, k = a.k, Is = a.Is;
@@ -908,14 +908,16 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
         }
         tc::mbar_init(&R.fullA, 1);
         tc::mbar_init(&R.fullS, 1);
+        tc::mbar_init(&R.fullH, 1);
         tc::fence_mbar_init();
         issue_a(a, P, a.L[0], r1, &R.fullA);
         issue_s(a, a.L[0], r3, o0, nrows, &R.fullS);
         iss_a = 1;
         iss_s = 1;
+        iss_h = 0;
     }
     __syncthreads();
-    int fillsA = 0, fillsS = 0;
+    int fillsA = 0, fillsS = 0, fillsH = 0;
     bool ok = true;
     for (int l = 0; l < a.n_layers; l++) {
         const Layer &L = a.L[l];
@@ -1226,17 +1228,22 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                 iss_a++;
             }
         }
-        // ---- every CTA's h (and h_s): the routed h's operand words staged in
-        // shared memory when they fit (else read by each down item), h_s always
-        if (tid == 0) fail = !wait_counter(a, a.cnt + 0, (unsigned)(l + 1) * (unsigned)G);
-        if (__syncthreads_or(fail)) { ok = false; break; }
-        const uint32_t *hop = a.hop;
-        if (P.stage_h && nrows > 0) {
-            uint4 *dst = reinterpret_cast<uint4 *>(dyn + P.off_hop);
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.hop);
-            for (int i = tid; i < T * k * I / 4; i += NT) dst[i] = __ldcg(src + i);
-            hop = reinterpret_cast<const uint32_t *>(dst);
+        // ---- every CTA's h (and h_s): the routed h's operand words come by one
+        // bulk copy into shared memory when they fit (else each down item reads
+        // them from global memory), in flight during the shared down rows; h_s
+        // by plain loads
+        if (tid == 0) {
+            fail = !wait_counter(a, a.cnt + 0, (unsigned)(l + 1) * (unsigned)G);
+            if (!fail && P.stage_h && nrows > 0) {
+                tc::fence_proxy_async_global();  // the other CTAs' h, acquired above, before the copy reads it
+                tc::fence_proxy_async_smem();    // the last layer's reads of the staging area before the copy writes it
+                tc::mbar_arrive_expect_tx(&R.fullH, (uint32_t)(T * k * I * 4));
+                bulk_g2s(dyn + P.off_hop, a.hop, (uint32_t)(T * k * I * 4), &R.fullH);
+                iss_h++;
+            }
         }
+        if (__syncthreads_or(fail)) { ok = false; break; }
+        const uint32_t *hop = P.stage_h ? reinterpret_cast<const uint32_t *>(dyn + P.off_hop) : a.hop;
         if (L.swg && nrows > 0)
             for (int i = tid; i < T * Is; i += NT) hsm[i] = __ldcg(a.hs + i);
         const bool okS = tc::mbar_wait(&R.fullS, (uint32_t)(fillsS & 1), kTimeoutNs);
@@ -1246,8 +1253,41 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             ok = false;
             break;
         }
+        // ---- shared down rows, one per warp, while the staged h is in flight
+        if (L.swg) {
+            for (int rr = warp; rr < nrows; rr += NW) {
+                const uint4 *wd = reinterpret_cast<const uint4 *>(r3 + (size_t)rr * Is * 2);
+                float p[T];
+#pragma unroll
+                for (int t = 0; t < T; t++) p[t] = 0.f;
+                for (int cc = lane; cc < Is / 8; cc += 32) {
+                    const uint4 Wv = wd[cc];
+                    const uint32_t Ww[4] = {Wv.x, Wv.y, Wv.z, Wv.w};
+#pragma unroll
+                    for (int t = 0; t < T; t++) {
+                        const float4 h0 = *reinterpret_cast<const float4 *>(hsm + (size_t)t * Is + 8 * cc);
+                        const float4 h1 = *reinterpret_cast<const float4 *>(hsm + (size_t)t * Is + 8 * cc + 4);
+                        const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+                        for (int j = 0; j < 4; j++) {
+                            p[t] = fmaf(__uint_as_float(Ww[j] << 16), hv[2 * j], p[t]);
+                            p[t] = fmaf(__uint_as_float(Ww[j] & 0xffff0000u), hv[2 * j + 1], p[t]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < T; t++) {
+                    const float sv = warp_sum(p[t]);
+                    if (lane == 0) sdn[t * 16 + rr] = sv;
+                }
+            }
+        }
+        if (P.stage_h && nrows > 0) {
+            if (!tc::mbar_wait(&R.fullH, (uint32_t)(fillsH & 1), kTimeoutNs)) fail = true;
+            fillsH++;
+        }
         // ---- C: routed down on the tensor cores
-        if (nrows > 0) {
+        if (nrows > 0 && !fail) {
             int g = 0, s2 = warp, slot = 0, fq = 0;
             while (s2 >= NSD2) {
                 s2 -= NSD2;
@@ -1282,36 +1322,6 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                     s2 -= NSD2;
                     g++;
                     if (++slot == P.nsd) { slot = 0; fq++; }
-                }
-            }
-        }
-        // shared down rows: one per warp, handed out from the last warp backwards
-        // (the warps with one routed item fewer)
-        if (L.swg && !fail) {
-            for (int rr = NW - 1 - warp; rr < nrows; rr += NW) {
-                const uint4 *wd = reinterpret_cast<const uint4 *>(r3 + (size_t)rr * Is * 2);
-                float p[T];
-#pragma unroll
-                for (int t = 0; t < T; t++) p[t] = 0.f;
-                for (int cc = lane; cc < Is / 8; cc += 32) {
-                    const uint4 Wv = wd[cc];
-                    const uint32_t Ww[4] = {Wv.x, Wv.y, Wv.z, Wv.w};
-#pragma unroll
-                    for (int t = 0; t < T; t++) {
-                        const float4 h0 = *reinterpret_cast<const float4 *>(hsm + (size_t)t * Is + 8 * cc);
-                        const float4 h1 = *reinterpret_cast<const float4 *>(hsm + (size_t)t * Is + 8 * cc + 4);
-                        const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-#pragma unroll
-                        for (int j = 0; j < 4; j++) {
-                            p[t] = fmaf(__uint_as_float(Ww[j] << 16), hv[2 * j], p[t]);
-                            p[t] = fmaf(__uint_as_float(Ww[j] & 0xffff0000u), hv[2 * j + 1], p[t]);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int t = 0; t < T; t++) {
-                    const float sv = warp_sum(p[t]);
-                    if (lane == 0) sdn[t * 16 + rr] = sv;
                 }
             }
         }
@@ -1357,6 +1367,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             if (iss_d[s]) tc::mbar_wait(&R.fullD[s], (uint32_t)((iss_d[s] - 1) & 1), kDrainNs);
         tc::mbar_wait(&R.fullA, (uint32_t)((iss_a - 1) & 1), kDrainNs);
         tc::mbar_wait(&R.fullS, (uint32_t)((iss_s - 1) & 1), kDrainNs);
+        if (iss_h) tc::mbar_wait(&R.fullH, (uint32_t)((iss_h - 1) & 1), kDrainNs);
     }
 }
 

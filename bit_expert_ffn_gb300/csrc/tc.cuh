@@ -83,6 +83,14 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Generic-proxy accesses to global memory ordered with later async-proxy
+// (bulk copy) accesses: data another CTA stored and this thread acquired
+// becomes visible to a copy this thread issues next.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
 {
