@@ -1339,14 +1339,28 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
         for (int i = tid; i < T * k * nrows; i += NT) {  // y of pair p, row rr: its super-tiles in order
             const int p = i / nrows, rr = i % nrows;
             float y = 0.f;
+#pragma unroll 8
             for (int s2 = 0; s2 < NSD2; s2++) y += pd[((size_t)p * NSD2 + s2) * 16 + rr];
             pd[(size_t)p * NSD2 * 16 + rr] = y;
         }
         __syncthreads();
         for (int i = tid; i < nrows * T; i += NT) {
             const int rr = i / T, t = i % T;
+            // every slot's weight and partial first (independent loads), then the sum in slot order
+            float wj[kMaxK], yj[kMaxK];
+#pragma unroll
+            for (int j = 0; j < kMaxK; j++) {
+                wj[j] = 0.f;
+                yj[j] = 0.f;
+                if (j < k) {
+                    wj[j] = R.w[t * k + j];
+                    yj[j] = pd[(size_t)R.inv[t * k + j] * NSD2 * 16 + rr];
+                }
+            }
             float sum = 0.f;
-            for (int j = 0; j < k; j++) sum = fmaf(R.w[t * k + j], pd[(size_t)R.inv[t * k + j] * NSD2 * 16 + rr], sum);
+#pragma unroll
+            for (int j = 0; j < kMaxK; j++)
+                if (j < k) sum = fmaf(wj[j], yj[j], sum);
             if (L.swg) sum += sdn[t * 16 + rr];
             const float nx = xown[t * 16 + rr] + sum;
             if (l + 1 < a.n_layers)
@@ -1354,7 +1368,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             else
                 a.x[(size_t)t * H + o0 + rr] = nx;
         }
-        if (tid == 0 && nrows > 0)
+        if (tid == NT - 1 && nrows > 0)  // (a thread that has no row to combine)
             for (int s = 0; s < P.nsd; s++) R.fills_d[s] += fills_of(s, ng, P.nsd);
         __syncthreads();
     }
