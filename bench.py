@@ -43,7 +43,7 @@ LAYERS, H, E, I, K_TOP, IS = 48, 2048, 512, 768, 10, 768
 # launches of an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid for the decode source with this SHA-256 prefix; reported as null once
 # that source changes, until it is captured again.
-DECODE_TRAFFIC = (1_363_556_352, "35001529e193df76")
+DECODE_TRAFFIC = (1_364_233_728, "e8d70efde53b08c5")
 EXPERT_BYTES = 1_474_560
 ROUTER_BYTES = E * H * 4
 SHARED_BYTES = 3 * H * IS * 2
