@@ -607,7 +607,7 @@ def main():
 
         torch.cuda.set_device(local)
         m.load()
-        print(json.dumps(bench_prefill3(m, torch.device("cuda", local))), flush=True)
+        print(json.dumps(bench_prefill3(m, torch.device("cuda", local), n_layers=args.layers)), flush=True)
         return
     if args.only_prefill:
         import torch
