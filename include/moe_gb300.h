@@ -314,7 +314,9 @@ typedef struct moe_layer_weights {
  *                      x[t] += S_l(u) + sum_j w_tj FFN_{l,ids_tj}(u)
  * (rms_eps < 0: u = bf16(x[t]), no normalisation; see moe_rms_norm_bf16)
  * with the routing of moe_router_topk (fp32 logits, ties to the lower id,
- * renormalised softmax weights) and fp32 dequantisation and accumulation.
+ * renormalised softmax weights), exact dequantisation (centred codes c - mid
+ * in fp16 on the tensor cores, the block scale applied in fp32) and fp32
+ * accumulation.
  *   layers   host array of n_layers descriptors (copied into the launch)
  *   x        [T][H] fp32, device, 16-byte aligned, in/out
  *   ids_out, w_out  [n_layers][T][k] device outputs of the routing, or both NULL
