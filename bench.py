@@ -41,9 +41,10 @@ sys.path.insert(0, ROOT)
 LAYERS, H, E, I, K_TOP, IS = 48, 2048, 512, 768, 10, 768
 # DRAM bytes (read + write) of one 48-layer fused decode launch, median of five
 # launches of an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
-# valid for the decode source with this SHA-256 prefix; reported as null once
-# that source changes, until it is captured again.
-DECODE_TRAFFIC = (1_364_233_728, "e8d70efde53b08c5")
+# valid for the decode source whose code (comments and whitespace removed) has
+# this SHA-256 prefix; reported as null once that code changes, until it is
+# captured again.
+DECODE_TRAFFIC = (1_364_233_728, "7bfaf09ef7faa009")
 EXPERT_BYTES = 1_474_560
 ROUTER_BYTES = E * H * 4
 SHARED_BYTES = 3 * H * IS * 2
@@ -575,11 +576,20 @@ def decode_traffic(path: str, n_layers: int):
     """The captured DRAM bytes of the timed launch, if they belong to the current source."""
     if path != "fused" or n_layers != LAYERS:
         return None
+    return DECODE_TRAFFIC[0] if decode_source_digest().startswith(DECODE_TRAFFIC[1]) else None
+
+
+def decode_source_digest() -> str:
+    """SHA-256 of the decode kernel's source with comments and whitespace removed (comment edits keep it)."""
     import hashlib
+    import re
+
     src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "bit_expert_ffn_gb300", "csrc", "decode_fused.cu")
-    with open(src, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()
-    return DECODE_TRAFFIC[0] if digest.startswith(DECODE_TRAFFIC[1]) else None
+    with open(src, encoding="utf-8") as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256("".join(text.split()).encode()).hexdigest()
 
 
 def main():

@@ -13,8 +13,9 @@
 //   B        routed gate/up: this CTA's share of the (group, 16-row tile)
 //            units, h = silu(dq(Wg_e) u) * dq(Wu_e) u, on the tensor cores
 //   -- h counter barrier (also covers h_s) --
-//   C        routed down dq(Wd_e) h and shared down Wd_s h_s of this CTA's
-//            output rows, then x[t][o] += sum_j w_tj y_j[o] + S[o]
+//   C        shared down Wd_s h_s (while every pair's h comes into shared
+//            memory by one bulk copy), then routed down dq(Wd_e) h of this
+//            CTA's output rows, then x[t][o] += sum_j w_tj y_j[o] + S[o]
 // The pages put a router, ten of 512 experts and an always-on shared expert
 // in each of 48 layers ("Strata Open-Source Runtime: Running a 125B-Parameter
 // Qwen3 Model on a 12GB GPU", section "The Model Itself") and sum the expert
@@ -22,9 +23,9 @@
 // Step 2); verify windows hold up to four tokens ("Strata serves a 125B MoE
 // ...", section "Six billion active parameters per token").
 //
-// Weights move by bulk asynchronous copies (TMA, one row per copy into padded
-// shared-memory slots) completing on mbarriers; the next layer's router and
-// shared-expert rows are fetched while this layer finishes.  Routed products
+// Weights move by bulk asynchronous copies (TMA; each copy one contiguous run
+// of code rows or of their scales) completing on mbarriers; the next layer's
+// router and shared-expert rows are fetched while this layer finishes.  Routed products
 // run on mma.sync fp16 tensor-core instructions: a 2-/3-bit code c is turned
 // into the exact fp16 value c - mid (one LOP3 + one HFMA2 per pair), the
 // MMA sums (c - mid)*u exactly per 32-weight block (one block per
