@@ -66,7 +66,7 @@ typedef struct CUstream_st *moe_stream_t;
 typedef enum moe_status {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1, /* a bad pointer, shape, code or scale           */
-    MOE_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement */
+    MOE_ERR_UNSUPPORTED = 2, /* a valid request this library does not implement */
     MOE_ERR_WORKSPACE = 3,   /* workspace smaller than *_workspace_size()     */
     MOE_ERR_CUDA = 4,        /* a CUDA runtime call failed                    */
     MOE_ERR_TIMEOUT = 5,     /* a device-side wait ran out of its time limit  */
