@@ -17,7 +17,9 @@ Prints one JSON line.  Besides the headline (one-token decode) it carries
 shared expert and the grouped expert GEMMs, with the tensor roofline of the
 expert call) and ``prefill_3bit_4k`` (4,096 tokens through a 48-layer stack
 of 3-bit experts, uniform and Zipf(1.4) routing reported separately, with
-both the tensor and the HBM fraction); ``--no-extra`` skips those three.  ``--impl reference`` times the
+both the tensor and the HBM fraction) and ``tiny_layer`` (the tiny
+configuration's time per layer call on each path); ``--no-extra`` skips
+those four.  ``--impl reference`` times the
 oracle (plain scalar CPU code) on a bounded sample of the same workload
 instead.  Under torchrun
 every rank runs an independent replica (the layer does not shard across GPUs
@@ -333,6 +335,37 @@ def bench_prefill(m, dev, reps: int = 3, T: int = 32768):
                                 "note": "fp16 operands (kind::f16, the bf16 rate)"}}
 
 
+def bench_tiny(m, dev, reps: int = 200):
+    """The tiny configuration (8 tokens, H=256, E=16, I=128, top-2, bf16 shared expert I=128): one layer
+    call (router, permutation, shared expert, routed experts) per path, CUDA events around `reps` calls;
+    launch latency bounds it, so only the time per call is reported."""
+    import torch
+
+    from bit_expert_ffn_gb300 import synth
+    from bit_expert_ffn_gb300.model import LayerShape, MoeLayer, StepBuffers, Workspace
+
+    T = 8
+    s = LayerShape(H=256, I=128, E=16, k=2, Is=128, bits=2)
+    L = MoeLayer(s, dev)
+    L.fill_device(seed=0, layer=0)
+    x = torch.from_numpy(synth.activations(0, T, s.H).view(np.int16)).to(dev)
+    out = torch.zeros(T, s.H, dtype=torch.float32, device=dev)
+    bufs, wsp = StepBuffers(T, s.E, s.k, dev), Workspace(dev)
+    res = {"workload": "tiny layer: 8 tokens, H=256, E=16, I=128, top-2, 2-bit, bf16 shared expert I=128"}
+    for name, path in (("decode_path_us", m.MOE_PATH_DECODE), ("prefill_path_us", m.MOE_PATH_PREFILL)):
+        for _ in range(10):
+            L.forward(x, T, out, wsp, bufs, accumulate=False, path=path)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            L.forward(x, T, out, wsp, bufs, accumulate=False, path=path)
+        e1.record()
+        torch.cuda.synchronize()
+        assert m.moe_check_status(L.status) == 0, m.moe_last_error()
+        res[name] = 1000.0 * e0.elapsed_time(e1) / reps
+    return res
+
+
 def bench_prefill3(m, dev, T: int = 4096, n_layers: int = LAYERS, reps: int = 3):
     """3-bit prefill: T tokens through the 48-layer residual stack (RMS-normalised bf16 input to each
     layer, fp32 residual stream), prefill path, with uniform and with Zipf(1.4) routing (the same weights,
@@ -539,6 +572,7 @@ def run_ours(args, world, rank, local):
     if not args.no_extra:  # the decode stack stays resident (36 GB of 288 GB)
         extra["prefill_32k"] = bench_prefill(m, dev)
         extra["prefill_3bit_4k"] = bench_prefill3(m, dev)
+        extra["tiny_layer"] = bench_tiny(m, dev)
 
     if rank == 0:
         cpu = None
