@@ -199,6 +199,69 @@ def oracle_decode_sample(n_layers: int, seed: int = 0, step: int = 0):
     return t_oracle, n_layers
 
 
+def activation_rows(seed, tokens, step=0):
+    """Rows `tokens` of synth.activations(seed, T, H, step) (bf16 bits), drawn alone."""
+    from bit_expert_ffn_gb300 import synth
+
+    key = synth.stream_key(seed, synth.TAG_X, step)
+    return np.stack([synth.f32_to_bf16_bits(synth.normal(key, H, start=int(t) * H)) for t in tokens])
+
+
+def oracle_prefill_sample(seed, layer, bits, x_bf16, zipf_s, threads):
+    """Seconds the oracle takes for the tokens x_bf16 [n][H] through one prefill layer, spread over
+    `threads` host threads (the oracle is C code called through ctypes, which releases the GIL): router
+    logits and top-10 of every token first, then the layer (shared expert and routed experts) on the
+    oracle's own routing.  The weights of the experts those tokens pick are drawn by the device generator
+    in between, untimed."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    from bit_expert_ffn_gb300 import synth
+    from bit_expert_ffn_gb300.model import draw_expert_parts
+
+    wr = synth.router_weights(seed, layer, E, H)
+    b = synth.zipf_bias(seed, layer, E, zipf_s)
+    shared = synth.shared_weights(seed, layer, H, IS)
+    n = x_bf16.shape[0]
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        t0 = time.perf_counter()
+        routed = list(pool.map(lambda t: oracle.topk(oracle.router_logits(x_bf16[t:t + 1], wr, b).astype(np.float32),
+                                                     K_TOP), range(n)))
+        t_route = time.perf_counter() - t0
+        ids = np.concatenate([r[0] for r in routed])
+        w = np.concatenate([r[1] for r in routed])
+        used = sorted(set(ids.ravel().tolist()))
+        remap = {e: i for i, e in enumerate(used)}
+        arena = draw_expert_parts(seed, layer, used, bits, H, I)
+        cids = np.vectorize(remap.get)(ids).astype(np.int32)
+        t0 = time.perf_counter()
+        list(pool.map(lambda t: oracle.moe_layer(bits, x_bf16[t:t + 1], cids[t:t + 1], w[t:t + 1], *arena,
+                                                 shared=shared), range(n)))
+        t_layer = time.perf_counter() - t0
+    return t_route + t_layer
+
+
+def prefill_cpu_baselines(n_tokens: int = 48):
+    """The oracle timed on token samples of the two prefill workloads, on every host core."""
+    import oracle
+    from bit_expert_ffn_gb300 import synth
+
+    threads = os.cpu_count() or 1
+    toks = sorted(np.random.default_rng(11).choice(32768, n_tokens, replace=False))
+    t = oracle_prefill_sample(1, 0, 2, activation_rows(1, toks), 1.1, threads)
+    c3 = {"value": n_tokens / t, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+          "sample": f"{n_tokens} of the 32,768 prompt tokens through the layer (router, top-10, shared and routed "
+                    f"experts), fp64 scalar C, {threads} host threads over the tokens"}
+    toks = sorted(np.random.default_rng(12).choice(4096, n_tokens, replace=False))
+    xin = activation_rows(4, toks)
+    xn = synth.f32_to_bf16_bits(oracle.rms_norm(synth.bf16_bits_to_f32(xin), 1e-6).astype(np.float32))
+    t = oracle_prefill_sample(4, 0, 3, xn, 0.0, threads)
+    c4 = {"value": n_tokens / (t * LAYERS), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+          "sample": f"{n_tokens} of the 4,096 tokens through layer 0 of the 3-bit stack (uniform routing), "
+                    f"extrapolated to the 48 layers (x48), fp64 scalar C, {threads} host threads over the tokens"}
+    return c3, c4
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -227,9 +290,11 @@ def run_reference(args, world, rank):
 def bench_verify(m, lib, layers, descs, dev, stream, steps: int, warmup: int):
     """4-token verify windows through the same stack (moe_decode_forward, T=4).
 
-    Bytes per step are counted from the routing the kernel reports: the union
-    of the 4 tokens' experts in every layer, plus every layer's router and
-    shared expert.
+    Bytes per step are counted from the routing the kernel reports for the
+    timed windows themselves (each timed call writes its ids into its own
+    slice of a device buffer, 1,920 ints per window): the union of the 4
+    tokens' experts in every layer, plus every layer's router and shared
+    expert.
     """
     import ctypes
 
@@ -241,17 +306,15 @@ def bench_verify(m, lib, layers, descs, dev, stream, steps: int, warmup: int):
     nb = m.moe_decode_workspace_size(T, H, I, E, K_TOP, IS)
     ws = torch.empty(nb, dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    ids = torch.empty(NL, T, K_TOP, dtype=torch.int32, device=dev)
-    wts = torch.empty(NL, T, K_TOP, dtype=torch.float32, device=dev)
     n_steps = warmup + steps
+    ids = torch.empty(n_steps, NL, T, K_TOP, dtype=torch.int32, device=dev)
+    wts = torch.empty(n_steps, NL, T, K_TOP, dtype=torch.float32, device=dev)
     X = torch.stack([torch.from_numpy(synth.bf16_bits_to_f32(synth.verify_window(100 + i, T, H))) for i in range(n_steps)]).to(dev)
     x = torch.zeros(T, H, dtype=torch.float32, device=dev)
     sptr = ctypes.c_void_p(stream.cuda_stream)
-    unions = []
 
-    def call(with_ids):
-        r = lib.moe_decode_forward(descs, NL, x.data_ptr(), T, K_TOP, m.RMS_EPS,
-                                   ids.data_ptr() if with_ids else None, wts.data_ptr() if with_ids else None,
+    def call(i):
+        r = lib.moe_decode_forward(descs, NL, x.data_ptr(), T, K_TOP, m.RMS_EPS, ids[i].data_ptr(), wts[i].data_ptr(),
                                    ws.data_ptr(), nb, st.data_ptr(), sptr)
         if r:
             raise m.MoeError(r, m.moe_last_error())
@@ -259,20 +322,19 @@ def bench_verify(m, lib, layers, descs, dev, stream, steps: int, warmup: int):
     with torch.cuda.stream(stream):
         for i in range(warmup):
             x.copy_(X[i])
-            call(True)
-            stream.synchronize()
-            unions.append(sum(len(set(ids[l].flatten().tolist())) for l in range(NL)))
+            call(i)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for i in range(warmup, n_steps):
             x.copy_(X[i])
-            call(False)
+            call(i)
         e1.record(stream)
     torch.cuda.synchronize()
     assert m.moe_check_status(st) == 0, m.moe_last_error()
     ms = e0.elapsed_time(e1) / steps
-    u = float(np.mean(unions))
+    timed = ids[warmup:].cpu().numpy()
+    u = float(np.mean([sum(len(set(timed[i, l].ravel().tolist())) for l in range(NL)) for i in range(steps)]))
     bytes_step = u * EXPERT_BYTES + NL * (ROUTER_BYTES + SHARED_BYTES)
     return {"workload": f"verify window: 4 tokens x {NL} layers, same stack (c + N(0, 0.3^2) per token)",
             "value": T / (ms / 1000.0), "unit": "tokens/s", "ms_per_step": ms,
@@ -581,6 +643,10 @@ def run_ours(args, world, rank, local):
             cpu = {"value": n_l / LAYERS / t_or, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                    "sample": "one token through 2 of the 48 layers, oracle compute only, scaled by 1/24 "
                              "(fp64 scalar C, one host core)"}
+            if "prefill_32k" in extra and "prefill_3bit_4k" in extra:
+                c3, c4 = prefill_cpu_baselines()
+                extra["prefill_32k"]["cpu_baseline"] = c3
+                extra["prefill_3bit_4k"]["cpu_baseline"] = c4
         kernel = (f"decode_kernel (moe_decode_forward: {NL} layers, one cooperative launch)" if args.path == "fused"
                   else f"whole modular step (CUDA graph of {kernels_per_step} launches)")
         line = {

@@ -21,6 +21,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "moe_gb300.h")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_NONFINITE, MOE_ERR_BOUNDS = 4, 5, 6, 7
+MOE_ERR_RANGE = 8
 MOE_F32, MOE_BF16 = 0, 1
 MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL = 0, 1, 2
 RMS_EPS = 1e-6  # normalisation in front of each stacked layer

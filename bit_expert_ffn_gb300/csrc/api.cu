@@ -85,6 +85,7 @@ const char *moe_status_name(moe_status s)
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
     case MOE_ERR_NONFINITE: return "MOE_ERR_NONFINITE";
     case MOE_ERR_BOUNDS: return "MOE_ERR_BOUNDS";
+    case MOE_ERR_RANGE: return "MOE_ERR_RANGE";
     }
     return "MOE_ERR_UNKNOWN";
 }
@@ -100,7 +101,7 @@ moe_status moe_check_status(int32_t *dev_status, int reset, moe_stream_t stream)
         MOE_CUDA_TRY(cudaStreamSynchronize(to_cuda(stream)));
     }
     if (v == 0) return MOE_OK;
-    moe_status s = (v >= 1 && v <= 7) ? (moe_status)v : MOE_ERR_CUDA;
+    moe_status s = (v >= 1 && v <= 8) ? (moe_status)v : MOE_ERR_CUDA;
     return fail(s, "a kernel reported %s through the device status word", moe_status_name(s));
 }
 

@@ -849,6 +849,7 @@ __device__ __forceinline__ void finalize_unit(const Args &a, const float *pslot,
             }
             hv = silu(gs) * us;
         }
+        if (t < n && !(fabsf(hv) < 65520.f)) set_status(a.status, MOE_ERR_RANGE);  // no finite fp16 part
         const uint16_t hi = f16_bits(hv);
         const uint16_t lo = f16_bits(hv - f16_val(hi));
         const uint16_t hi8 = (uint16_t)__shfl_down_sync(0xffffffffu, (unsigned)hi, 8);
@@ -1005,7 +1006,9 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                         const int b = 8 * q + warp;
                         const uint16_t uv = f32_to_bf16(xr[t][q] * R.inv_rms[t]);
                         xb[(size_t)t * H + tid + 256 * q] = uv;
-                        const uint16_t uh = f16_bits(bf16_to_f32(uv));  // exact for |u| >= 2^-17
+                        const float uf = bf16_to_f32(uv);
+                        if (!(fabsf(uf) < 65520.f)) set_status(a.status, MOE_ERR_RANGE);  // no finite fp16
+                        const uint16_t uh = f16_bits(uf);  // exact for 2^-17 <= |u| < 65520
                         const uint16_t up = (uint16_t)__shfl_down_sync(0xffffffffu, (unsigned)uh, 8);
                         if ((lane & 8) == 0)
                             reinterpret_cast<uint32_t *>(xp + ((size_t)t * (H / 32) + b) * P.xp_stride)

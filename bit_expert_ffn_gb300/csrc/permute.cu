@@ -214,6 +214,8 @@ extern "C" moe_status moe_permute(const int32_t *ids, int T, int k, int E, int32
 // moe_permute_noalloc: the three-pass sort above with its scratch in a fixed
 // device array of this library instead of a caller workspace.
 // --------------------------------------------------------------------------
+#include <cuda.h>
+
 #include <mutex>
 
 namespace moe {
@@ -222,23 +224,47 @@ namespace moe {
 constexpr int64_t kNoAllocScratchInts = 32768;  // chunks * E <= 32768 -> 2 x 128 KiB
 static __device__ __align__(256) int32_t g_permute_scratch[2 * kNoAllocScratchInts];
 
-// Device address of g_permute_scratch on the current device, looked up once
-// per device (with that device current) and cached.
+// The current CUDA context through the driver's cuCtxGetCurrent, found by
+// the runtime's entry-point query (no link against the driver library).
+static CUcontext current_context()
+{
+    using Fn = CUresult (*)(CUcontext *);
+    static Fn fn = []() -> Fn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<Fn>(p);
+    }();
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
+// Device address of g_permute_scratch on the current device, looked up with
+// that device current and cached together with the context it belongs to: a
+// new context on the device (after cudaDeviceReset, say, which unloads the
+// library's device code) finds the cached context changed and looks the
+// address up again.
 static moe_status permute_scratch_address(int32_t **out)
 {
     static std::mutex mu;
     static int32_t *addr[64] = {nullptr};
+    static CUcontext ctx[64] = {nullptr};
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return fail(MOE_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    const CUcontext cur = current_context();  // NULL before the runtime has made one current
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    if (!addr[dev] || !cur || cur != ctx[dev]) {
         void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);
+        cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);  // makes the primary context current
         if (e != cudaSuccess)
             return fail(MOE_ERR_CUDA, "cudaGetSymbolAddress(g_permute_scratch) on device %d: %s", dev,
                         cudaGetErrorString(e));
         addr[dev] = static_cast<int32_t *>(p);
+        ctx[dev] = current_context();
     }
     *out = addr[dev];
     return MOE_OK;

@@ -33,11 +33,16 @@
 //               hands the up rows' values to the gate rows' warps).
 // Keeping the weights out of shared memory leaves its bandwidth to the
 // pairs' rows, which the tensor cores read there.
-// Operands are fp16: x (bf16) converts exactly, the weights (c - mid) * s
-// round once to fp16, h rounds to fp16 between the two GEMMs, and each pair's
-// down output y (fp32 accumulated) is stored as fp16 for the combine, which
-// halves the bytes of the layer's largest intermediate.  Every wait is
-// bounded: after about 2 s the CTA records MOE_ERR_TIMEOUT and stops.
+// Operands are fp16: x (bf16) converts exactly while 2^-14 <= |x| <= 65504
+// (smaller values keep fewer bits, down to 2^-24, and bf16 values of 65536 or
+// more have no finite fp16), the weights (c - mid) * s round once to fp16, h
+// rounds to fp16 between the two GEMMs, and each pair's down output y (fp32
+// accumulated) is stored as fp16 for the combine, which halves the bytes of
+// the layer's largest intermediate.  A value that leaves fp16's finite range
+// on the way (|x|, |(c - mid) s|, |h| or |y| rounding to 65520 or more, or a
+// non-finite one) sets MOE_ERR_RANGE; the kernels still write every output
+// (such entries become infinite).  Every wait is bounded: after about 2 s the
+// CTA records MOE_ERR_TIMEOUT and stops.
 //
 // Inside every 16-element group of the reduction dimension the operands are
 // stored in the order 0,8,1,9,...,7,15 (both x/h and the weights, so the
@@ -85,6 +90,8 @@ constexpr int CODE_WARP = 25;  // waits for free code slots for the code TMA iss
 constexpr int EPI_WARP0 = 4;
 constexpr int NC_MAX = 8;
 constexpr unsigned long long kWaitNs = 2000000000ull;
+// fp32 values of this magnitude or more (and NaN) round to a non-finite fp16
+constexpr float kF16Limit = 65520.f;
 
 // Shared-memory plan per bit width: the code entry carries the 3-bit high
 // planes only for 3 bits, which leaves room for fewer entries.
@@ -408,6 +415,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         const int q = warp - EPI_WARP0;  // TMEM lane quadrant: weight rows 32q .. 32q+31 of the tile
         float *xch = reinterpret_cast<float *>(dyn + C::OFF_E + OFF_XCH);
         char *stg = dyn + C::OFF_E + q * (SWIGLU ? STG_H : STG_DOWN);  // this warp's staging block
+        bool out_of_range = false;  // an h or y value that has no finite fp16
         int j = 0;
         // the gate/up warps meet at named barriers, so they decide together
         // whether to stop (the OR over the four warps); the down warps alone
@@ -450,7 +458,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
 #pragma unroll
                         for (int i = 0; i < 32; i++) {
                             float g = __uint_as_float(r[i]);
-                            hv[i] = __half_as_ushort(__float2half_rn(silu_fast(g) * xb[i * 64 + q * 32 + lane]));
+                            const float hf = silu_fast(g) * xb[i * 64 + q * 32 + lane];
+                            out_of_range |= i < nv && !(fabsf(hf) < kF16Limit);
+                            hv[i] = __half_as_ushort(__float2half_rn(hf));
                         }
                         if (full) {
                             uint16_t *sb = reinterpret_cast<uint16_t *>(stg);
@@ -474,6 +484,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                 } else {
                     int o0 = t.rt * 128 + q * 32;
                     if (o0 < a.rows) {
+#pragma unroll
+                        for (int i = 0; i < 32; i++)
+                            out_of_range |= i < nv && !(fabsf(__uint_as_float(r[i])) < kF16Limit);
                         if (full) {
                             uint16_t *sb = reinterpret_cast<uint16_t *>(stg);
                             if (lane == 0) tc::bulk_wait_read<0>();
@@ -501,6 +514,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             if (lane == 0) tc::mbar_arrive(&S.acc_empty[acc]);
         }
         if (lane == 0) tc::bulk_wait_all();
+        if (__any_sync(0xffffffffu, out_of_range) && lane == 0) set_status(a.status, MOE_ERR_RANGE);
         __syncwarp();
     } else if (warp >= DQ_WARP0 && warp < DQ_WARP0 + DQ_WARPS) {
         // ---------------- dequantisation into TMEM: warp = (lane quadrant qd, step group jg); the
@@ -511,7 +525,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         const int r = qd * 32 + lane;  // weight row of the tile = TMEM lane
         const uint32_t tq = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)TM_A;
         int base = 0;  // steps of the earlier tiles
-        bool aborted = false;
+        bool aborted = false, scale_out_of_range = false;
         int4 nxt = tile_entry(a, blockIdx.x, total);
         for (int tile = blockIdx.x; tile < total && !S.abort && !aborted; tile += gridDim.x) {
             Tile t = make_tile(a, nxt, tile);
@@ -542,6 +556,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                     if (a.scale_tma) sc = lds32(cs + C_SC + r * 16 + (kb & 3) * 4);
                     if (BITS == 3) hw = *reinterpret_cast<const uint2 *>(cs + C_HI + r * 16 + (kb & 1) * 8);
                 }
+                // (c - mid) s leaves fp16's range when |s| max|c - mid| rounds past 65504
+                if (valid) {
+                    const float2 sf = __half22float2(*reinterpret_cast<const __half2 *>(&sc));
+                    constexpr float kMaxCode = BITS == 2 ? 1.5f : 3.5f;
+                    scale_out_of_range |= !(fabsf(sf.x) * kMaxCode < kF16Limit) || !(fabsf(sf.y) * kMaxCode < kF16Limit);
+                }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&S.cempty[c.s]);
                 ok = lane == 0 && sa.reuse ? tc::mbar_wait_sleep(&S.aempty[sa.s], sa.par ^ 1, kWaitNs) : true;  // usually ahead
@@ -569,6 +589,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             if (lane == 0) set_status(a.status, MOE_ERR_TIMEOUT);
             S.abort = 1;
         }
+        if (__any_sync(0xffffffffu, scale_out_of_range) && lane == 0) set_status(a.status, MOE_ERR_RANGE);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -578,10 +599,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     }
 }
 
-// x_g[p][16g + perm16(m)] = fp16(x[tok(p)][16g + m]) for the valid pairs.
+// x_g[p][16g + perm16(m)] = fp16(x[tok(p)][16g + m]) for the valid pairs; an
+// x without a finite fp16 sets MOE_ERR_RANGE.
 __global__ void gather_x_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm,
-                                const int32_t *__restrict__ offsets, int E, int k, int H, uint16_t *__restrict__ xg)
+                                const int32_t *__restrict__ offsets, int E, int k, int H, uint16_t *__restrict__ xg,
+                                int32_t *__restrict__ status)
 {
+    bool out_of_range = false;
     int n = offsets[E];
     int groups = H / 16;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)n * groups;
@@ -599,6 +623,8 @@ __global__ void gather_x_kernel(const uint16_t *__restrict__ x, const int32_t *_
         }
         uint32_t o[8];
 #pragma unroll
+        for (int mm = 0; mm < 16; mm++) out_of_range |= !(fabsf(f[mm]) < kF16Limit);
+#pragma unroll
         for (int mm = 0; mm < 8; mm++) {
             __half2 hv = __floats2half2_rn(f[mm], f[mm + 8]);
             o[mm] = *reinterpret_cast<uint32_t *>(&hv);
@@ -607,6 +633,7 @@ __global__ void gather_x_kernel(const uint16_t *__restrict__ x, const int32_t *_
         dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
         dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
+    if (out_of_range) set_status(status, MOE_ERR_RANGE);
 }
 
 template <int BITS, bool SWIGLU>
@@ -675,7 +702,7 @@ static moe_status run_tc(const moe_expert_arena &A, const uint16_t *x, int T, co
     if (st != MOE_OK) return st;
     int64_t gthreads = n * (A.H / 16);
     int gblocks = (int)std::min<int64_t>((gthreads + 255) / 256, (int64_t)sm_count() * 16);
-    gather_x_kernel<<<gblocks, 256, 0, s>>>(x, perm, offsets, A.E, k, A.H, d.xg);
+    gather_x_kernel<<<gblocks, 256, 0, s>>>(x, perm, offsets, A.E, k, A.H, d.xg, status);
     st = check_launch("gather_x");
     if (st != MOE_OK) return st;
     int rbH = BITS == 2 ? A.H / 4 : A.H / 4 + A.H / 8;

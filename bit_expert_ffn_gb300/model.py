@@ -43,6 +43,30 @@ def device_normal(key: int, n: int, sigma: float, kind: int, out: torch.Tensor, 
         raise RuntimeError(f"moe_synth_normal failed ({r})")
 
 
+def draw_expert_parts(seed, layer, experts, bits, H, I, dev="cuda"):
+    """Logical codes and fp16 scales of the given experts from the seeded
+    generator's device implementation (the streams of synth.expert_codes and
+    synth.expert_scales, to which it is tested equal), copied to the host.
+    Returns six numpy arrays [n][...]: gate codes, gate scales, up codes, up
+    scales, down codes, down scales (the order oracle.moe_layer takes)."""
+    n = len(experts)
+    gu = torch.empty(n, 2 * I * H, dtype=torch.uint8, device=dev)
+    d = torch.empty(n, H * I, dtype=torch.uint8, device=dev)
+    gus = torch.empty(n, 2 * I * (H // 32), dtype=torch.int16, device=dev)
+    ds = torch.empty(n, H * (I // 32), dtype=torch.int16, device=dev)
+    for j, e in enumerate(experts):
+        e = int(e)
+        device_codes(synth.stream_key(seed, synth.TAG_GU_CODES, layer, e), 2 * I * H, bits, gu[j])
+        device_codes(synth.stream_key(seed, synth.TAG_D_CODES, layer, e), H * I, bits, d[j])
+        device_normal(synth.stream_key(seed, synth.TAG_GU_SCALES, layer, e), 2 * I * (H // 32), 0.02, 2, gus[j])
+        device_normal(synth.stream_key(seed, synth.TAG_D_SCALES, layer, e), H * (I // 32), 0.02, 2, ds[j])
+    gu = gu.cpu().numpy().reshape(n, 2, I, H)
+    gus = gus.cpu().numpy().view(np.uint16).reshape(n, 2, I, H // 32)
+    d = d.cpu().numpy().reshape(n, H, I)
+    ds = ds.cpu().numpy().view(np.uint16).reshape(n, H, I // 32)
+    return [np.ascontiguousarray(a) for a in (gu[:, 0], gus[:, 0], gu[:, 1], gus[:, 1], d, ds)]
+
+
 @dataclass
 class LayerShape:
     H: int = 2048

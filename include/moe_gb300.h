@@ -31,7 +31,8 @@
  *    the host before anything is launched and leave all buffers untouched.
  *    A non-OK return also sets a thread-local message, moe_last_error(),
  *    that names the argument and, for sizes, the bytes or MiB involved.
- *  - Device-detected errors (bad ids, NaN logits, codes that do not fit) are
+ *  - Device-detected errors (bad ids, NaN logits, codes that do not fit,
+ *    values outside the range of an fp16 tensor-core operand) are
  *    written into a caller-provided int32 status word in device memory
  *    (dev_status; the first error wins, 0 means OK; it may be NULL, in which
  *    case such errors are not reported).  Read it with moe_check_status().
@@ -43,7 +44,9 @@
  *    moe_check_status(), which synchronises the stream it is given.  Scratch
  *    memory comes from a caller-provided workspace whose size the matching
  *    *_workspace_size() call returns; a smaller workspace returns
- *    MOE_ERR_WORKSPACE with the bytes needed in the message.
+ *    MOE_ERR_WORKSPACE with the bytes needed in the message.  One call is the
+ *    exception: moe_permute_noalloc keeps its scratch in a fixed array inside
+ *    the library (its own comment states the size, limit and sharing).
  *  - Asynchrony.  Work is enqueued on `stream` and returns at once.
  *  - Shapes.  H and I are multiples of 32; 1 <= E <= 1024;
  *    1 <= k <= min(E, 16); T >= 0 (T = 0 is a no-op that returns MOE_OK).
@@ -71,7 +74,10 @@ typedef enum moe_status {
     MOE_ERR_CUDA = 4,        /* a CUDA runtime call failed                    */
     MOE_ERR_TIMEOUT = 5,     /* a device-side wait ran out of its time limit  */
     MOE_ERR_NONFINITE = 6,   /* a NaN router logit                            */
-    MOE_ERR_BOUNDS = 7       /* an expert id outside [0, E)                   */
+    MOE_ERR_BOUNDS = 7,      /* an expert id outside [0, E)                   */
+    MOE_ERR_RANGE = 8        /* a value outside the finite range of the fp16
+                                operands the tensor cores take (see the PREFILL
+                                path of moe_expert_forward, moe_decode_forward) */
 } moe_status;
 
 typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
@@ -131,7 +137,13 @@ moe_status moe_pack_experts(int bits, int64_t n_mats, int64_t rows, int64_t cols
                             const uint8_t *codes, const uint16_t *scales, uint8_t *packed_codes,
                             uint16_t *packed_scales, int32_t *dev_status, moe_stream_t stream);
 
-/* Inverse of moe_pack_experts for the code plane: packed -> one code per byte. */
+/*
+ * Inverse of moe_pack_experts for the code plane: packed -> one code per byte
+ * (codes [n_mats][rows][cols], device).  The pages store the routed experts
+ * at 2 bits per weight and count their bytes ("How Strata runs a
+ * 125-billion-parameter model ...", introduction and the Step 1 byte-census
+ * table); this call recovers the logical codes from that storage.
+ */
 moe_status moe_unpack_experts(int bits, int64_t n_mats, int64_t rows, int64_t cols,
                               const uint8_t *packed_codes, uint8_t *codes, moe_stream_t stream);
 
@@ -194,6 +206,12 @@ moe_status moe_router_topk(const uint16_t *x_bf16, int T, int H, const float *w_
  *              hold it (the softmax's limit).
  * A NaN logit sets *dev_status = MOE_ERR_NONFINITE; that token's ids are set
  * to 0..k-1 and its weights to 1/k.
+ * The pages: the router keeps the 10 best of 512 experts for each token and
+ * layer ("Strata Open-Source Runtime ...", section "The Model Itself"), and
+ * ranks 0..9 carry decreasing router weights ("How Strata runs a
+ * 125-billion-parameter model ...", Step 2, "Verify-window route tail
+ * skip").  This call is the selection step alone, so that a test can feed
+ * both this library and a reference the same fp32 logits.
  */
 moe_status moe_topk_from_logits(const float *logits, int T, int E, int k, int32_t *ids, float *w,
                                 int32_t *dev_status, moe_stream_t stream);
@@ -235,8 +253,10 @@ moe_status moe_permute(const int32_t *ids, int T, int k, int E, int32_t *offsets
  *     MOE_ERR_INVALID_ARG with the sizes in the message.
  *   - Outputs, errors and ordering are those of moe_permute.
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     that device current) and caches it together with the device's current
+ *     context; a call under a new context (after cudaDeviceReset, say) looks
+ *     it up again.  Make the first call on a device, and the first after a
+ *     reset, before any stream capture.
  *   - Every call on a device shares the one array, and each call overwrites
  *     the cells it reads (nothing needs clearing between calls); calls whose
  *     kernels overlap on the GPU (other streams, other host threads) race on
@@ -258,8 +278,27 @@ moe_status moe_permute_noalloc(const int32_t *ids, int T, int k, int E, int32_t 
  *        the fp32 result).
  * DECODE: fp32 dequantisation and accumulation; a token's result does not
  *   depend on which other tokens share the call (bit-identical alone or in a
- *   group).  PREFILL: grouped GEMM over the experts' token lists.
+ *   group).
+ * PREFILL: grouped GEMM over the experts' token lists.  With H and I
+ *   multiples of 64 (2-bit) or 128 (3-bit) it runs on the tensor cores with
+ *   fp16 operands: x converts to fp16 (exact for 2^-14 <= |x| <= 65504,
+ *   fewer bits below, none below 2^-25), the weights (c - mid) s round once to
+ *   fp16, h = silu(g) u rounds to fp16 between the two projections and each
+ *   pair's y = Wd_e h is kept as fp16 until the combine (fp32 accumulation
+ *   throughout; relative L2 error about 4e-4 on N(0,1) inputs).  The caller
+ *   keeps every one of these inside fp16's finite range: |x|, |h| and |y|
+ *   below 65504 and every block scale with |s| * max|c - mid| below 65520
+ *   (max|c - mid| = 1.5 for 2 bits, 3.5 for 3 bits).  RMS-normalised inputs
+ *   (|x| of order 1) and weight scales of order 0.02 stay far inside.  A value
+ *   outside it sets *dev_status = MOE_ERR_RANGE and the affected outputs are
+ *   not finite.  Other shapes take an fp32 FFMA form with no such limit.
  * Workspace: moe_expert_forward_workspace_size for the same arguments.
+ * The pages: each token's routed experts run on the GPU and their finished
+ * output vectors are summed there, weighted by the router ("How Strata runs
+ * a 125-billion-parameter model ...", Step 2, "Dynamic PCIe and CPU
+ * co-execution"); long prompts are read in chunks of tokens ("Strata
+ * Open-Source Runtime ...", section "Prefill and Long Context"), which the
+ * PREFILL path serves as one grouped GEMM per chunk.
  */
 moe_status moe_expert_forward_workspace_size(const moe_expert_arena *arena, int T, int k,
                                              moe_path path, size_t *bytes);
@@ -320,7 +359,10 @@ typedef struct moe_layer_weights {
  *   layers   host array of n_layers descriptors (copied into the launch)
  *   x        [T][H] fp32, device, 16-byte aligned, in/out
  *   ids_out, w_out  [n_layers][T][k] device outputs of the routing, or both NULL
- * A token's result does not depend on the other tokens of the call.  Shapes:
+ * A token's result does not depend on the other tokens of the call.  The
+ * tensor-core operands are fp16: u must stay below 65520 in magnitude (always
+ * so when normalised, |u| <= sqrt(H)) and so must h = silu(g) u; a value
+ * outside sets *dev_status = MOE_ERR_RANGE.  Shapes:
  * H a multiple of 256 with at most 16 output rows per SM (H <= 2432 on 152
  * SMs), I a multiple of 128 up to 4096, shared_I a multiple of 64 up to 4096,
  * E <= 1024, k <= 16; MOE_ERR_UNSUPPORTED when the buffers do not fit in

@@ -33,3 +33,31 @@ def u16(t):
 
 def bf16_rne(a):
     return synth.f32_to_bf16_bits(np.asarray(a, np.float32))
+
+
+def device_expert_parts(seed, layer, experts, bits, H, I):
+    """The picked experts' logical codes and scales, drawn by the device generator (model.draw_expert_parts)."""
+    from bit_expert_ffn_gb300.model import draw_expert_parts
+
+    return draw_expert_parts(seed, layer, experts, bits, H, I)
+
+
+def oracle_sampled_layer(seed, layer, bits, H, I, x_bf16, ids, w, shared, pool=None):
+    """oracle.moe_layer for the tokens of x_bf16 [T][H] with the given routing,
+    regenerating only the experts they picked (on the device generator).
+    With a thread pool the tokens run in parallel (the oracle is C code called
+    through ctypes, which releases the GIL)."""
+    import oracle
+
+    used = sorted(set(int(e) for e in np.asarray(ids).ravel()))
+    remap = {e: i for i, e in enumerate(used)}
+    arena = device_expert_parts(seed, layer, used, bits, H, I)
+    cids = np.vectorize(remap.get)(np.asarray(ids)).astype(np.int32).reshape(np.shape(ids))
+    w = np.asarray(w, np.float64)
+
+    def one(t):
+        return oracle.moe_layer(bits, x_bf16[t:t + 1], cids[t:t + 1], w[t:t + 1], *arena, shared=shared)[0]
+
+    T = x_bf16.shape[0]
+    rows = list(pool.map(one, range(T))) if pool is not None else [one(t) for t in range(T)]
+    return np.stack(rows)

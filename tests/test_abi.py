@@ -32,6 +32,7 @@ def test_status_names(lib):
     assert m.moe_status_name(0) == "MOE_OK"
     assert m.moe_status_name(7) == "MOE_ERR_BOUNDS"
     assert m.moe_status_name(6) == "MOE_ERR_NONFINITE"
+    assert m.moe_status_name(8) == "MOE_ERR_RANGE"
 
 
 def test_packed_size_census(lib):

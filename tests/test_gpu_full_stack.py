@@ -1,0 +1,194 @@
+"""GPU parity at the benchmarked sizes.
+
+* The 48-layer decode stack (H=2048, E=512, I=768, top-10, 2-bit experts,
+  Zipf(1.1) routing, bf16 shared expert I=768) through moe_decode_forward for
+  one token and for a 4-token verify window:
+    - one 48-layer launch is bit-identical (output, ids, weights) to 48
+      consecutive one-layer launches on the same weights, since the kernel's
+      arithmetic for a layer does not depend on its position in the stack;
+    - teacher forcing: every one-layer launch, fed the x_l that the previous
+      launch produced, matches the oracle's layer (on the kernel's routing,
+      with only the picked experts regenerated) within 2e-5 relative L2;
+    - every layer's ids equal the oracle's own top-10 of its own logits on the
+      same input, except at near-ties that fp32 summation order may flip.
+* The 32,768-token prefill layer (the same shapes, one layer): routing and
+  permutation checked whole, the layer output on sampled tokens, among them
+  tokens routed to the three most loaded experts.
+
+The pages put 48 layers of a router, ten of 512 experts and a shared expert
+in the model and verify windows of up to four tokens ("Strata serves a 125B
+MoE at 94 tokens/s from a 12 GB card and 64 GB of RAM", section "Six billion
+active parameters per token"; "Strata Open-Source Runtime: Running a
+125B-Parameter Qwen3 Model on a 12GB GPU", sections "The Model Itself" and
+"Prefill and Long Context").
+"""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+import torch
+
+import bit_expert_ffn_gb300 as m
+import oracle
+from bit_expert_ffn_gb300 import synth
+from bit_expert_ffn_gb300.model import LayerShape, MoeLayer, StepBuffers, Workspace, device_normal
+from helpers import oracle_sampled_layer, rel_l2
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+LAYERS = 48
+SEED = 0          # the decode benchmark's weights
+TIGHT = 2e-5
+
+
+def device_shared(seed, layer, H, Is):
+    """bf16 shared-expert weights (wg, wu, wd) of the seeded generator, drawn on the device."""
+    out = []
+    for tag, n, shape in ((synth.TAG_SHARED_G, Is * H, (Is, H)), (synth.TAG_SHARED_U, Is * H, (Is, H)),
+                          (synth.TAG_SHARED_D, H * Is, (H, Is))):
+        t = torch.empty(n, dtype=torch.int16, device=DEV)
+        device_normal(synth.stream_key(seed, tag, layer), n, 0.02, 1, t)
+        out.append(t.cpu().numpy().view(np.uint16).reshape(shape))
+    return tuple(out)
+
+
+def device_router(seed, layer, E, H):
+    t = torch.empty(E * H, dtype=torch.float32, device=DEV)
+    device_normal(synth.stream_key(seed, synth.TAG_ROUTER, layer), E * H, 0.02, 0, t)
+    return t.cpu().numpy().reshape(E, H)
+
+
+def layer_input(xr):
+    """bf16 of the normalised residual stream, the input a stacked layer takes."""
+    return synth.f32_to_bf16_bits(oracle.rms_norm(np.asarray(xr, np.float32), m.RMS_EPS).astype(np.float32))
+
+
+def run_fused(layers, x0, k):
+    T = x0.shape[0]
+    s = layers[0].s
+    x = torch.from_numpy(np.ascontiguousarray(x0, np.float32)).to(DEV)
+    n = len(layers)
+    ids = torch.empty(n, T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(n, T, k, dtype=torch.float32, device=DEV)
+    nb = m.moe_decode_workspace_size(T, s.H, s.I, s.E, k, s.Is)
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.moe_decode_forward([L.weights() for L in layers], x, T, k, m.RMS_EPS, ids, w, ws, nb, st)
+    assert m.moe_check_status(st) == 0, m.moe_last_error()
+    return x.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
+
+
+def near_tie_tokens(lg, k):
+    """Tokens whose k+1 largest logits hold two within the logit tolerance of each other."""
+    scale = max(np.abs(lg).max(), 1.0)
+    top = -np.sort(-lg, axis=1)[:, :k + 1]
+    return np.min(top[:, :-1] - top[:, 1:], axis=1) < 2e-5 * scale
+
+
+@pytest.fixture(scope="module")
+def decode_stack(moe):
+    s = LayerShape()
+    layers = []
+    for l in range(LAYERS):
+        L = MoeLayer(s, DEV)
+        L.fill_device(SEED, l, zipf_s=1.1)
+        layers.append(L)
+    torch.cuda.synchronize()
+    for L in layers:
+        assert m.moe_check_status(L.status) == 0
+    yield layers
+    del layers
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_decode_stack_teacher_forced(moe, decode_stack, T):
+    s = decode_stack[0].s
+    k = s.k
+    if T == 1:
+        x0 = synth.bf16_bits_to_f32(synth.activations(SEED, 1, s.H, step=7))
+    else:
+        x0 = synth.bf16_bits_to_f32(synth.verify_window(100, 4, s.H))
+    # one launch through the whole stack
+    x_all, ids_all, w_all = run_fused(decode_stack, x0, k)
+    # the same stack as 48 one-layer launches, each fed the previous one's output
+    xs, ids1, w1 = [x0.astype(np.float32)], [], []
+    for L in decode_stack:
+        x, i, w = run_fused([L], xs[-1], k)
+        xs.append(x)
+        ids1.append(i[0])
+        w1.append(w[0])
+    assert np.array_equal(ids_all, np.stack(ids1))
+    assert np.array_equal(w_all.view(np.uint32), np.stack(w1).view(np.uint32))
+    assert np.array_equal(x_all.view(np.uint32), xs[-1].view(np.uint32))
+    assert np.all(np.isfinite(x_all))
+
+    errs, flips, nears = [], 0, 0
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as pool:
+        for l in range(LAYERS):
+            xin = layer_input(xs[l])
+            shared = device_shared(SEED, l, s.H, s.Is)
+            want = oracle_sampled_layer(SEED, l, 2, s.H, s.I, xin, ids1[l], w1[l], shared, pool)
+            got = xs[l + 1].astype(np.float64) - xs[l].astype(np.float64)
+            errs.append(rel_l2(got, want))
+            # the oracle's own routing on the same input
+            lg = oracle.router_logits(xin, device_router(SEED, l, s.E, s.H), synth.zipf_bias(SEED, l, s.E, 1.1))
+            oids, _ = oracle.topk(lg.astype(np.float32), k)
+            near = near_tie_tokens(lg, k)
+            nears += int(near.sum())
+            same = np.all(oids == ids1[l], axis=1)
+            flips += int((~same).sum())
+            assert np.all(same | near), f"layer {l}: routing differs from the oracle's away from a near-tie"
+    worst = max(errs)
+    assert worst <= TIGHT, f"worst layer rel. L2 {worst:.3g} (layer {int(np.argmax(errs))})"
+    print(f"T={T}: worst layer rel. L2 {worst:.3g}, mean {np.mean(errs):.3g}; "
+          f"{nears} near-tie token-layers, {flips} routed differently from the oracle's own logits")
+
+
+def test_prefill_32k_sampled(moe):
+    """One layer over a 32,768-token prompt (the prefill benchmark's inputs)."""
+    seed, layer, T = 1, 0, 32768
+    s = LayerShape()
+    L = MoeLayer(s, DEV)
+    L.fill_device(seed, layer, zipf_s=1.1)
+    x = synth.activations(seed, T, s.H)
+    bufs = StepBuffers(T, s.E, s.k, DEV)
+    ws = Workspace(DEV)
+    out = torch.zeros(T, s.H, dtype=torch.float32, device=DEV)
+    L.forward(torch.from_numpy(x.view(np.int16)).to(DEV), T, out, ws, bufs, accumulate=False,
+              path=m.MOE_PATH_PREFILL)
+    assert m.moe_check_status(L.status) == 0, m.moe_last_error()
+    ids = bufs.ids.cpu().numpy()
+    w = bufs.w.cpu().numpy()
+    gl = bufs.logits.cpu().numpy()
+    # routing: the oracle's selection on the GPU's own logits, every token (rule i)
+    oids, ow = oracle.topk(gl, s.k)
+    assert np.array_equal(ids, oids)
+    np.testing.assert_allclose(w, ow, rtol=1e-6, atol=1e-7)
+    # permutation: bit-exact, every pair
+    oo, op, oi = oracle.permute(ids, s.E)
+    assert np.array_equal(bufs.offsets.cpu().numpy(), oo)
+    assert np.array_equal(bufs.perm.cpu().numpy(), op)
+    assert np.array_equal(bufs.inv.cpu().numpy(), oi)
+    # layer output on sampled tokens: the first, middle and last token of each
+    # of the three most loaded experts' lists, plus random ones
+    counts = np.diff(oo)
+    assert counts.max() > 16384 and (counts % 32 != 0).any()
+    tokens = set()
+    for e in np.argsort(-counts, kind="stable")[:3]:
+        lst = op[oo[e]:oo[e + 1]] // s.k
+        tokens.update(int(t) for t in (lst[0], lst[len(lst) // 2], lst[-1]))
+    tokens.update(int(t) for t in np.random.default_rng(5).choice(T, 10, replace=False))
+    tokens = sorted(tokens)
+    assert len(tokens) >= 16
+    got = out[tokens].cpu().numpy()
+    shared = synth.shared_weights(seed, layer, s.H, s.Is)
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as pool:
+        want = oracle_sampled_layer(seed, layer, 2, s.H, s.I, x[tokens], ids[tokens], w[tokens], shared, pool)
+    # fp16 operands on the tensor cores: weights (c - mid) s and h rounded once (about 4e-4)
+    assert rel_l2(got, want) <= 1e-3
+    # the router's fp32 logits against the oracle's on the sampled tokens
+    ol = oracle.router_logits(x[tokens], synth.router_weights(seed, layer, s.E, s.H),
+                              synth.zipf_bias(seed, layer, s.E, 1.1))
+    assert np.abs(gl[tokens] - ol).max() <= 1e-5 * np.abs(ol).max()

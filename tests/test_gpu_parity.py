@@ -400,3 +400,88 @@ def test_full_size_3bit_prefill_sampled(moe, zipf):
     tokens = sorted(np.random.default_rng(1).choice(T, 6, replace=False))
     want = sampled_reference(seed, layer, 3, s.H, s.I, x, ids, w, shared, tokens)
     assert rel_l2(got[tokens], want) <= prefill_tol(s.H, s.I, 3)
+
+
+# ---------------------------------------------------------------- fp16 operand range
+
+def _scaled_scales(a, f):
+    """fp16 scale bits times f (rounded to fp16)."""
+    return (a.view(np.float16).astype(np.float32) * np.float32(f)).astype(np.float16).view(np.uint16)
+
+
+def _range_layer(scale_factor=1.0, bits=2, H=256, I=128, E=16, k=4):
+    arena, wr, b, shared = host_layer(seed=31, bits=bits, H=H, I=I, E=E, Is=128)
+    arena = list(arena)
+    for i in (1, 3, 5):
+        arena[i] = _scaled_scales(arena[i], scale_factor)
+    L = MoeLayer(LayerShape(H=H, I=I, E=E, k=k, Is=128, bits=bits), DEV)
+    L.load_host(arena[0], arena[1], arena[2], arena[3], arena[4], arena[5], wr, b, shared)
+    return L, arena, shared
+
+
+@pytest.mark.parametrize("x_factor,scale_factor,bits", [(30.0, 1.0, 2), (1.0, 10.0, 2), (20.0, 1.0, 3)])
+def test_prefill_large_values_inside_fp16_match_oracle(moe, x_factor, scale_factor, bits):
+    """Activations or block scales well above the workloads' (|x| about 30, scales about 0.2) that keep x, h
+    and y inside fp16's range still match the oracle within the fp16-operand tolerance."""
+    L, arena, shared = _range_layer(scale_factor, bits=bits)
+    x = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(synth.activations(32, 300, 256)) * np.float32(x_factor))
+    got, bufs = run_layer(L, x, 300, m.MOE_PATH_PREFILL)
+    want = oracle.moe_layer(bits, x, bufs.ids.cpu().numpy(), bufs.w.cpu().numpy().astype(np.float64), *arena,
+                            shared=shared)
+    assert np.all(np.isfinite(got))
+    assert rel_l2(got, want) <= prefill_tol(256, 128, bits)
+
+
+def _prefill_status(L, x, T):
+    bufs = StepBuffers(T, L.s.E, L.s.k)
+    out = torch.zeros(T, L.s.H, dtype=torch.float32, device=DEV)
+    L.forward(dev_u16(x), T, out, Workspace(DEV), bufs, accumulate=False, path=m.MOE_PATH_PREFILL)
+    return m.moe_check_status(L.status), out
+
+
+def test_prefill_reports_x_outside_fp16(moe):
+    L, _, _ = _range_layer()
+    x = synth.activations(33, 300, 256)
+    x[5, 17] = synth.f32_to_bf16_bits(np.array([1e5], np.float32))[0]  # no finite fp16
+    st, out = _prefill_status(L, x, 300)
+    assert st == m.MOE_ERR_RANGE
+    # the other tokens are unaffected and the context is still usable
+    assert bool(torch.isfinite(out[6:]).all())
+    st, _ = _prefill_status(L, synth.activations(33, 300, 256), 300)
+    assert st == 0
+
+
+def test_prefill_reports_h_outside_fp16(moe):
+    """|x| of about 1e3 is a finite fp16, but h = silu(g) u then reaches about 1e6."""
+    L, _, _ = _range_layer()
+    x = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(synth.activations(34, 300, 256)) * np.float32(1000.0))
+    st, _ = _prefill_status(L, x, 300)
+    assert st == m.MOE_ERR_RANGE
+
+
+def test_prefill_reports_scale_outside_fp16(moe):
+    """A block scale of 50,000 makes (c - 1.5) s = 75,000 for the extreme codes."""
+    arena, wr, b, shared = host_layer(seed=35, bits=2, H=256, I=128, E=16, Is=128)
+    arena = list(arena)
+    arena[1] = arena[1].copy()
+    arena[1][:, :, :] = np.float16(50000.0).view(np.uint16)
+    L = MoeLayer(LayerShape(H=256, I=128, E=16, k=4, Is=128, bits=2), DEV)
+    L.load_host(*arena, wr, b, shared)
+    st, _ = _prefill_status(L, synth.activations(35, 300, 256), 300)
+    assert st == m.MOE_ERR_RANGE
+
+
+def test_fused_decode_reports_u_outside_fp16(moe):
+    """Without the normalisation (rms_eps < 0) u = bf16(x) is the MMA operand: |x| = 1e5 has no finite fp16."""
+    L, _, _ = _range_layer()
+    x = synth.bf16_bits_to_f32(synth.activations(36, 1, 256)).copy()
+    x[0, 3] = 1e5
+    xd = torch.from_numpy(x).to(DEV)
+    nb = m.moe_decode_workspace_size(1, 256, 128, 16, 4, 128)
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.moe_decode_forward([L.weights()], xd, 1, 4, -1.0, None, None, ws, nb, st)
+    assert m.moe_check_status(st) == m.MOE_ERR_RANGE
+    xd = torch.from_numpy(synth.bf16_bits_to_f32(synth.activations(36, 1, 256)).copy()).to(DEV)
+    m.moe_decode_forward([L.weights()], xd, 1, 4, -1.0, None, None, ws, nb, st)
+    assert m.moe_check_status(st) == 0
