@@ -58,6 +58,22 @@ constexpr unsigned kAbort = 0x80000000u;
 template <int T>
 __host__ __device__ constexpr int warps_for() { return T == 1 ? 16 : 8; }
 
+// Phase trace for development builds, compiled out unless MOE_DECODE_TRACE is
+// defined: thread 0 of every CTA stamps the global timer at the phase
+// boundaries of every layer (moe_decode_trace_read copies the stamps out).
+#ifdef MOE_DECODE_TRACE
+constexpr int kTracePhases = 12;
+__device__ unsigned long long g_decode_trace[kMaxLayers][160][kTracePhases];
+#define MOE_TRACE(P)                                                                     \
+    do {                                                                                 \
+        if (threadIdx.x == 0 && blockIdx.x < 160) g_decode_trace[l][blockIdx.x][P] = tc::now_ns(); \
+    } while (0)
+#else
+#define MOE_TRACE(P) \
+    do {             \
+    } while (0)
+#endif
+
 struct Layer {
     const uint8_t *gu_codes;
     const uint16_t *gu_scales;
@@ -924,6 +940,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
     for (int l = 0; l < a.n_layers; l++) {
         const Layer &L = a.L[l];
         bool fail = false;
+        MOE_TRACE(0);
         int r0, rh, q0, qh;
         split_range(E, cta, G, r0, rh);
         split_range(Is, cta, G, q0, qh);
@@ -985,6 +1002,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             }
         }
         if (__syncthreads_or(fail)) { ok = false; break; }
+        MOE_TRACE(1);
         if (tid < T) {
             float inv = 1.0f;
             if (a.rms_eps >= 0.f) {
@@ -1023,6 +1041,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             ok = false;
             break;
         }
+        MOE_TRACE(2);
         // items: this CTA's router rows, then its shared gate/up rows (A'),
         // spread over the warps; A' overlaps the wait for the other CTAs' logits,
         // and the h counter after phase B also covers h_s
@@ -1087,6 +1106,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             }
         }
         __syncthreads();  // poll only once this CTA's own rows are done (fewer spinning requests in L2)
+        MOE_TRACE(3);
         // ---- routing: all logits, top-k per token, groups of pairs
         {
             // all requests first (one round trip when the logits are ready), then late ones
@@ -1117,6 +1137,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             }
         }
         if (__syncthreads_or(fail)) { ok = false; break; }
+        MOE_TRACE(4);
         unsigned nan_mask = 0;
         for (int t = 0; t < T; t++)
             if (topk_cta(lg + (size_t)t * E, E, k, R, t, reinterpret_cast<uint32_t *>(r1),
@@ -1134,6 +1155,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             a.ids_out[(size_t)l * T * k + tid] = R.ids[tid];
             a.w_out[(size_t)l * T * k + tid] = R.w[tid];
         }
+        MOE_TRACE(5);
         const int ng = R.ngroups, NU = ng * tiles;
         int u0, u1;
         split_range(NU, cta, G, u0, u1);
@@ -1223,6 +1245,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             ok = false;
             break;
         }
+        MOE_TRACE(6);
         if (tid == 0) {
             for (int s = 0; s < P.nsu; s++) R.fills_u[s] += fills_of(s, nu, P.nsu);
             red_release_add(a.cnt + 0, 1u);
@@ -1247,6 +1270,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             }
         }
         if (__syncthreads_or(fail)) { ok = false; break; }
+        MOE_TRACE(7);
         const uint32_t *hop = P.stage_h ? reinterpret_cast<const uint32_t *>(dyn + P.off_hop) : a.hop;
         if (L.swg && nrows > 0)
             for (int i = tid; i < T * Is; i += NT) hsm[i] = __ldcg(a.hs + i);
@@ -1257,6 +1281,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             ok = false;
             break;
         }
+        MOE_TRACE(8);
         // ---- shared down rows, one per warp, while the staged h is in flight
         if (L.swg) {
             for (int rr = warp; rr < nrows; rr += NW) {
@@ -1290,6 +1315,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             if (!tc::mbar_wait(&R.fullH, (uint32_t)(fillsH & 1), kTimeoutNs)) fail = true;
             fillsH++;
         }
+        MOE_TRACE(9);
         // ---- C: routed down on the tensor cores
         if (nrows > 0 && !fail) {
             int g = 0, s2 = warp, slot = 0, fq = 0;
@@ -1334,6 +1360,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             ok = false;
             break;
         }
+        MOE_TRACE(10);
         if (tid == 0 && l + 1 < a.n_layers) {  // the shared down rows are consumed: fetch the next layer's
             tc::fence_proxy_async_smem();
             issue_s(a, a.L[l + 1], r3, o0, nrows, &R.fullS);
@@ -1375,6 +1402,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
         if (tid == NT - 1 && nrows > 0)  // (a thread that has no row to combine)
             for (int s = 0; s < P.nsd; s++) R.fills_d[s] += fills_of(s, ng, P.nsd);
         __syncthreads();
+        MOE_TRACE(11);
     }
     // ---- on an early exit, let every copy in flight land before the CTA ends
     if (!ok && tid == 0) {
@@ -1625,6 +1653,14 @@ extern "C" moe_status moe_decode_forward(const moe_layer_weights *layers, int n_
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cooperative launch of the fused decode: %s", cudaGetErrorString(e));
     return MOE_OK;
 }
+
+#ifdef MOE_DECODE_TRACE
+extern "C" int moe_decode_trace_read(unsigned long long *host)
+{
+    if (cudaDeviceSynchronize() != cudaSuccess) return 1;
+    return cudaMemcpyFromSymbol(host, fused::g_decode_trace, sizeof(fused::g_decode_trace)) != cudaSuccess;
+}
+#endif
 
 extern "C" moe_status moe_selftest_barrier(unsigned extra_arrivals, int timeout_ms, void *ws, size_t ws_bytes,
                                            int32_t *dev_status, moe_stream_t stream)
