@@ -62,6 +62,13 @@ class moe_layer_weights(ctypes.Structure):
     ]
 
 
+class moe_decode_options(ctypes.Structure):
+    _fields_ = [
+        ("route_tail_skip", ctypes.c_int32),
+        ("hot_experts", ctypes.c_void_p),
+    ]
+
+
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int
 _I64 = ctypes.c_int64
@@ -89,6 +96,8 @@ _SIGS = {
     "moe_decode_workspace_size": [_I32, _I32, _I32, _I32, _I32, _I32, _PSZ],
     "moe_decode_forward": [ctypes.POINTER(moe_layer_weights), _I32, _P, _I32, _I32, ctypes.c_float, _P, _P, _P, _SZ,
                            _P, _P],
+    "moe_decode_forward_ex": [ctypes.POINTER(moe_layer_weights), _I32, _P, _I32, _I32, ctypes.c_float,
+                              ctypes.POINTER(moe_decode_options), _P, _P, _P, _SZ, _P, _P],
     "moe_rms_norm_bf16": [_P, _P, _I32, _I32, ctypes.c_float, _P],
     "moe_selftest_barrier": [ctypes.c_uint, _I32, _P, _SZ, _P, _P],
 }
@@ -276,6 +285,17 @@ def moe_decode_forward(layers, x, T, k, rms_eps=RMS_EPS, ids_out=None, w_out=Non
     arr = (moe_layer_weights * len(layers))(*layers)
     _check(lib().moe_decode_forward(arr, len(layers), _ptr(x), T, k, rms_eps, _ptr(ids_out), _ptr(w_out), _ptr(ws),
                                     ws_bytes, _ptr(dev_status), _stream(stream)), "moe_decode_forward")
+
+
+def moe_decode_forward_ex(layers, x, T, k, rms_eps=RMS_EPS, route_tail_skip=0, hot_experts=None, ids_out=None,
+                          w_out=None, ws=None, ws_bytes=0, dev_status=None, stream=None):
+    """moe_decode_forward with options: route_tail_skip (rank threshold, 0 = off) and hot_experts (a device
+    uint32 tensor [n_layers][(E + 31) // 32] of bit masks, or None)."""
+    arr = (moe_layer_weights * len(layers))(*layers)
+    opts = moe_decode_options(int(route_tail_skip), _ptr(hot_experts))
+    _check(lib().moe_decode_forward_ex(arr, len(layers), _ptr(x), T, k, rms_eps, ctypes.byref(opts), _ptr(ids_out),
+                                       _ptr(w_out), _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)),
+           "moe_decode_forward_ex")
 
 
 def moe_rms_norm_bf16(x, out, T, H, eps=None, stream=None):

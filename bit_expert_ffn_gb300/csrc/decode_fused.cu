@@ -98,6 +98,8 @@ struct Args {
     int32_t *ids_out;  // [n_layers][T][k] or NULL
     float *w_out;
     int32_t *status;
+    int tail_skip;          // route-tail skip from this rank on (0: off)
+    const uint32_t *hot;    // [n_layers][(E + 31) / 32] hot-expert bit masks, or NULL (no cache hints)
 };
 
 // Shared-memory plan (host-computed): strides, slot sizes, byte offsets.
@@ -119,6 +121,7 @@ struct Routing {
     float w[kMaxPairs];
     int perm[kMaxPairs];  // sorted position -> flat t*k+j
     int inv[kMaxPairs];   // flat -> sorted position
+    int key[kMaxPairs];   // expert of each pair, INT32_MAX for a pair the route-tail skip leaves out
     int g_e[kMaxPairs], g_p0[kMaxPairs], g_n[kMaxPairs];
     int tok_of[kMaxPairs];  // sorted position -> token
     int ngroups;
@@ -181,6 +184,45 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                      tc::smem_u32(dst)),
                  "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
                  : "memory");
+}
+
+// The same copy with an L2 eviction-priority hint (a policy from createpolicy).
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            tc::smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(tc::smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// A weight copy: with hot-expert masks given, marked experts' weights carry an
+// L2 evict-last hint (they stay in L2 from one decode step to the next) and
+// every other weight an evict-first hint; without masks, a plain copy.
+__device__ __forceinline__ void weight_g2s(const Args &a, bool hot, void *dst, const void *src, uint32_t bytes,
+                                           uint64_t *bar)
+{
+    if (a.hot == nullptr) bulk_g2s(dst, src, bytes, bar);
+    else bulk_g2s_hint(dst, src, bytes, bar, hot ? policy_evict_last() : policy_evict_first());
+}
+
+__device__ __forceinline__ bool is_hot(const Args &a, int l, int e)
+{
+    return a.hot != nullptr && ((a.hot[(size_t)l * ((a.E + 31) >> 5) + (e >> 5)] >> (e & 31)) & 1u);
 }
 
 __device__ __forceinline__ bool aborted(const Args &a) { return (ld_acquire(a.cnt + 2) & kAbort) != 0; }
@@ -449,12 +491,15 @@ __device__ void topk_weights(Routing &R, int t, int k, bool nan_token)
     }
 }
 
-// Sort the T*k pairs by (expert, flat index) and cut them into groups (one
-// warp; n <= 64 pairs, two per lane, ranks by shuffles).
+// Sort the T*k pairs by (key, flat index) and cut the kept ones (key below
+// INT32_MAX) into groups of one expert each (one warp; n <= 64 pairs, two per
+// lane, ranks by shuffles).  The pairs left out sort after every kept one.
 __device__ void build_groups(Routing &R, int n)
 {
     const int lane = lane_id();
-    const int e0 = lane < n ? R.ids[lane] : INT32_MAX, e1 = lane + 32 < n ? R.ids[lane + 32] : INT32_MAX;
+    const int e0 = lane < n ? R.key[lane] : INT32_MAX, e1 = lane + 32 < n ? R.key[lane + 32] : INT32_MAX;
+    const int nk = __popc(__ballot_sync(0xffffffffu, lane < n && e0 != INT32_MAX)) +
+                   __popc(__ballot_sync(0xffffffffu, lane + 32 < n && e1 != INT32_MAX));
     int r0 = 0, r1 = 0;
     const int n0 = n < 32 ? n : 32;
 #pragma unroll 4
@@ -482,13 +527,13 @@ __device__ void build_groups(Routing &R, int n)
     __syncwarp();
     int seen = 0;
 #pragma unroll 1
-    for (int b = 0; b < n; b += 32) {
+    for (int b = 0; b < nk; b += 32) {
         const int p = b + lane;
         bool start = false;
         int e = 0;
-        if (p < n) {
-            e = R.ids[R.perm[p]];
-            start = p == 0 || R.ids[R.perm[p - 1]] != e;
+        if (p < nk) {
+            e = R.key[R.perm[p]];
+            start = p == 0 || R.key[R.perm[p - 1]] != e;
         }
         const unsigned m = __ballot_sync(0xffffffffu, start);
         if (start) {
@@ -500,8 +545,32 @@ __device__ void build_groups(Routing &R, int n)
     }
     __syncwarp();
 #pragma unroll 1
-    for (int g = lane; g < seen; g += 32) R.g_n[g] = (g + 1 < seen ? R.g_p0[g + 1] : n) - R.g_p0[g];
+    for (int g = lane; g < seen; g += 32) R.g_n[g] = (g + 1 < seen ? R.g_p0[g + 1] : nk) - R.g_p0[g];
     if (lane == 0) R.ngroups = seen;
+    __syncwarp();
+}
+
+// The expert key of every pair (one warp): its expert id, or INT32_MAX when
+// the route-tail skip leaves it out.  From rank a.tail_skip on, a pair is
+// left out when no token of the call keeps its expert at a lower rank and the
+// expert is not marked hot ("How Strata runs a 125-billion-parameter model
+// ...", Step 2, "Verify-window route tail skip": an expert every token of a
+// verify window ranks at the tail of its top-10 contributes almost nothing,
+// and every expert resident in the fast tier is kept).  The kept pairs'
+// weights are left as they are (not renormalised).
+__device__ void mark_pairs(const Args &a, Routing &R, int n, int k, int l)
+{
+    for (int i = lane_id(); i < n; i += 32) {
+        const int e = R.ids[i];
+        bool drop = false;
+        if (a.tail_skip > 0 && i % k >= a.tail_skip && !is_hot(a, l, e)) {
+            drop = true;
+#pragma unroll 1
+            for (int q = 0; q < n; q++)
+                if (q % k < a.tail_skip && R.ids[q] == e) drop = false;
+        }
+        R.key[i] = drop ? INT32_MAX : e;
+    }
     __syncwarp();
 }
 
@@ -795,10 +864,10 @@ __device__ void issue_a(const Args &a, const Plan &P, const Layer &L, char *r1, 
     if (!L.swg) qh = q0;
     uint32_t rb = (uint32_t)(rh - r0) * a.H * 4u, qb = (uint32_t)(qh - q0) * a.H * 2u;
     tc::mbar_arrive_expect_tx(bar, rb + 2 * qb);
-    if (rb) bulk_g2s(r1, L.w_router + (size_t)r0 * a.H, rb, bar);
+    if (rb) weight_g2s(a, false, r1, L.w_router + (size_t)r0 * a.H, rb, bar);
     if (qb) {
-        bulk_g2s(r1 + rb, L.swg + (size_t)q0 * a.H, qb, bar);
-        bulk_g2s(r1 + rb + qb, L.swu + (size_t)q0 * a.H, qb, bar);
+        weight_g2s(a, false, r1 + rb, L.swg + (size_t)q0 * a.H, qb, bar);
+        weight_g2s(a, false, r1 + rb + qb, L.swu + (size_t)q0 * a.H, qb, bar);
     }
 }
 
@@ -807,13 +876,13 @@ __device__ void issue_s(const Args &a, const Layer &L, char *r3, int o0, int nro
 {
     uint32_t b = (L.swg && nrows > 0) ? (uint32_t)nrows * a.Is * 2u : 0u;
     tc::mbar_arrive_expect_tx(bar, b);
-    if (b) bulk_g2s(r3, L.swd + (size_t)o0 * a.Is, b, bar);
+    if (b) weight_g2s(a, false, r3, L.swd + (size_t)o0 * a.Is, b, bar);
 }
 
 // Unit u (group u / (I/16), rows 16 rt .. 16 rt + 15 of gate and of up) into
 // a unit slot, as four contiguous copies: gate codes, up codes (16 rows each),
-// gate scales, up scales.  One thread.
-__device__ void issue_unit(const Args &a, const Plan &P, const Layer &L, const Routing &R, int u, char *slot,
+// gate scales, up scales.  One thread.  l: the layer (for the hot-expert mask).
+__device__ void issue_unit(const Args &a, const Plan &P, const Layer &L, const Routing &R, int l, int u, char *slot,
                            uint64_t *bar)
 {
     const int tiles = a.I / 16;
@@ -822,24 +891,26 @@ __device__ void issue_unit(const Args &a, const Plan &P, const Layer &L, const R
     const uint32_t cb = 16u * P.cb_gu, sb = 16u * P.sb_gu;
     const char *sc = reinterpret_cast<const char *>(L.gu_scales);
     tc::fence_proxy_async_smem();
+    const bool hot = is_hot(a, l, e);
     tc::mbar_arrive_expect_tx(bar, 2 * (cb + sb));
-    bulk_g2s(slot, L.gu_codes + rg * P.cb_gu, cb, bar);
-    bulk_g2s(slot + cb, L.gu_codes + ru * P.cb_gu, cb, bar);
-    bulk_g2s(slot + 2 * cb, sc + rg * P.sb_gu, sb, bar);
-    bulk_g2s(slot + 2 * cb + sb, sc + ru * P.sb_gu, sb, bar);
+    weight_g2s(a, hot, slot, L.gu_codes + rg * P.cb_gu, cb, bar);
+    weight_g2s(a, hot, slot + cb, L.gu_codes + ru * P.cb_gu, cb, bar);
+    weight_g2s(a, hot, slot + 2 * cb, sc + rg * P.sb_gu, sb, bar);
+    weight_g2s(a, hot, slot + 2 * cb + sb, sc + ru * P.sb_gu, sb, bar);
 }
 
 // Down rows [o0, o0 + nrows) of group g's expert into a down slot: the code
 // rows (contiguous) and their scales, two copies.  One thread.
-__device__ void issue_down(const Args &a, const Plan &P, const Layer &L, const Routing &R, int g, int o0, int nrows,
-                           char *slot, uint64_t *bar)
+__device__ void issue_down(const Args &a, const Plan &P, const Layer &L, const Routing &R, int l, int g, int o0,
+                           int nrows, char *slot, uint64_t *bar)
 {
     const size_t row0 = (size_t)R.g_e[g] * a.H + o0;
+    const bool hot = is_hot(a, l, R.g_e[g]);
     tc::fence_proxy_async_smem();
     tc::mbar_arrive_expect_tx(bar, (uint32_t)nrows * (P.cb_d + P.sb_d));
-    bulk_g2s(slot, L.d_codes + row0 * P.cb_d, (uint32_t)nrows * P.cb_d, bar);
-    bulk_g2s(slot + 16 * P.cb_d, reinterpret_cast<const char *>(L.d_scales) + row0 * P.sb_d, (uint32_t)nrows * P.sb_d,
-             bar);
+    weight_g2s(a, hot, slot, L.d_codes + row0 * P.cb_d, (uint32_t)nrows * P.cb_d, bar);
+    weight_g2s(a, hot, slot + 16 * P.cb_d, reinterpret_cast<const char *>(L.d_scales) + row0 * P.sb_d,
+               (uint32_t)nrows * P.sb_d, bar);
 }
 
 // The number of fills a ring slot s receives when n items go through nslot slots.
@@ -1147,6 +1218,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
         if (warp < T) topk_weights(R, warp, k, (nan_mask >> warp) & 1u);
         __syncthreads();
         if (warp == 0) {
+            mark_pairs(a, R, T * k, k, l);
             build_groups(R, T * k);
             pair_tokens(R, T * k, k);
         }
@@ -1164,11 +1236,11 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             const int nui = min(nu, P.nsu), ndi = nrows > 0 ? min(ng, P.nsd) : 0;
             for (int j = lane; j < nui + ndi; j += 32) {
                 if (j < nui) {
-                    issue_unit(a, P, L, R, u0 + j, r1 + (size_t)j * P.unitB, &R.fullU[j]);
+                    issue_unit(a, P, L, R, l, u0 + j, r1 + (size_t)j * P.unitB, &R.fullU[j]);
                     iss_u[j]++;
                 } else {
                     const int g = j - nui;
-                    issue_down(a, P, L, R, g, o0, nrows, r2 + (size_t)g * P.downB, &R.fullD[g]);
+                    issue_down(a, P, L, R, l, g, o0, nrows, r2 + (size_t)g * P.downB, &R.fullD[g]);
                     iss_d[g]++;
                 }
             }
@@ -1216,7 +1288,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                     if (lane == 0) {
                         atomicExch(&R.ucnt[slot], 0);
                         if (ul + P.nsu < nu) {
-                            issue_unit(a, P, L, R, u + P.nsu, r1 + (size_t)slot * P.unitB, &R.fullU[slot]);
+                            issue_unit(a, P, L, R, l, u + P.nsu, r1 + (size_t)slot * P.unitB, &R.fullU[slot]);
                             iss_u[slot]++;
                         }
                     }
@@ -1343,7 +1415,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                     if (last && lane == 0) {
                         atomicExch(&R.dcnt[slot], 0);
                         if (g + P.nsd < ng) {
-                            issue_down(a, P, L, R, g + P.nsd, o0, nrows, r2 + (size_t)slot * P.downB, &R.fullD[slot]);
+                            issue_down(a, P, L, R, l, g + P.nsd, o0, nrows, r2 + (size_t)slot * P.downB, &R.fullD[slot]);
                             iss_d[slot]++;
                         }
                     }
@@ -1385,7 +1457,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                 yj[j] = 0.f;
                 if (j < k) {
                     wj[j] = R.w[t * k + j];
-                    yj[j] = pd[(size_t)R.inv[t * k + j] * NSD2 * 16 + rr];
+                    if (R.key[t * k + j] != INT32_MAX) yj[j] = pd[(size_t)R.inv[t * k + j] * NSD2 * 16 + rr];
                 }
             }
             float sum = 0.f;
@@ -1549,9 +1621,10 @@ extern "C" moe_status moe_decode_workspace_size(int T, int H, int I, int E, int 
     return MOE_OK;
 }
 
-extern "C" moe_status moe_decode_forward(const moe_layer_weights *layers, int n_layers, float *x, int T, int k,
-                                         float rms_eps, int32_t *ids_out, float *w_out, void *ws, size_t ws_bytes,
-                                         int32_t *dev_status, moe_stream_t stream)
+extern "C" moe_status moe_decode_forward_ex(const moe_layer_weights *layers, int n_layers, float *x, int T, int k,
+                                            float rms_eps, const moe_decode_options *opts, int32_t *ids_out,
+                                            float *w_out, void *ws, size_t ws_bytes, int32_t *dev_status,
+                                            moe_stream_t stream)
 {
     using namespace fused;
     MOE_REQUIRE(layers && n_layers >= 0, "layers is NULL or n_layers < 0");
@@ -1565,8 +1638,14 @@ extern "C" moe_status moe_decode_forward(const moe_layer_weights *layers, int n_
     if (st != MOE_OK) return st;
     MOE_REQUIRE(x && aligned16(x), "x must be a 16-byte aligned device pointer");
     MOE_REQUIRE(!ids_out == !w_out, "ids_out and w_out must both be given or both be NULL");
+    const int tail_skip = opts ? opts->route_tail_skip : 0;
+    const uint32_t *hot = opts ? opts->hot_experts : nullptr;
+    MOE_REQUIRE(tail_skip >= 0 && tail_skip <= k, "route_tail_skip must be in [0, k] (got %d)", tail_skip);
+    MOE_REQUIRE(!hot || (reinterpret_cast<uintptr_t>(hot) & 3u) == 0, "hot_experts must be 4-byte aligned");
     Args a;
     memset(&a, 0, sizeof a);
+    a.tail_skip = tail_skip;
+    a.hot = hot;
     for (int l = 0; l < n_layers; l++) {
         const moe_layer_weights &W = layers[l];
         const moe_expert_arena &A = W.experts;
@@ -1661,6 +1740,14 @@ extern "C" int moe_decode_trace_read(unsigned long long *host)
     return cudaMemcpyFromSymbol(host, fused::g_decode_trace, sizeof(fused::g_decode_trace)) != cudaSuccess;
 }
 #endif
+
+extern "C" moe_status moe_decode_forward(const moe_layer_weights *layers, int n_layers, float *x, int T, int k,
+                                         float rms_eps, int32_t *ids_out, float *w_out, void *ws, size_t ws_bytes,
+                                         int32_t *dev_status, moe_stream_t stream)
+{
+    return moe_decode_forward_ex(layers, n_layers, x, T, k, rms_eps, nullptr, ids_out, w_out, ws, ws_bytes, dev_status,
+                                 stream);
+}
 
 extern "C" moe_status moe_selftest_barrier(unsigned extra_arrivals, int timeout_ms, void *ws, size_t ws_bytes,
                                            int32_t *dev_status, moe_stream_t stream)

@@ -380,6 +380,47 @@ moe_status moe_decode_forward(const moe_layer_weights *layers, int n_layers, flo
                               int32_t *dev_status, moe_stream_t stream);
 
 /*
+ * Options of moe_decode_forward_ex (all zero: the exact layer of
+ * moe_decode_forward).
+ *
+ * route_tail_skip (an approximation, off at 0): from this rank on (0-based
+ *   slot in the token's top-k order), a (token, slot) pair is left out of the
+ *   layer -- its expert's weights are neither fetched nor multiplied -- when
+ *   no token of the call keeps that expert at a lower rank and the expert is
+ *   not marked hot.  The other pairs keep their weights (no renormalisation),
+ *   so a token's output loses the left-out terms w_j FFN_j(u).  The pages
+ *   skip, in a verify window of up to four tokens, the experts every token
+ *   ranks 7, 8 or 9 of its top-10 (rank threshold 7) unless the expert is in
+ *   the fast memory tier, trading a small shift of the output distribution
+ *   for fewer expert reads ("How Strata runs a 125-billion-parameter model
+ *   ...", Step 2, "Verify-window route tail skip").  Must be in [0, k].
+ *   ids_out / w_out still report the router's full selection.
+ * hot_experts (device, [n_layers][(E + 31) / 32] uint32 bit masks, bit e of
+ *   layer l set for a hot expert, or NULL): the copies of a marked expert's
+ *   weights carry an L2 evict-last hint and every other weight copy an
+ *   evict-first hint, so that the marked experts stay in the 129 MB L2 from
+ *   one decode step to the next -- the on-chip counterpart of the pages'
+ *   adaptive expert cache ("How Strata runs ...", Step 1, "Tier 1: GPU VRAM
+ *   ... adaptive expert cache"; "Strata serves a 125B MoE ...", "Where the
+ *   weights live").  The results are the same bits with or without masks.
+ *   The caller chooses the set (for instance from the routing the previous
+ *   steps reported through ids_out) and may change it between calls.
+ */
+typedef struct moe_decode_options {
+    int32_t route_tail_skip;
+    const uint32_t *hot_experts;
+} moe_decode_options;
+
+/*
+ * moe_decode_forward with options (opts may be NULL: moe_decode_forward).
+ * Every other argument, the shapes, workspace and errors are those of
+ * moe_decode_forward.
+ */
+moe_status moe_decode_forward_ex(const moe_layer_weights *layers, int n_layers, float *x, int T, int k,
+                                 float rms_eps, const moe_decode_options *opts, int32_t *ids_out, float *w_out,
+                                 void *ws, size_t ws_bytes, int32_t *dev_status, moe_stream_t stream);
+
+/*
  * Self-test of the grid barrier's time limit used by moe_decode_forward: one
  * cooperative launch (one CTA per SM) runs a single barrier whose target is
  * `extra_arrivals` above the number of CTAs.  With extra_arrivals = 0 it

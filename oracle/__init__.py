@@ -243,3 +243,35 @@ def rms_norm(x_f32: np.ndarray, eps: float) -> np.ndarray:
     y = np.zeros((T, H), np.float64)
     lib().oracle_rms_norm(T, H, _p(x), float(eps), _p(y))
     return y
+
+
+def route_tail_skip(ids: np.ndarray, rank: int, hot=None) -> np.ndarray:
+    """Pairs a verify window leaves out under the route-tail skip.
+
+    "How Strata runs a 125-billion-parameter model on a single 12 GB to 24 GB
+    graphics card", Step 2, "Verify-window route tail skip": an expert that
+    every token of the window ranks at the very tail of its top-10 (ranks
+    7, 8, 9 for the threshold 7) contributes almost nothing and is skipped;
+    an expert ranked below the threshold by at least one token, or resident
+    in the fast tier (`hot`), is kept.  Reading taken: a pair (t, j) is left
+    out when j >= rank, its expert is not hot, and no pair of the window keeps
+    that expert at a rank below the threshold; the kept pairs keep their
+    weights.  rank 0 leaves nothing out.
+
+    ids [T][k] int -> bool [T][k], True for a pair left out.
+    """
+    ids = np.asarray(ids)
+    T, k = ids.shape
+    hot = set() if hot is None else set(int(e) for e in hot)
+    out = np.zeros((T, k), bool)
+    if rank <= 0:
+        return out
+    early = set()
+    for t in range(T):
+        for j in range(min(rank, k)):
+            early.add(int(ids[t, j]))
+    for t in range(T):
+        for j in range(rank, k):
+            e = int(ids[t, j])
+            out[t, j] = e not in early and e not in hot
+    return out

@@ -210,3 +210,84 @@ def test_long_stack_stays_finite(moe):
     x0 = synth.bf16_bits_to_f32(synth.activations(12, 2, 256))
     x, ids, w = run_fused(layers, x0, 2)
     assert np.all(np.isfinite(x))
+
+
+# ---------------------------------------------------------------- options: route-tail skip, hot-expert hints
+
+def run_fused_ex(layers, x0, k, tail=0, hot=None):
+    T, H = x0.shape
+    s = layers[0].s
+    x = torch.from_numpy(x0.copy()).to(DEV)
+    n = len(layers)
+    ids = torch.empty(n, T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(n, T, k, dtype=torch.float32, device=DEV)
+    nb = m.moe_decode_workspace_size(T, s.H, s.I, s.E, k, s.Is)
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.moe_decode_forward_ex([L.weights() for L in layers], x, T, k, m.RMS_EPS, tail, hot, ids, w, ws, nb, st)
+    assert m.moe_check_status(st) == 0, m.moe_last_error()
+    return x.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
+
+
+def hot_masks(n_layers, E, hot_sets):
+    words = (E + 31) // 32
+    mask = np.zeros((n_layers, words), np.uint32)
+    for l, hs in enumerate(hot_sets):
+        for e in hs:
+            mask[l, e // 32] |= np.uint32(1 << (e % 32))
+    return torch.from_numpy(mask.view(np.int32)).to(DEV)
+
+
+@pytest.mark.parametrize("T,rank", [(1, 7), (4, 7), (4, 3), (3, 1)])
+def test_route_tail_skip_matches_oracle(moe, T, rank):
+    """One layer with the skip: the oracle's layer with the left-out pairs' weights set to zero."""
+    layers, hosts = tiny_stack(1, k=10, E=24)
+    x0 = synth.bf16_bits_to_f32(synth.verify_window(13 + T, T, 256))
+    x1, ids, w = run_fused_ex(layers, x0, 10, tail=rank)
+    drop = oracle.route_tail_skip(ids[0], rank)
+    if T == 1:
+        assert drop.sum() == 10 - rank
+    assert drop.any()
+    weff = np.where(drop, 0.0, w[0].astype(np.float64))
+    want = oracle_stack(2, x0, ids, weff[None], hosts)
+    assert rel_l2(x1 - x0, want - x0) <= 2e-5
+    # and the exact layer differs by the left-out terms
+    exact, ids2, _ = run_fused(layers, x0, 10)
+    assert np.array_equal(ids, ids2)
+    assert not np.array_equal(exact, x1)
+
+
+def test_route_tail_skip_three_layers(moe):
+    layers, hosts = tiny_stack(3, k=10, E=24)
+    x0 = synth.bf16_bits_to_f32(synth.verify_window(17, 4, 256))
+    x3, ids, w = run_fused_ex(layers, x0, 10, tail=7)
+    weff = np.stack([np.where(oracle.route_tail_skip(ids[l], 7), 0.0, w[l].astype(np.float64)) for l in range(3)])
+    want = oracle_stack(2, x0, ids, weff, hosts)
+    assert rel_l2(x3 - x0, want - x0) <= 1e-4
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_options_off_and_hot_masks_keep_the_exact_bits(moe, T):
+    """route_tail_skip 0 or k leaves nothing out; hot-expert masks only add cache hints."""
+    layers, _ = tiny_stack(2, k=10, E=24)
+    x0 = synth.bf16_bits_to_f32(synth.verify_window(19, T, 256))
+    exact, ids, w = run_fused(layers, x0, 10)
+    rng = np.random.default_rng(T)
+    hot = hot_masks(2, 24, [rng.choice(24, 5, replace=False), rng.choice(24, 5, replace=False)])
+    for tail, hm in ((0, None), (10, None), (0, hot)):
+        got, gids, gw = run_fused_ex(layers, x0, 10, tail=tail, hot=hm)
+        assert np.array_equal(got.view(np.uint32), exact.view(np.uint32))
+        assert np.array_equal(gids, ids) and np.array_equal(gw.view(np.uint32), w.view(np.uint32))
+
+
+def test_route_tail_skip_keeps_hot_experts(moe):
+    layers, hosts = tiny_stack(1, k=10, E=24)
+    x0 = synth.bf16_bits_to_f32(synth.verify_window(23, 4, 256))
+    _, ids, _ = run_fused(layers, x0, 10)
+    tail_experts = sorted(set(ids[0][:, 7:].ravel().tolist()))
+    hot_set = tail_experts[:2]
+    x1, ids1, w1 = run_fused_ex(layers, x0, 10, tail=7, hot=hot_masks(1, 24, [hot_set]))
+    drop = oracle.route_tail_skip(ids1[0], 7, hot=hot_set)
+    weff = np.where(drop, 0.0, w1[0].astype(np.float64))
+    want = oracle_stack(2, x0, ids1, weff[None], hosts)
+    assert rel_l2(x1 - x0, want - x0) <= 2e-5

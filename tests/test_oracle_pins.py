@@ -440,3 +440,53 @@ def test_rms_norm_properties():
     np.testing.assert_allclose(oracle.rms_norm(x * np.float32(8.0), 0.0), y, rtol=1e-12)  # scale invariant
     ref = x.astype(np.float64) / np.sqrt((x.astype(np.float64) ** 2).mean(axis=1, keepdims=True) + 1e-6)
     np.testing.assert_allclose(oracle.rms_norm(x, 1e-6), ref, rtol=1e-13)
+
+
+# ---------------------------------------------------------------- route-tail skip
+# "How Strata runs a 125-billion-parameter model ...", Step 2, "Verify-window
+# route tail skip": experts every token of the window ranks 7..9 are skipped,
+# experts ranked 0..6 by at least one token and fast-tier ones are kept.
+
+def test_route_tail_skip_single_token_drops_ranks_7_to_9():
+    ids = np.array([[40, 41, 42, 43, 44, 45, 46, 47, 48, 49]])
+    got = oracle.route_tail_skip(ids, 7)
+    assert got.tolist() == [[False] * 7 + [True] * 3]
+
+
+def test_route_tail_skip_keeps_an_expert_another_token_ranks_early():
+    # token 1 ranks expert 9 first: token 0's rank-9 pair is kept; expert 8 is
+    # at the tail for both tokens: both its pairs go; expert 7 only in token 0's tail
+    ids = np.array([[0, 1, 2, 3, 4, 5, 6, 7, 8, 9],
+                    [9, 10, 11, 12, 13, 14, 15, 16, 8, 17]])
+    got = oracle.route_tail_skip(ids, 7)
+    want = np.zeros((2, 10), bool)
+    want[0, 7] = want[0, 8] = True   # 7 and 8 nobody ranks early; 9 is kept
+    want[1, 7] = want[1, 8] = want[1, 9] = True  # 16, 8, 17
+    assert np.array_equal(got, want)
+
+
+def test_route_tail_skip_hot_experts_and_off():
+    ids = np.array([[0, 1, 2, 3, 4, 5, 6, 7, 8, 9]])
+    assert oracle.route_tail_skip(ids, 7, hot=[8]).tolist() == [[False] * 7 + [True, False, True]]
+    assert not oracle.route_tail_skip(ids, 0).any()
+    assert not oracle.route_tail_skip(ids, 10).any()
+    # a threshold of 1 keeps only what some token ranks first
+    ids2 = np.array([[3, 1], [1, 3]])
+    assert not oracle.route_tail_skip(ids2, 1).any()
+    assert oracle.route_tail_skip(np.array([[3, 1], [2, 4]]), 1).tolist() == [[False, True], [False, True]]
+
+
+def test_route_tail_skip_brute_force_definition():
+    """Against the definition enumerated over every (token, slot) of random windows."""
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        T, k, E = rng.integers(1, 5), rng.integers(1, 11), rng.integers(10, 30)
+        ids = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+        r = int(rng.integers(0, k + 1))
+        hot = set(rng.choice(E, 3, replace=False).tolist())
+        got = oracle.route_tail_skip(ids, r, hot)
+        for t in range(T):
+            for j in range(k):
+                e = ids[t, j]
+                early = any(ids[tt, jj] == e for tt in range(T) for jj in range(k) if jj < r)
+                assert got[t, j] == (r > 0 and j >= r and e not in hot and not early)
