@@ -22,6 +22,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "moe_gb300.h")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_NONFINITE, MOE_ERR_BOUNDS = 4, 5, 6, 7
 MOE_ERR_RANGE = 8
+MOE_ID_NOT_LOCAL = -1
 MOE_F32, MOE_BF16 = 0, 1
 MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL = 0, 1, 2
 RMS_EPS = 1e-6  # normalisation in front of each stacked layer
@@ -85,6 +86,7 @@ _SIGS = {
     "moe_router_topk": [_P, _I32, _I32, _P, _P, _I32, _I32, _P, _P, _P, _P, _SZ, _P, _P],
     "moe_topk_from_logits": [_P, _I32, _I32, _I32, _P, _P, _P, _P],
     "moe_permute_workspace_size": [_I32, _I32, _I32, _PSZ],
+    "moe_shard_ids": [_P, _I64, _I32, _I32, _P, _P],
     "moe_permute": [_P, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P, _P],
     "moe_permute_noalloc": [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P],
     "moe_expert_forward_workspace_size": [ctypes.POINTER(moe_expert_arena), _I32, _I32, _I32, _PSZ],
@@ -235,6 +237,11 @@ def moe_permute_workspace_size(T, k, E):
 def moe_permute(ids, T, k, E, offsets, perm, inv_perm, ws=None, ws_bytes=0, dev_status=None, stream=None):
     _check(lib().moe_permute(_ptr(ids), T, k, E, _ptr(offsets), _ptr(perm), _ptr(inv_perm), _ptr(ws), ws_bytes,
                              _ptr(dev_status), _stream(stream)), "moe_permute")
+
+
+def moe_shard_ids(ids, n, e0, e_count, local_ids, stream=None):
+    """ids of the shard holding experts [e0, e0 + e_count): local id, or MOE_ID_NOT_LOCAL for other shards."""
+    _check(lib().moe_shard_ids(_ptr(ids), n, e0, e_count, _ptr(local_ids), _stream(stream)), "moe_shard_ids")
 
 
 def moe_permute_noalloc(ids, T, k, E, offsets, perm, inv_perm, dev_status=None, stream=None):

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t *__re
     for (int f = tid; f < n; f += blockDim.x) {
         int id = ids[f];
         if (id >= 0 && id < E) atomicAdd(&cnt[id], 1);
-        else set_status(status, MOE_ERR_BOUNDS);
+        else if (id != MOE_ID_NOT_LOCAL) set_status(status, MOE_ERR_BOUNDS);
     }
     __syncthreads();
     int v = tid < E ? cnt[tid] : 0;
@@ -111,7 +111,7 @@ __global__ void permute_count_kernel(const int32_t *__restrict__ ids, int64_t n,
     for (int64_t f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
         int id = ids[f];
         if (id >= 0 && id < E) atomicAdd(&h[id], 1);
-        else set_status(status, MOE_ERR_BOUNDS);
+        else if (id != MOE_ID_NOT_LOCAL) set_status(status, MOE_ERR_BOUNDS);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) counts[(int64_t)blockIdx.x * E + e] = h[e];
@@ -156,9 +156,32 @@ __global__ void permute_place_kernel(const int32_t *__restrict__ ids, int64_t n,
 
 static int64_t n_chunks_for(int64_t n) { return (n + kPermChunk - 1) / kPermChunk; }
 
+// local[i] = ids[i] - e0 for ids in [e0, e0 + e_count), MOE_ID_NOT_LOCAL otherwise.
+__global__ void shard_ids_kernel(const int32_t *__restrict__ ids, int64_t n, int e0, int e_count,
+                                 int32_t *__restrict__ local)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int id = ids[i];
+        local[i] = (id >= e0 && id - e0 < e_count) ? id - e0 : MOE_ID_NOT_LOCAL;
+    }
+}
+
 }  // namespace moe
 
 using namespace moe;
+
+extern "C" moe_status moe_shard_ids(const int32_t *ids, int64_t n, int e0, int e_count, int32_t *local_ids,
+                                    moe_stream_t stream)
+{
+    MOE_REQUIRE(n >= 0, "n must be >= 0");
+    MOE_REQUIRE(e0 >= 0 && e_count >= 1 && e_count <= 1024, "e0 >= 0 and 1 <= e_count <= 1024 (got %d, %d)", e0,
+                e_count);
+    if (n == 0) return MOE_OK;
+    MOE_REQUIRE(ids && local_ids, "NULL pointer");
+    const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)sm_count() * 8);
+    shard_ids_kernel<<<(unsigned)blocks, 256, 0, to_cuda(stream)>>>(ids, n, e0, e_count, local_ids);
+    return check_launch("shard_ids");
+}
 
 extern "C" moe_status moe_permute_workspace_size(int T, int k, int E, size_t *bytes)
 {

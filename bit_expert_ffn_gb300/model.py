@@ -20,8 +20,8 @@ import torch
 
 from . import (MOE_F32, MOE_PATH_AUTO, RMS_EPS, load, make_arena, moe_expert_forward, moe_expert_forward_workspace_size,
                moe_f32_to_bf16, moe_pack_experts, moe_permute, moe_permute_workspace_size, moe_rms_norm_bf16,
-               moe_router_topk, moe_router_workspace_size, moe_shared_expert, moe_shared_expert_workspace_size, synth,
-               synth_lib)
+               moe_router_topk, moe_router_workspace_size, moe_shard_ids, moe_shared_expert,
+               moe_shared_expert_workspace_size, synth, synth_lib)
 
 
 def _u16(a: np.ndarray, dev) -> torch.Tensor:
@@ -130,8 +130,9 @@ class MoeLayer:
         sc = _u16(np.asarray(scales, np.uint16).reshape(-1), self.dev)
         moe_pack_experts(self.s.bits, E, rows, cols, c, sc, pc, ps, self.status)
 
-    def fill_device(self, seed: int, layer: int, zipf_s: float = 0.0, chunk_experts: int = 64):
-        """Draw every tensor of the layer on the device with the seeded generator and pack it."""
+    def fill_device(self, seed: int, layer: int, zipf_s: float = 0.0, chunk_experts: int = 64, expert_base: int = 0):
+        """Draw every tensor of the layer on the device with the seeded generator and pack it.  With
+        expert_base > 0 the arena holds experts expert_base .. expert_base + E - 1 of the layer (a shard)."""
         s = self.s
         H, I, E, bits = s.H, s.I, s.E, s.bits
         for mat, (rows, cols, tag_c, tag_s, pc, ps) in enumerate((
@@ -145,7 +146,7 @@ class MoeLayer:
             for e0 in range(0, E, chunk_experts):
                 ne = min(chunk_experts, E - e0)
                 for j in range(ne):
-                    e = e0 + j
+                    e = expert_base + e0 + j
                     device_codes(synth.stream_key(seed, tag_c, layer, e), per, bits, tmp_c[j * per:(j + 1) * per])
                     device_normal(synth.stream_key(seed, tag_s, layer, e), nsc, 0.02, 2, tmp_s[j * nsc:(j + 1) * nsc])
                 moe_pack_experts(bits, ne, rows, cols, tmp_c, tmp_s, pc[e0 * cb:(e0 + ne) * cb],
@@ -202,6 +203,7 @@ class StepBuffers:
         self.ids = torch.empty(max(T, 1), k, dtype=torch.int32, device=d)
         self.w = torch.empty(max(T, 1), k, dtype=torch.float32, device=d)
         self.offsets = torch.empty(E + 1, dtype=torch.int32, device=d)
+        self.local_ids = torch.empty(max(T, 1), k, dtype=torch.int32, device=d)  # a shard's ids (expert parallelism)
         self.perm = torch.empty(max(T * k, 1), dtype=torch.int32, device=d)
         self.inv = torch.empty(max(T * k, 1), dtype=torch.int32, device=d)
 
@@ -220,3 +222,75 @@ def _pk(bits, rows, cols):
     from . import moe_packed_size
 
     return moe_packed_size(bits, rows, cols)
+
+
+# ---------------------------------------------------------------- expert parallelism
+
+def expert_shards(E: int, world: int):
+    """Contiguous, balanced expert ranges [e0, e1) of a layer for `world` shards (the first E % world
+    shards hold one expert more); together they cover [0, E) once."""
+    if world < 1 or world > E:
+        raise ValueError(f"cannot split {E} experts over {world} shards")
+    base, extra = divmod(E, world)
+    out, e0 = [], 0
+    for r in range(world):
+        n = base + (1 if r < extra else 0)
+        out.append((e0, e0 + n))
+        e0 += n
+    return out
+
+
+def ep_all_reduce(out: torch.Tensor, group=None):
+    """Sum a shard's partial layer output over the ranks of `group` in place (NCCL on GPUs, gloo on CPU)."""
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size(group) > 1:
+        dist.all_reduce(out, op=dist.ReduceOp.SUM, group=group)
+    return out
+
+
+class ShardedMoeLayer:
+    """One layer's experts [e0, e1) on this rank (expert parallelism), the router replicated on every rank and
+    the shared expert on rank 0 only.  forward() adds this rank's part of the layer to `out`; after
+    ep_all_reduce over the ranks every rank holds the whole layer.  Activations are replicated (every rank
+    has every token), so no dispatch of token rows is needed: each rank computes the pairs routed to its
+    experts and the reduction combines them."""
+
+    def __init__(self, shape: LayerShape, rank: int, world: int, dev="cuda"):
+        self.s = shape
+        self.rank, self.world = rank, world
+        self.e0, self.e1 = expert_shards(shape.E, world)[rank]
+        local = LayerShape(H=shape.H, I=shape.I, E=self.e1 - self.e0, k=shape.k, Is=shape.Is, bits=shape.bits)
+        self.local = MoeLayer(local, dev)
+        self.dev = self.local.dev
+        self.router_w = torch.empty(shape.E, shape.H, dtype=torch.float32, device=self.dev)
+        self.router_b = torch.zeros(shape.E, dtype=torch.float32, device=self.dev)
+        self.status = self.local.status
+
+    def fill_device(self, seed: int, layer: int, zipf_s: float = 0.0):
+        s = self.s
+        self.local.fill_device(seed, layer, zipf_s, expert_base=self.e0)
+        device_normal(synth.stream_key(seed, synth.TAG_ROUTER, layer), s.E * s.H, 0.02, 0, self.router_w)
+        self.router_b.copy_(torch.from_numpy(synth.zipf_bias(seed, layer, s.E, zipf_s)))
+        if self.rank != 0:
+            self.local.shared = None
+
+    def forward(self, x_bf16, T, out_f32, ws: Workspace, bufs: "StepBuffers", path=MOE_PATH_AUTO):
+        """out_f32 += (rank 0: S(x)) + sum over this rank's pairs of w_j FFN_j(x), through library calls only."""
+        s, L = self.s, self.local
+        El = self.e1 - self.e0
+        rws = moe_router_workspace_size(T, s.H, s.E, True)
+        pws = moe_permute_workspace_size(T, s.k, El)
+        ews = moe_expert_forward_workspace_size(L.arena, T, s.k, path)
+        sws = moe_shared_expert_workspace_size(s.H, s.Is, T) if L.shared is not None else 0
+        buf = ws.get(max(rws, pws, ews, sws))
+        moe_router_topk(x_bf16, T, s.H, self.router_w, self.router_b, s.E, s.k, bufs.logits, bufs.ids, bufs.w,
+                        buf if rws else None, rws, dev_status=self.status)
+        moe_shard_ids(bufs.ids, T * s.k, self.e0, El, bufs.local_ids)
+        moe_permute(bufs.local_ids, T, s.k, El, bufs.offsets, bufs.perm, bufs.inv, buf if pws else None, pws,
+                    dev_status=self.status)
+        if L.shared is not None:
+            moe_shared_expert(*L.shared, s.H, s.Is, x_bf16, T, out_f32, MOE_F32, True, buf, sws,
+                              dev_status=self.status)
+        moe_expert_forward(L.arena, x_bf16, T, bufs.local_ids, bufs.w, s.k, bufs.offsets, bufs.perm, bufs.inv,
+                           out_f32, MOE_F32, True, path, buf, ews, dev_status=self.status)

@@ -225,14 +225,35 @@ moe_status moe_topk_from_logits(const float *logits, int T, int E, int k, int32_
  *   offsets [E+1]: offsets[e] = pairs with id < e, offsets[E] = T*k;
  *   perm    [T*k]: perm[p] = t*k + j of the p-th pair in (expert, t*k+j) order;
  *   inv_perm[T*k]: inv_perm[perm[p]] = p.
- * Bit-exact and deterministic.  An id outside [0, E) sets *dev_status to
- * MOE_ERR_BOUNDS; that pair is left out (offsets then count only valid
- * pairs, its inv_perm entry is -1 and perm entries past offsets[E] are -1).
+ * Bit-exact and deterministic.  An id of MOE_ID_NOT_LOCAL (-1) marks a pair
+ * that another expert shard computes (see moe_shard_ids): it is left out
+ * without an error.  Any other id outside [0, E) sets *dev_status to
+ * MOE_ERR_BOUNDS and is left out the same way.  A left-out pair is not
+ * counted in offsets, its inv_perm entry is -1 and perm entries past
+ * offsets[E] are -1; moe_expert_forward skips such pairs (they add nothing
+ * to their token's output).
  * The pages group the tokens of a verify window that share an expert
  * ("Strata serves a 125B MoE ...", section "Six billion active parameters
  * per token").
  */
 moe_status moe_permute_workspace_size(int T, int k, int E, size_t *bytes);
+
+/* The id of a (token, slot) pair whose expert lives on another shard. */
+#define MOE_ID_NOT_LOCAL (-1)
+
+/*
+ * Expert parallelism: the ids of the shard that holds experts
+ * [e0, e0 + e_count) of a layer.  local_ids[i] = ids[i] - e0 for ids in that
+ * range, MOE_ID_NOT_LOCAL otherwise (n ids, device).  A shard then runs
+ * moe_permute(local_ids, ..., E = e_count) and moe_expert_forward on an arena
+ * of its e_count experts with the full routing weights: its output is the sum
+ * of its own experts' terms, and the sum of all shards' outputs (plus the
+ * shared expert once) is the layer.  The pages run the layer on one GPU;
+ * sharding the 512 experts of a layer over several GPUs is this library's
+ * extension for GPUs that serve the whole model from memory.
+ */
+moe_status moe_shard_ids(const int32_t *ids, int64_t n, int e0, int e_count, int32_t *local_ids,
+                         moe_stream_t stream);
 moe_status moe_permute(const int32_t *ids, int T, int k, int E, int32_t *offsets, int32_t *perm,
                        int32_t *inv_perm, void *ws, size_t ws_bytes, int32_t *dev_status,
                        moe_stream_t stream);

@@ -192,7 +192,7 @@ def test_permute_equals_oracle(moe, T, k, E):
 
 
 def test_permute_bad_id_reports_bounds(moe):
-    ids = np.array([[0, 3], [9, 1], [2, -1]], np.int32)
+    ids = np.array([[0, 3], [9, 1], [2, -3]], np.int32)
     off = torch.empty(6, dtype=torch.int32, device=DEV)
     perm = torch.empty(6, dtype=torch.int32, device=DEV)
     inv = torch.empty(6, dtype=torch.int32, device=DEV)
