@@ -213,16 +213,20 @@ __device__ __forceinline__ uint64_t policy_evict_first()
 // A weight copy: with hot-expert masks given, marked experts' weights carry an
 // L2 evict-last hint (they stay in L2 from one decode step to the next) and
 // every other weight an evict-first hint; without masks, a plain copy.
+// OPT: the kernel variant that honours the options (route-tail skip, hot
+// masks); the plain variant compiles them away.
+template <bool OPT>
 __device__ __forceinline__ void weight_g2s(const Args &a, bool hot, void *dst, const void *src, uint32_t bytes,
                                            uint64_t *bar)
 {
-    if (a.hot == nullptr) bulk_g2s(dst, src, bytes, bar);
+    if (!OPT || a.hot == nullptr) bulk_g2s(dst, src, bytes, bar);
     else bulk_g2s_hint(dst, src, bytes, bar, hot ? policy_evict_last() : policy_evict_first());
 }
 
+template <bool OPT>
 __device__ __forceinline__ bool is_hot(const Args &a, int l, int e)
 {
-    return a.hot != nullptr && ((a.hot[(size_t)l * ((a.E + 31) >> 5) + (e >> 5)] >> (e & 31)) & 1u);
+    return OPT && a.hot != nullptr && ((a.hot[(size_t)l * ((a.E + 31) >> 5) + (e >> 5)] >> (e & 31)) & 1u);
 }
 
 __device__ __forceinline__ bool aborted(const Args &a) { return (ld_acquire(a.cnt + 2) & kAbort) != 0; }
@@ -494,12 +498,15 @@ __device__ void topk_weights(Routing &R, int t, int k, bool nan_token)
 // Sort the T*k pairs by (key, flat index) and cut the kept ones (key below
 // INT32_MAX) into groups of one expert each (one warp; n <= 64 pairs, two per
 // lane, ranks by shuffles).  The pairs left out sort after every kept one.
+template <bool OPT>
 __device__ void build_groups(Routing &R, int n)
 {
     const int lane = lane_id();
-    const int e0 = lane < n ? R.key[lane] : INT32_MAX, e1 = lane + 32 < n ? R.key[lane + 32] : INT32_MAX;
-    const int nk = __popc(__ballot_sync(0xffffffffu, lane < n && e0 != INT32_MAX)) +
-                   __popc(__ballot_sync(0xffffffffu, lane + 32 < n && e1 != INT32_MAX));
+    const int *key = OPT ? R.key : R.ids;
+    const int e0 = lane < n ? key[lane] : INT32_MAX, e1 = lane + 32 < n ? key[lane + 32] : INT32_MAX;
+    const int nk = OPT ? __popc(__ballot_sync(0xffffffffu, lane < n && e0 != INT32_MAX)) +
+                             __popc(__ballot_sync(0xffffffffu, lane + 32 < n && e1 != INT32_MAX))
+                       : n;
     int r0 = 0, r1 = 0;
     const int n0 = n < 32 ? n : 32;
 #pragma unroll 4
@@ -532,8 +539,8 @@ __device__ void build_groups(Routing &R, int n)
         bool start = false;
         int e = 0;
         if (p < nk) {
-            e = R.key[R.perm[p]];
-            start = p == 0 || R.key[R.perm[p - 1]] != e;
+            e = key[R.perm[p]];
+            start = p == 0 || key[R.perm[p - 1]] != e;
         }
         const unsigned m = __ballot_sync(0xffffffffu, start);
         if (start) {
@@ -563,7 +570,7 @@ __device__ void mark_pairs(const Args &a, Routing &R, int n, int k, int l)
     for (int i = lane_id(); i < n; i += 32) {
         const int e = R.ids[i];
         bool drop = false;
-        if (a.tail_skip > 0 && i % k >= a.tail_skip && !is_hot(a, l, e)) {
+        if (a.tail_skip > 0 && i % k >= a.tail_skip && !is_hot<true>(a, l, e)) {
             drop = true;
 #pragma unroll 1
             for (int q = 0; q < n; q++)
@@ -856,6 +863,7 @@ __device__ __forceinline__ void split_range(int n, int c, int G, int &lo, int &h
 }
 
 // Router rows and shared gate/up rows of layer L into region r1 (one thread).
+template <bool OPT>
 __device__ void issue_a(const Args &a, const Plan &P, const Layer &L, char *r1, uint64_t *bar)
 {
     int r0, rh, q0, qh;
@@ -864,24 +872,26 @@ __device__ void issue_a(const Args &a, const Plan &P, const Layer &L, char *r1, 
     if (!L.swg) qh = q0;
     uint32_t rb = (uint32_t)(rh - r0) * a.H * 4u, qb = (uint32_t)(qh - q0) * a.H * 2u;
     tc::mbar_arrive_expect_tx(bar, rb + 2 * qb);
-    if (rb) weight_g2s(a, false, r1, L.w_router + (size_t)r0 * a.H, rb, bar);
+    if (rb) weight_g2s<OPT>(a, false, r1, L.w_router + (size_t)r0 * a.H, rb, bar);
     if (qb) {
-        weight_g2s(a, false, r1 + rb, L.swg + (size_t)q0 * a.H, qb, bar);
-        weight_g2s(a, false, r1 + rb + qb, L.swu + (size_t)q0 * a.H, qb, bar);
+        weight_g2s<OPT>(a, false, r1 + rb, L.swg + (size_t)q0 * a.H, qb, bar);
+        weight_g2s<OPT>(a, false, r1 + rb + qb, L.swu + (size_t)q0 * a.H, qb, bar);
     }
 }
 
 // Shared down rows [o0, o0 + nrows) of layer L into region r3 (one thread).
+template <bool OPT>
 __device__ void issue_s(const Args &a, const Layer &L, char *r3, int o0, int nrows, uint64_t *bar)
 {
     uint32_t b = (L.swg && nrows > 0) ? (uint32_t)nrows * a.Is * 2u : 0u;
     tc::mbar_arrive_expect_tx(bar, b);
-    if (b) weight_g2s(a, false, r3, L.swd + (size_t)o0 * a.Is, b, bar);
+    if (b) weight_g2s<OPT>(a, false, r3, L.swd + (size_t)o0 * a.Is, b, bar);
 }
 
 // Unit u (group u / (I/16), rows 16 rt .. 16 rt + 15 of gate and of up) into
 // a unit slot, as four contiguous copies: gate codes, up codes (16 rows each),
 // gate scales, up scales.  One thread.  l: the layer (for the hot-expert mask).
+template <bool OPT>
 __device__ void issue_unit(const Args &a, const Plan &P, const Layer &L, const Routing &R, int l, int u, char *slot,
                            uint64_t *bar)
 {
@@ -891,25 +901,26 @@ __device__ void issue_unit(const Args &a, const Plan &P, const Layer &L, const R
     const uint32_t cb = 16u * P.cb_gu, sb = 16u * P.sb_gu;
     const char *sc = reinterpret_cast<const char *>(L.gu_scales);
     tc::fence_proxy_async_smem();
-    const bool hot = is_hot(a, l, e);
+    const bool hot = is_hot<OPT>(a, l, e);
     tc::mbar_arrive_expect_tx(bar, 2 * (cb + sb));
-    weight_g2s(a, hot, slot, L.gu_codes + rg * P.cb_gu, cb, bar);
-    weight_g2s(a, hot, slot + cb, L.gu_codes + ru * P.cb_gu, cb, bar);
-    weight_g2s(a, hot, slot + 2 * cb, sc + rg * P.sb_gu, sb, bar);
-    weight_g2s(a, hot, slot + 2 * cb + sb, sc + ru * P.sb_gu, sb, bar);
+    weight_g2s<OPT>(a, hot, slot, L.gu_codes + rg * P.cb_gu, cb, bar);
+    weight_g2s<OPT>(a, hot, slot + cb, L.gu_codes + ru * P.cb_gu, cb, bar);
+    weight_g2s<OPT>(a, hot, slot + 2 * cb, sc + rg * P.sb_gu, sb, bar);
+    weight_g2s<OPT>(a, hot, slot + 2 * cb + sb, sc + ru * P.sb_gu, sb, bar);
 }
 
 // Down rows [o0, o0 + nrows) of group g's expert into a down slot: the code
 // rows (contiguous) and their scales, two copies.  One thread.
+template <bool OPT>
 __device__ void issue_down(const Args &a, const Plan &P, const Layer &L, const Routing &R, int l, int g, int o0,
                            int nrows, char *slot, uint64_t *bar)
 {
     const size_t row0 = (size_t)R.g_e[g] * a.H + o0;
-    const bool hot = is_hot(a, l, R.g_e[g]);
+    const bool hot = is_hot<OPT>(a, l, R.g_e[g]);
     tc::fence_proxy_async_smem();
     tc::mbar_arrive_expect_tx(bar, (uint32_t)nrows * (P.cb_d + P.sb_d));
-    weight_g2s(a, hot, slot, L.d_codes + row0 * P.cb_d, (uint32_t)nrows * P.cb_d, bar);
-    weight_g2s(a, hot, slot + 16 * P.cb_d, reinterpret_cast<const char *>(L.d_scales) + row0 * P.sb_d,
+    weight_g2s<OPT>(a, hot, slot, L.d_codes + row0 * P.cb_d, (uint32_t)nrows * P.cb_d, bar);
+    weight_g2s<OPT>(a, hot, slot + 16 * P.cb_d, reinterpret_cast<const char *>(L.d_scales) + row0 * P.sb_d,
                (uint32_t)nrows * P.sb_d, bar);
 }
 
@@ -953,7 +964,7 @@ __device__ __forceinline__ void finalize_unit(const Args &a, const float *pslot,
 
 // ------------------------------------------------------------ the kernel
 
-template <int T, int BITS>
+template <int T, int BITS, bool OPT>
 __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __grid_constant__ Args a,
                                                                          const __grid_constant__ Plan P)
 {
@@ -999,8 +1010,8 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
         tc::mbar_init(&R.fullS, 1);
         tc::mbar_init(&R.fullH, 1);
         tc::fence_mbar_init();
-        issue_a(a, P, a.L[0], r1, &R.fullA);
-        issue_s(a, a.L[0], r3, o0, nrows, &R.fullS);
+        issue_a<OPT>(a, P, a.L[0], r1, &R.fullA);
+        issue_s<OPT>(a, a.L[0], r3, o0, nrows, &R.fullS);
         iss_a = 1;
         iss_s = 1;
         iss_h = 0;
@@ -1218,8 +1229,8 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
         if (warp < T) topk_weights(R, warp, k, (nan_mask >> warp) & 1u);
         __syncthreads();
         if (warp == 0) {
-            mark_pairs(a, R, T * k, k, l);
-            build_groups(R, T * k);
+            if constexpr (OPT) mark_pairs(a, R, T * k, k, l);
+            build_groups<OPT>(R, T * k);
             pair_tokens(R, T * k, k);
         }
         __syncthreads();
@@ -1236,11 +1247,11 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             const int nui = min(nu, P.nsu), ndi = nrows > 0 ? min(ng, P.nsd) : 0;
             for (int j = lane; j < nui + ndi; j += 32) {
                 if (j < nui) {
-                    issue_unit(a, P, L, R, l, u0 + j, r1 + (size_t)j * P.unitB, &R.fullU[j]);
+                    issue_unit<OPT>(a, P, L, R, l, u0 + j, r1 + (size_t)j * P.unitB, &R.fullU[j]);
                     iss_u[j]++;
                 } else {
                     const int g = j - nui;
-                    issue_down(a, P, L, R, l, g, o0, nrows, r2 + (size_t)g * P.downB, &R.fullD[g]);
+                    issue_down<OPT>(a, P, L, R, l, g, o0, nrows, r2 + (size_t)g * P.downB, &R.fullD[g]);
                     iss_d[g]++;
                 }
             }
@@ -1288,7 +1299,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                     if (lane == 0) {
                         atomicExch(&R.ucnt[slot], 0);
                         if (ul + P.nsu < nu) {
-                            issue_unit(a, P, L, R, l, u + P.nsu, r1 + (size_t)slot * P.unitB, &R.fullU[slot]);
+                            issue_unit<OPT>(a, P, L, R, l, u + P.nsu, r1 + (size_t)slot * P.unitB, &R.fullU[slot]);
                             iss_u[slot]++;
                         }
                     }
@@ -1323,7 +1334,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
             red_release_add(a.cnt + 0, 1u);
             if (l + 1 < a.n_layers) {
                 tc::fence_proxy_async_smem();
-                issue_a(a, P, a.L[l + 1], r1, &R.fullA);
+                issue_a<OPT>(a, P, a.L[l + 1], r1, &R.fullA);
                 iss_a++;
             }
         }
@@ -1415,7 +1426,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                     if (last && lane == 0) {
                         atomicExch(&R.dcnt[slot], 0);
                         if (g + P.nsd < ng) {
-                            issue_down(a, P, L, R, l, g + P.nsd, o0, nrows, r2 + (size_t)slot * P.downB, &R.fullD[slot]);
+                            issue_down<OPT>(a, P, L, R, l, g + P.nsd, o0, nrows, r2 + (size_t)slot * P.downB, &R.fullD[slot]);
                             iss_d[slot]++;
                         }
                     }
@@ -1435,7 +1446,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
         MOE_TRACE(10);
         if (tid == 0 && l + 1 < a.n_layers) {  // the shared down rows are consumed: fetch the next layer's
             tc::fence_proxy_async_smem();
-            issue_s(a, a.L[l + 1], r3, o0, nrows, &R.fullS);
+            issue_s<OPT>(a, a.L[l + 1], r3, o0, nrows, &R.fullS);
             iss_s++;
         }
         // ---- combine in slot order, residual update, x_{l+1} out
@@ -1457,7 +1468,7 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                 yj[j] = 0.f;
                 if (j < k) {
                     wj[j] = R.w[t * k + j];
-                    if (R.key[t * k + j] != INT32_MAX) yj[j] = pd[(size_t)R.inv[t * k + j] * NSD2 * 16 + rr];
+                    if (!OPT || R.key[t * k + j] != INT32_MAX) yj[j] = pd[(size_t)R.inv[t * k + j] * NSD2 * 16 + rr];
                 }
             }
             float sum = 0.f;
@@ -1491,31 +1502,31 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
 
 // ------------------------------------------------------------ host side
 
-template <int T, int BITS>
+template <int T, int BITS, bool OPT>
 static cudaError_t launch(const Args &a, const Plan &P, int grid, cudaStream_t s)
 {
-    auto fn = decode_kernel<T, BITS>;
+    auto fn = decode_kernel<T, BITS, OPT>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, P.smem);
     if (e != cudaSuccess) return e;
     void *args[] = {const_cast<Args *>(&a), const_cast<Plan *>(&P)};
     return cudaLaunchCooperativeKernel((const void *)fn, dim3(grid), dim3(warps_for<T>() * 32), args, (size_t)P.smem, s);
 }
 
-template <int T, int BITS>
+template <int T, int BITS, bool OPT>
 static cudaError_t attributes(size_t *static_smem)
 {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, decode_kernel<T, BITS>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, decode_kernel<T, BITS, OPT>);
     if (e == cudaSuccess) *static_smem = fa.sharedSizeBytes;
     return e;
 }
 
-template <int T, int BITS>
+template <int T, int BITS, bool OPT>
 static cudaError_t occupancy(int *blocks, int smem)
 {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, BITS, OPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, decode_kernel<T, BITS>, warps_for<T>() * 32, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, decode_kernel<T, BITS, OPT>, warps_for<T>() * 32, smem);
 }
 
 struct Ws {
@@ -1695,16 +1706,25 @@ extern "C" moe_status moe_decode_forward_ex(const moe_layer_weights *layers, int
     a.status = dev_status;
     cudaError_t e = cudaSuccess;
     size_t static_smem = 0;
-#define MOE_F_DISPATCH(FN, ...)                       \
-    switch (T * 10 + bits) {                          \
-    case 12: e = FN<1, 2>(__VA_ARGS__); break;        \
-    case 13: e = FN<1, 3>(__VA_ARGS__); break;        \
-    case 22: e = FN<2, 2>(__VA_ARGS__); break;        \
-    case 23: e = FN<2, 3>(__VA_ARGS__); break;        \
-    case 32: e = FN<3, 2>(__VA_ARGS__); break;        \
-    case 33: e = FN<3, 3>(__VA_ARGS__); break;        \
-    case 42: e = FN<4, 2>(__VA_ARGS__); break;        \
-    default: e = FN<4, 3>(__VA_ARGS__); break;        \
+    const bool opt = tail_skip > 0 || hot != nullptr;
+#define MOE_F_DISPATCH(FN, ...)                                \
+    switch (T * 100 + bits * 10 + (opt ? 1 : 0)) {             \
+    case 120: e = FN<1, 2, false>(__VA_ARGS__); break;         \
+    case 121: e = FN<1, 2, true>(__VA_ARGS__); break;          \
+    case 130: e = FN<1, 3, false>(__VA_ARGS__); break;         \
+    case 131: e = FN<1, 3, true>(__VA_ARGS__); break;          \
+    case 220: e = FN<2, 2, false>(__VA_ARGS__); break;         \
+    case 221: e = FN<2, 2, true>(__VA_ARGS__); break;          \
+    case 230: e = FN<2, 3, false>(__VA_ARGS__); break;         \
+    case 231: e = FN<2, 3, true>(__VA_ARGS__); break;          \
+    case 320: e = FN<3, 2, false>(__VA_ARGS__); break;         \
+    case 321: e = FN<3, 2, true>(__VA_ARGS__); break;          \
+    case 330: e = FN<3, 3, false>(__VA_ARGS__); break;         \
+    case 331: e = FN<3, 3, true>(__VA_ARGS__); break;          \
+    case 420: e = FN<4, 2, false>(__VA_ARGS__); break;         \
+    case 421: e = FN<4, 2, true>(__VA_ARGS__); break;          \
+    case 430: e = FN<4, 3, false>(__VA_ARGS__); break;         \
+    default: e = FN<4, 3, true>(__VA_ARGS__); break;           \
     }
     MOE_F_DISPATCH(attributes, &static_smem)
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "decode kernel attributes: %s", cudaGetErrorString(e));
