@@ -821,6 +821,38 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_only_hot(local: int):
+    """Profiling aid: 3 plain 48-layer decode steps, then bench_decode_hot (16 steps that record the routing,
+    3 warm-up and 3 timed steps with the hot masks), so one capture holds launches of both variants."""
+    import torch
+
+    import bit_expert_ffn_gb300 as m
+    from bit_expert_ffn_gb300 import synth
+    from bit_expert_ffn_gb300.model import LayerShape, MoeLayer
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = m.load()
+    s = LayerShape()
+    layers = []
+    for layer in range(LAYERS):
+        L = MoeLayer(s, dev)
+        L.fill_device(seed=0, layer=layer, zipf_s=1.1)
+        layers.append(L)
+    descs = (m.moe_layer_weights * LAYERS)(*[L.weights() for L in layers])
+    X = torch.from_numpy(synth.bf16_bits_to_f32(synth.activations(0, 40, H)).reshape(40, H)).to(dev)
+    nb = m.moe_decode_workspace_size(1, H, I, E, K_TOP, IS)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    x = torch.empty(1, H, device=dev)
+    for i in range(3):
+        x.copy_(X[i:i + 1])
+        m.moe_decode_forward([L.weights() for L in layers], x, 1, K_TOP, m.RMS_EPS, None, None, ws, nb, st)
+    torch.cuda.synchronize()
+    r = bench_decode_hot(m, lib, descs, dev, torch.cuda.Stream(device=dev), X, steps=3, warmup=3)
+    print(json.dumps({k: v for k, v in r.items() if k != "workload"}), flush=True)
+
+
 def decode_traffic(path: str, n_layers: int):
     """The captured DRAM bytes of the timed launch, if they belong to the current source."""
     if path != "fused" or n_layers != LAYERS:
@@ -852,6 +884,8 @@ def main():
     ap.add_argument("--only-prefill", action="store_true", help="run only the 32K-prefill measurement (profiling)")
     ap.add_argument("--only-prefill3", action="store_true",
                     help="run only the 3-bit 4,096-token 48-layer prefill measurement (profiling)")
+    ap.add_argument("--only-hot", action="store_true",
+                    help="run only the decode with hot-expert L2 hints, after 3 plain decode steps (profiling)")
     ap.add_argument("--path", default="fused", choices=["fused", "modular"])
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers per step (48 is the workload; fewer only "
                     "for profiling captures)")
@@ -876,6 +910,9 @@ def main():
         torch.cuda.set_device(local)
         m.load()
         print(json.dumps(bench_prefill(m, torch.device("cuda", local))), flush=True)
+        return
+    if args.only_hot:
+        run_only_hot(local)
         return
     if args.impl == "reference":
         run_reference(args, world, rank)
