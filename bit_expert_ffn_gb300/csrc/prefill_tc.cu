@@ -600,38 +600,41 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
 }
 
 // x_g[p][16g + perm16(m)] = fp16(x[tok(p)][16g + m]) for the valid pairs; an
-// x without a finite fp16 sets MOE_ERR_RANGE.
+// x without a finite fp16 sets MOE_ERR_RANGE.  One warp per pair row (its
+// token looked up once), lanes over the row's 16-element groups, so loads and
+// stores are coalesced 16-byte accesses.
 __global__ void gather_x_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm,
                                 const int32_t *__restrict__ offsets, int E, int k, int H, uint16_t *__restrict__ xg,
                                 int32_t *__restrict__ status)
 {
     bool out_of_range = false;
-    int n = offsets[E];
-    int groups = H / 16;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)n * groups;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        int p = (int)(i / groups), g = (int)(i % groups);
-        int tok = perm[p] / k;
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)tok * H + 16 * g);
-        uint4 a0 = src[0], a1 = src[1];
-        uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        float f[16];
+    const int n = offsets[E];
+    const int groups = H / 16, lane = lane_id();
+    const int warps = (int)(gridDim.x * blockDim.x >> 5);
+    for (int p = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); p < n; p += warps) {
+        const int tok = perm[p] / k;
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)tok * H);
+        uint4 *dst = reinterpret_cast<uint4 *>(xg + (int64_t)p * H);
+        for (int g = lane; g < groups; g += 32) {
+            const uint4 a0 = __ldg(src + 2 * g), a1 = __ldg(src + 2 * g + 1);
+            const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            float f[16];
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-            f[2 * j] = __uint_as_float(w[j] << 16);
-            f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+            for (int j = 0; j < 8; j++) {
+                f[2 * j] = __uint_as_float(w[j] << 16);
+                f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+            }
+#pragma unroll
+            for (int mm = 0; mm < 16; mm++) out_of_range |= !(fabsf(f[mm]) < kF16Limit);
+            uint32_t o[8];
+#pragma unroll
+            for (int mm = 0; mm < 8; mm++) {
+                __half2 hv = __floats2half2_rn(f[mm], f[mm + 8]);
+                o[mm] = *reinterpret_cast<uint32_t *>(&hv);
+            }
+            dst[2 * g] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[2 * g + 1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
-        uint32_t o[8];
-#pragma unroll
-        for (int mm = 0; mm < 16; mm++) out_of_range |= !(fabsf(f[mm]) < kF16Limit);
-#pragma unroll
-        for (int mm = 0; mm < 8; mm++) {
-            __half2 hv = __floats2half2_rn(f[mm], f[mm + 8]);
-            o[mm] = *reinterpret_cast<uint32_t *>(&hv);
-        }
-        uint4 *dst = reinterpret_cast<uint4 *>(xg + (int64_t)p * H + 16 * g);
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
     if (out_of_range) set_status(status, MOE_ERR_RANGE);
 }
@@ -700,8 +703,7 @@ static moe_status run_tc(const moe_expert_arena &A, const uint16_t *x, int T, co
     tile_table_kernel<<<(A.E + 255) / 256, 256, 0, s>>>(offsets, d.mt_prefix, A.E, BT, d.table);
     st = check_launch("tile_table");
     if (st != MOE_OK) return st;
-    int64_t gthreads = n * (A.H / 16);
-    int gblocks = (int)std::min<int64_t>((gthreads + 255) / 256, (int64_t)sm_count() * 16);
+    int gblocks = (int)std::max<int64_t>(1, std::min<int64_t>((n + 7) / 8, (int64_t)sm_count() * 16));  // 8 rows per CTA
     gather_x_kernel<<<gblocks, 256, 0, s>>>(x, perm, offsets, A.E, k, A.H, d.xg, status);
     st = check_launch("gather_x");
     if (st != MOE_OK) return st;
