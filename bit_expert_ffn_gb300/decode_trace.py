@@ -25,7 +25,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 OUT = os.path.join(HERE, "_build_trace")
 PHASES = ["x gather", "rms + operands + router rows in", "router + shared rows", "logits in", "routing",
-          "copy issue + shared down", "gate/up", "h barrier", "staged h", "down items", "combine"]
+          "copy issue + gate/up", "h barrier", "shared-down rows in", "shared down + staged h", "down items",
+          "combine"]
 
 
 def build_traced() -> str:
