@@ -41,12 +41,13 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 LAYERS, H, E, I, K_TOP, IS = 48, 2048, 512, 768, 10, 768
-# DRAM bytes (read + write) of one 48-layer fused decode launch, median of five
-# launches of an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
+# DRAM bytes (read + write) of one 48-layer fused decode launch, median of the
+# 18 plain launches after the first in an ncu capture of `bench.py --only-hot`
+# (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid for the decode source whose code (comments and whitespace removed) has
 # this SHA-256 prefix; reported as null once that code changes, until it is
 # captured again.
-DECODE_TRAFFIC = (1_364_233_728, "7bfaf09ef7faa009")
+DECODE_TRAFFIC = (1_364_074_880, "8e1023583c484e5a")
 EXPERT_BYTES = 1_474_560
 ROUTER_BYTES = E * H * 4
 SHARED_BYTES = 3 * H * IS * 2
