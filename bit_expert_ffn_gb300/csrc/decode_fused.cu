@@ -55,8 +55,11 @@ constexpr int kRedV = 256;  // fixed number of partial sums in the RMS reduction
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr unsigned kAbort = 0x80000000u;
 
+// Sixteen warps per CTA whatever the number of tokens: with more than one
+// token the tensor-core items run one token at a time (the one-token item's
+// 128 registers), so the warps keep enough work in flight.
 template <int T>
-__host__ __device__ constexpr int warps_for() { return T == 1 ? 16 : 8; }
+__host__ __device__ constexpr int warps_for() { return 16; }
 
 // Phase trace for development builds, compiled out unless MOE_DECODE_TRACE is
 // defined: thread 0 of every CTA stamps the global timer at the phase
@@ -662,9 +665,9 @@ __device__ __forceinline__ void gu_load_ops(GuOps<T> &O, int s, int n, const int
 // column c sums block 8s+c.  Writes per-row partial sums (over the
 // super-tile's 8 blocks) of s_block * sum_i (c_i - mid) u_i to `pgu`
 // [2][NST][16][T].
-template <int T, int BITS>
+template <int T, int BITS, int TS = T>
 __device__ __forceinline__ void gu_item(const Plan &P, const char *slot, int mtx, int s, int n, const GuOps<T> &O,
-                                        int H, float *pgu)
+                                        int H, float *pgu, int t_off = 0)
 {
     const int lane = lane_id(), gid = lane >> 2, tig = lane & 3;
     const int cbr = P.cb_gu;
@@ -728,8 +731,8 @@ __device__ __forceinline__ void gu_item(const Plan &P, const char *slot, int mtx
             p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
             if (tig == 0) {
                 const int NST = H / 256;
-                pgu[((mtx * NST + s) * 16 + gid) * T + t] = p0;
-                pgu[((mtx * NST + s) * 16 + gid + 8) * T + t] = p1;
+                pgu[((mtx * NST + s) * 16 + gid) * TS + t_off + t] = p0;
+                pgu[((mtx * NST + s) * 16 + gid + 8) * TS + t_off + t] = p1;
             }
         }
     }
@@ -1281,9 +1284,19 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
 #pragma unroll
             for (int t = 0; t < kMaxT; t++) tok[t] = t < n ? R.tok_of[p0 + t] : 0;
             float *pslot = pgu + (size_t)slot * per_unit * 16 * T;
-            GuOps<T> ops;
-            gu_load_ops<T>(ops, s, n, tok, xp, H, P.xp_stride, zero16);
-            gu_item<T, BITS>(P, r1 + (size_t)slot * P.unitB, mtx, s, n, ops, H, pslot);
+            if constexpr (T == 1) {
+                GuOps<T> ops;
+                gu_load_ops<T>(ops, s, n, tok, xp, H, P.xp_stride, zero16);
+                gu_item<T, BITS>(P, r1 + (size_t)slot * P.unitB, mtx, s, n, ops, H, pslot);
+            } else {
+#pragma unroll 1
+                for (int t = 0; t < n; t++) {  // one token at a time: the one-token item's registers
+                    const int tk[kMaxT] = {tok[t], 0, 0, 0};
+                    GuOps<1> ops;
+                    gu_load_ops<1>(ops, s, 1, tk, xp, H, P.xp_stride, zero16);
+                    gu_item<1, BITS, T>(P, r1 + (size_t)slot * P.unitB, mtx, s, 1, ops, H, pslot, t);
+                }
+            }
             if (ring) {  // slots are reused: the last item of a unit finalises it and refills the slot
                 __syncwarp();
                 int last = 0;
@@ -1413,8 +1426,15 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                     fail = true;
                     break;
                 }
-                down_item<T, BITS>(P, r2 + (size_t)slot * P.downB, s2, R.g_n[g], R.g_p0[g], hop, P.stage_h != 0, zero16,
-                                   I, pd);
+                if constexpr (T == 1) {
+                    down_item<T, BITS>(P, r2 + (size_t)slot * P.downB, s2, R.g_n[g], R.g_p0[g], hop, P.stage_h != 0,
+                                       zero16, I, pd);
+                } else {
+#pragma unroll 1
+                    for (int t = 0; t < R.g_n[g]; t++)
+                        down_item<1, BITS>(P, r2 + (size_t)slot * P.downB, s2, 1, R.g_p0[g] + t, hop, P.stage_h != 0,
+                                           zero16, I, pd);
+                }
                 if (ng > P.nsd) {  // slots are reused: the last item of a group refills its slot
                     __syncwarp();
                     int last = 0;
