@@ -1230,8 +1230,9 @@ __global__ void __launch_bounds__(warps_for<T>() * 32, 1) decode_kernel(const __
                 nan_mask |= 1u << t;
         if (nan_mask && tid == 0) set_status(a.status, MOE_ERR_NONFINITE);
         if (warp < T) topk_weights(R, warp, k, (nan_mask >> warp) & 1u);
-        __syncthreads();
+        if (T > 1) __syncthreads();
         if (warp == 0) {
+            __syncwarp();
             if constexpr (OPT) mark_pairs(a, R, T * k, k, l);
             build_groups<OPT>(R, T * k);
             pair_tokens(R, T * k, k);
