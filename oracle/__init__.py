@@ -77,6 +77,22 @@ def _bind(path):
     L.oracle_moe_layer.restype = i32
     L.oracle_rms_norm.argtypes = [i32, i32, P, dbl, P]
     L.oracle_rms_norm.restype = None
+    L.oracle_fp16_round.argtypes = [dbl]
+    L.oracle_fp16_round.restype = dbl
+    L.oracle_e4m3_round.argtypes = [dbl]
+    L.oracle_e4m3_round.restype = dbl
+    L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    L.oracle_e4m3_to_double.restype = dbl
+    L.oracle_fp16_round_array.argtypes = [i64, P, P]
+    L.oracle_fp16_round_array.restype = None
+    L.oracle_e4m3_round_array.argtypes = [i64, P, P]
+    L.oracle_e4m3_round_array.restype = None
+    L.oracle_fp8_exponent.argtypes = [dbl]
+    L.oracle_fp8_exponent.restype = i32
+    L.oracle_expert_ffn_fp8.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, P]
+    L.oracle_expert_ffn_fp8.restype = i32
+    L.oracle_moe_layer_fp8.argtypes = L.oracle_moe_layer.argtypes
+    L.oracle_moe_layer_fp8.restype = i32
     return L
 
 
@@ -202,6 +218,44 @@ def expert_ffn(bits, gate_codes, gate_scales, up_codes, up_scales, down_codes, d
     return y
 
 
+def expert_ffn_fp8(bits, gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, x):
+    """The FP8 variant of one routed expert on one token (e4m3 operands with
+    power-of-two scales, see oracle_expert_ffn_fp8); x fp64 [H] -> y fp64 [H]."""
+    gc, uc, dc = (_c(a, np.uint8) for a in (gate_codes, up_codes, down_codes))
+    gs, us, ds = (_c(a, np.uint16) for a in (gate_scales, up_scales, down_scales))
+    I, H = gc.shape
+    x = _c(x, np.float64)
+    y = np.zeros(H, np.float64)
+    st = lib().oracle_expert_ffn_fp8(bits, H, I, _p(gc), _p(gs), _p(uc), _p(us), _p(dc), _p(ds), _p(x), _p(y))
+    if st != OK:
+        raise OracleError(st, "expert_ffn_fp8")
+    return y
+
+
+def fp16_round(v) -> np.ndarray:
+    """Nearest binary16 values (ties to even, past 65504 -> inf), as fp64."""
+    v = _c(np.atleast_1d(v), np.float64)
+    out = np.zeros_like(v)
+    lib().oracle_fp16_round_array(v.size, _p(v), _p(out))
+    return out
+
+
+def e4m3_round(v) -> np.ndarray:
+    """Nearest e4m3 values (ties to even, saturating at +-448), as fp64."""
+    v = _c(np.atleast_1d(v), np.float64)
+    out = np.zeros_like(v)
+    lib().oracle_e4m3_round_array(v.size, _p(v), _p(out))
+    return out
+
+
+def e4m3_to_double(b: int) -> float:
+    return lib().oracle_e4m3_to_double(int(b))
+
+
+def fp8_exponent(amax: float) -> int:
+    return int(lib().oracle_fp8_exponent(float(amax)))
+
+
 def shared_expert(wg, wu, wd, x):
     wg, wu, wd = (_c(a, np.uint16) for a in (wg, wu, wd))
     I, H = wg.shape
@@ -212,8 +266,9 @@ def shared_expert(wg, wu, wd, x):
 
 
 def moe_layer(bits, x_bf16, ids, w, gate_codes, gate_scales, up_codes, up_scales, down_codes,
-              down_scales, shared=None):
-    """Layer output fp64 [T][H] for given routing.  Arena arrays are [E][...] logical codes."""
+              down_scales, shared=None, fp8=False):
+    """Layer output fp64 [T][H] for given routing.  Arena arrays are [E][...] logical codes.
+    fp8=True runs the routed experts in their FP8 variant (oracle_expert_ffn_fp8)."""
     x_bf16 = _c(x_bf16, np.uint16)
     ids = _c(ids, np.int32)
     w = _c(w, np.float64)
@@ -228,9 +283,9 @@ def moe_layer(bits, x_bf16, ids, w, gate_codes, gate_scales, up_codes, up_scales
         swg, swu, swd = (_c(a, np.uint16) for a in shared)
         Is = swg.shape[0]
     out = np.zeros((T, H), np.float64)
-    st = lib().oracle_moe_layer(bits, T, H, I, E, k, _p(x_bf16), _p(ids), _p(w), _p(gc), _p(gs),
-                                _p(uc), _p(us), _p(dc), _p(ds), Is, _p(swg), _p(swu), _p(swd),
-                                _p(out))
+    fn = lib().oracle_moe_layer_fp8 if fp8 else lib().oracle_moe_layer
+    st = fn(bits, T, H, I, E, k, _p(x_bf16), _p(ids), _p(w), _p(gc), _p(gs),
+            _p(uc), _p(us), _p(dc), _p(ds), Is, _p(swg), _p(swu), _p(swd), _p(out))
     if st != OK:
         raise OracleError(st, "moe_layer")
     return out

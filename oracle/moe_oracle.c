@@ -38,7 +38,11 @@
  *   - routing: softmax over all E logits, keep the k largest logits (ties to
  *     the lower expert id), renormalise the kept probabilities to sum to 1;
  *   - the shared expert is added with weight 1 (no gate);
- *   - bit layout of the packed codes (the pages give none), see oracle_pack.
+ *   - bit layout of the packed codes (the pages give none), see oracle_pack;
+ *   - the FP8 variant of the routed experts (oracle_expert_ffn_fp8): the pages
+ *     run no 8-bit arithmetic, so its scheme -- e4m3 operands with one
+ *     power-of-two scale per weight row, per token and per h vector -- is this
+ *     library's own approximation of oracle_expert_ffn, stated there.
  */
 #include <math.h>
 #include <stdint.h>
@@ -80,6 +84,76 @@ double oracle_bf16_to_double(uint16_t b)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* Nearest binary16 value to v, ties to the even mantissa; magnitudes that
+ * round past the largest finite value (65504) give +-inf, NaN stays NaN. */
+double oracle_fp16_round(double v)
+{
+    if (isnan(v) || isinf(v) || v == 0.0) return v;
+    double a = fabs(v);
+    int e;
+    frexp(a, &e);                           /* a = m 2^e, 1/2 <= m < 1: floor(log2 a) = e - 1 */
+    int E = e - 1 < -14 ? -14 : e - 1;      /* below 2^-14 the spacing stays 2^-24 */
+    double q = ldexp(1.0, E - 10);          /* spacing of the values in [2^E, 2^(E+1)) */
+    double r = nearbyint(a / q) * q;        /* default rounding mode: nearest, ties to even */
+    if (r > 65504.0) r = INFINITY;
+    return copysign(r, v);
+}
+
+/*
+ * e4m3, the 8-bit float of the FP8 variant: sign, 4 exponent bits (bias 7),
+ * 3 mantissa bits.  Exponent field 0 holds the subnormals m * 2^-9; exponent
+ * field 15 with mantissa 7 is NaN; there are no infinities, so the largest
+ * finite magnitude is 1.75 * 2^8 = 448.
+ */
+double oracle_e4m3_to_double(uint8_t b)
+{
+    int sign = b >> 7, exp = (b >> 3) & 15, man = b & 7;
+    if (exp == 15 && man == 7) return NAN;
+    double v = exp == 0 ? ldexp((double)man, -9) : ldexp((double)(8 + man), exp - 10);
+    return sign ? -v : v;
+}
+
+/* Nearest e4m3 value to v, ties to the even mantissa; magnitudes past 448
+ * give +-448 (saturation), NaN stays NaN. */
+double oracle_e4m3_round(double v)
+{
+    if (isnan(v) || v == 0.0) return v;
+    if (isinf(v)) return copysign(448.0, v);
+    double a = fabs(v);
+    int e;
+    frexp(a, &e);
+    int E = e - 1 < -6 ? -6 : e - 1;        /* below 2^-6 the spacing stays 2^-9 */
+    double q = ldexp(1.0, E - 3);
+    double r = nearbyint(a / q) * q;
+    if (r > 448.0) r = 448.0;
+    return copysign(r, v);
+}
+
+void oracle_fp16_round_array(int64_t n, const double *in, double *out)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_fp16_round(in[i]);
+}
+
+void oracle_e4m3_round_array(int64_t n, const double *in, double *out)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_e4m3_round(in[i]);
+}
+
+/*
+ * The power-of-two exponent that brings a set of values whose largest
+ * magnitude is amax into e4m3's range: amax * 2^e lands in [128, 256), so
+ * e = 7 - floor(log2 amax), clamped to [-64, 64]; e = 0 when amax is 0 (or
+ * not finite, which the callers report).
+ */
+int oracle_fp8_exponent(double amax)
+{
+    if (amax == 0.0 || !isfinite(amax)) return 0;
+    int e;
+    frexp(amax, &e);
+    int k = 7 - (e - 1);
+    return k < -64 ? -64 : (k > 64 ? 64 : k);
 }
 
 /* The value a code stands for: (c - (2^bits - 1)/2) * s.  Exact in double. */
@@ -311,6 +385,96 @@ void oracle_expert_ffn(int bits, int H, int I, const uint8_t *gate_codes, const 
 }
 
 /*
+ * The FP8 variant of one routed expert on one token.  Every operand of the
+ * three products is an e4m3 value after a power-of-two scaling; the products
+ * are summed exactly (in double here) and the scaling undone afterwards:
+ *   x:   one exponent ex for the token, x8_i = e4m3(x_i 2^ex);
+ *   W:   one exponent kw_r per weight row, from the largest magnitude a code
+ *        of the row can stand for (max|c - mid| times the row's largest |s|):
+ *        W8_ri = e4m3(dq(W_ri) 2^kw_r);
+ *   g_r = 2^-(kw_r + ex) sum_i Wg8_ri x8_i,  u_r likewise;
+ *   h_r = fp16(silu(g_r) u_r)  (h is held in fp16 between the two products);
+ *   eh from max_r |h_r|,  h8_r = e4m3(h_r 2^eh);
+ *   y_o = 2^-(kw_o + eh) sum_r Wd8_or h8_r.
+ * The exponents follow oracle_fp8_exponent.  Returns ORACLE_ERR_NONFINITE when
+ * x, a scale or an h is not finite (h past fp16's range); y is then not set.
+ */
+static void fp8_weight_exponents(int bits, int rows, int cols, const uint16_t *scales, int *kw)
+{
+    double maxc = (bits == 3) ? 3.5 : 1.5;
+    for (int o = 0; o < rows; o++) {
+        double m = 0.0;
+        for (int b = 0; b < cols / 32; b++) {
+            double s = fabs(oracle_fp16_to_double(scales[(int64_t)o * (cols / 32) + b]));
+            if (s > m) m = s;
+        }
+        kw[o] = oracle_fp8_exponent(maxc * m);
+    }
+}
+
+/* y[o] = 2^-(kw_o + ex) sum_i e4m3(dq(W[o][i]) 2^kw_o) x8[i] for x8 already scaled by 2^ex. */
+static void fp8_matvec(int bits, int rows, int cols, const uint8_t *codes, const uint16_t *scales,
+                       const double *x8, int ex, double *y)
+{
+    int *kw = (int *)malloc(sizeof(int) * (size_t)rows);
+    fp8_weight_exponents(bits, rows, cols, scales, kw);
+    for (int o = 0; o < rows; o++) {
+        double acc = 0.0;
+        for (int i = 0; i < cols; i++) {
+            double wq = oracle_e4m3_round(ldexp(oracle_dequant(bits, codes[(int64_t)o * cols + i],
+                                                               scales[(int64_t)o * (cols / 32) + i / 32]),
+                                                kw[o]));
+            acc += wq * x8[i];
+        }
+        y[o] = ldexp(acc, -(kw[o] + ex));
+    }
+    free(kw);
+}
+
+/* Rounds a vector to e4m3 after its power-of-two scaling; returns the exponent. */
+static int fp8_vector(int n, const double *v, double *v8)
+{
+    double amax = 0.0;
+    for (int i = 0; i < n; i++)
+        if (fabs(v[i]) > amax) amax = fabs(v[i]);
+    int e = oracle_fp8_exponent(amax);
+    for (int i = 0; i < n; i++) v8[i] = oracle_e4m3_round(ldexp(v[i], e));
+    return e;
+}
+
+int oracle_expert_ffn_fp8(int bits, int H, int I, const uint8_t *gate_codes, const uint16_t *gate_scales,
+                          const uint8_t *up_codes, const uint16_t *up_scales, const uint8_t *down_codes,
+                          const uint16_t *down_scales, const double *x, double *y)
+{
+    for (int i = 0; i < H; i++)
+        if (!isfinite(x[i])) return ORACLE_ERR_NONFINITE;
+    for (int64_t i = 0; i < (int64_t)I * (H / 32); i++)
+        if (!isfinite(oracle_fp16_to_double(gate_scales[i])) || !isfinite(oracle_fp16_to_double(up_scales[i])))
+            return ORACLE_ERR_NONFINITE;
+    for (int64_t i = 0; i < (int64_t)H * (I / 32); i++)
+        if (!isfinite(oracle_fp16_to_double(down_scales[i]))) return ORACLE_ERR_NONFINITE;
+    double *x8 = (double *)malloc(sizeof(double) * (size_t)H);
+    double *g = (double *)malloc(sizeof(double) * (size_t)I);
+    double *u = (double *)malloc(sizeof(double) * (size_t)I);
+    int status = ORACLE_OK;
+    int ex = fp8_vector(H, x, x8);
+    fp8_matvec(bits, I, H, gate_codes, gate_scales, x8, ex, g);
+    fp8_matvec(bits, I, H, up_codes, up_scales, x8, ex, u);
+    for (int r = 0; r < I; r++) {
+        g[r] = oracle_fp16_round(silu(g[r]) * u[r]);
+        if (!isfinite(g[r])) status = ORACLE_ERR_NONFINITE;
+    }
+    if (status == ORACLE_OK) {
+        int eh = fp8_vector(I, g, u);   /* u now holds h8 */
+        fp8_matvec(bits, H, I, down_codes, down_scales, u, eh, y);
+    }
+    free(x8);
+    free(g);
+    free(u);
+    return status;
+}
+
+/*
  * The always-on shared expert on one token, bf16 weights:
  *   wg, wu [I][H], wd [H][I];  y = wd (silu(wg x) * (wu x)).
  */
@@ -346,12 +510,13 @@ void oracle_shared_expert(int H, int I, const uint16_t *wg, const uint16_t *wu, 
  *   the routed sum taken in slot order j = 0..k-1.
  * An id outside [0, E) returns ORACLE_ERR_BOUNDS.
  */
-int oracle_moe_layer(int bits, int T, int H, int I, int E, int k, const uint16_t *x_bf16,
+static int moe_layer(int fp8, int bits, int T, int H, int I, int E, int k, const uint16_t *x_bf16,
                      const int32_t *ids, const double *w, const uint8_t *gate_codes,
                      const uint16_t *gate_scales, const uint8_t *up_codes, const uint16_t *up_scales,
                      const uint8_t *down_codes, const uint16_t *down_scales, int Is,
                      const uint16_t *swg, const uint16_t *swu, const uint16_t *swd, double *out)
 {
+    int status = ORACLE_OK;
     for (int64_t f = 0; f < (int64_t)T * k; f++)
         if (ids[f] < 0 || ids[f] >= E) return ORACLE_ERR_BOUNDS;
     double *x = (double *)malloc(sizeof(double) * (size_t)H);
@@ -367,9 +532,19 @@ int oracle_moe_layer(int bits, int T, int H, int I, int E, int k, const uint16_t
         double *routed = (double *)calloc((size_t)H, sizeof(double));
         for (int j = 0; j < k; j++) {
             int e = ids[(int64_t)t * k + j];
-            oracle_expert_ffn(bits, H, I, gate_codes + e * gu_codes, gate_scales + e * gu_scales,
-                              up_codes + e * gu_codes, up_scales + e * gu_scales,
-                              down_codes + e * d_codes, down_scales + e * d_scales, x, y);
+            if (fp8) {
+                int st = oracle_expert_ffn_fp8(bits, H, I, gate_codes + e * gu_codes, gate_scales + e * gu_scales,
+                                               up_codes + e * gu_codes, up_scales + e * gu_scales,
+                                               down_codes + e * d_codes, down_scales + e * d_scales, x, y);
+                if (st != ORACLE_OK) {
+                    status = st;
+                    continue;
+                }
+            } else {
+                oracle_expert_ffn(bits, H, I, gate_codes + e * gu_codes, gate_scales + e * gu_scales,
+                                  up_codes + e * gu_codes, up_scales + e * gu_scales,
+                                  down_codes + e * d_codes, down_scales + e * d_scales, x, y);
+            }
             for (int i = 0; i < H; i++) routed[i] += w[(int64_t)t * k + j] * y[i];
         }
         for (int i = 0; i < H; i++) o[i] += routed[i];
@@ -377,7 +552,29 @@ int oracle_moe_layer(int bits, int T, int H, int I, int E, int k, const uint16_t
     }
     free(x);
     free(y);
-    return ORACLE_OK;
+    return status;
+}
+
+int oracle_moe_layer(int bits, int T, int H, int I, int E, int k, const uint16_t *x_bf16,
+                     const int32_t *ids, const double *w, const uint8_t *gate_codes,
+                     const uint16_t *gate_scales, const uint8_t *up_codes, const uint16_t *up_scales,
+                     const uint8_t *down_codes, const uint16_t *down_scales, int Is,
+                     const uint16_t *swg, const uint16_t *swu, const uint16_t *swd, double *out)
+{
+    return moe_layer(0, bits, T, H, I, E, k, x_bf16, ids, w, gate_codes, gate_scales, up_codes, up_scales,
+                     down_codes, down_scales, Is, swg, swu, swd, out);
+}
+
+/* The same layer with the routed experts in the FP8 variant (oracle_expert_ffn_fp8);
+ * ORACLE_ERR_NONFINITE when one of them reports it. */
+int oracle_moe_layer_fp8(int bits, int T, int H, int I, int E, int k, const uint16_t *x_bf16,
+                         const int32_t *ids, const double *w, const uint8_t *gate_codes,
+                         const uint16_t *gate_scales, const uint8_t *up_codes, const uint16_t *up_scales,
+                         const uint8_t *down_codes, const uint16_t *down_scales, int Is,
+                         const uint16_t *swg, const uint16_t *swu, const uint16_t *swd, double *out)
+{
+    return moe_layer(1, bits, T, H, I, E, k, x_bf16, ids, w, gate_codes, gate_scales, up_codes, up_scales,
+                     down_codes, down_scales, Is, swg, swu, swd, out);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -42,9 +42,10 @@ def device_expert_parts(seed, layer, experts, bits, H, I):
     return draw_expert_parts(seed, layer, experts, bits, H, I)
 
 
-def oracle_sampled_layer(seed, layer, bits, H, I, x_bf16, ids, w, shared, pool=None):
+def oracle_sampled_layer(seed, layer, bits, H, I, x_bf16, ids, w, shared, pool=None, fp8=False):
     """oracle.moe_layer for the tokens of x_bf16 [T][H] with the given routing,
-    regenerating only the experts they picked (on the device generator).
+    regenerating only the experts they picked (on the device generator);
+    fp8=True takes the routed experts in their FP8 variant.
     With a thread pool the tokens run in parallel (the oracle is C code called
     through ctypes, which releases the GIL)."""
     import oracle
@@ -56,7 +57,8 @@ def oracle_sampled_layer(seed, layer, bits, H, I, x_bf16, ids, w, shared, pool=N
     w = np.asarray(w, np.float64)
 
     def one(t):
-        return oracle.moe_layer(bits, x_bf16[t:t + 1], cids[t:t + 1], w[t:t + 1], *arena, shared=shared)[0]
+        return oracle.moe_layer(bits, x_bf16[t:t + 1], cids[t:t + 1], w[t:t + 1], *arena, shared=shared,
+                                fp8=fp8)[0]
 
     T = x_bf16.shape[0]
     rows = list(pool.map(one, range(T))) if pool is not None else [one(t) for t in range(T)]

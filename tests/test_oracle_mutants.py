@@ -42,6 +42,19 @@ MUTANTS = [
     ("bf16 read as the low half", "uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
     ("rms norm without the mean", "double r = sqrt(ss / (double)H + eps);", "double r = sqrt(ss + eps);"),
     ("rms norm eps outside the root", "double r = sqrt(ss / (double)H + eps);", "double r = sqrt(ss / (double)H) + eps;"),
+    ("e4m3 subnormal spacing", "int E = e - 1 < -6 ? -6 : e - 1;", "int E = e - 1 < -7 ? -7 : e - 1;"),
+    ("e4m3 mantissa width", "double q = ldexp(1.0, E - 3);", "double q = ldexp(1.0, E - 4);"),
+    ("e4m3 without saturation", "if (r > 448.0) r = 448.0;", "if (r > 480.0) r = 480.0;"),
+    ("e4m3 exponent bias", "ldexp((double)(8 + man), exp - 10)", "ldexp((double)(8 + man), exp - 9)"),
+    ("fp16 rounding width", "double q = ldexp(1.0, E - 10);", "double q = ldexp(1.0, E - 9);"),
+    ("fp8 scaling exponent off by one", "int k = 7 - (e - 1);", "int k = 8 - (e - 1);"),
+    ("fp8 input scaling not undone", "y[o] = ldexp(acc, -(kw[o] + ex));", "y[o] = ldexp(acc, -kw[o]);"),
+    ("fp8 h not held in fp16", "g[r] = oracle_fp16_round(silu(g[r]) * u[r]);", "g[r] = silu(g[r]) * u[r];"),
+    ("fp8 gate and up swapped", "g[r] = oracle_fp16_round(silu(g[r]) * u[r]);",
+     "g[r] = oracle_fp16_round(silu(u[r]) * g[r]);"),
+    ("fp8 row exponent from the first block", "for (int b = 0; b < cols / 32; b++) {", "for (int b = 0; b < 1; b++) {"),
+    ("fp8 row exponent from the 2-bit levels for 3 bits", "double maxc = (bits == 3) ? 3.5 : 1.5;",
+     "double maxc = 1.5;"),
 ]
 
 PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]

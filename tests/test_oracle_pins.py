@@ -416,6 +416,215 @@ def test_layer_3bit_vs_dense_numpy():
 
 
 # ---------------------------------------------------------------------------
+# the FP8 variant: e4m3 and fp16 rounding, the scaling exponent, the expert
+# ---------------------------------------------------------------------------
+
+def e4m3_table():
+    """Every e4m3 byte decoded by torch's float8_e4m3fn (a library routine)."""
+    torch = pytest.importorskip("torch")
+    b = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return b.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e4m3_decode_all_codes():
+    ref = e4m3_table()
+    got = np.array([oracle.e4m3_to_double(b) for b in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2  # 0x7F, 0xFF
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6 and got[0x38] == 1.0
+
+
+def brute_e4m3(v, table):
+    """Nearest finite e4m3 value by enumeration; a tie goes to the code whose
+    mantissa is even (the byte's lowest bit clear)."""
+    codes = [c for c in range(256) if not np.isnan(table[c])]
+    d = np.array([abs(v - table[c]) for c in codes])
+    best = np.flatnonzero(d == d.min())
+    cands = [codes[i] for i in best]
+    if len(cands) > 1:
+        even = [c for c in cands if c & 1 == 0]
+        cands = even or cands
+    val = table[cands[0]]
+    return math.copysign(abs(val), v) if val == 0 else val
+
+
+def test_e4m3_round_brute_force_and_library():
+    torch = pytest.importorskip("torch")
+    table = e4m3_table()
+    rng = np.random.default_rng(11)
+    fin = np.unique(table[~np.isnan(table)])
+    mids = (fin[1:] + fin[:-1]) / 2  # exact ties
+    vals = np.concatenate([
+        np.exp2(rng.uniform(-14, 10, 3000)) * rng.choice([-1, 1], 3000),
+        mids, -mids, mids * (1 + 2.0 ** -30), mids * (1 - 2.0 ** -30),
+        [448.0, 455.9, 464.0, 479.0, 480.0, 1e4, 1e6, -1e4, 2.0 ** -10, 2.0 ** -11, 3 * 2.0 ** -11],
+    ])
+    got = oracle.e4m3_round(vals)
+    want = np.array([brute_e4m3(v, table) for v in vals])
+    assert np.array_equal(got, want)
+    # torch's own conversion agrees inside the finite range (inputs exact in fp32)
+    v32 = vals.astype(np.float32)
+    inr = np.abs(v32) < 448
+    t = torch.from_numpy(v32[inr]).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(oracle.e4m3_round(v32[inr].astype(np.float64)), t)
+    assert list(oracle.e4m3_round([np.inf, 1e30, -1e30])) == [448.0, 448.0, -448.0] and np.isnan(oracle.e4m3_round([np.nan])[0])
+
+
+def test_fp16_round_vs_numpy():
+    rng = np.random.default_rng(12)
+    f16 = np.arange(0, 0x7C00, 37, dtype=np.uint32).astype(np.uint16).view(np.float16).astype(np.float64)
+    ulp = np.spacing(f16.astype(np.float16)).astype(np.float64)
+    vals = np.concatenate([
+        np.exp2(rng.uniform(-26, 16, 3000)) * rng.choice([-1, 1], 3000),
+        f16 + ulp / 2, f16 + ulp / 2 * (1 + 2.0 ** -40), -(f16 + ulp / 2),
+        [65504.0, 65519.0, 65520.0, 70000.0, 2.0 ** -25, 3 * 2.0 ** -26],
+    ])
+    got = oracle.fp16_round(vals)
+    with np.errstate(over="ignore"):
+        want = vals.astype(np.float16).astype(np.float64)
+    assert np.array_equal(got, want)
+
+
+def test_fp8_exponent_closed_forms():
+    cases = {1.0: 7, 1.999: 7, 2.0: 6, 0.75: 8, 255.0: 0, 256.0: -1, 2.0 ** -57: 64, 2.0 ** -60: 64,
+             2.0 ** 71: -64, 2.0 ** 70: -63, 0.0: 0, float("inf"): 0}
+    for a, e in cases.items():
+        assert oracle.fp8_exponent(a) == e, a
+    rng = np.random.default_rng(13)
+    for a in np.exp2(rng.uniform(-50, 60, 500)):
+        e = oracle.fp8_exponent(a)
+        assert 128 <= a * 2.0 ** e < 256
+
+
+def fp8_closed_form_expert():
+    """H = I = 64.  Gate rows: +0.5 * 128 on block 0, scale 0 on block 1, so
+    g = 64 (silu(64) = 64 in double); up rows: +0.5 on both blocks, so
+    u = (1 + 2^-4 + 2^-12) / 2 and h = 32 (1 + 2^-4 + 2^-12); down rows:
+    +1.5 with block scales 1 and 4.  x = (1 at 0, 2^-4 at 32, 2^-12 at 33).
+    Every operand but h is exact in e4m3 after its scaling.  h rounds to
+    fp16 34 = 32 * 1.0625, then h * 2^2 = 136 is an e4m3 tie between 128 and
+    144 and goes to 128: the effective h is 32 in every row, and
+    y_o = 32 * 1.5 * 32 + 32 * (1.5 * 4) * 32 = 7680."""
+    H = I = 64
+    gc = np.full((I, H), 2, np.uint8)
+    uc = np.full((I, H), 2, np.uint8)
+    dc = np.full((H, I), 3, np.uint8)
+    f16 = lambda v: np.float16(v).view(np.uint16)
+    gs = np.tile(np.array([f16(128.0), f16(0.0)], np.uint16), (I, 1))
+    us = np.full((I, 2), f16(1.0), np.uint16)
+    ds = np.tile(np.array([f16(1.0), f16(4.0)], np.uint16), (H, 1))
+    x = np.zeros(H)
+    x[0], x[32], x[33] = 1.0, 2.0 ** -4, 2.0 ** -12
+    return gc, gs, uc, us, dc, ds, x
+
+
+def test_expert_ffn_fp8_closed_form():
+    gc, gs, uc, us, dc, ds, x = fp8_closed_form_expert()
+    got = oracle.expert_ffn_fp8(2, gc, gs, uc, us, dc, ds, x)
+    assert np.array_equal(got, np.full(64, 7680.0))
+    # the exact expert on the same input: h = 32 (1 + 2^-4 + 2^-12) unrounded
+    exact = oracle.expert_ffn(2, gc, gs, uc, us, dc, ds, x)
+    np.testing.assert_allclose(exact, np.full(64, 240.0 * 32 * (1 + 2.0 ** -4 + 2.0 ** -12)), rtol=1e-14)
+
+
+@pytest.mark.parametrize("bits", [2, 3])
+def test_expert_ffn_fp8_vs_library_roundings(bits):
+    """The FP8 expert rebuilt from library roundings (torch's e4m3 cast,
+    numpy's fp16 cast) and numpy's dense products, the exponents by frexp."""
+    torch = pytest.importorskip("torch")
+    H, I = 256, 128
+    maxc = (2 ** bits - 1) / 2.0
+    gc, uc, dc = synth.expert_codes(7, 0, 2, bits, H, I)
+    gus, ds = synth.expert_scales(7, 0, 2, H, I)
+    x = synth.bf16_bits_to_f32(synth.activations(7, 1, H))[0].astype(np.float64)
+
+    def expo(a):
+        m, e = np.frexp(a)
+        return np.where(a == 0, 0, np.clip(8 - e, -64, 64))
+
+    def e4m3(v):  # v exact in fp32 here
+        return torch.from_numpy(np.asarray(v, np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+    def fp8_dense(codes, scales):
+        w = dense(bits, codes, scales)
+        kw = expo(maxc * np.abs(scales.view(np.float16).astype(np.float64)).max(axis=1))
+        return e4m3(w * np.exp2(kw)[:, None]), kw
+
+    ex = expo(np.abs(x).max())
+    x8 = e4m3(x * 2.0 ** ex)
+    wg, kg = fp8_dense(gc, gus[0])
+    wu, ku = fp8_dense(uc, gus[1])
+    wd, kd = fp8_dense(dc, ds)
+    g = (wg @ x8) * np.exp2(-(kg + ex))
+    u = (wu @ x8) * np.exp2(-(ku + ex))
+    h = (g * expit(g) * u).astype(np.float16).astype(np.float64)
+    eh = expo(np.abs(h).max())
+    h8 = e4m3(h * 2.0 ** eh)
+    want = (wd @ h8) * np.exp2(-(kd + eh))
+    got = oracle.expert_ffn_fp8(bits, gc, gus[0], uc, gus[1], dc, ds, x)
+    assert np.linalg.norm(got - want) <= 1e-12 * np.linalg.norm(want)
+    # and it is an approximation of the exact expert at the size e4m3 implies
+    exact = oracle.expert_ffn(bits, gc, gus[0], uc, gus[1], dc, ds, x)
+    err = np.linalg.norm(got - exact) / np.linalg.norm(exact)
+    assert 5e-3 < err < 0.15, err
+
+
+def test_expert_ffn_fp8_power_of_two_scalings():
+    """Scaling a down row's block scales by 2^j scales that output by 2^j
+    exactly; scaling every up scale by 2^j scales the whole output by 2^j
+    (h moves by 2^j in fp16's normal range, its exponent absorbs it)."""
+    bits, H, I = 2, 128, 64
+    gc, uc, dc = synth.expert_codes(8, 0, 1, bits, H, I)
+    gus, ds = synth.expert_scales(8, 0, 1, H, I)
+    x = synth.bf16_bits_to_f32(synth.activations(8, 1, H))[0].astype(np.float64)
+    base = oracle.expert_ffn_fp8(bits, gc, gus[0], uc, gus[1], dc, ds, x)
+    sc = lambda a, j: (a.view(np.float16).astype(np.float64) * 2.0 ** j).astype(np.float16).view(np.uint16)
+    ds2 = ds.copy()
+    ds2[5] = sc(ds[5], 3)
+    got = oracle.expert_ffn_fp8(bits, gc, gus[0], uc, gus[1], dc, ds2, x)
+    want = base.copy()
+    want[5] *= 8.0
+    assert np.array_equal(got, want)
+    got = oracle.expert_ffn_fp8(bits, gc, gus[0], uc, sc(gus[1], -2), dc, ds, x)
+    assert np.array_equal(got, base / 4.0)
+
+
+def test_expert_ffn_fp8_nonfinite():
+    gc, gs, uc, us, dc, ds, x = fp8_closed_form_expert()
+    x2 = x.copy()
+    x2[3] = np.inf
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.expert_ffn_fp8(2, gc, gs, uc, us, dc, ds, x2)
+    assert e.value.status == oracle.ERR_NONFINITE
+    us2 = us.copy()
+    us2[0, 0] = np.uint16(0x7C00)  # +inf scale
+    with pytest.raises(oracle.OracleError):
+        oracle.expert_ffn_fp8(2, gc, gs, uc, us2, dc, ds, x)
+
+
+def test_layer_fp8_equals_per_token_sum():
+    x, wr, arena, shared, k = small_layer(seed=9)
+    ids, w = oracle.topk(oracle.router_logits(x, wr).astype(np.float32), k)
+    out = oracle.moe_layer(2, x, ids, w, *arena, shared=shared, fp8=True)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    gate, gsc, up, usc, down, dsc = arena
+    for t in range(x.shape[0]):
+        ref = oracle.shared_expert(*shared, xf[t])
+        for j in range(k):
+            e = ids[t, j]
+            ref = ref + w[t, j] * oracle.expert_ffn_fp8(2, gate[e], gsc[e], up[e], usc[e], down[e], dsc[e], xf[t])
+        assert np.linalg.norm(out[t] - ref) <= 1e-12 * np.linalg.norm(ref)
+    # zero scales leave exactly the shared expert
+    zero = list(arena)
+    for i in (1, 3, 5):
+        zero[i] = np.zeros_like(arena[i])
+    out0 = oracle.moe_layer(2, x, ids, w, *zero, shared=shared, fp8=True)
+    for t in range(x.shape[0]):
+        assert np.array_equal(out0[t], oracle.shared_expert(*shared, xf[t]))
+
+
+# ---------------------------------------------------------------------------
 # residual-stream normalisation in front of each stacked layer
 # ---------------------------------------------------------------------------
 
