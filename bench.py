@@ -47,7 +47,7 @@ LAYERS, H, E, I, K_TOP, IS = 48, 2048, 512, 768, 10, 768
 # valid for the decode source whose code (comments and whitespace removed) has
 # this SHA-256 prefix; reported as null once that code changes, until it is
 # captured again.
-DECODE_TRAFFIC = (1_364_074_880, "8e1023583c484e5a")
+DECODE_TRAFFIC = (1_363_879_552, "f50f7317dca4e112")
 EXPERT_BYTES = 1_474_560
 ROUTER_BYTES = E * H * 4
 SHARED_BYTES = 3 * H * IS * 2
