@@ -24,7 +24,7 @@ MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_NONFINITE, MOE_ERR_BOUNDS = 4, 5, 6, 7
 MOE_ERR_RANGE = 8
 MOE_ID_NOT_LOCAL = -1
 MOE_F32, MOE_BF16 = 0, 1
-MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL = 0, 1, 2
+MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL, MOE_PATH_PREFILL_FP8 = 0, 1, 2, 3
 RMS_EPS = 1e-6  # normalisation in front of each stacked layer
 
 _lock = threading.Lock()

@@ -214,7 +214,13 @@ extern "C" moe_status moe_expert_forward_workspace_size(const moe_expert_arena *
     MOE_REQUIRE(bytes, "bytes is NULL");
     MOE_REQUIRE(T >= 0 && k >= 1 && k <= 16, "T >= 0 and 1 <= k <= 16");
     moe_path p = resolve_path(path, T);
+    MOE_REQUIRE(p == MOE_PATH_DECODE || p == MOE_PATH_PREFILL || p == MOE_PATH_PREFILL_FP8, "unknown path %d",
+                (int)path);
+    if (p == MOE_PATH_PREFILL_FP8 && !prefill_fp8_supported(*arena))
+        return fail(MOE_ERR_UNSUPPORTED, "the FP8 prefill takes 2-bit arenas with H and I multiples of 128 "
+                    "(got bits=%d H=%d I=%d)", arena->bits, arena->H, arena->I);
     if (p == MOE_PATH_DECODE) *bytes = decode_ws(*arena, T, k, nullptr).bytes;
+    else if (p == MOE_PATH_PREFILL_FP8) *bytes = prefill_fp8_workspace_bytes(*arena, T, k);
     else *bytes = prefill_workspace_bytes(*arena, T, k);
     return MOE_OK;
 }
@@ -234,17 +240,27 @@ extern "C" moe_status moe_expert_forward(const moe_expert_arena *arena, const ui
     MOE_REQUIRE(x_bf16 && ids && w && offsets && perm && inv_perm && out, "NULL pointer");
     MOE_REQUIRE(aligned16(x_bf16), "x_bf16 must be 16-byte aligned");
     moe_path p = resolve_path(path, T);
-    MOE_REQUIRE(p == MOE_PATH_DECODE || p == MOE_PATH_PREFILL, "unknown path %d", (int)path);
+    MOE_REQUIRE(p == MOE_PATH_DECODE || p == MOE_PATH_PREFILL || p == MOE_PATH_PREFILL_FP8, "unknown path %d",
+                (int)path);
     if (p == MOE_PATH_DECODE)
         MOE_REQUIRE(T <= 8, "the decode path takes at most 8 tokens (got %d); use MOE_PATH_PREFILL", T);
-    size_t need = p == MOE_PATH_DECODE ? decode_ws(*arena, T, k, nullptr).bytes : prefill_workspace_bytes(*arena, T, k);
+    if (p == MOE_PATH_PREFILL_FP8 && !prefill_fp8_supported(*arena))
+        return fail(MOE_ERR_UNSUPPORTED, "the FP8 prefill takes 2-bit arenas with H and I multiples of 128 "
+                    "(got bits=%d H=%d I=%d)", arena->bits, arena->H, arena->I);
+    size_t need = p == MOE_PATH_DECODE        ? decode_ws(*arena, T, k, nullptr).bytes
+                  : p == MOE_PATH_PREFILL_FP8 ? prefill_fp8_workspace_bytes(*arena, T, k)
+                                              : prefill_workspace_bytes(*arena, T, k);
     if (need && (!ws || ws_bytes < need))
         return fail(MOE_ERR_WORKSPACE, "expert_forward (%s, T=%d) needs %zu bytes (%.2f MiB) of workspace, got %zu",
-                    p == MOE_PATH_DECODE ? "decode" : "prefill", T, need, mib((double)need), ws ? ws_bytes : (size_t)0);
+                    p == MOE_PATH_DECODE ? "decode" : p == MOE_PATH_PREFILL_FP8 ? "fp8 prefill" : "prefill", T,
+                    need, mib((double)need), ws ? ws_bytes : (size_t)0);
     MOE_REQUIRE(!ws || aligned16(ws), "workspace must be 16-byte aligned");
     cudaStream_t s = to_cuda(stream);
     if (p == MOE_PATH_DECODE)
         return decode_forward(*arena, x_bf16, T, ids, w, k, offsets, perm, inv_perm, out, out_dtype, accumulate, ws, s);
+    if (p == MOE_PATH_PREFILL_FP8)
+        return prefill_fp8_forward(*arena, x_bf16, T, w, k, offsets, perm, inv_perm, out, out_dtype, accumulate, ws,
+                                   dev_status, s);
     return prefill_forward(*arena, x_bf16, T, ids, w, k, offsets, perm, inv_perm, out, out_dtype, accumulate, ws,
                            dev_status, s);
 }

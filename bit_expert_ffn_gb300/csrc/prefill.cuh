@@ -40,6 +40,13 @@ moe_status prefill_tc_forward(const moe_expert_arena &A, const uint16_t *x, int 
                               const int32_t *offsets, const int32_t *perm, const int32_t *inv, void *out, moe_dtype dt,
                               int accumulate, void *ws, int32_t *dev_status, cudaStream_t s);
 
+// FP8 variant (prefill_tc.cu): 2-bit arenas, H and I multiples of 128.
+bool prefill_fp8_supported(const moe_expert_arena &A);
+size_t prefill_fp8_workspace_bytes(const moe_expert_arena &A, int T, int k);
+moe_status prefill_fp8_forward(const moe_expert_arena &A, const uint16_t *x, int T, const float *w, int k,
+                               const int32_t *offsets, const int32_t *perm, const int32_t *inv, void *out,
+                               moe_dtype dt, int accumulate, void *ws, int32_t *dev_status, cudaStream_t s);
+
 moe_status launch_combine(const float *y, const float *w, const int32_t *inv, int T, int k, int H, void *out,
                           moe_dtype dt, int accumulate, cudaStream_t s);
 // fp16 rows of y (16-byte aligned, H a multiple of 8).

@@ -68,9 +68,9 @@ constexpr int BM = 128;  // weight rows per tile (MMA M); gate/up: 64 gate + 64 
 constexpr int BT = 192;  // sorted pairs per tile at most (MMA N, multiples of 32)
 constexpr int BK = 64;   // reduction per step: one 128-byte swizzle row of fp16
 constexpr int B_BYTES = BT * BK * 2;   // one step of the pairs' rows
-constexpr int C_LO = 0;                // code entry: low codes, 16 B per row
-constexpr int C_SC = BM * 16;          //             scales of four steps, 16 B per row
-constexpr int C_HI = 2 * BM * 16;      //             3-bit high planes of two steps, 16 B per row
+constexpr int C_LO = 0;                // code entry: low codes, 16 B (FP8: 32 B) per row,
+                                       //   then scales of four (FP8: two) steps, 16 B per row,
+constexpr int C_HI = 2 * BM * 16;      //   then 3-bit high planes of two steps, 16 B per row
 constexpr int NA = 4, NB = 6;          // weight ring (TMEM), pair ring (shared memory)
 // TMEM columns: two accumulators of BT fp32 columns, then the weight ring
 // (a 64-wide fp16 step is 32 columns).
@@ -93,11 +93,17 @@ constexpr unsigned long long kWaitNs = 2000000000ull;
 // fp32 values of this magnitude or more (and NaN) round to a non-finite fp16
 constexpr float kF16Limit = 65520.f;
 
-// Shared-memory plan per bit width: the code entry carries the 3-bit high
-// planes only for 3 bits, which leaves room for fewer entries.
-template <int BITS>
+// Shared-memory plan per bit width and operand type: the code entry carries
+// the 3-bit high planes only for 3 bits, which leaves room for fewer entries.
+// A step of the FP8 variant (2 bits only) covers 128 elements of the
+// reduction: 32 bytes of codes per row, and four block scales.
+template <int BITS, bool FP8 = false>
 struct Cfg {
-    static constexpr int C_BYTES = BITS == 2 ? 2 * BM * 16 : 3 * BM * 16;
+    static_assert(!FP8 || BITS == 2, "the FP8 variant takes 2-bit codes");
+    static constexpr int BKE = FP8 ? 128 : BK;          // reduction elements per step (128 bytes of a pair row)
+    static constexpr int CODE_STEP = FP8 ? 32 : 16;     // code bytes per weight row and step
+    static constexpr int C_SC = BM * CODE_STEP;         // offset of the scales in a code entry
+    static constexpr int C_BYTES = FP8 ? BM * 32 + BM * 16 : (BITS == 2 ? 2 * BM * 16 : 3 * BM * 16);
     static constexpr int NC = BITS == 2 ? 8 : 6;
     static constexpr int OFF_B = 0;
     static constexpr int OFF_C = OFF_B + NB * B_BYTES;
@@ -122,6 +128,9 @@ struct Args {
     uint16_t *h_out;  // gate/up: fp16 [pairs][I] (columns permuted within 16-groups)
     uint16_t *y_out;  // down: fp16 [pairs][H]
     int32_t *status;
+    // FP8 variant: the power-of-two exponents of the operands' scalings
+    const int8_t *kw;       // per weight row, [E][code_rows]
+    const int32_t *pexp;    // per pair: x's (gate/up) or h's (down)
 };
 
 struct Shared {
@@ -199,6 +208,64 @@ __device__ __forceinline__ void dq_group(uint32_t w, uint32_t hw, uint32_t sc, u
 #undef MOE_DQ
 }
 
+// ---- FP8 variant ------------------------------------------------------------
+// Stored position, inside its 16-element group, of element m in the FP8
+// operands: the even elements first, then the odd ones (the order in which
+// lut_word below decodes a code word).
+__host__ __device__ __forceinline__ int pos8(int m) { return (m >> 1) | ((m & 1) << 3); }
+
+// 2^e as an fp32 for e in [-126, 127].
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
+
+// The exponent that scales a set of magnitudes with maximum amax (>= 0,
+// finite) into [128, 256): 7 - floor(log2 amax), clamped to [-64, 64]; 0 for
+// amax = 0.  fp32 subnormal maxima clamp to 64.
+__device__ __forceinline__ int fp8_exponent(float amax)
+{
+    if (amax == 0.f) return 0;
+    const int be = (__float_as_int(amax) >> 23) & 0xff;
+    const int k = be == 0 ? 64 : 7 - (be - 127);
+    return k < -64 ? -64 : (k > 64 ? 64 : k);
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// e4m3 bytes of two fp32 values, rounded to nearest (ties to even) with
+// saturation: the low byte is lo's, the high byte hi's.
+__device__ __forceinline__ uint32_t e4m3x2(float hi, float lo)
+{
+    uint16_t h;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(hi), "f"(lo));
+    return h;
+}
+
+// The four e4m3 values a 2-bit block with scale S = s 2^kw stands for, one
+// byte per code: e4m3((c - 1.5) S) for c = 0..3.  Each is rounded once from
+// its exact value (1.5 S and 0.5 S are exact in fp32), and e4m3 rounding is
+// symmetric, so the negative entries are the positive ones with the sign bit.
+__device__ __forceinline__ uint32_t lut_2bit(float S)
+{
+    const uint32_t h = e4m3x2(1.5f * S, 0.5f * S);  // byte 0: 0.5 S, byte 1: 1.5 S
+    return prmt(h, 0u, 0x1001u) ^ 0x8080u;          // bytes: -1.5 S, -0.5 S, 0.5 S, 1.5 S
+}
+
+// A word of sixteen 2-bit codes (weight j at bits 2j..2j+1) as sixteen e4m3
+// bytes, one byte select per four weights: o[0] holds weights 0, 2, 4, 6,
+// o[1] 8, 10, 12, 14, o[2] 1, 3, 5, 7 and o[3] 9, 11, 13, 15 (pos8 order).
+__device__ __forceinline__ void lut_word(uint32_t w, uint32_t lut, uint32_t *o)
+{
+    const uint32_t ev = w & 0x33333333u, od = (w >> 2) & 0x33333333u;  // one code per nibble
+    o[0] = prmt(lut, 0u, ev);
+    o[1] = prmt(lut, 0u, ev >> 16);
+    o[2] = prmt(lut, 0u, od);
+    o[3] = prmt(lut, 0u, od >> 16);
+}
+
 // silu with a fast division: h is rounded to fp16 right after, far coarser
 // than the approximation's couple of fp32 ulps.
 __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
@@ -217,7 +284,7 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, int n, int issued, in
     }
 }
 
-template <int BITS, bool SWIGLU>
+template <int BITS, bool SWIGLU, bool FP8>
 __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_constant__ Args a,
                                                              const __grid_constant__ CUtensorMap tok_map,
                                                              const __grid_constant__ CUtensorMap tok_full_map,
@@ -225,7 +292,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                                                              const __grid_constant__ CUtensorMap scale_map,
                                                              const __grid_constant__ CUtensorMap out_map)
 {
-    using C = Cfg<BITS>;
+    using C = Cfg<BITS, FP8>;
     extern __shared__ __align__(1024) char dyn_raw[];
     char *dyn = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
     __shared__ Shared S;
@@ -264,7 +331,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     tc::tc_fence_after();
     const uint32_t tmem = S.tmem;
     const int total = *a.ntt * a.rtiles;
-    const int nk = a.K / BK;
+    const int nk = a.K / C::BKE;
 
     if (warp == 0 || warp == 3 || warp == RING_WARP || warp == CODE_WARP) {
         // ---------------- TMA: warps 24 and 25 wait for free pair and code slots and
@@ -276,7 +343,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         // waiter and its issuer.
         // roles: 0 pair waiter, 1 pair issuer, 2 code issuer, 3 code waiter
         const int role = warp == RING_WARP ? 0 : warp == 0 ? 1 : warp == 3 ? 2 : 3;
-        const uint32_t cbytes = (BITS == 3 ? 2 * BM * 16 : BM * 16) + (a.scale_tma ? BM * 16 : 0);
+        const uint32_t cbytes = (BITS == 3 ? 2 * BM * 16 : BM * C::CODE_STEP) + (a.scale_tma ? BM * 16 : 0);
         int it = 0;
         bool stop = false;
         int4 nxt = tile_entry(a, blockIdx.x, total);
@@ -301,10 +368,11 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                     if (role == 1 && lane == 0) {
                         char *bs = dyn + C::OFF_B + b.s * B_BYTES;
                         if (t.n32 * 32 == BT) {  // a full tile: one box of BT rows
-                            tc::tma_load_2d(bs, &tok_full_map, kb * BK, t.p0, &S.bfull[b.s]);
+                            tc::tma_load_2d(bs, &tok_full_map, kb * C::BKE, t.p0, &S.bfull[b.s]);
                         } else {
                             for (int i = 0; i < t.n32; i++)
-                                tc::tma_load_2d(bs + i * 32 * BK * 2, &tok_map, kb * BK, t.p0 + 32 * i, &S.bfull[b.s]);
+                                tc::tma_load_2d(bs + i * 32 * BK * 2, &tok_map, kb * C::BKE, t.p0 + 32 * i,
+                                                &S.bfull[b.s]);
                         }
                     }
                 }
@@ -320,11 +388,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                     }
                     if (role == 2 && lane == 0) {
                         char *cs = dyn + C::OFF_C + c.s * C::C_BYTES;
-                        tc::tma_load_2d(cs + C_LO, &code_map, kb * 16, r0, &S.cfull[c.s]);
-                        tc::tma_load_2d(cs + C_LO + 64 * 16, &code_map, kb * 16, r1, &S.cfull[c.s]);
-                        if (a.scale_tma) {
-                            tc::tma_load_2d(cs + C_SC, &scale_map, (kb >> 2) * 8, r0, &S.cfull[c.s]);
-                            tc::tma_load_2d(cs + C_SC + 64 * 16, &scale_map, (kb >> 2) * 8, r1, &S.cfull[c.s]);
+                        tc::tma_load_2d(cs + C_LO, &code_map, kb * C::CODE_STEP, r0, &S.cfull[c.s]);
+                        tc::tma_load_2d(cs + C_LO + 64 * C::CODE_STEP, &code_map, kb * C::CODE_STEP, r1,
+                                        &S.cfull[c.s]);
+                        if (a.scale_tma) {  // 16 B of scales per row: four steps (FP8: two)
+                            const int sx = (FP8 ? kb >> 1 : kb >> 2) * 8;
+                            tc::tma_load_2d(cs + C::C_SC, &scale_map, sx, r0, &S.cfull[c.s]);
+                            tc::tma_load_2d(cs + C::C_SC + 64 * 16, &scale_map, sx, r1, &S.cfull[c.s]);
                         }
                         if (BITS == 3) {
                             tc::tma_load_2d(cs + C_HI, &code_map, a.hi_x + (kb >> 1) * 16, r0, &S.cfull[c.s]);
@@ -389,9 +459,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                         const uint32_t abase = tmem + (uint32_t)(TM_A + sa.s * 32);
                         const uint32_t bbase = tc::smem_u32(dyn + C::OFF_B + sb.s * B_BYTES);
 #pragma unroll
-                        for (int k16 = 0; k16 < BK / 16; k16++)
-                            tc::mma_f16_ts(d, abase + k16 * 8, tc::desc_kmajor_sw128(bbase + k16 * 32), idesc,
-                                           ((kb + j) | k16) ? 1u : 0u);
+                        for (int k16 = 0; k16 < BK / 16; k16++) {  // 32 bytes of K per instruction
+                            if constexpr (FP8)
+                                tc::mma_f8_ts(d, abase + k16 * 8, tc::desc_kmajor_sw128(bbase + k16 * 32), idesc,
+                                              ((kb + j) | k16) ? 1u : 0u);
+                            else
+                                tc::mma_f16_ts(d, abase + k16 * 8, tc::desc_kmajor_sw128(bbase + k16 * 32), idesc,
+                                               ((kb + j) | k16) ? 1u : 0u);
+                        }
                         tc::mma_commit(&S.aempty[sa.s]);
                         tc::mma_commit(&S.bempty[sb.s]);
                     }
@@ -435,6 +510,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             Tile t = make_tile(a, nxt, tile);
             nxt = tile_entry(a, tile + gridDim.x, total);
             uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BT);
+            float frow = 1.f;  // FP8: 2^-kw of this lane's weight row (kw from fp16 scales lies in [-9, 31])
+            if constexpr (FP8) {
+                const int orow = SWIGLU ? t.rt * 64 + (q & 1) * 32 + lane : t.rt * 128 + q * 32 + lane;
+                const int64_t mrow = SWIGLU && q >= 2 ? (int64_t)a.up_rows + orow : orow;
+                if (orow < a.rows) frow = exp2i(-__ldg(a.kw + (int64_t)t.e * a.code_rows + mrow));
+            }
             for (int ch = 0; ch < t.n32; ch++) {
                 uint32_t r[32];
                 __syncwarp();
@@ -443,6 +524,15 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                 int tok0 = ch * 32;
                 bool full = tok0 + 32 <= t.cnt;
                 int nv = min(32, t.cnt - tok0);
+                if constexpr (FP8) {
+                    // undo the operands' scalings: 2^-kw of the weight row, then 2^-e of pair i (e in
+                    // [-64, 64]); the two factors are exact, so their order does not matter while the
+                    // product stays a normal fp32
+                    const float fpair = exp2i(-(tok0 + lane < t.cnt ? __ldg(a.pexp + t.p0 + tok0 + lane) : 0));
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        r[i] = __float_as_uint(__uint_as_float(r[i]) * frow * __shfl_sync(0xffffffffu, fpair, i));
+                }
                 if (SWIGLU) {
                     float *xb = xch + (ch & 1) * (XCH_BYTES / 4);
                     if (q >= 2) {
@@ -453,7 +543,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                     tc::named_sync(1, 128);
                     int orow0 = t.rt * 64 + q * 32;  // first output row of this warp
                     if (q < 2 && orow0 < a.rows) {
-                        int pos = (lane & ~15) + perm16(lane & 15);  // stored column within the warp's 32
+                        // stored column within the warp's 32
+                        int pos = (lane & ~15) + (FP8 ? pos8(lane & 15) : perm16(lane & 15));
                         uint16_t hv[32];
 #pragma unroll
                         for (int i = 0; i < 32; i++) {
@@ -535,12 +626,19 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             int64_t mrow = SWIGLU && r >= 64 ? (int64_t)a.up_rows + orow : orow;
             // scales from global memory only when they cannot come by TMA
             const uint16_t *sp = a.scales + (int64_t)t.e * a.scales_expert_stride + mrow * a.scale_row;
+            float p2kw = 1.f;  // FP8: 2^kw, the scaling of this weight row (kw in [-9, 31])
+            if constexpr (FP8)
+                if (valid) p2kw = exp2i(__ldg(a.kw + (int64_t)t.e * a.code_rows + mrow));
             // the steps of this tile that belong to group jg: global step index = jg (mod 4)
             for (int kb = (jg - base) & 3; kb < nk; kb += 4) {
                 const int it = base + kb;
                 Slot c = slot_of(it, C::NC), sa = slot_of(it, NA);
                 uint32_t sc = 0;  // the step's two block scales (low half: first block)
-                if (valid && !a.scale_tma) sc = (uint32_t)__ldg(sp + 2 * kb) | ((uint32_t)__ldg(sp + 2 * kb + 1) << 16);
+                uint2 sc4 = make_uint2(0u, 0u);  // FP8: the step's four block scales
+                if (valid && !a.scale_tma) {
+                    if constexpr (FP8) sc4 = __ldg(reinterpret_cast<const uint2 *>(sp + 4 * kb));
+                    else sc = (uint32_t)__ldg(sp + 2 * kb) | ((uint32_t)__ldg(sp + 2 * kb + 1) << 16);
+                }
                 // the warp moves as one (its TMEM stores need all lanes): lane 0 waits
                 bool ok = lane == 0 ? tc::mbar_wait(&S.cfull[c.s], c.par, kWaitNs) : true;
                 if (!__shfl_sync(0xffffffffu, ok, 0)) {
@@ -549,18 +647,32 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                 }
                 // codes of this step into registers, then the code slot is free
                 const char *cs = dyn + C::OFF_C + c.s * C::C_BYTES;
-                uint4 cw = make_uint4(0u, 0u, 0u, 0u);
+                uint4 cw = make_uint4(0u, 0u, 0u, 0u), cw1 = make_uint4(0u, 0u, 0u, 0u);
                 uint2 hw = make_uint2(0u, 0u);
                 if (valid) {
-                    cw = *reinterpret_cast<const uint4 *>(cs + C_LO + r * 16);
-                    if (a.scale_tma) sc = lds32(cs + C_SC + r * 16 + (kb & 3) * 4);
+                    cw = *reinterpret_cast<const uint4 *>(cs + C_LO + r * C::CODE_STEP);
+                    if constexpr (FP8) {
+                        cw1 = *reinterpret_cast<const uint4 *>(cs + C_LO + r * C::CODE_STEP + 16);
+                        if (a.scale_tma) sc4 = *reinterpret_cast<const uint2 *>(cs + C::C_SC + r * 16 + (kb & 1) * 8);
+                    } else {
+                        if (a.scale_tma) sc = lds32(cs + C::C_SC + r * 16 + (kb & 3) * 4);
+                    }
                     if (BITS == 3) hw = *reinterpret_cast<const uint2 *>(cs + C_HI + r * 16 + (kb & 1) * 8);
                 }
-                // (c - mid) s leaves fp16's range when |s| max|c - mid| rounds past 65504
                 if (valid) {
-                    const float2 sf = __half22float2(*reinterpret_cast<const __half2 *>(&sc));
-                    constexpr float kMaxCode = BITS == 2 ? 1.5f : 3.5f;
-                    scale_out_of_range |= !(fabsf(sf.x) * kMaxCode < kF16Limit) || !(fabsf(sf.y) * kMaxCode < kF16Limit);
+                    if constexpr (FP8) {
+                        // the e4m3 scaling takes any finite scale
+                        const float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(&sc4.x));
+                        const float2 s23 = __half22float2(*reinterpret_cast<const __half2 *>(&sc4.y));
+                        scale_out_of_range |= !isfinite(s01.x) || !isfinite(s01.y) || !isfinite(s23.x) ||
+                                              !isfinite(s23.y);
+                    } else {
+                        // (c - mid) s leaves fp16's range when |s| max|c - mid| rounds past 65504
+                        const float2 sf = __half22float2(*reinterpret_cast<const __half2 *>(&sc));
+                        constexpr float kMaxCode = BITS == 2 ? 1.5f : 3.5f;
+                        scale_out_of_range |=
+                            !(fabsf(sf.x) * kMaxCode < kF16Limit) || !(fabsf(sf.y) * kMaxCode < kF16Limit);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&S.cempty[c.s]);
@@ -570,13 +682,32 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                     break;
                 }
                 tc::tc_fence_after();
-                const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+                if constexpr (FP8) {
+                    // 128 weights: four 32-weight blocks, each a byte table of its four e4m3 values
+                    // and two code words decoded by byte selects into eight TMEM columns
+                    const uint32_t words[8] = {cw.x, cw.y, cw.z, cw.w, cw1.x, cw1.y, cw1.z, cw1.w};
 #pragma unroll
-                for (int gq = 0; gq < 4; gq++) {  // 16-weight group gq of block gq / 2
-                    uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                    const uint32_t hb = gq < 2 ? hw.x : hw.y;
-                    if (valid) dq_group<BITS>(words[gq], (gq & 1) ? hb >> 8 : hb, gq < 2 ? sc & 0xffffu : sc >> 16, v);
-                    tc::tmem_st_32x32b_x8(tq + (uint32_t)(sa.s * 32 + gq * 8), v);
+                    for (int b = 0; b < 4; b++) {
+                        uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                        if (valid) {
+                            const uint32_t sw = b < 2 ? sc4.x : sc4.y;
+                            const uint16_t sh = (uint16_t)((b & 1) ? sw >> 16 : sw & 0xffffu);
+                            const uint32_t lut = lut_2bit(__half2float(__ushort_as_half(sh)) * p2kw);
+                            lut_word(words[2 * b], lut, v);
+                            lut_word(words[2 * b + 1], lut, v + 4);
+                        }
+                        tc::tmem_st_32x32b_x8(tq + (uint32_t)(sa.s * 32 + b * 8), v);
+                    }
+                } else {
+                    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                    for (int gq = 0; gq < 4; gq++) {  // 16-weight group gq of block gq / 2
+                        uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                        const uint32_t hb = gq < 2 ? hw.x : hw.y;
+                        if (valid)
+                            dq_group<BITS>(words[gq], (gq & 1) ? hb >> 8 : hb, gq < 2 ? sc & 0xffffu : sc >> 16, v);
+                        tc::tmem_st_32x32b_x8(tq + (uint32_t)(sa.s * 32 + gq * 8), v);
+                    }
                 }
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
@@ -639,17 +770,141 @@ __global__ void gather_x_kernel(const uint16_t *__restrict__ x, const int32_t *_
     if (out_of_range) set_status(status, MOE_ERR_RANGE);
 }
 
-template <int BITS, bool SWIGLU>
+template <int BITS, bool SWIGLU, bool FP8 = false>
 static moe_status launch_gemm(const Args &a, const CUtensorMap &tok, const CUtensorMap &tok_full,
                               const CUtensorMap &codes, const CUtensorMap &scales, const CUtensorMap &out, int grid,
                               cudaStream_t s)
 {
-    auto fn = tc_gemm_kernel<BITS, SWIGLU>;
-    const int smem = Cfg<BITS>::SMEM;
+    auto fn = tc_gemm_kernel<BITS, SWIGLU, FP8>;
+    const int smem = Cfg<BITS, FP8>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "tc gemm attribute: %s", cudaGetErrorString(e));
     fn<<<grid, THREADS, smem, s>>>(a, tok, tok_full, codes, scales, out);
-    return check_launch(SWIGLU ? "tc_gemm_gateup" : "tc_gemm_down");
+    return check_launch(SWIGLU ? (FP8 ? "tc_gemm_gateup_fp8" : "tc_gemm_gateup")
+                               : (FP8 ? "tc_gemm_down_fp8" : "tc_gemm_down"));
+}
+
+// ---- FP8 variant: the operands' exponents and e4m3 copies -------------------
+
+// kw[e][row] = the exponent of weight row `row` of expert e, from the largest
+// magnitude a code of the row can stand for (1.5 times its largest |s|), for
+// the experts that have pairs (the others are never read).  A non-finite
+// scale sets MOE_ERR_RANGE.
+__global__ void fp8_row_exponent_kernel(const uint16_t *__restrict__ scales, const int32_t *__restrict__ offsets,
+                                        int E, int rows, int blocks, int8_t *__restrict__ kw,
+                                        int32_t *__restrict__ status)
+{
+    bool bad = false;
+    const int64_t n = (int64_t)E * rows;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int e = (int)(i / rows);
+        if (offsets[e + 1] == offsets[e]) continue;
+        const uint16_t *sp = scales + i * blocks;
+        uint32_t mx = 0;  // largest |s| as fp16 bits (magnitudes order like the bits; inf and NaN above all)
+        if (blocks % 8 == 0) {
+            for (int b = 0; b < blocks; b += 8) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(sp + b));
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; j++) mx = max(mx, max(w[j] & 0x7fffu, (w[j] >> 16) & 0x7fffu));
+            }
+        } else {
+            for (int b = 0; b < blocks; b++) mx = max(mx, (uint32_t)__ldg(sp + b) & 0x7fffu);
+        }
+        bad |= mx >= 0x7c00u;
+        kw[i] = (int8_t)(mx >= 0x7c00u ? 0 : fp8_exponent(1.5f * __half2float(__ushort_as_half((uint16_t)mx))));
+    }
+    if (bad) set_status(status, MOE_ERR_RANGE);
+}
+
+// x8[p][16g + pos8(m)] = e4m3(x[tok(p)][16g + m] 2^ex[p]), ex[p] the exponent
+// of the token's largest |x|.  One warp per pair row: the row is read once for
+// its maximum and once more (from cache) to convert it.  A non-finite x, or a
+// row whose largest |x| still exceeds e4m3's range after the largest
+// down-scaling (2^-64), sets MOE_ERR_RANGE.
+__global__ void gather_x_fp8_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm,
+                                    const int32_t *__restrict__ offsets, int E, int k, int H, uint8_t *__restrict__ x8,
+                                    int32_t *__restrict__ pexp, int32_t *__restrict__ status)
+{
+    bool out_of_range = false;
+    const int n = offsets[E];
+    const int groups = H / 16, lane = lane_id();
+    const int warps = (int)(gridDim.x * blockDim.x >> 5);
+    for (int p = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); p < n; p += warps) {
+        const int tok = perm[p] / k;
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)tok * H);
+        uint32_t mx = 0;  // largest |x| as bf16 bits
+        for (int g = lane; g < groups; g += 32) {
+            const uint4 a0 = __ldg(src + 2 * g), a1 = __ldg(src + 2 * g + 1);
+            const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int j = 0; j < 8; j++) mx = max(mx, max(w[j] & 0x7fffu, (w[j] >> 16) & 0x7fffu));
+        }
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        const float amax = __uint_as_float(mx << 16);
+        const int ex = mx >= 0x7f80u ? 0 : fp8_exponent(amax);
+        out_of_range |= mx >= 0x7f80u || amax * exp2i(ex) >= 464.f;
+        if (lane == 0) pexp[p] = ex;
+        const float sc = exp2i(ex);
+        uint4 *dst = reinterpret_cast<uint4 *>(x8 + (int64_t)p * H);
+        for (int g = lane; g < groups; g += 32) {
+            const uint4 a0 = __ldg(src + 2 * g), a1 = __ldg(src + 2 * g + 1);
+            const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            float f[16];
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                f[2 * j] = __uint_as_float(w[j] << 16) * sc;
+                f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u) * sc;
+            }
+            // stored bytes 0-3: elements 0, 2, 4, 6; 4-7: 8, 10, 12, 14; 8-11: 1, 3, 5, 7; 12-15: 9, 11, 13, 15
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const int m0 = (q & 1) * 8 + (q >> 1);  // element at the word's first byte
+                o[q] = e4m3x2(f[m0 + 2], f[m0]) | (e4m3x2(f[m0 + 6], f[m0 + 4]) << 16);
+            }
+            dst[g] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    if (out_of_range) set_status(status, MOE_ERR_RANGE);
+}
+
+// h8[p][i] = e4m3(h[p][i] 2^eh[p]), eh[p] the exponent of the pair's largest
+// |h|; positions stay as the gate/up epilogue stored them.  One warp per pair
+// row.  (An h past fp16's range was reported by that epilogue.)
+__global__ void quantise_h_kernel(const uint16_t *__restrict__ h, const int32_t *__restrict__ offsets, int E, int I,
+                                  uint8_t *__restrict__ h8, int32_t *__restrict__ pexp)
+{
+    const int n = offsets[E];
+    const int chunks = I / 8, lane = lane_id();
+    const int warps = (int)(gridDim.x * blockDim.x >> 5);
+    for (int p = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); p < n; p += warps) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(h + (int64_t)p * I);
+        uint32_t mx = 0;  // largest |h| as fp16 bits
+        for (int c = lane; c < chunks; c += 32) {
+            const uint4 v = src[c];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; j++) mx = max(mx, max(w[j] & 0x7fffu, (w[j] >> 16) & 0x7fffu));
+        }
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        const int eh = mx >= 0x7c00u ? 0 : fp8_exponent(__half2float(__ushort_as_half((uint16_t)mx)));
+        if (lane == 0) pexp[p] = eh;
+        const float sc = exp2i(eh);
+        uint2 *dst = reinterpret_cast<uint2 *>(h8 + (int64_t)p * I);
+        for (int c = lane; c < chunks; c += 32) {
+            const uint4 v = src[c];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[2];
+#pragma unroll
+            for (int j = 0; j < 2; j++) {
+                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&w[2 * j]));
+                const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&w[2 * j + 1]));
+                o[j] = e4m3x2(a.y * sc, a.x * sc) | (e4m3x2(b.y * sc, b.x * sc) << 16);
+            }
+            dst[c] = make_uint2(o[0], o[1]);
+        }
+    }
 }
 
 }  // namespace ptc
@@ -658,23 +913,41 @@ struct PtcWs {
     int32_t *mt_prefix;
     int4 *table;
     uint16_t *xg, *h, *y;
+    // FP8 variant
+    uint8_t *x8, *h8;
+    int32_t *ex, *eh;
+    int8_t *kw_gu, *kw_d;
     size_t bytes;
 };
 
-static PtcWs ptc_ws(const moe_expert_arena &A, int T, int k, void *base)
+// Workspace carve-up (256-byte aligned pieces): tile prefix and table, then
+// the pairs' x rows (fp16, or e4m3 for FP8), h (fp16), y (fp16), and for FP8
+// the e4m3 h, the per-pair exponents and the per-row exponents.
+static PtcWs ptc_ws(const moe_expert_arena &A, int T, int k, void *base, bool fp8 = false)
 {
-    PtcWs w;
+    PtcWs w = {};
     size_t n = (size_t)T * k;
-    size_t tb = align256((A.E + 1) * sizeof(int32_t));
-    size_t tab = align256((n / ptc::BT + A.E + 1) * sizeof(int4));  // pair tiles: at most n/BT + one partial per expert
-    size_t xb = align256(n * A.H * 2), hb = align256(n * A.I * 2), yb = align256(n * A.H * 2);
     char *b = static_cast<char *>(base);
-    w.mt_prefix = reinterpret_cast<int32_t *>(b);
-    w.table = b ? reinterpret_cast<int4 *>(b + tb) : nullptr;
-    w.xg = b ? reinterpret_cast<uint16_t *>(b + tb + tab) : nullptr;
-    w.h = b ? reinterpret_cast<uint16_t *>(b + tb + tab + xb) : nullptr;
-    w.y = b ? reinterpret_cast<uint16_t *>(b + tb + tab + xb + hb) : nullptr;
-    w.bytes = tb + tab + xb + hb + yb;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        char *p = b ? b + off : nullptr;
+        off += align256(bytes);
+        return p;
+    };
+    w.mt_prefix = reinterpret_cast<int32_t *>(take((A.E + 1) * sizeof(int32_t)));
+    w.table = reinterpret_cast<int4 *>(take((n / ptc::BT + A.E + 1) * sizeof(int4)));  // at most n/BT + one partial per expert
+    if (fp8) w.x8 = reinterpret_cast<uint8_t *>(take(n * A.H));
+    else w.xg = reinterpret_cast<uint16_t *>(take(n * A.H * 2));
+    w.h = reinterpret_cast<uint16_t *>(take(n * A.I * 2));
+    w.y = reinterpret_cast<uint16_t *>(take(n * A.H * 2));
+    if (fp8) {
+        w.h8 = reinterpret_cast<uint8_t *>(take(n * A.I));
+        w.ex = reinterpret_cast<int32_t *>(take(n * sizeof(int32_t)));
+        w.eh = reinterpret_cast<int32_t *>(take(n * sizeof(int32_t)));
+        w.kw_gu = reinterpret_cast<int8_t *>(take((size_t)A.E * 2 * A.I));
+        w.kw_d = reinterpret_cast<int8_t *>(take((size_t)A.E * A.H));
+    }
+    w.bytes = off;
     return w;
 }
 
@@ -689,6 +962,18 @@ bool prefill_tc_supported(const moe_expert_arena &A)
 }
 
 size_t prefill_tc_workspace_bytes(const moe_expert_arena &A, int T, int k) { return ptc_ws(A, T, k, nullptr).bytes; }
+
+// The FP8 variant takes 2-bit arenas whose H and I are multiples of 128 (a
+// step reduces over 128 elements).
+bool prefill_fp8_supported(const moe_expert_arena &A)
+{
+    return A.bits == 2 && prefill_tc_supported(A) && A.H % 128 == 0 && A.I % 128 == 0;
+}
+
+size_t prefill_fp8_workspace_bytes(const moe_expert_arena &A, int T, int k)
+{
+    return ptc_ws(A, T, k, nullptr, true).bytes;
+}
 
 template <int BITS>
 static moe_status run_tc(const moe_expert_arena &A, const uint16_t *x, int T, const float *w, int k,
@@ -771,6 +1056,108 @@ static moe_status run_tc(const moe_expert_arena &A, const uint16_t *x, int T, co
     st = launch_gemm<BITS, false>(b, mtok, mtokf, mcode, mscale, mout, grid, s);
     if (st != MOE_OK) return st;
     return launch_combine_f16(d.y, w, inv, T, k, A.H, out, dt, accumulate, s);
+}
+
+// The FP8 variant: the weights' row exponents, the pairs' e4m3 x rows, the
+// gate/up GEMM (h in fp16), h to e4m3, the down GEMM, the combine.
+static moe_status run_fp8(const moe_expert_arena &A, const uint16_t *x, int T, const float *w, int k,
+                          const int32_t *offsets, const int32_t *perm, const int32_t *inv, void *out, moe_dtype dt,
+                          int accumulate, const PtcWs &d, int32_t *status, cudaStream_t s)
+{
+    using namespace ptc;
+    using C = Cfg<2, true>;
+    int64_t n = (int64_t)T * k;
+    tile_prefix_kernel<<<1, 1024, 0, s>>>(offsets, A.E, BT, d.mt_prefix);
+    moe_status st = check_launch("tile_prefix");
+    if (st != MOE_OK) return st;
+    tile_table_kernel<<<(A.E + 255) / 256, 256, 0, s>>>(offsets, d.mt_prefix, A.E, BT, d.table);
+    st = check_launch("tile_table");
+    if (st != MOE_OK) return st;
+    const int sms = sm_count();
+    fp8_row_exponent_kernel<<<sms * 4, 256, 0, s>>>(A.gu_scales, offsets, A.E, 2 * A.I, A.H / 32, d.kw_gu, status);
+    st = check_launch("fp8_row_exponent");
+    if (st != MOE_OK) return st;
+    fp8_row_exponent_kernel<<<sms * 4, 256, 0, s>>>(A.d_scales, offsets, A.E, A.H, A.I / 32, d.kw_d, status);
+    st = check_launch("fp8_row_exponent");
+    if (st != MOE_OK) return st;
+    const int gblocks = (int)std::max<int64_t>(1, std::min<int64_t>((n + 7) / 8, (int64_t)sms * 16));  // 8 rows per CTA
+    gather_x_fp8_kernel<<<gblocks, 256, 0, s>>>(x, perm, offsets, A.E, k, A.H, d.x8, d.ex, status);
+    st = check_launch("gather_x_fp8");
+    if (st != MOE_OK) return st;
+    const int rbH = A.H / 4, rbI = A.I / 4;
+    const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    // gate/up: codes [E * 2I][rbH], pairs' e4m3 rows x8 [n][H] -> h [n][I] (fp16)
+    CUtensorMap mtok, mtokf, mcode, mscale, mout;
+    st = make_tmap_2d(&mtok, d.x8, U8, 1, n, A.H, C::BKE, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == MOE_OK) st = make_tmap_2d(&mtokf, d.x8, U8, 1, n, A.H, C::BKE, BT, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == MOE_OK)
+        st = make_tmap_2d(&mcode, A.gu_codes, U8, 1, (int64_t)A.E * 2 * A.I, rbH, C::CODE_STEP, 64,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st == MOE_OK) st = make_tmap_2d(&mout, d.h, F16, 2, n, A.I, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+    const bool sc_gu = A.H % 256 == 0;  // scale rows (H/32 fp16) are 16-byte multiples
+    mscale = mcode;
+    if (st == MOE_OK && sc_gu)
+        st = make_tmap_2d(&mscale, A.gu_scales, F16, 2, (int64_t)A.E * 2 * A.I, A.H / 32, 8, 64,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != MOE_OK) return st;
+    Args a = {};
+    a.scale_tma = sc_gu;
+    a.scales = A.gu_scales;
+    a.scales_expert_stride = (int64_t)2 * A.I * (A.H / 32);
+    a.code_rows = (int64_t)2 * A.I;
+    a.scale_row = A.H / 32;
+    a.K = A.H;
+    a.rows = A.I;
+    a.up_rows = A.I;
+    a.rtiles = (A.I + 63) / 64;
+    a.table = d.table;
+    a.ntt = d.mt_prefix + A.E;
+    a.h_out = d.h;
+    a.status = status;
+    a.kw = d.kw_gu;
+    a.pexp = d.ex;
+    st = launch_gemm<2, true, true>(a, mtok, mtokf, mcode, mscale, mout, sms, s);
+    if (st != MOE_OK) return st;
+    quantise_h_kernel<<<gblocks, 256, 0, s>>>(d.h, offsets, A.E, A.I, d.h8, d.eh);
+    st = check_launch("quantise_h");
+    if (st != MOE_OK) return st;
+    // down: codes [E * H][rbI], e4m3 h8 [n][I] -> y [n][H] (fp16)
+    st = make_tmap_2d(&mtok, d.h8, U8, 1, n, A.I, C::BKE, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == MOE_OK) st = make_tmap_2d(&mtokf, d.h8, U8, 1, n, A.I, C::BKE, BT, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == MOE_OK)
+        st = make_tmap_2d(&mcode, A.d_codes, U8, 1, (int64_t)A.E * A.H, rbI, C::CODE_STEP, 64,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st == MOE_OK) st = make_tmap_2d(&mout, d.y, F16, 2, n, A.H, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+    const bool sc_d = A.I % 256 == 0;
+    mscale = mcode;
+    if (st == MOE_OK && sc_d)
+        st = make_tmap_2d(&mscale, A.d_scales, F16, 2, (int64_t)A.E * A.H, A.I / 32, 8, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != MOE_OK) return st;
+    Args b = a;
+    b.scale_tma = sc_d;
+    b.scales = A.d_scales;
+    b.scales_expert_stride = (int64_t)A.H * (A.I / 32);
+    b.code_rows = A.H;
+    b.scale_row = A.I / 32;
+    b.K = A.I;
+    b.rows = A.H;
+    b.up_rows = 0;
+    b.rtiles = (A.H + 127) / 128;
+    b.h_out = nullptr;
+    b.y_out = d.y;
+    b.kw = d.kw_d;
+    b.pexp = d.eh;
+    st = launch_gemm<2, false, true>(b, mtok, mtokf, mcode, mscale, mout, sms, s);
+    if (st != MOE_OK) return st;
+    return launch_combine_f16(d.y, w, inv, T, k, A.H, out, dt, accumulate, s);
+}
+
+moe_status prefill_fp8_forward(const moe_expert_arena &A, const uint16_t *x, int T, const float *w, int k,
+                               const int32_t *offsets, const int32_t *perm, const int32_t *inv, void *out,
+                               moe_dtype dt, int accumulate, void *ws, int32_t *dev_status, cudaStream_t s)
+{
+    PtcWs d = ptc_ws(A, T, k, ws, true);
+    return run_fp8(A, x, T, w, k, offsets, perm, inv, out, dt, accumulate, d, dev_status, s);
 }
 
 moe_status prefill_tc_forward(const moe_expert_arena &A, const uint16_t *x, int T, const float *w, int k,

@@ -189,6 +189,20 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f8f6f4 with e4m3 A and B (the
+// instruction descriptor's format fields are 0 for e4m3, as for fp16): A is M
+// rows in TMEM lanes, K packed four 8-bit elements per 32-bit column; one
+// instruction reduces over K = 32.
+__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on the mbarrier once all previously issued tcgen05 MMAs of this thread completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar)
 {

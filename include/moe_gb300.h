@@ -76,16 +76,19 @@ typedef enum moe_status {
     MOE_ERR_NONFINITE = 6,   /* a NaN router logit                            */
     MOE_ERR_BOUNDS = 7,      /* an expert id outside [0, E)                   */
     MOE_ERR_RANGE = 8        /* a value outside the finite range of the fp16
-                                operands the tensor cores take (see the PREFILL
-                                path of moe_expert_forward, moe_decode_forward) */
+                                or e4m3 operands the tensor cores take (see the
+                                PREFILL and PREFILL_FP8 paths of
+                                moe_expert_forward, moe_decode_forward) */
 } moe_status;
 
 typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 
 typedef enum moe_path {
-    MOE_PATH_AUTO = 0,    /* DECODE for T <= 8, PREFILL otherwise           */
-    MOE_PATH_DECODE = 1,  /* dequant-fused GEMVs on CUDA cores, fp32 maths  */
-    MOE_PATH_PREFILL = 2  /* grouped GEMM over the experts' token lists     */
+    MOE_PATH_AUTO = 0,        /* DECODE for T <= 8, PREFILL otherwise (never FP8) */
+    MOE_PATH_DECODE = 1,      /* dequant-fused GEMVs on CUDA cores, fp32 maths  */
+    MOE_PATH_PREFILL = 2,     /* grouped GEMM over the experts' token lists     */
+    MOE_PATH_PREFILL_FP8 = 3  /* the same GEMMs on e4m3 operands: an opt-in
+                                 approximation, see moe_expert_forward       */
 } moe_path;
 
 /* Message for the last non-OK status returned on this thread ("" if none). */
@@ -313,6 +316,21 @@ moe_status moe_permute_noalloc(const int32_t *ids, int T, int k, int E, int32_t 
  *   (|x| of order 1) and weight scales of order 0.02 stay far inside.  A value
  *   outside it sets *dev_status = MOE_ERR_RANGE and the affected outputs are
  *   not finite.  Other shapes take an fp32 FFMA form with no such limit.
+ * PREFILL_FP8: the PREFILL GEMMs with e4m3 operands (kind::f8f6f4 tensor-core
+ *   instructions), an opt-in approximation that AUTO never picks.  2-bit
+ *   arenas with H and I multiples of 128 only; anything else returns
+ *   MOE_ERR_UNSUPPORTED.  Every operand is an e4m3 value after a power-of-two
+ *   scaling 2^e with e = 7 - floor(log2 m) (clamped to [-64, 64]), m the
+ *   largest magnitude it covers: one e per weight row (m = 1.5 times the
+ *   row's largest |s|), per pair for x, and per pair for h, which is first
+ *   rounded to fp16 as in PREFILL; each weight is e4m3((c - 1.5) s 2^e),
+ *   rounded once.  Products accumulate in fp32 and the scalings are undone on
+ *   the accumulators; y is kept as fp16 until the combine.  The rounding of
+ *   three operands to 3 mantissa bits costs a relative L2 error of about
+ *   6e-2 on one expert's output and about 3e-2 on a layer whose bf16 shared
+ *   expert is added (H=2048, I=768, N(0,1) inputs), not the 1e-3 of PREFILL.
+ *   MOE_ERR_RANGE: a non-finite x or block scale, an |x| above 464 * 2^64, or
+ *   an h or y outside fp16's range (as in PREFILL).
  * Workspace: moe_expert_forward_workspace_size for the same arguments.
  * The pages: each token's routed experts run on the GPU and their finished
  * output vectors are summed there, weighted by the router ("How Strata runs

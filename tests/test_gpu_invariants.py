@@ -1,5 +1,5 @@
-"""Invariants of the layer on the GPU paths, which hold whatever the oracle
-says: all block scales zero leaves only the shared expert; identical experts
+"""Invariants of the layer on the GPU paths (the FP8 prefill included), which
+hold whatever the oracle says: all block scales zero leaves only the shared expert; identical experts
 make the routed sum one expert's output (the weights sum to one); renaming
 the experts together with their router rows and biases changes nothing."""
 import numpy as np
@@ -14,7 +14,7 @@ from helpers import host_layer, rel_l2
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 H, I, E, K, IS, T = 256, 128, 16, 2, 128, 8
-PATHS = [m.MOE_PATH_DECODE, m.MOE_PATH_PREFILL]
+PATHS = [m.MOE_PATH_DECODE, m.MOE_PATH_PREFILL, m.MOE_PATH_PREFILL_FP8]
 
 
 def layer(arena, wr, b, shared, bits=2):
@@ -45,6 +45,8 @@ def fused(layers, x0, T_):
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("bits", [2, 3])
 def test_zero_scales_leave_the_shared_expert(moe, path, bits):
+    if path == m.MOE_PATH_PREFILL_FP8 and bits == 3:
+        pytest.skip("the FP8 prefill takes 2-bit codes")
     arena, wr, b, shared = host_layer(seed=31, bits=bits, H=H, I=I, E=E, Is=IS, zipf=1.1)
     arena = [a if i % 2 == 0 else np.zeros_like(a) for i, a in enumerate(arena)]  # every scale +0
     L = layer(arena, wr, b, shared, bits)

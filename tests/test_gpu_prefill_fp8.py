@@ -1,0 +1,178 @@
+"""The FP8 prefill (MOE_PATH_PREFILL_FP8) on the GPU.
+
+Parity: the path computes the FP8 variant of the routed experts that the
+oracle states (oracle_expert_ffn_fp8: e4m3 operands after power-of-two
+scalings per weight row, per token and per h vector, h rounded to fp16
+first).  Both sides round x and the weights identically (the same inputs,
+the same round-to-nearest-even e4m3), and h identically except where fp32
+accumulation moves an h across an fp16 or e4m3 rounding boundary, which is
+rare; y is held in fp16 before the combine (about 1.4e-4 relative).  So the
+layer output is compared with the oracle's FP8 layer at FP8_TOL.
+
+Approximation: the same outputs against the exact layer (oracle_moe_layer)
+measure what the e4m3 operands cost.  The stated target for an FP8 prefill
+is a relative L2 error of 2e-2; this scheme measures about 3e-2 on the
+full-size layer (about 6e-2 on one expert's output: the three roundings to
+3 mantissa bits, weights about 4.8e-2, x about 3.5e-2, h about 2.7e-2), so
+the target is not met; the tests hold the path to its own measured levels
+(FP8_ROUTED_BOUND, FP8_LAYER_BOUND) and print the figures.  On the small
+layers below the shared expert carries less of the output and the layer
+error is larger (up to about 5e-2).
+"""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+import torch
+
+import bit_expert_ffn_gb300 as m
+import oracle
+from bit_expert_ffn_gb300 import synth
+from bit_expert_ffn_gb300.model import LayerShape, MoeLayer, StepBuffers, Workspace
+from helpers import host_layer, oracle_sampled_layer, rel_l2
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+FP8 = m.MOE_PATH_PREFILL_FP8
+FP8_TOL = 1e-3           # routed sum against the oracle's FP8 routed sum (measured 2e-4 to 3e-4)
+FP8_ROUTED_BOUND = 0.1   # routed sum against the exact one (measured about 6e-2 at H=2048, I=768)
+FP8_LAYER_BOUND = 5e-2   # full-size layer against the exact layer (measured about 3e-2; the target is 2e-2)
+
+
+def dev_u16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.uint16).view(np.int16)).to(DEV)
+
+
+def make_layer(bits=2, H=256, I=128, E=16, k=4, Is=128, zipf=1.4, seed=0):
+    arena, wr, b, shared = host_layer(seed=seed, bits=bits, H=H, I=I, E=E, Is=Is, zipf=zipf)
+    L = MoeLayer(LayerShape(H=H, I=I, E=E, k=k, Is=Is, bits=bits), DEV)
+    L.load_host(*arena, wr, b, shared)
+    return L, arena, shared
+
+
+def run(L, x, T, path=FP8, with_shared=True):
+    bufs = StepBuffers(T, L.s.E, L.s.k)
+    out = torch.zeros(T, L.s.H, dtype=torch.float32, device=DEV)
+    L.forward(dev_u16(x), T, out, Workspace(DEV), bufs, accumulate=False, path=path, with_shared=with_shared)
+    return m.moe_check_status(L.status), out.cpu().numpy(), bufs
+
+
+@pytest.mark.parametrize("T,E,k,H,I", [
+    (8, 16, 2, 256, 128),
+    (300, 16, 4, 256, 128),
+    (3000, 32, 10, 256, 128),   # several 192-pair tiles per expert and ragged ones
+    (700, 16, 4, 640, 384),     # five 128-row down tiles, six 64-row gate/up tiles
+    (1, 16, 4, 256, 128),
+])
+def test_fp8_matches_the_fp8_oracle(moe, T, E, k, H, I):
+    """The routed sum alone against the oracle's FP8 routed sum (the shared expert, exact on both sides,
+    would dilute a mistake), then the whole layer against the exact one."""
+    L, arena, shared = make_layer(H=H, I=I, E=E, k=k, seed=T)
+    x = synth.activations(T, T, H)
+    st, routed, bufs = run(L, x, T, with_shared=False)
+    assert st == 0, m.moe_last_error()
+    counts = np.diff(bufs.offsets.cpu().numpy())
+    if T >= 300:
+        assert (counts % 32 != 0).any()  # ragged pair tiles
+    if T == 3000:
+        assert counts.max() > 2 * 192
+    ids = bufs.ids.cpu().numpy()
+    w = bufs.w.cpu().numpy().astype(np.float64)
+    want8 = oracle.moe_layer(2, x, ids, w, *arena, shared=None, fp8=True)
+    e8 = rel_l2(routed, want8)
+    er = rel_l2(routed, oracle.moe_layer(2, x, ids, w, *arena, shared=None))
+    st, layer, _ = run(L, x, T)
+    assert st == 0, m.moe_last_error()
+    ex = rel_l2(layer, oracle.moe_layer(2, x, ids, w, *arena, shared=shared))
+    print(f"T={T} H={H} I={I}: routed sum vs the FP8 oracle {e8:.3g}, vs the exact routed sum {er:.3g}; "
+          f"layer vs the exact layer {ex:.3g}")
+    assert e8 <= FP8_TOL
+    assert er <= FP8_ROUTED_BOUND
+
+
+def test_fp8_32k_prefill_sampled(moe):
+    """The 32,768-token prefill layer (H=2048, E=512, I=768, top-10, Zipf(1.1), weights drawn on the GPU):
+    sampled tokens, among them tokens of the three most loaded experts, against both oracles."""
+    seed, layer, T = 1, 0, 32768
+    s = LayerShape()
+    L = MoeLayer(s, DEV)
+    L.fill_device(seed, layer, zipf_s=1.1)
+    x = synth.activations(seed, T, s.H)
+    st, routed, bufs = run(L, x, T, with_shared=False)
+    assert st == 0, m.moe_last_error()
+    st, got, _ = run(L, x, T)
+    assert st == 0, m.moe_last_error()
+    ids = bufs.ids.cpu().numpy()
+    w = bufs.w.cpu().numpy()
+    offsets, perm = bufs.offsets.cpu().numpy(), bufs.perm.cpu().numpy()
+    counts = np.diff(offsets)
+    tokens = set()
+    for e in np.argsort(-counts, kind="stable")[:3]:
+        lst = perm[offsets[e]:offsets[e + 1]] // s.k
+        tokens.update(int(t) for t in (lst[0], lst[len(lst) // 2], lst[-1]))
+    tokens.update(int(t) for t in np.random.default_rng(6).choice(T, 7, replace=False))
+    tokens = sorted(tokens)
+    shared = synth.shared_weights(seed, layer, s.H, s.Is)
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as pool:
+        want8 = oracle_sampled_layer(seed, layer, 2, s.H, s.I, x[tokens], ids[tokens], w[tokens], None, pool,
+                                     fp8=True)
+        exact = oracle_sampled_layer(seed, layer, 2, s.H, s.I, x[tokens], ids[tokens], w[tokens], shared, pool)
+    e8, ex = rel_l2(routed[tokens], want8), rel_l2(got[tokens], exact)
+    print(f"32K prefill, {len(tokens)} sampled tokens: routed sum vs the FP8 oracle {e8:.3g}, layer vs the exact "
+          f"layer {ex:.3g} (the 2e-2 target is not met)")
+    assert e8 <= FP8_TOL
+    assert ex <= FP8_LAYER_BOUND
+
+
+def test_fp8_is_close_to_the_fp16_prefill(moe):
+    """The two tensor-core prefills on the same layer differ by the FP8 rounding only."""
+    L, arena, shared = make_layer(H=256, I=128, E=16, k=4, seed=41)
+    x = synth.activations(41, 500, 256)
+    st8, y8, _ = run(L, x, 500, with_shared=False)
+    st16, y16, _ = run(L, x, 500, m.MOE_PATH_PREFILL, with_shared=False)
+    assert st8 == 0 and st16 == 0
+    assert 1e-3 < rel_l2(y8, y16) <= FP8_ROUTED_BOUND
+
+
+@pytest.mark.parametrize("bits,H,I", [(3, 256, 128), (2, 320, 192), (2, 256, 192)])
+def test_fp8_rejects_what_it_does_not_implement(moe, bits, H, I):
+    L, _, _ = make_layer(bits=bits, H=H, I=I)
+    with pytest.raises(m.MoeError) as e:
+        run(L, synth.activations(1, 40, H), 40)
+    assert e.value.status == m.MOE_ERR_UNSUPPORTED
+
+
+def test_fp8_reports_nonfinite_x_and_scales(moe):
+    L, arena, shared = make_layer(seed=43)
+    x = synth.activations(43, 200, 256)
+    # past e4m3's range even after the largest down-scaling (464 * 2^64), yet finite for the router
+    x[7, 3] = synth.f32_to_bf16_bits(np.array([1e30], np.float32))[0]
+    st, out, _ = run(L, x, 200, with_shared=False)
+    assert st == m.MOE_ERR_RANGE
+    st, _, _ = run(L, synth.activations(43, 200, 256), 200)  # the context is still usable
+    assert st == 0
+    # moe_pack_experts refuses a non-finite scale, so plant one in the packed arena directly: down row 3,
+    # block 1 of every expert
+    L.d_scales.view(16, 256, 128 // 32)[:, 3, 1] = 0x7C00  # +inf
+    st, _, _ = run(L, synth.activations(44, 200, 256), 200, with_shared=False)
+    assert st == m.MOE_ERR_RANGE
+
+
+def test_fp8_wide_scales_keep_their_precision(moe):
+    """Activations 1000 times larger and gate/up block scales 1000 times smaller than the workloads' (fp16
+    subnormal scales among them) leave the FP8 result where it was relative to the oracle: the power-of-two
+    scalings absorb both.  (The down scales stay, so y keeps clear of fp16's subnormals, where its fp16
+    copy before the combine would lose bits the oracle keeps.)"""
+    arena, wr, b, shared = host_layer(seed=45, H=256, I=128, E=16, Is=128, zipf=1.4)
+    arena = list(arena)
+    for i in (1, 3):
+        arena[i] = (arena[i].view(np.float16).astype(np.float32) * np.float32(1e-3)).astype(np.float16).view(np.uint16)
+    L = MoeLayer(LayerShape(H=256, I=128, E=16, k=4, Is=128), DEV)
+    L.load_host(*arena, wr, b, shared)
+    x = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(synth.activations(45, 300, 256)) * np.float32(1000.0))
+    st, got, bufs = run(L, x, 300, with_shared=False)
+    assert st == 0, m.moe_last_error()
+    want8 = oracle.moe_layer(2, x, bufs.ids.cpu().numpy(), bufs.w.cpu().numpy().astype(np.float64), *arena,
+                             shared=None, fp8=True)
+    assert rel_l2(got, want8) <= FP8_TOL
