@@ -77,11 +77,13 @@ constexpr int NA = 4, NB = 6;          // weight ring (TMEM), pair ring (shared 
 constexpr int TM_A = 2 * BT;
 static_assert(TM_A + NA * 32 <= 512, "TMEM columns");
 constexpr int XCH_BYTES = 32 * 64 * 4;  // up values of one 32-pair chunk: 64 rows, fp32
-// Epilogue area.  down: four fp32 32 x 32 staging blocks; gate/up: two fp16
-// 32 x 32 staging blocks, then two exchange buffers.
-constexpr int STG_DOWN = 32 * 32 * 4, STG_H = 32 * 32 * 2;
-constexpr int OFF_XCH = 2 * STG_H;
-constexpr int EPI_BYTES = OFF_XCH + 2 * XCH_BYTES > 4 * STG_DOWN ? OFF_XCH + 2 * XCH_BYTES : 4 * STG_DOWN;
+// Epilogue area.  Every storing warp has two fp16 32 x 32 staging blocks used
+// in turn, so one chunk's TMA store can still be reading a block while the
+// next chunk fills the other.  down: four warps x two blocks; gate/up: the
+// two gate warps x two blocks, then two exchange buffers.
+constexpr int STG = 32 * 32 * 2;
+constexpr int OFF_XCH = 2 * 2 * STG;
+constexpr int EPI_BYTES = OFF_XCH + 2 * XCH_BYTES > 4 * 2 * STG ? OFF_XCH + 2 * XCH_BYTES : 4 * 2 * STG;
 constexpr int THREADS = 832;
 constexpr int DQ_WARP0 = 8;  // warps 8..23 dequantise: four threads per weight row
 constexpr int DQ_WARPS = 16;
@@ -489,14 +491,25 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         // ---------------- epilogue: TMEM -> registers -> shared (transposed) -> TMA store
         const int q = warp - EPI_WARP0;  // TMEM lane quadrant: weight rows 32q .. 32q+31 of the tile
         float *xch = reinterpret_cast<float *>(dyn + C::OFF_E + OFF_XCH);
-        char *stg = dyn + C::OFF_E + q * (SWIGLU ? STG_H : STG_DOWN);  // this warp's staging block
+        char *stg = dyn + C::OFF_E + q * 2 * STG;  // this warp's two staging blocks (gate/up: warps 0, 1)
         bool out_of_range = false;  // an h or y value that has no finite fp16
-        int j = 0;
+        int j = 0, nst = 0;         // nst: TMA stores this warp issued (block nst & 1 is next)
         // the gate/up warps meet at named barriers, so they decide together
         // whether to stop (the OR over the four warps); the down warps alone
         int4 nxt = tile_entry(a, blockIdx.x, total);
         for (int tile = blockIdx.x; tile < total && (SWIGLU || !S.abort); tile += gridDim.x, j++) {
             int acc = j & 1, v = j >> 1;
+            Tile t = make_tile(a, nxt, tile);
+            nxt = tile_entry(a, tile + gridDim.x, total);
+            // FP8: the exponents this tile needs are loaded before the accumulator wait (and each
+            // chunk's pair exponents one chunk ahead), so their latency hides behind the wait
+            int kwr = 0, pe_next = 0;
+            if constexpr (FP8) {
+                const int orow = SWIGLU ? t.rt * 64 + (q & 1) * 32 + lane : t.rt * 128 + q * 32 + lane;
+                const int64_t mrow = SWIGLU && q >= 2 ? (int64_t)a.up_rows + orow : orow;
+                if (orow < a.rows) kwr = __ldg(a.kw + (int64_t)t.e * a.code_rows + mrow);
+                if (lane < t.cnt) pe_next = __ldg(a.pexp + t.p0 + lane);
+            }
             bool stop = !tc::mbar_wait_sleep(&S.acc_full[acc], v & 1, kWaitNs);
             stop = __any_sync(0xffffffffu, stop);  // the warp's TMEM loads need all its lanes
             if (stop) {
@@ -507,28 +520,26 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             if (SWIGLU) stop = tc::named_sync_or(2, 128, stop);
             if (stop) break;
             tc::tc_fence_after();
-            Tile t = make_tile(a, nxt, tile);
-            nxt = tile_entry(a, tile + gridDim.x, total);
             uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BT);
-            float frow = 1.f;  // FP8: 2^-kw of this lane's weight row (kw from fp16 scales lies in [-9, 31])
-            if constexpr (FP8) {
-                const int orow = SWIGLU ? t.rt * 64 + (q & 1) * 32 + lane : t.rt * 128 + q * 32 + lane;
-                const int64_t mrow = SWIGLU && q >= 2 ? (int64_t)a.up_rows + orow : orow;
-                if (orow < a.rows) frow = exp2i(-__ldg(a.kw + (int64_t)t.e * a.code_rows + mrow));
-            }
+            const float frow = exp2i(-kwr);  // FP8: 2^-kw of this lane's weight row (kw lies in [-9, 31])
             for (int ch = 0; ch < t.n32; ch++) {
                 uint32_t r[32];
                 __syncwarp();
                 tc::tmem_ld_32x32b_x32(tbase + ch * 32, r);
-                tc::tmem_ld_wait();
                 int tok0 = ch * 32;
                 bool full = tok0 + 32 <= t.cnt;
                 int nv = min(32, t.cnt - tok0);
+                int pe = 0;
+                if constexpr (FP8) {
+                    pe = pe_next;
+                    if (tok0 + 32 + lane < t.cnt) pe_next = __ldg(a.pexp + t.p0 + tok0 + 32 + lane);
+                }
+                tc::tmem_ld_wait();
                 if constexpr (FP8) {
                     // undo the operands' scalings: 2^-kw of the weight row, then 2^-e of pair i (e in
                     // [-64, 64]); the two factors are exact, so their order does not matter while the
                     // product stays a normal fp32
-                    const float fpair = exp2i(-(tok0 + lane < t.cnt ? __ldg(a.pexp + t.p0 + tok0 + lane) : 0));
+                    const float fpair = exp2i(-pe);
 #pragma unroll
                     for (int i = 0; i < 32; i++)
                         r[i] = __float_as_uint(__uint_as_float(r[i]) * frow * __shfl_sync(0xffffffffu, fpair, i));
@@ -554,8 +565,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                             hv[i] = __half_as_ushort(__float2half_rn(hf));
                         }
                         if (full) {
-                            uint16_t *sb = reinterpret_cast<uint16_t *>(stg);
-                            if (lane == 0) tc::bulk_wait_read<0>();
+                            // the block's previous store (two stores back) has finished reading it
+                            uint16_t *sb = reinterpret_cast<uint16_t *>(stg + (nst & 1) * STG);
+                            if (lane == 0) tc::bulk_wait_read<1>();
                             __syncwarp();
 #pragma unroll
                             for (int i = 0; i < 32; i++) sb[i * 32 + pos] = hv[i];
@@ -565,6 +577,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                                 tc::tma_store_2d(&out_map, orow0, t.p0 + tok0, sb);
                                 tc::bulk_commit();
                             }
+                            nst++;
                         } else {
                             uint16_t *dst = a.h_out + (int64_t)(t.p0 + tok0) * a.rows + orow0 + pos;
 #pragma unroll
@@ -579,8 +592,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                         for (int i = 0; i < 32; i++)
                             out_of_range |= i < nv && !(fabsf(__uint_as_float(r[i])) < kF16Limit);
                         if (full) {
-                            uint16_t *sb = reinterpret_cast<uint16_t *>(stg);
-                            if (lane == 0) tc::bulk_wait_read<0>();
+                            uint16_t *sb = reinterpret_cast<uint16_t *>(stg + (nst & 1) * STG);
+                            if (lane == 0) tc::bulk_wait_read<1>();
                             __syncwarp();
 #pragma unroll
                             for (int i = 0; i < 32; i++)
@@ -591,6 +604,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                                 tc::tma_store_2d(&out_map, o0, t.p0 + tok0, sb);
                                 tc::bulk_commit();
                             }
+                            nst++;
                         } else {
                             uint16_t *dst = a.y_out + (int64_t)(t.p0 + tok0) * a.rows + o0 + lane;
 #pragma unroll
