@@ -17,11 +17,13 @@
 //               ring (shared memory, several steps ahead);
 //   warp 0      TMA: the pairs' fp16 rows of each step into the pair ring
 //               (shared memory, 128-byte swizzle);
-//   warps 24-25 wait for free slots of the pair and code rings and hand
+//   warps 16-17 wait for free slots of the pair and code rings and hand
 //               them to the two TMA warps (an mbarrier call right after
 //               queued copies would stall the issuing thread);
-//   warps 8-23  dequantise codes straight into the weight ring in TMEM
-//               (tcgen05.st; a warp per lane quadrant and 16-weight group);
+//   warps 8-15  dequantise codes straight into the weight ring in TMEM
+//               (tcgen05.st; a warp per lane quadrant, two warps per
+//               quadrant taking every other step: more warps only add
+//               issue-slot contention with the MMA and epilogue warps);
 //   warp 1      tcgen05.mma M=128, N=32..192, K=16 with the weights read
 //               from TMEM and the pairs from shared memory, into two TMEM
 //               accumulator buffers (the epilogue of one tile overlaps the
@@ -84,11 +86,11 @@ constexpr int XCH_BYTES = 32 * 64 * 4;  // up values of one 32-pair chunk: 64 ro
 constexpr int STG = 32 * 32 * 2;
 constexpr int OFF_XCH = 2 * 2 * STG;
 constexpr int EPI_BYTES = OFF_XCH + 2 * XCH_BYTES > 4 * 2 * STG ? OFF_XCH + 2 * XCH_BYTES : 4 * 2 * STG;
-constexpr int THREADS = 832;
-constexpr int DQ_WARP0 = 8;  // warps 8..23 dequantise: four threads per weight row
-constexpr int DQ_WARPS = 16;
-constexpr int RING_WARP = 24;  // waits for free pair slots for the pair TMA issuer
-constexpr int CODE_WARP = 25;  // waits for free code slots for the code TMA issuer
+constexpr int THREADS = 576;
+constexpr int DQ_WARP0 = 8;  // warps 8..15 dequantise: two threads per weight row, each every other step
+constexpr int DQ_WARPS = 8;
+constexpr int RING_WARP = 16;  // waits for free pair slots for the pair TMA issuer
+constexpr int CODE_WARP = 17;  // waits for free code slots for the code TMA issuer
 constexpr int EPI_WARP0 = 4;
 constexpr int NC_MAX = 8;
 constexpr unsigned long long kWaitNs = 2000000000ull;
@@ -301,7 +303,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     const int warp = warp_id(), lane = lane_id();
     if (threadIdx.x == 0) {
         for (int s = 0; s < NA; s++) {
-            tc::mbar_init(&S.afull[s], DQ_WARPS / 4);
+            tc::mbar_init(&S.afull[s], 4);  // the four lane-quadrant warps of a step
             tc::mbar_init(&S.aempty[s], 1);
         }
         for (int s = 0; s < NB; s++) {
@@ -310,7 +312,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         }
         for (int s = 0; s < C::NC; s++) {
             tc::mbar_init(&S.cfull[s], 1);
-            tc::mbar_init(&S.cempty[s], DQ_WARPS / 4);
+            tc::mbar_init(&S.cempty[s], 4);
         }
         for (int i = 0; i < 2; i++) {
             tc::mbar_init(&S.acc_full[i], 1);
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     const int nk = a.K / C::BKE;
 
     if (warp == 0 || warp == 3 || warp == RING_WARP || warp == CODE_WARP) {
-        // ---------------- TMA: warps 24 and 25 wait for free pair and code slots and
+        // ---------------- TMA: warps 16 and 17 wait for free pair and code slots and
         // post the expected bytes; they hand each step over by named barriers 4
         // (pair rows, issued by warp 0) and 5 (codes and scales, issued by warp 3),
         // so the issuing threads make no mbarrier calls between their copies.
@@ -623,7 +625,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         __syncwarp();
     } else if (warp >= DQ_WARP0 && warp < DQ_WARP0 + DQ_WARPS) {
         // ---------------- dequantisation into TMEM: warp = (lane quadrant qd, step group jg); the
-        // four warps of group jg take every fourth step, each a whole 64-wide step of its 32 rows
+        // four warps of group jg take every other step, each a whole step of its 32 rows
         // (one 16-byte read of the row's codes, four 16-weight groups, one store wait per step)
         const int dw = warp - DQ_WARP0;
         const int qd = warp & 3, jg = dw >> 2;
@@ -643,8 +645,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             float p2kw = 1.f;  // FP8: 2^kw, the scaling of this weight row (kw in [-9, 31])
             if constexpr (FP8)
                 if (valid) p2kw = exp2i(__ldg(a.kw + (int64_t)t.e * a.code_rows + mrow));
-            // the steps of this tile that belong to group jg: global step index = jg (mod 4)
-            for (int kb = (jg - base) & 3; kb < nk; kb += 4) {
+            // the steps of this tile that belong to group jg: global step index = jg (mod 2)
+            for (int kb = (jg - base) & 1; kb < nk; kb += 2) {
                 const int it = base + kb;
                 Slot c = slot_of(it, C::NC), sa = slot_of(it, NA);
                 uint32_t sc = 0;  // the step's two block scales (low half: first block)
