@@ -749,7 +749,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
 // x_g[p][16g + perm16(m)] = fp16(x[tok(p)][16g + m]) for the valid pairs; an
 // x without a finite fp16 sets MOE_ERR_RANGE.  One warp per pair row (its
 // token looked up once), lanes over the row's 16-element groups, so loads and
-// stores are coalesced 16-byte accesses.
+// stores are coalesced 16-byte accesses; each lane issues the loads of up to
+// four groups before converting any, so several reads are in flight.
 __global__ void gather_x_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm,
                                 const int32_t *__restrict__ offsets, int E, int k, int H, uint16_t *__restrict__ xg,
                                 int32_t *__restrict__ status)
@@ -762,25 +763,39 @@ __global__ void gather_x_kernel(const uint16_t *__restrict__ x, const int32_t *_
         const int tok = perm[p] / k;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)tok * H);
         uint4 *dst = reinterpret_cast<uint4 *>(xg + (int64_t)p * H);
-        for (int g = lane; g < groups; g += 32) {
-            const uint4 a0 = __ldg(src + 2 * g), a1 = __ldg(src + 2 * g + 1);
-            const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            float f[16];
+        for (int g0 = 0; g0 < groups; g0 += 4 * 32) {
+            uint4 a[4][2];
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
-                f[2 * j] = __uint_as_float(w[j] << 16);
-                f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+            for (int u = 0; u < 4; u++) {
+                const int g = g0 + u * 32 + lane;
+                if (g < groups) {
+                    a[u][0] = __ldg(src + 2 * g);
+                    a[u][1] = __ldg(src + 2 * g + 1);
+                }
             }
 #pragma unroll
-            for (int mm = 0; mm < 16; mm++) out_of_range |= !(fabsf(f[mm]) < kF16Limit);
-            uint32_t o[8];
+            for (int u = 0; u < 4; u++) {
+                const int g = g0 + u * 32 + lane;
+                if (g >= groups) continue;
+                const uint32_t w[8] = {a[u][0].x, a[u][0].y, a[u][0].z, a[u][0].w,
+                                       a[u][1].x, a[u][1].y, a[u][1].z, a[u][1].w};
+                float f[16];
 #pragma unroll
-            for (int mm = 0; mm < 8; mm++) {
-                __half2 hv = __floats2half2_rn(f[mm], f[mm + 8]);
-                o[mm] = *reinterpret_cast<uint32_t *>(&hv);
+                for (int j = 0; j < 8; j++) {
+                    f[2 * j] = __uint_as_float(w[j] << 16);
+                    f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+                }
+#pragma unroll
+                for (int mm = 0; mm < 16; mm++) out_of_range |= !(fabsf(f[mm]) < kF16Limit);
+                uint32_t o[8];
+#pragma unroll
+                for (int mm = 0; mm < 8; mm++) {
+                    __half2 hv = __floats2half2_rn(f[mm], f[mm + 8]);
+                    o[mm] = *reinterpret_cast<uint32_t *>(&hv);
+                }
+                dst[2 * g] = make_uint4(o[0], o[1], o[2], o[3]);
+                dst[2 * g + 1] = make_uint4(o[4], o[5], o[6], o[7]);
             }
-            dst[2 * g] = make_uint4(o[0], o[1], o[2], o[3]);
-            dst[2 * g + 1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
     }
     if (out_of_range) set_status(status, MOE_ERR_RANGE);
@@ -849,12 +864,34 @@ __global__ void gather_x_fp8_kernel(const uint16_t *__restrict__ x, const int32_
     for (int p = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); p < n; p += warps) {
         const int tok = perm[p] / k;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)tok * H);
+        // rows of up to 128 groups stay in registers between the two passes; longer ones are read twice
+        const bool held = groups <= 4 * 32;
+        uint4 a[4][2];
         uint32_t mx = 0;  // largest |x| as bf16 bits
-        for (int g = lane; g < groups; g += 32) {
-            const uint4 a0 = __ldg(src + 2 * g), a1 = __ldg(src + 2 * g + 1);
-            const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        if (held) {
 #pragma unroll
-            for (int j = 0; j < 8; j++) mx = max(mx, max(w[j] & 0x7fffu, (w[j] >> 16) & 0x7fffu));
+            for (int u = 0; u < 4; u++) {
+                const int g = u * 32 + lane;
+                a[u][0] = a[u][1] = make_uint4(0u, 0u, 0u, 0u);
+                if (g < groups) {
+                    a[u][0] = __ldg(src + 2 * g);
+                    a[u][1] = __ldg(src + 2 * g + 1);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const uint32_t w[8] = {a[u][0].x, a[u][0].y, a[u][0].z, a[u][0].w,
+                                       a[u][1].x, a[u][1].y, a[u][1].z, a[u][1].w};
+#pragma unroll
+                for (int j = 0; j < 8; j++) mx = max(mx, max(w[j] & 0x7fffu, (w[j] >> 16) & 0x7fffu));
+            }
+        } else {
+            for (int g = lane; g < groups; g += 32) {
+                const uint4 a0 = __ldg(src + 2 * g), a1 = __ldg(src + 2 * g + 1);
+                const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                for (int j = 0; j < 8; j++) mx = max(mx, max(w[j] & 0x7fffu, (w[j] >> 16) & 0x7fffu));
+            }
         }
         mx = __reduce_max_sync(0xffffffffu, mx);
         const float amax = __uint_as_float(mx << 16);
@@ -863,8 +900,8 @@ __global__ void gather_x_fp8_kernel(const uint16_t *__restrict__ x, const int32_
         if (lane == 0) pexp[p] = ex;
         const float sc = exp2i(ex);
         uint4 *dst = reinterpret_cast<uint4 *>(x8 + (int64_t)p * H);
-        for (int g = lane; g < groups; g += 32) {
-            const uint4 a0 = __ldg(src + 2 * g), a1 = __ldg(src + 2 * g + 1);
+        // stored bytes 0-3: elements 0, 2, 4, 6; 4-7: 8, 10, 12, 14; 8-11: 1, 3, 5, 7; 12-15: 9, 11, 13, 15
+        auto put = [&](const uint4 &a0, const uint4 &a1, int g) {
             const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             float f[16];
 #pragma unroll
@@ -872,7 +909,6 @@ __global__ void gather_x_fp8_kernel(const uint16_t *__restrict__ x, const int32_
                 f[2 * j] = __uint_as_float(w[j] << 16) * sc;
                 f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u) * sc;
             }
-            // stored bytes 0-3: elements 0, 2, 4, 6; 4-7: 8, 10, 12, 14; 8-11: 1, 3, 5, 7; 12-15: 9, 11, 13, 15
             uint32_t o[4];
 #pragma unroll
             for (int q = 0; q < 4; q++) {
@@ -880,6 +916,13 @@ __global__ void gather_x_fp8_kernel(const uint16_t *__restrict__ x, const int32_
                 o[q] = e4m3x2(f[m0 + 2], f[m0]) | (e4m3x2(f[m0 + 6], f[m0 + 4]) << 16);
             }
             dst[g] = make_uint4(o[0], o[1], o[2], o[3]);
+        };
+        if (held) {
+#pragma unroll
+            for (int u = 0; u < 4; u++)
+                if (u * 32 + lane < groups) put(a[u][0], a[u][1], u * 32 + lane);
+        } else {
+            for (int g = lane; g < groups; g += 32) put(__ldg(src + 2 * g), __ldg(src + 2 * g + 1), g);
         }
     }
     if (out_of_range) set_status(status, MOE_ERR_RANGE);
@@ -896,21 +939,33 @@ __global__ void quantise_h_kernel(const uint16_t *__restrict__ h, const int32_t 
     const int warps = (int)(gridDim.x * blockDim.x >> 5);
     for (int p = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); p < n; p += warps) {
         const uint4 *src = reinterpret_cast<const uint4 *>(h + (int64_t)p * I);
+        // rows of up to 128 chunks of eight stay in registers between the two passes
+        const bool held = chunks <= 4 * 32;
+        uint4 v[4];
         uint32_t mx = 0;  // largest |h| as fp16 bits
-        for (int c = lane; c < chunks; c += 32) {
-            const uint4 v = src[c];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        auto amax = [&](const uint4 &c) {
+            const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
             for (int j = 0; j < 4; j++) mx = max(mx, max(w[j] & 0x7fffu, (w[j] >> 16) & 0x7fffu));
+        };
+        if (held) {
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (u * 32 + lane < chunks) v[u] = src[u * 32 + lane];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; u++) amax(v[u]);
+        } else {
+            for (int c = lane; c < chunks; c += 32) amax(src[c]);
         }
         mx = __reduce_max_sync(0xffffffffu, mx);
         const int eh = mx >= 0x7c00u ? 0 : fp8_exponent(__half2float(__ushort_as_half((uint16_t)mx)));
         if (lane == 0) pexp[p] = eh;
         const float sc = exp2i(eh);
         uint2 *dst = reinterpret_cast<uint2 *>(h8 + (int64_t)p * I);
-        for (int c = lane; c < chunks; c += 32) {
-            const uint4 v = src[c];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        auto put = [&](const uint4 &c, int i) {
+            const uint32_t w[4] = {c.x, c.y, c.z, c.w};
             uint32_t o[2];
 #pragma unroll
             for (int j = 0; j < 2; j++) {
@@ -918,7 +973,14 @@ __global__ void quantise_h_kernel(const uint16_t *__restrict__ h, const int32_t 
                 const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&w[2 * j + 1]));
                 o[j] = e4m3x2(a.y * sc, a.x * sc) | (e4m3x2(b.y * sc, b.x * sc) << 16);
             }
-            dst[c] = make_uint2(o[0], o[1]);
+            dst[i] = make_uint2(o[0], o[1]);
+        };
+        if (held) {
+#pragma unroll
+            for (int u = 0; u < 4; u++)
+                if (u * 32 + lane < chunks) put(v[u], u * 32 + lane);
+        } else {
+            for (int c = lane; c < chunks; c += 32) put(src[c], c);
         }
     }
 }
