@@ -51,6 +51,17 @@
 // product is unchanged): a code word then dequantises with one LOP3 and one
 // fp16 FMA per pair of weights.
 //
+// The FP8 variant (MOE_PATH_PREFILL_FP8, 2-bit codes) runs the same kernel
+// on e4m3 operands (tcgen05.mma kind::f8f6f4, K = 32 per instruction): a
+// step still moves 128 bytes of every pair row and fills 32 TMEM columns per
+// weight row, but covers 128 reduction elements.  Every operand carries a
+// power-of-two scaling -- one exponent per weight row (from the row's largest
+// block scale), per pair for x and per pair for h -- which the epilogue
+// undoes on the fp32 accumulators.  A 32-weight block decodes through a
+// four-entry byte table of its e4m3 values (one conversion per block) and
+// byte selects, which put the even elements of each 16-group before the odd
+// ones; x and h are stored in that order too.
+//
 // The pages place the routed experts' FFN on the GPU and add their outputs
 // ("How Strata runs a 125-billion-parameter model on a single 12 GB to 24 GB
 // graphics card", Step 2) and read long prompts in chunks of tokens
