@@ -64,6 +64,8 @@ def run(L, x, T, path=FP8, with_shared=True):
     (3000, 32, 10, 256, 128),   # several 192-pair tiles per expert and ragged ones
     (700, 16, 4, 640, 384),     # five 128-row down tiles, six 64-row gate/up tiles
     (1, 16, 4, 256, 128),
+    (50, 1, 1, 128, 128),       # one expert, top-1, one reduction step per GEMM
+    (33, 3, 3, 128, 128),       # every expert in every token's top-3
 ])
 def test_fp8_matches_the_fp8_oracle(moe, T, E, k, H, I):
     """The routed sum alone against the oracle's FP8 routed sum (the shared expert, exact on both sides,
