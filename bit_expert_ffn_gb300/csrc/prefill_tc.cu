@@ -92,17 +92,19 @@ static_assert(TM_A + NA * 32 <= 512, "TMEM columns");
 constexpr int XCH_BYTES = 32 * 64 * 4;  // up values of one 32-pair chunk: 64 rows, fp32
 // Epilogue area.  Every storing warp has two fp16 32 x 32 staging blocks used
 // in turn, so one chunk's TMA store can still be reading a block while the
-// next chunk fills the other.  down: four warps x two blocks; gate/up: the
-// two gate warps x two blocks, then two exchange buffers.
+// next chunk fills the other.  down: eight warps x two blocks; gate/up: the
+// four gate warps x two blocks, then one exchange buffer per warp set.
 constexpr int STG = 32 * 32 * 2;
-constexpr int OFF_XCH = 2 * 2 * STG;
-constexpr int EPI_BYTES = OFF_XCH + 2 * XCH_BYTES > 4 * 2 * STG ? OFF_XCH + 2 * XCH_BYTES : 4 * 2 * STG;
-constexpr int THREADS = 576;
+constexpr int OFF_XCH = 4 * 2 * STG;
+constexpr int EPI_BYTES = OFF_XCH + 2 * XCH_BYTES > 8 * 2 * STG ? OFF_XCH + 2 * XCH_BYTES : 8 * 2 * STG;
+// 22 warps: 0-3, 16-17 producers and MMA, 4-7 epilogue, 8-15 dequantisation,
+// 18-21 the FP8 variant's second epilogue set (the fp16 kernels launch 18 warps)
 constexpr int DQ_WARP0 = 8;  // warps 8..15 dequantise: two threads per weight row, each every other step
 constexpr int DQ_WARPS = 8;
 constexpr int RING_WARP = 16;  // waits for free pair slots for the pair TMA issuer
 constexpr int CODE_WARP = 17;  // waits for free code slots for the code TMA issuer
-constexpr int EPI_WARP0 = 4;
+constexpr int EPI_WARP0 = 4;   // epilogue warps 4..7 and, for FP8, 18..21 (the odd 32-pair chunks);
+constexpr int EPI_WARP1 = 18;  // a warp reads TMEM lane quadrant warp % 4
 constexpr int NC_MAX = 8;
 constexpr unsigned long long kWaitNs = 2000000000ull;
 // fp32 values of this magnitude or more (and NaN) round to a non-finite fp16
@@ -120,6 +122,10 @@ struct Cfg {
     static constexpr int C_SC = BM * CODE_STEP;         // offset of the scales in a code entry
     static constexpr int C_BYTES = FP8 ? BM * 32 + BM * 16 : (BITS == 2 ? 2 * BM * 16 : 3 * BM * 16);
     static constexpr int NC = BITS == 2 ? 8 : 6;
+    // epilogue warp sets: the FP8 tiles' MMAs are short enough that a second set of four
+    // epilogue warps pays; with fp16 operands the extra warps only take issue slots
+    static constexpr int NSET = FP8 ? 2 : 1;
+    static constexpr int THREADS = FP8 ? 704 : 576;
     static constexpr int OFF_B = 0;
     static constexpr int OFF_C = OFF_B + NB * B_BYTES;
     static constexpr int OFF_E = OFF_C + NC * C_BYTES;
@@ -300,7 +306,7 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, int n, int issued, in
 }
 
 template <int BITS, bool SWIGLU, bool FP8>
-__global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_constant__ Args a,
+__global__ void __launch_bounds__(Cfg<BITS, FP8>::THREADS, 1) tc_gemm_kernel(const __grid_constant__ Args a,
                                                              const __grid_constant__ CUtensorMap tok_map,
                                                              const __grid_constant__ CUtensorMap tok_full_map,
                                                              const __grid_constant__ CUtensorMap code_map,
@@ -327,7 +333,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         }
         for (int i = 0; i < 2; i++) {
             tc::mbar_init(&S.acc_full[i], 1);
-            tc::mbar_init(&S.acc_empty[i], 4);
+            tc::mbar_init(&S.acc_empty[i], 4 * C::NSET);
         }
         tc::mbar_init(&S.mma_done, 1);
         S.abort = 0;
@@ -500,15 +506,21 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             tc::mma_commit(&S.mma_done);
             if (!tc::mbar_wait(&S.mma_done, 0, kWaitNs)) set_status(a.status, MOE_ERR_TIMEOUT);
         }
-    } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + 4) {
-        // ---------------- epilogue: TMEM -> registers -> shared (transposed) -> TMA store
-        const int q = warp - EPI_WARP0;  // TMEM lane quadrant: weight rows 32q .. 32q+31 of the tile
+    } else if ((warp >= EPI_WARP0 && warp < EPI_WARP0 + 4) ||
+               (C::NSET == 2 && warp >= EPI_WARP1 && warp < EPI_WARP1 + 4)) {
+        // ---------------- epilogue: TMEM -> registers -> shared (transposed) -> TMA store.  With two
+        // sets of four warps (one per TMEM lane quadrant each) they take the even and the odd
+        // 32-pair chunks of a tile, so two chunks drain at once.
+        const int q = warp & 3;  // TMEM lane quadrant: weight rows 32q .. 32q+31 of the tile
+        const int set = warp >= EPI_WARP1 ? 1 : 0;
+        const int xbar = set ? 6 : 1;  // the set's named barrier for the gate/up exchange
         float *xch = reinterpret_cast<float *>(dyn + C::OFF_E + OFF_XCH);
-        char *stg = dyn + C::OFF_E + q * 2 * STG;  // this warp's two staging blocks (gate/up: warps 0, 1)
+        // this warp's two staging blocks (gate/up: only the gate warps store)
+        char *stg = dyn + C::OFF_E + (SWIGLU ? set * 2 + (q & 1) : set * 4 + q) * 2 * STG;
         bool out_of_range = false;  // an h or y value that has no finite fp16
         int j = 0, nst = 0;         // nst: TMA stores this warp issued (block nst & 1 is next)
         // the gate/up warps meet at named barriers, so they decide together
-        // whether to stop (the OR over the four warps); the down warps alone
+        // whether to stop (the OR over the eight warps); the down warps alone
         int4 nxt = tile_entry(a, blockIdx.x, total);
         for (int tile = blockIdx.x; tile < total && (SWIGLU || !S.abort); tile += gridDim.x, j++) {
             int acc = j & 1, v = j >> 1;
@@ -521,7 +533,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                 const int orow = SWIGLU ? t.rt * 64 + (q & 1) * 32 + lane : t.rt * 128 + q * 32 + lane;
                 const int64_t mrow = SWIGLU && q >= 2 ? (int64_t)a.up_rows + orow : orow;
                 if (orow < a.rows) kwr = __ldg(a.kw + (int64_t)t.e * a.code_rows + mrow);
-                if (lane < t.cnt) pe_next = __ldg(a.pexp + t.p0 + lane);
+                if (set * 32 + lane < t.cnt) pe_next = __ldg(a.pexp + t.p0 + set * 32 + lane);
             }
             bool stop = !tc::mbar_wait_sleep(&S.acc_full[acc], v & 1, kWaitNs);
             stop = __any_sync(0xffffffffu, stop);  // the warp's TMEM loads need all its lanes
@@ -530,12 +542,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                 S.abort = 1;
             }
             stop = stop || S.abort;
-            if (SWIGLU) stop = tc::named_sync_or(2, 128, stop);
+            if (SWIGLU) stop = tc::named_sync_or(2, 128 * C::NSET, stop);
             if (stop) break;
             tc::tc_fence_after();
             uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BT);
             const float frow = exp2i(-kwr);  // FP8: 2^-kw of this lane's weight row (kw lies in [-9, 31])
-            for (int ch = 0; ch < t.n32; ch++) {
+            for (int ch = set; ch < t.n32; ch += C::NSET) {
                 uint32_t r[32];
                 __syncwarp();
                 tc::tmem_ld_32x32b_x32(tbase + ch * 32, r);
@@ -545,7 +557,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                 int pe = 0;
                 if constexpr (FP8) {
                     pe = pe_next;
-                    if (tok0 + 32 + lane < t.cnt) pe_next = __ldg(a.pexp + t.p0 + tok0 + 32 + lane);
+                    if (tok0 + 64 + lane < t.cnt) pe_next = __ldg(a.pexp + t.p0 + tok0 + 64 + lane);  // FP8: 2 sets
                 }
                 tc::tmem_ld_wait();
                 if constexpr (FP8) {
@@ -558,13 +570,16 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
                         r[i] = __float_as_uint(__uint_as_float(r[i]) * frow * __shfl_sync(0xffffffffu, fpair, i));
                 }
                 if (SWIGLU) {
-                    float *xb = xch + (ch & 1) * (XCH_BYTES / 4);
+                    // up rows: hand the values to the warps holding the gate rows.  One set alternates
+                    // two exchange buffers (a barrier per chunk); with two sets each has one buffer and
+                    // waits, before writing it, for its gate warps to have read the previous chunk.
+                    float *xb = xch + (C::NSET == 2 ? set : (ch & 1)) * (XCH_BYTES / 4);
+                    if (C::NSET == 2) tc::named_sync(xbar, 128);
                     if (q >= 2) {
-                        // up rows: hand the values to the warps holding the gate rows
 #pragma unroll
                         for (int i = 0; i < 32; i++) xb[i * 64 + (q - 2) * 32 + lane] = __uint_as_float(r[i]);
                     }
-                    tc::named_sync(1, 128);
+                    tc::named_sync(xbar, 128);
                     int orow0 = t.rt * 64 + q * 32;  // first output row of this warp
                     if (q < 2 && orow0 < a.rows) {
                         // stored column within the warp's 32
@@ -821,7 +836,7 @@ static moe_status launch_gemm(const Args &a, const CUtensorMap &tok, const CUten
     const int smem = Cfg<BITS, FP8>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "tc gemm attribute: %s", cudaGetErrorString(e));
-    fn<<<grid, THREADS, smem, s>>>(a, tok, tok_full, codes, scales, out);
+    fn<<<grid, Cfg<BITS, FP8>::THREADS, smem, s>>>(a, tok, tok_full, codes, scales, out);
     return check_launch(SWIGLU ? (FP8 ? "tc_gemm_gateup_fp8" : "tc_gemm_gateup")
                                : (FP8 ? "tc_gemm_down_fp8" : "tc_gemm_down"));
 }
