@@ -178,3 +178,37 @@ def test_fp8_wide_scales_keep_their_precision(moe):
     want8 = oracle.moe_layer(2, x, bufs.ids.cpu().numpy(), bufs.w.cpu().numpy().astype(np.float64), *arena,
                              shared=None, fp8=True)
     assert rel_l2(got, want8) <= FP8_TOL
+
+
+def _sweep_cases(n=10, seed=2024):
+    """Seeded random layer shapes for the tensor-core prefills: H and I multiples of 128 (64 for some fp16
+    cases), 1 to 64 experts, top-1 to top-10, 1 to 2,500 tokens, Zipf(1.4) or uniform routing."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        E = int(rng.choice([1, 3, 8, 16, 33, 64]))
+        k = int(rng.integers(1, min(E, 10) + 1))
+        H = int(rng.choice([128, 256, 384, 640, 1024]))
+        I = int(rng.choice([128, 256, 384, 512]))
+        T = int(rng.choice([1, 7, 64, 300, 1000, 2500]))
+        while T > 1 and T * k * H * I > 5e8:  # keeps the scalar oracle to seconds
+            T //= 2
+        cases.append((T, E, k, H, I, float(rng.choice([0.0, 1.4])), 100 + i))
+    return cases
+
+
+@pytest.mark.parametrize("T,E,k,H,I,zipf,seed", _sweep_cases())
+def test_tensor_core_prefills_random_shapes(moe, T, E, k, H, I, zipf, seed):
+    """Both tensor-core prefills on random shapes: the FP8 routed sum against the oracle's FP8 variant
+    (FP8_TOL) and the fp16-operand layer against the exact oracle (1e-3)."""
+    L, arena, shared = make_layer(H=H, I=I, E=E, k=k, zipf=zipf, seed=seed)
+    x = synth.activations(seed, T, H)
+    st, routed, bufs = run(L, x, T, with_shared=False)
+    assert st == 0, m.moe_last_error()
+    ids = bufs.ids.cpu().numpy()
+    w = bufs.w.cpu().numpy().astype(np.float64)
+    assert rel_l2(routed, oracle.moe_layer(2, x, ids, w, *arena, shared=None, fp8=True)) <= FP8_TOL
+    st, layer, bufs16 = run(L, x, T, m.MOE_PATH_PREFILL)
+    assert st == 0, m.moe_last_error()
+    assert np.array_equal(bufs16.ids.cpu().numpy(), ids)
+    assert rel_l2(layer, oracle.moe_layer(2, x, ids, w, *arena, shared=shared)) <= 1e-3
