@@ -317,7 +317,8 @@ moe_status moe_permute_noalloc(const int32_t *ids, int T, int k, int E, int32_t 
  *   outside it sets *dev_status = MOE_ERR_RANGE and the affected outputs are
  *   not finite.  Other shapes take an fp32 FFMA form with no such limit.
  * PREFILL_FP8: the PREFILL GEMMs with e4m3 operands (kind::f8f6f4 tensor-core
- *   instructions), an opt-in approximation that AUTO never picks.  2-bit
+ *   instructions), an opt-in approximation that AUTO never picks.  The pages
+ *   run no 8-bit arithmetic; this scheme is the library's own.  2-bit
  *   arenas with H and I multiples of 128 only; anything else returns
  *   MOE_ERR_UNSUPPORTED.  Every operand is an e4m3 value after a power-of-two
  *   scaling 2^e with e = 7 - floor(log2 m) (clamped to [-64, 64]), m the
