@@ -478,15 +478,16 @@ __global__ void __launch_bounds__(Cfg<BITS, FP8>::THREADS, 1) tc_gemm_kernel(con
                     for (int j = 0; j < ns; j++) {
                         const Slot sa = slot_of(it + j, NA), sb = slot_of(it + j, NB);
                         const uint32_t abase = tmem + (uint32_t)(TM_A + sa.s * 32);
-                        const uint32_t bbase = tc::smem_u32(dyn + C::OFF_B + sb.s * B_BYTES);
+                        // the step's B descriptor once; each instruction's 32 bytes of K advance its start
+                        // address field (bytes / 16) by 2, which stays inside the 14-bit field
+                        const uint64_t bdesc = tc::desc_kmajor_sw128(tc::smem_u32(dyn + C::OFF_B + sb.s * B_BYTES));
+                        const uint32_t acc0 = (kb + j) ? 1u : 0u;
 #pragma unroll
                         for (int k16 = 0; k16 < BK / 16; k16++) {  // 32 bytes of K per instruction
                             if constexpr (FP8)
-                                tc::mma_f8_ts(d, abase + k16 * 8, tc::desc_kmajor_sw128(bbase + k16 * 32), idesc,
-                                              ((kb + j) | k16) ? 1u : 0u);
+                                tc::mma_f8_ts(d, abase + k16 * 8, bdesc + (uint64_t)(2 * k16), idesc, k16 ? 1u : acc0);
                             else
-                                tc::mma_f16_ts(d, abase + k16 * 8, tc::desc_kmajor_sw128(bbase + k16 * 32), idesc,
-                                               ((kb + j) | k16) ? 1u : 0u);
+                                tc::mma_f16_ts(d, abase + k16 * 8, bdesc + (uint64_t)(2 * k16), idesc, k16 ? 1u : acc0);
                         }
                         tc::mma_commit(&S.aempty[sa.s]);
                         tc::mma_commit(&S.bempty[sb.s]);
