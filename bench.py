@@ -590,7 +590,8 @@ def bench_tiny(m, dev, reps: int = 200):
 def bench_prefill3(m, dev, T: int = 4096, n_layers: int = LAYERS, reps: int = 3):
     """3-bit prefill: T tokens through the 48-layer residual stack (RMS-normalised bf16 input to each
     layer, fp32 residual stream), prefill path, with uniform and with Zipf(1.4) routing (the same weights,
-    only the router bias changes).  CUDA events around each full 48-layer pass."""
+    only the router bias changes).  CUDA events around each full 48-layer pass.  The same passes through
+    the FP8 prefill (an approximation) are reported under "fp8", against twice the bf16 peak."""
     import torch
 
     from bit_expert_ffn_gb300 import synth
@@ -615,13 +616,16 @@ def bench_prefill3(m, dev, T: int = 4096, n_layers: int = LAYERS, reps: int = 3)
     peak_t, kind_t = peaks_bf16()
     peak_b, kind_b = peaks()
 
-    def one_pass():
+    def one_pass(path):
         for L in layers:
             m.moe_rms_norm_bf16(x, xb, T, s.H, m.RMS_EPS)
-            L.forward(xb, T, x, wsp, bufs, accumulate=True, path=m.MOE_PATH_PREFILL)
+            L.forward(xb, T, x, wsp, bufs, accumulate=True, path=path)
 
-    res = {}
-    for name, zs in (("uniform", 0.0), ("zipf_1.4", 1.4)):
+    res, res8 = {}, {}
+    for (name, zs), path in [(z, p) for p in (m.MOE_PATH_PREFILL, m.MOE_PATH_PREFILL_FP8)
+                             for z in (("uniform", 0.0), ("zipf_1.4", 1.4))]:
+        fp8 = path == m.MOE_PATH_PREFILL_FP8
+        out, pk = (res8, 2 * peak_t) if fp8 else (res, peak_t)
         for l, L in enumerate(layers):
             L.router_b.copy_(torch.from_numpy(synth.zipf_bias(4, l, s.E, zs)))
         # experts touched per layer (untimed pass, layer by layer)
@@ -629,14 +633,14 @@ def bench_prefill3(m, dev, T: int = 4096, n_layers: int = LAYERS, reps: int = 3)
         used = 0
         for L in layers:
             m.moe_rms_norm_bf16(x, xb, T, s.H, m.RMS_EPS)
-            L.forward(xb, T, x, wsp, bufs, accumulate=True, path=m.MOE_PATH_PREFILL)
+            L.forward(xb, T, x, wsp, bufs, accumulate=True, path=path)
             used += int((torch.diff(bufs.offsets) > 0).sum().item())
         times = []
         for r in range(reps + 2):
             x.copy_(x0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-            one_pass()
+            one_pass(path)
             e1.record()
             torch.cuda.synchronize()
             if r >= 2:
@@ -648,11 +652,11 @@ def bench_prefill3(m, dev, T: int = 4096, n_layers: int = LAYERS, reps: int = 3)
         nbytes = used * expert_bytes + n_layers * fixed_bytes
         tfl = flop_layer * n_layers / (ms / 1000.0) / 1e12
         gbs = nbytes / (ms / 1000.0) / 1e9
-        res[name] = {"value": T / (ms / 1000.0), "unit": "tokens/s", "ms_per_pass": ms,
+        out[name] = {"value": T / (ms / 1000.0), "unit": "tokens/s", "ms_per_pass": ms,
                      "experts_used_per_layer": used / n_layers,
-                     "tensor": {"achieved": tfl, "peak": peak_t, "unit": "TFLOP/s", "frac": tfl / peak_t,
-                                "peak_kind": kind_t, "flop": flop_layer * n_layers,
-                                "note": "routed expert FLOP only"},
+                     "tensor": {"achieved": tfl, "peak": pk, "unit": "TFLOP/s", "frac": tfl / pk,
+                                "peak_kind": kind_t + (" bf16 x 2 (e4m3)" if fp8 else ""),
+                                "flop": flop_layer * n_layers, "note": "routed expert FLOP only"},
                      "hbm": {"achieved": gbs, "peak": peak_b, "unit": "GB/s", "frac": gbs / peak_b,
                              "peak_kind": kind_b, "bytes": nbytes,
                              "note": "touched experts + router + shared expert, each read once"}}
@@ -660,7 +664,9 @@ def bench_prefill3(m, dev, T: int = 4096, n_layers: int = LAYERS, reps: int = 3)
     torch.cuda.empty_cache()
     return {"workload": f"3-bit prefill: {T} tokens x {n_layers} layers (residual stack), H=2048, E=512, I=768, "
                         "top-10, 3-bit experts (8 levels, 32-weight blocks, fp16 scales), bf16 shared expert",
-            **res}
+            **res,
+            "fp8": {"workload": "the same passes through the FP8 prefill (e4m3 operands, an approximation; "
+                                "tests/test_gpu_prefill_fp8.py reports its error against the exact layer)", **res8}}
 
 
 def run_ours(args, world, rank, local):

@@ -81,9 +81,9 @@ constexpr int BM = 128;  // weight rows per tile (MMA M); gate/up: 64 gate + 64 
 constexpr int BT = 192;  // sorted pairs per tile at most (MMA N, multiples of 32)
 constexpr int BK = 64;   // reduction per step: one 128-byte swizzle row of fp16
 constexpr int B_BYTES = BT * BK * 2;   // one step of the pairs' rows
-constexpr int C_LO = 0;                // code entry: low codes, 16 B (FP8: 32 B) per row,
-                                       //   then scales of four (FP8: two) steps, 16 B per row,
-constexpr int C_HI = 2 * BM * 16;      //   then 3-bit high planes of two steps, 16 B per row
+constexpr int C_LO = 0;                // code entry: low codes, 16 B (FP8: 32 B) per row, then scales of
+                                       //   four (FP8: two) steps, then 3-bit high planes of two (FP8: one)
+                                       //   steps, 16 B per row each (offsets in Cfg)
 constexpr int NA = 4, NB = 6;          // weight ring (TMEM), pair ring (shared memory)
 // TMEM columns: two accumulators of BT fp32 columns, then the weight ring
 // (a 64-wide fp16 step is 32 columns).
@@ -112,16 +112,18 @@ constexpr float kF16Limit = 65520.f;
 
 // Shared-memory plan per bit width and operand type: the code entry carries
 // the 3-bit high planes only for 3 bits, which leaves room for fewer entries.
-// A step of the FP8 variant (2 bits only) covers 128 elements of the
-// reduction: 32 bytes of codes per row, and four block scales.
+// A step of the FP8 variant covers 128 elements of the reduction: 32 bytes
+// of low codes per row, four block scales, and (3 bits) 16 bytes of high bits.
 template <int BITS, bool FP8 = false>
 struct Cfg {
-    static_assert(!FP8 || BITS == 2, "the FP8 variant takes 2-bit codes");
     static constexpr int BKE = FP8 ? 128 : BK;          // reduction elements per step (128 bytes of a pair row)
-    static constexpr int CODE_STEP = FP8 ? 32 : 16;     // code bytes per weight row and step
+    static constexpr int CODE_STEP = FP8 ? 32 : 16;     // low-code bytes per weight row and step
     static constexpr int C_SC = BM * CODE_STEP;         // offset of the scales in a code entry
-    static constexpr int C_BYTES = FP8 ? BM * 32 + BM * 16 : (BITS == 2 ? 2 * BM * 16 : 3 * BM * 16);
-    static constexpr int NC = BITS == 2 ? 8 : 6;
+    static constexpr int C_HI = C_SC + BM * 16;         // offset of the 3-bit high planes (16 B per row)
+    static constexpr int C_BYTES = C_SC + BM * 16 + (BITS == 3 ? BM * 16 : 0);
+    // code-ring entries (an FP8 entry covers twice the reduction; with 3 bits five leave room for the
+    // static spreading table)
+    static constexpr int NC = BITS == 2 ? 8 : (FP8 ? 5 : 6);
     // epilogue warp sets: the FP8 tiles' MMAs are short enough that a second set of four
     // epilogue warps pays; with fp16 operands the extra warps only take issue slots
     static constexpr int NSET = FP8 ? 2 : 1;
@@ -287,6 +289,42 @@ __device__ __forceinline__ void lut_word(uint32_t w, uint32_t lut, uint32_t *o)
     o[3] = prmt(lut, 0u, od >> 16);
 }
 
+// The eight e4m3 values a 3-bit block with scale S stands for, e4m3((c - 3.5) S):
+// hi holds codes 4..7 (0.5 S .. 3.5 S, each rounded once from its exact
+// value), lo codes 0..3 (the same magnitudes in reverse order, sign bit set).
+__device__ __forceinline__ void lut_3bit(float S, uint32_t &lo, uint32_t &hi)
+{
+    hi = e4m3x2(1.5f * S, 0.5f * S) | (e4m3x2(3.5f * S, 2.5f * S) << 16);
+    lo = prmt(hi, 0u, 0x0123u) ^ 0x80808080u;
+}
+
+// Byte b's bit j (the high bit of the j-th weight of a gathered byte: the
+// even or odd weights 0, 2, 4, 6 of a 16-weight word at j = 0, 2, 4, 6 and
+// 8, 10, 12, 14 at j = 1, 3, 5, 7) moved to bit 2 of the nibble that
+// lut_word's byte select gives that weight.
+__host__ __device__ __forceinline__ uint32_t spread_byte(int b)
+{
+    uint32_t v = 0;
+    for (int j = 0; j < 8; j++)
+        if ((b >> j) & 1) v |= 1u << (4 * ((j & 1) ? 4 + (j >> 1) : j >> 1) + 2);
+    return v;
+}
+
+// A word of sixteen 3-bit codes: low bits w (weight j at bits 2j..2j+1),
+// high bits hw as laid out for the word's half of the block (weights 0-7 at
+// bits 0-7, 8-15 at bits 16-23); output as lut_word's.
+__device__ __forceinline__ void lut_word3(uint32_t w, uint32_t hw, uint32_t lo, uint32_t hi, const uint32_t *spread,
+                                          uint32_t *o)
+{
+    const uint32_t be = (hw & 0x55u) | ((hw >> 15) & 0xAAu);         // high bits of the even weights
+    const uint32_t bo = ((hw >> 1) & 0x55u) | ((hw >> 16) & 0xAAu);  // and of the odd ones
+    const uint32_t ev = (w & 0x33333333u) | spread[be], od = ((w >> 2) & 0x33333333u) | spread[bo];
+    o[0] = prmt(lo, hi, ev);
+    o[1] = prmt(lo, hi, ev >> 16);
+    o[2] = prmt(lo, hi, od);
+    o[3] = prmt(lo, hi, od >> 16);
+}
+
 // silu with a fast division: h is rounded to fp16 right after, far coarser
 // than the approximation's couple of fp32 ulps.
 __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
@@ -311,9 +349,15 @@ __global__ void __launch_bounds__(Cfg<BITS, FP8>::THREADS, 1) tc_gemm_kernel(con
                                                              const __grid_constant__ CUtensorMap tok_full_map,
                                                              const __grid_constant__ CUtensorMap code_map,
                                                              const __grid_constant__ CUtensorMap scale_map,
-                                                             const __grid_constant__ CUtensorMap out_map)
+                                                             const __grid_constant__ CUtensorMap out_map,
+                                                             const __grid_constant__ CUtensorMap hi_map)
 {
     using C = Cfg<BITS, FP8>;
+    // FP8 with 3-bit codes: the high bits of eight weights (a byte) spread to bit 2 of the nibbles of
+    // their byte-select word
+    __shared__ uint32_t spread8[(FP8 && BITS == 3) ? 256 : 1];
+    if constexpr (FP8 && BITS == 3)
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) spread8[i] = spread_byte(i);
     extern __shared__ __align__(1024) char dyn_raw[];
     char *dyn = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
     __shared__ Shared S;
@@ -346,6 +390,7 @@ __global__ void __launch_bounds__(Cfg<BITS, FP8>::THREADS, 1) tc_gemm_kernel(con
         tc::tma_prefetch_desc(&code_map);
         if (a.scale_tma) tc::tma_prefetch_desc(&scale_map);
         tc::tma_prefetch_desc(&out_map);
+        if (FP8 && BITS == 3) tc::tma_prefetch_desc(&hi_map);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -364,7 +409,7 @@ __global__ void __launch_bounds__(Cfg<BITS, FP8>::THREADS, 1) tc_gemm_kernel(con
         // waiter and its issuer.
         // roles: 0 pair waiter, 1 pair issuer, 2 code issuer, 3 code waiter
         const int role = warp == RING_WARP ? 0 : warp == 0 ? 1 : warp == 3 ? 2 : 3;
-        const uint32_t cbytes = (BITS == 3 ? 2 * BM * 16 : BM * C::CODE_STEP) + (a.scale_tma ? BM * 16 : 0);
+        const uint32_t cbytes = BM * C::CODE_STEP + (BITS == 3 ? BM * 16 : 0) + (a.scale_tma ? BM * 16 : 0);
         int it = 0;
         bool stop = false;
         int4 nxt = tile_entry(a, blockIdx.x, total);
@@ -417,9 +462,11 @@ __global__ void __launch_bounds__(Cfg<BITS, FP8>::THREADS, 1) tc_gemm_kernel(con
                             tc::tma_load_2d(cs + C::C_SC, &scale_map, sx, r0, &S.cfull[c.s]);
                             tc::tma_load_2d(cs + C::C_SC + 64 * 16, &scale_map, sx, r1, &S.cfull[c.s]);
                         }
-                        if (BITS == 3) {
-                            tc::tma_load_2d(cs + C_HI, &code_map, a.hi_x + (kb >> 1) * 16, r0, &S.cfull[c.s]);
-                            tc::tma_load_2d(cs + C_HI + 64 * 16, &code_map, a.hi_x + (kb >> 1) * 16, r1,
+                        if (BITS == 3) {  // 16 B of high bits per row: two steps (FP8: one)
+                            const CUtensorMap *hm = FP8 ? &hi_map : &code_map;
+                            const int hx = a.hi_x + (FP8 ? kb : kb >> 1) * 16;
+                            tc::tma_load_2d(cs + C::C_HI, hm, hx, r0, &S.cfull[c.s]);
+                            tc::tma_load_2d(cs + C::C_HI + 64 * 16, hm, hx, r1,
                                             &S.cfull[c.s]);
                         }
                     }
@@ -692,6 +739,7 @@ __global__ void __launch_bounds__(Cfg<BITS, FP8>::THREADS, 1) tc_gemm_kernel(con
                 const char *cs = dyn + C::OFF_C + c.s * C::C_BYTES;
                 uint4 cw = make_uint4(0u, 0u, 0u, 0u), cw1 = make_uint4(0u, 0u, 0u, 0u);
                 uint2 hw = make_uint2(0u, 0u);
+                uint4 hw4 = make_uint4(0u, 0u, 0u, 0u);  // FP8, 3 bits: one high-bit word per block
                 if (valid) {
                     cw = *reinterpret_cast<const uint4 *>(cs + C_LO + r * C::CODE_STEP);
                     if constexpr (FP8) {
@@ -700,7 +748,10 @@ __global__ void __launch_bounds__(Cfg<BITS, FP8>::THREADS, 1) tc_gemm_kernel(con
                     } else {
                         if (a.scale_tma) sc = lds32(cs + C::C_SC + r * 16 + (kb & 3) * 4);
                     }
-                    if (BITS == 3) hw = *reinterpret_cast<const uint2 *>(cs + C_HI + r * 16 + (kb & 1) * 8);
+                    if constexpr (BITS == 3) {
+                        if constexpr (FP8) hw4 = *reinterpret_cast<const uint4 *>(cs + C::C_HI + r * 16);
+                        else hw = *reinterpret_cast<const uint2 *>(cs + C::C_HI + r * 16 + (kb & 1) * 8);
+                    }
                 }
                 if (valid) {
                     if constexpr (FP8) {
@@ -729,15 +780,24 @@ __global__ void __launch_bounds__(Cfg<BITS, FP8>::THREADS, 1) tc_gemm_kernel(con
                     // 128 weights: four 32-weight blocks, each a byte table of its four e4m3 values
                     // and two code words decoded by byte selects into eight TMEM columns
                     const uint32_t words[8] = {cw.x, cw.y, cw.z, cw.w, cw1.x, cw1.y, cw1.z, cw1.w};
+                    const uint32_t hws[4] = {hw4.x, hw4.y, hw4.z, hw4.w};
 #pragma unroll
                     for (int b = 0; b < 4; b++) {
                         uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
                         if (valid) {
                             const uint32_t sw = b < 2 ? sc4.x : sc4.y;
                             const uint16_t sh = (uint16_t)((b & 1) ? sw >> 16 : sw & 0xffffu);
-                            const uint32_t lut = lut_2bit(__half2float(__ushort_as_half(sh)) * p2kw);
-                            lut_word(words[2 * b], lut, v);
-                            lut_word(words[2 * b + 1], lut, v + 4);
+                            const float S = __half2float(__ushort_as_half(sh)) * p2kw;
+                            if constexpr (BITS == 2) {
+                                const uint32_t lut = lut_2bit(S);
+                                lut_word(words[2 * b], lut, v);
+                                lut_word(words[2 * b + 1], lut, v + 4);
+                            } else {
+                                uint32_t lo, hi;
+                                lut_3bit(S, lo, hi);
+                                lut_word3(words[2 * b], hws[b], lo, hi, spread8, v);
+                                lut_word3(words[2 * b + 1], hws[b] >> 8, lo, hi, spread8, v + 4);
+                            }
                         }
                         tc::tmem_st_32x32b_x8(tq + (uint32_t)(sa.s * 32 + b * 8), v);
                     }
@@ -831,13 +891,13 @@ __global__ void gather_x_kernel(const uint16_t *__restrict__ x, const int32_t *_
 template <int BITS, bool SWIGLU, bool FP8 = false>
 static moe_status launch_gemm(const Args &a, const CUtensorMap &tok, const CUtensorMap &tok_full,
                               const CUtensorMap &codes, const CUtensorMap &scales, const CUtensorMap &out, int grid,
-                              cudaStream_t s)
+                              cudaStream_t s, const CUtensorMap *hi = nullptr)
 {
     auto fn = tc_gemm_kernel<BITS, SWIGLU, FP8>;
     const int smem = Cfg<BITS, FP8>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "tc gemm attribute: %s", cudaGetErrorString(e));
-    fn<<<grid, Cfg<BITS, FP8>::THREADS, smem, s>>>(a, tok, tok_full, codes, scales, out);
+    fn<<<grid, Cfg<BITS, FP8>::THREADS, smem, s>>>(a, tok, tok_full, codes, scales, out, hi ? *hi : codes);
     return check_launch(SWIGLU ? (FP8 ? "tc_gemm_gateup_fp8" : "tc_gemm_gateup")
                                : (FP8 ? "tc_gemm_down_fp8" : "tc_gemm_down"));
 }
@@ -845,11 +905,11 @@ static moe_status launch_gemm(const Args &a, const CUtensorMap &tok, const CUten
 // ---- FP8 variant: the operands' exponents and e4m3 copies -------------------
 
 // kw[e][row] = the exponent of weight row `row` of expert e, from the largest
-// magnitude a code of the row can stand for (1.5 times its largest |s|), for
-// the experts that have pairs (the others are never read).  A non-finite
-// scale sets MOE_ERR_RANGE.
+// magnitude a code of the row can stand for (maxc = max|c - mid|, 1.5 or 3.5,
+// times its largest |s|), for the experts that have pairs (the others are
+// never read).  A non-finite scale sets MOE_ERR_RANGE.
 __global__ void fp8_row_exponent_kernel(const uint16_t *__restrict__ scales, const int32_t *__restrict__ offsets,
-                                        int E, int rows, int blocks, int8_t *__restrict__ kw,
+                                        int E, int rows, int blocks, float maxc, int8_t *__restrict__ kw,
                                         int32_t *__restrict__ status)
 {
     bool bad = false;
@@ -870,7 +930,7 @@ __global__ void fp8_row_exponent_kernel(const uint16_t *__restrict__ scales, con
             for (int b = 0; b < blocks; b++) mx = max(mx, (uint32_t)__ldg(sp + b) & 0x7fffu);
         }
         bad |= mx >= 0x7c00u;
-        kw[i] = (int8_t)(mx >= 0x7c00u ? 0 : fp8_exponent(1.5f * __half2float(__ushort_as_half((uint16_t)mx))));
+        kw[i] = (int8_t)(mx >= 0x7c00u ? 0 : fp8_exponent(maxc * __half2float(__ushort_as_half((uint16_t)mx))));
     }
     if (bad) set_status(status, MOE_ERR_RANGE);
 }
@@ -1068,11 +1128,11 @@ bool prefill_tc_supported(const moe_expert_arena &A)
 
 size_t prefill_tc_workspace_bytes(const moe_expert_arena &A, int T, int k) { return ptc_ws(A, T, k, nullptr).bytes; }
 
-// The FP8 variant takes 2-bit arenas whose H and I are multiples of 128 (a
-// step reduces over 128 elements).
+// The FP8 variant takes arenas whose H and I are multiples of 128 (a step
+// reduces over 128 elements).
 bool prefill_fp8_supported(const moe_expert_arena &A)
 {
-    return A.bits == 2 && prefill_tc_supported(A) && A.H % 128 == 0 && A.I % 128 == 0;
+    return (A.bits == 2 || A.bits == 3) && prefill_tc_supported(A) && A.H % 128 == 0 && A.I % 128 == 0;
 }
 
 size_t prefill_fp8_workspace_bytes(const moe_expert_arena &A, int T, int k)
@@ -1165,12 +1225,14 @@ static moe_status run_tc(const moe_expert_arena &A, const uint16_t *x, int T, co
 
 // The FP8 variant: the weights' row exponents, the pairs' e4m3 x rows, the
 // gate/up GEMM (h in fp16), h to e4m3, the down GEMM, the combine.
+template <int BITS>
 static moe_status run_fp8(const moe_expert_arena &A, const uint16_t *x, int T, const float *w, int k,
                           const int32_t *offsets, const int32_t *perm, const int32_t *inv, void *out, moe_dtype dt,
                           int accumulate, const PtcWs &d, int32_t *status, cudaStream_t s)
 {
     using namespace ptc;
-    using C = Cfg<2, true>;
+    using C = Cfg<BITS, true>;
+    const float maxc = BITS == 2 ? 1.5f : 3.5f;
     int64_t n = (int64_t)T * k;
     tile_prefix_kernel<<<1, 1024, 0, s>>>(offsets, A.E, BT, d.mt_prefix);
     moe_status st = check_launch("tile_prefix");
@@ -1179,25 +1241,30 @@ static moe_status run_fp8(const moe_expert_arena &A, const uint16_t *x, int T, c
     st = check_launch("tile_table");
     if (st != MOE_OK) return st;
     const int sms = sm_count();
-    fp8_row_exponent_kernel<<<sms * 4, 256, 0, s>>>(A.gu_scales, offsets, A.E, 2 * A.I, A.H / 32, d.kw_gu, status);
+    fp8_row_exponent_kernel<<<sms * 4, 256, 0, s>>>(A.gu_scales, offsets, A.E, 2 * A.I, A.H / 32, maxc, d.kw_gu,
+                                                     status);
     st = check_launch("fp8_row_exponent");
     if (st != MOE_OK) return st;
-    fp8_row_exponent_kernel<<<sms * 4, 256, 0, s>>>(A.d_scales, offsets, A.E, A.H, A.I / 32, d.kw_d, status);
+    fp8_row_exponent_kernel<<<sms * 4, 256, 0, s>>>(A.d_scales, offsets, A.E, A.H, A.I / 32, maxc, d.kw_d, status);
     st = check_launch("fp8_row_exponent");
     if (st != MOE_OK) return st;
     const int gblocks = (int)std::max<int64_t>(1, std::min<int64_t>((n + 7) / 8, (int64_t)sms * 16));  // 8 rows per CTA
     gather_x_fp8_kernel<<<gblocks, 256, 0, s>>>(x, perm, offsets, A.E, k, A.H, d.x8, d.ex, status);
     st = check_launch("gather_x_fp8");
     if (st != MOE_OK) return st;
-    const int rbH = A.H / 4, rbI = A.I / 4;
+    const int rbH = BITS == 2 ? A.H / 4 : A.H / 4 + A.H / 8, rbI = BITS == 2 ? A.I / 4 : A.I / 4 + A.I / 8;
     const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    // gate/up: codes [E * 2I][rbH], pairs' e4m3 rows x8 [n][H] -> h [n][I] (fp16)
-    CUtensorMap mtok, mtokf, mcode, mscale, mout;
+    // gate/up: codes [E * 2I][rbH], pairs' e4m3 rows x8 [n][H] -> h [n][I] (fp16); for 3 bits the high
+    // planes come through a map of 16-byte boxes
+    CUtensorMap mtok, mtokf, mcode, mscale, mout, mhi;
     st = make_tmap_2d(&mtok, d.x8, U8, 1, n, A.H, C::BKE, 32, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st == MOE_OK) st = make_tmap_2d(&mtokf, d.x8, U8, 1, n, A.H, C::BKE, BT, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st == MOE_OK)
         st = make_tmap_2d(&mcode, A.gu_codes, U8, 1, (int64_t)A.E * 2 * A.I, rbH, C::CODE_STEP, 64,
                           CU_TENSOR_MAP_SWIZZLE_NONE);
+    mhi = mcode;
+    if (st == MOE_OK && BITS == 3)
+        st = make_tmap_2d(&mhi, A.gu_codes, U8, 1, (int64_t)A.E * 2 * A.I, rbH, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st == MOE_OK) st = make_tmap_2d(&mout, d.h, F16, 2, n, A.I, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
     const bool sc_gu = A.H % 256 == 0;  // scale rows (H/32 fp16) are 16-byte multiples
     mscale = mcode;
@@ -1215,13 +1282,14 @@ static moe_status run_fp8(const moe_expert_arena &A, const uint16_t *x, int T, c
     a.rows = A.I;
     a.up_rows = A.I;
     a.rtiles = (A.I + 63) / 64;
+    a.hi_x = A.H / 4;
     a.table = d.table;
     a.ntt = d.mt_prefix + A.E;
     a.h_out = d.h;
     a.status = status;
     a.kw = d.kw_gu;
     a.pexp = d.ex;
-    st = launch_gemm<2, true, true>(a, mtok, mtokf, mcode, mscale, mout, sms, s);
+    st = launch_gemm<BITS, true, true>(a, mtok, mtokf, mcode, mscale, mout, sms, s, &mhi);
     if (st != MOE_OK) return st;
     quantise_h_kernel<<<gblocks, 256, 0, s>>>(d.h, offsets, A.E, A.I, d.h8, d.eh);
     st = check_launch("quantise_h");
@@ -1232,6 +1300,9 @@ static moe_status run_fp8(const moe_expert_arena &A, const uint16_t *x, int T, c
     if (st == MOE_OK)
         st = make_tmap_2d(&mcode, A.d_codes, U8, 1, (int64_t)A.E * A.H, rbI, C::CODE_STEP, 64,
                           CU_TENSOR_MAP_SWIZZLE_NONE);
+    mhi = mcode;
+    if (st == MOE_OK && BITS == 3)
+        st = make_tmap_2d(&mhi, A.d_codes, U8, 1, (int64_t)A.E * A.H, rbI, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st == MOE_OK) st = make_tmap_2d(&mout, d.y, F16, 2, n, A.H, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
     const bool sc_d = A.I % 256 == 0;
     mscale = mcode;
@@ -1248,11 +1319,12 @@ static moe_status run_fp8(const moe_expert_arena &A, const uint16_t *x, int T, c
     b.rows = A.H;
     b.up_rows = 0;
     b.rtiles = (A.H + 127) / 128;
+    b.hi_x = A.I / 4;
     b.h_out = nullptr;
     b.y_out = d.y;
     b.kw = d.kw_d;
     b.pexp = d.eh;
-    st = launch_gemm<2, false, true>(b, mtok, mtokf, mcode, mscale, mout, sms, s);
+    st = launch_gemm<BITS, false, true>(b, mtok, mtokf, mcode, mscale, mout, sms, s, &mhi);
     if (st != MOE_OK) return st;
     return launch_combine_f16(d.y, w, inv, T, k, A.H, out, dt, accumulate, s);
 }
@@ -1262,7 +1334,8 @@ moe_status prefill_fp8_forward(const moe_expert_arena &A, const uint16_t *x, int
                                moe_dtype dt, int accumulate, void *ws, int32_t *dev_status, cudaStream_t s)
 {
     PtcWs d = ptc_ws(A, T, k, ws, true);
-    return run_fp8(A, x, T, w, k, offsets, perm, inv, out, dt, accumulate, d, dev_status, s);
+    if (A.bits == 2) return run_fp8<2>(A, x, T, w, k, offsets, perm, inv, out, dt, accumulate, d, dev_status, s);
+    return run_fp8<3>(A, x, T, w, k, offsets, perm, inv, out, dt, accumulate, d, dev_status, s);
 }
 
 moe_status prefill_tc_forward(const moe_expert_arena &A, const uint16_t *x, int T, const float *w, int k,

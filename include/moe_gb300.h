@@ -318,14 +318,14 @@ moe_status moe_permute_noalloc(const int32_t *ids, int T, int k, int E, int32_t 
  *   not finite.  Other shapes take an fp32 FFMA form with no such limit.
  * PREFILL_FP8: the PREFILL GEMMs with e4m3 operands (kind::f8f6f4 tensor-core
  *   instructions), an opt-in approximation that AUTO never picks.  The pages
- *   run no 8-bit arithmetic; this scheme is the library's own.  2-bit
- *   arenas with H and I multiples of 128 only; anything else returns
+ *   run no 8-bit arithmetic; this scheme is the library's own.  2- and
+ *   3-bit arenas with H and I multiples of 128 only; anything else returns
  *   MOE_ERR_UNSUPPORTED.  Every operand is an e4m3 value after a power-of-two
  *   scaling 2^e with e = 7 - floor(log2 m) (clamped to [-64, 64]), m the
- *   largest magnitude it covers: one e per weight row (m = 1.5 times the
- *   row's largest |s|), per pair for x, and per pair for h, which is first
- *   rounded to fp16 as in PREFILL; each weight is e4m3((c - 1.5) s 2^e),
- *   rounded once.  Products accumulate in fp32 and the scalings are undone on
+ *   largest magnitude it covers: one e per weight row (m = max|c - mid|
+ *   times the row's largest |s|), per pair for x, and per pair for h, which
+ *   is first rounded to fp16 as in PREFILL; each weight is
+ *   e4m3((c - mid) s 2^e), rounded once.  Products accumulate in fp32 and the scalings are undone on
  *   the accumulators; y is kept as fp16 until the combine.  The rounding of
  *   three operands to 3 mantissa bits costs a relative L2 error of about
  *   6e-2 on one expert's output and about 3e-2 on a layer whose bf16 shared

@@ -45,8 +45,6 @@ def fused(layers, x0, T_):
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("bits", [2, 3])
 def test_zero_scales_leave_the_shared_expert(moe, path, bits):
-    if path == m.MOE_PATH_PREFILL_FP8 and bits == 3:
-        pytest.skip("the FP8 prefill takes 2-bit codes")
     arena, wr, b, shared = host_layer(seed=31, bits=bits, H=H, I=I, E=E, Is=IS, zipf=1.1)
     arena = [a if i % 2 == 0 else np.zeros_like(a) for i, a in enumerate(arena)]  # every scale +0
     L = layer(arena, wr, b, shared, bits)
