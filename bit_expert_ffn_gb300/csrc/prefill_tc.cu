@@ -833,23 +833,19 @@ __global__ void __launch_bounds__(Cfg<BITS, FP8>::THREADS, 1) tc_gemm_kernel(con
     }
 }
 
-// x_g[p][16g + perm16(m)] = fp16(x[tok(p)][16g + m]) for the valid pairs; an
-// x without a finite fp16 sets MOE_ERR_RANGE.  One warp per pair row (its
-// token looked up once), lanes over the row's 16-element groups, so loads and
-// stores are coalesced 16-byte accesses; each lane issues the loads of up to
-// four groups before converting any, so several reads are in flight.
-__global__ void gather_x_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm,
-                                const int32_t *__restrict__ offsets, int E, int k, int H, uint16_t *__restrict__ xg,
-                                int32_t *__restrict__ status)
+// x_g[p][16g + perm16(m)] = fp16(x[t][16g + m]) for every pair p = inv[t*k + j]
+// of token t (pairs with inv < 0 are not in this call); an x without a
+// finite fp16 sets MOE_ERR_RANGE.  One warp per token: its row is read once
+// (in token order, so each x row comes from memory once) and written to each
+// of its pair rows; lanes take the row's 16-element groups, 16-byte accesses.
+__global__ void gather_x_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ inv, int T, int k,
+                                int H, uint16_t *__restrict__ xg, int32_t *__restrict__ status)
 {
     bool out_of_range = false;
-    const int n = offsets[E];
     const int groups = H / 16, lane = lane_id();
     const int warps = (int)(gridDim.x * blockDim.x >> 5);
-    for (int p = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); p < n; p += warps) {
-        const int tok = perm[p] / k;
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)tok * H);
-        uint4 *dst = reinterpret_cast<uint4 *>(xg + (int64_t)p * H);
+    for (int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); t < T; t += warps) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)t * H);
         for (int g0 = 0; g0 < groups; g0 += 4 * 32) {
             uint4 a[4][2];
 #pragma unroll
@@ -860,6 +856,7 @@ __global__ void gather_x_kernel(const uint16_t *__restrict__ x, const int32_t *_
                     a[u][1] = __ldg(src + 2 * g + 1);
                 }
             }
+            uint4 o[4][2];
 #pragma unroll
             for (int u = 0; u < 4; u++) {
                 const int g = g0 + u * 32 + lane;
@@ -874,14 +871,27 @@ __global__ void gather_x_kernel(const uint16_t *__restrict__ x, const int32_t *_
                 }
 #pragma unroll
                 for (int mm = 0; mm < 16; mm++) out_of_range |= !(fabsf(f[mm]) < kF16Limit);
-                uint32_t o[8];
+                uint32_t h[8];
 #pragma unroll
                 for (int mm = 0; mm < 8; mm++) {
                     __half2 hv = __floats2half2_rn(f[mm], f[mm + 8]);
-                    o[mm] = *reinterpret_cast<uint32_t *>(&hv);
+                    h[mm] = *reinterpret_cast<uint32_t *>(&hv);
                 }
-                dst[2 * g] = make_uint4(o[0], o[1], o[2], o[3]);
-                dst[2 * g + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+                o[u][0] = make_uint4(h[0], h[1], h[2], h[3]);
+                o[u][1] = make_uint4(h[4], h[5], h[6], h[7]);
+            }
+            for (int j = 0; j < k; j++) {
+                const int p = __ldg(inv + (int64_t)t * k + j);
+                if (p < 0) continue;
+                uint4 *dst = reinterpret_cast<uint4 *>(xg + (int64_t)p * H);
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    const int g = g0 + u * 32 + lane;
+                    if (g < groups) {
+                        dst[2 * g] = o[u][0];
+                        dst[2 * g + 1] = o[u][1];
+                    }
+                }
             }
         }
     }
@@ -935,24 +945,23 @@ __global__ void fp8_row_exponent_kernel(const uint16_t *__restrict__ scales, con
     if (bad) set_status(status, MOE_ERR_RANGE);
 }
 
-// x8[p][16g + pos8(m)] = e4m3(x[tok(p)][16g + m] 2^ex[p]), ex[p] the exponent
-// of the token's largest |x|.  One warp per pair row: the row is read once for
-// its maximum and once more (from cache) to convert it.  A non-finite x, or a
-// row whose largest |x| still exceeds e4m3's range after the largest
-// down-scaling (2^-64), sets MOE_ERR_RANGE.
-__global__ void gather_x_fp8_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm,
-                                    const int32_t *__restrict__ offsets, int E, int k, int H, uint8_t *__restrict__ x8,
-                                    int32_t *__restrict__ pexp, int32_t *__restrict__ status)
+// x8[p][16g + pos8(m)] = e4m3(x[t][16g + m] 2^ex[p]) for every pair p =
+// inv[t*k + j] of token t (pairs with inv < 0 are not in this call), ex the
+// exponent of the token's largest |x|.  One warp per token: the row is read
+// once (rows of up to 2,048 elements are kept in registers between the
+// maximum and the conversion), converted once, and written to each of its pair
+// rows.  A non-finite x, or a row whose largest |x| still exceeds e4m3's range
+// after the largest down-scaling (2^-64), sets MOE_ERR_RANGE.
+__global__ void gather_x_fp8_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ inv, int T, int k,
+                                    int H, uint8_t *__restrict__ x8, int32_t *__restrict__ pexp,
+                                    int32_t *__restrict__ status)
 {
     bool out_of_range = false;
-    const int n = offsets[E];
     const int groups = H / 16, lane = lane_id();
     const int warps = (int)(gridDim.x * blockDim.x >> 5);
-    for (int p = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); p < n; p += warps) {
-        const int tok = perm[p] / k;
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)tok * H);
-        // rows of up to 128 groups stay in registers between the two passes; longer ones are read twice
-        const bool held = groups <= 4 * 32;
+    const bool held = groups <= 4 * 32;
+    for (int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); t < T; t += warps) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)t * H);
         uint4 a[4][2];
         uint32_t mx = 0;  // largest |x| as bf16 bits
         if (held) {
@@ -984,11 +993,9 @@ __global__ void gather_x_fp8_kernel(const uint16_t *__restrict__ x, const int32_
         const float amax = __uint_as_float(mx << 16);
         const int ex = mx >= 0x7f80u ? 0 : fp8_exponent(amax);
         out_of_range |= mx >= 0x7f80u || amax * exp2i(ex) >= 464.f;
-        if (lane == 0) pexp[p] = ex;
         const float sc = exp2i(ex);
-        uint4 *dst = reinterpret_cast<uint4 *>(x8 + (int64_t)p * H);
         // stored bytes 0-3: elements 0, 2, 4, 6; 4-7: 8, 10, 12, 14; 8-11: 1, 3, 5, 7; 12-15: 9, 11, 13, 15
-        auto put = [&](const uint4 &a0, const uint4 &a1, int g) {
+        auto conv = [&](const uint4 &a0, const uint4 &a1) {
             const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             float f[16];
 #pragma unroll
@@ -1002,14 +1009,29 @@ __global__ void gather_x_fp8_kernel(const uint16_t *__restrict__ x, const int32_
                 const int m0 = (q & 1) * 8 + (q >> 1);  // element at the word's first byte
                 o[q] = e4m3x2(f[m0 + 2], f[m0]) | (e4m3x2(f[m0 + 6], f[m0 + 4]) << 16);
             }
-            dst[g] = make_uint4(o[0], o[1], o[2], o[3]);
+            return make_uint4(o[0], o[1], o[2], o[3]);
         };
         if (held) {
+            uint4 c[4];
 #pragma unroll
-            for (int u = 0; u < 4; u++)
-                if (u * 32 + lane < groups) put(a[u][0], a[u][1], u * 32 + lane);
+            for (int u = 0; u < 4; u++) c[u] = conv(a[u][0], a[u][1]);
+            for (int j = 0; j < k; j++) {
+                const int p = __ldg(inv + (int64_t)t * k + j);
+                if (p < 0) continue;
+                if (lane == 0) pexp[p] = ex;
+                uint4 *dst = reinterpret_cast<uint4 *>(x8 + (int64_t)p * H);
+#pragma unroll
+                for (int u = 0; u < 4; u++)
+                    if (u * 32 + lane < groups) dst[u * 32 + lane] = c[u];
+            }
         } else {
-            for (int g = lane; g < groups; g += 32) put(__ldg(src + 2 * g), __ldg(src + 2 * g + 1), g);
+            for (int j = 0; j < k; j++) {
+                const int p = __ldg(inv + (int64_t)t * k + j);
+                if (p < 0) continue;
+                if (lane == 0) pexp[p] = ex;
+                uint4 *dst = reinterpret_cast<uint4 *>(x8 + (int64_t)p * H);
+                for (int g = lane; g < groups; g += 32) dst[g] = conv(__ldg(src + 2 * g), __ldg(src + 2 * g + 1));
+            }
         }
     }
     if (out_of_range) set_status(status, MOE_ERR_RANGE);
@@ -1153,8 +1175,8 @@ static moe_status run_tc(const moe_expert_arena &A, const uint16_t *x, int T, co
     tile_table_kernel<<<(A.E + 255) / 256, 256, 0, s>>>(offsets, d.mt_prefix, A.E, BT, d.table);
     st = check_launch("tile_table");
     if (st != MOE_OK) return st;
-    int gblocks = (int)std::max<int64_t>(1, std::min<int64_t>((n + 7) / 8, (int64_t)sm_count() * 16));  // 8 rows per CTA
-    gather_x_kernel<<<gblocks, 256, 0, s>>>(x, perm, offsets, A.E, k, A.H, d.xg, status);
+    const int tblocks = std::max(1, std::min((T + 7) / 8, sm_count() * 16));  // 8 tokens per CTA
+    gather_x_kernel<<<tblocks, 256, 0, s>>>(x, inv, T, k, A.H, d.xg, status);
     st = check_launch("gather_x");
     if (st != MOE_OK) return st;
     int rbH = BITS == 2 ? A.H / 4 : A.H / 4 + A.H / 8;
@@ -1249,7 +1271,8 @@ static moe_status run_fp8(const moe_expert_arena &A, const uint16_t *x, int T, c
     st = check_launch("fp8_row_exponent");
     if (st != MOE_OK) return st;
     const int gblocks = (int)std::max<int64_t>(1, std::min<int64_t>((n + 7) / 8, (int64_t)sms * 16));  // 8 rows per CTA
-    gather_x_fp8_kernel<<<gblocks, 256, 0, s>>>(x, perm, offsets, A.E, k, A.H, d.x8, d.ex, status);
+    const int tblocks = std::max(1, std::min((T + 7) / 8, sms * 16));  // 8 tokens per CTA
+    gather_x_fp8_kernel<<<tblocks, 256, 0, s>>>(x, inv, T, k, A.H, d.x8, d.ex, status);
     st = check_launch("gather_x_fp8");
     if (st != MOE_OK) return st;
     const int rbH = BITS == 2 ? A.H / 4 : A.H / 4 + A.H / 8, rbI = BITS == 2 ? A.I / 4 : A.I / 4 + A.I / 8;
