@@ -15,8 +15,8 @@
 // each as deep as its producer's latency asks:
 //   warp 3      TMA: packed codes and scales of each step into the code
 //               ring (shared memory, several steps ahead);
-//   warp 0      TMA: the pairs' fp16 rows of each step into the pair ring
-//               (shared memory, 128-byte swizzle);
+//   warp 0      TMA: the pairs' fp16 (FP8: e4m3) rows of each step into the
+//               pair ring (shared memory, 128-byte swizzle);
 //   warps 16-17 wait for free slots of the pair and code rings and hand
 //               them to the two TMA warps (an mbarrier call right after
 //               queued copies would stall the issuing thread);
@@ -32,7 +32,9 @@
 //               for warp 1, handing each ready step over by a named barrier;
 //   warps 4-7   epilogue: TMEM -> registers, transposed through shared
 //               memory, written by TMA stores (the gate/up epilogue first
-//               hands the up rows' values to the gate rows' warps).
+//               hands the up rows' values to the gate rows' warps); the
+//               FP8 kernels add warps 18-21, a second set that takes the
+//               odd 32-pair chunks of each tile.
 // Keeping the weights out of shared memory leaves its bandwidth to the
 // pairs' rows, which the tensor cores read there.
 // Operands are fp16: x (bf16) converts exactly while 2^-14 <= |x| <= 65504
